@@ -1,0 +1,359 @@
+#!/usr/bin/env python3
+"""Benchmark of the W8A8 INT8 projection Linear on one GB300 (or N replicas).
+
+Workload (the attention projection of the MiniMax-H3 DiT at native width):
+X BF16 [8192, 5376] ~ N(0,1) with 0.5% of entries x30; four Linears Q, K, V, O
+with weights [5376, 5376] ~ N(0, 0.02) quantised per output channel to INT8
+with FP32 scales (untimed, offline), BF16 biases ~ N(0, 0.1); seed 1.
+
+One step = the whole hot path over that batch: the per-token activation
+quantisation of X, then the four INT8 GEMMs with the fused dequant + bias +
+BF16 epilogue.  The metric is INT8 tera-operations per second, 2*M*N*K per
+Linear (multiply and add counted separately), whole-job over all ranks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun every rank runs an independent replica (the projection shards
+by token rows with no exchange; see the design notes), and rank 0 prints one
+JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W8A8 Linear INT8 TOPS at K=5376 and % of GB300 dense INT8 peak"
+M, N, K, LINEARS = 8192, 5376, 5376, ("q", "k", "v", "o")
+OPS_PER_STEP = 2 * M * N * K * len(LINEARS)
+WORKLOAD = ("attn projection: X BF16 [8192,5376] N(0,1)+0.5% x30 outliers; Q,K,V,O W [5376,5376] "
+            "N(0,0.02)->per-channel INT8 + FP32 scales; BF16 bias N(0,0.1); seed 1")
+L2_FLUSH_BYTES = 512 << 20
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --- CPU baseline: the oracle, as it stands, on a bounded sample -------------------
+
+def cpu_oracle_sample(case, qws, target_s: float = 12.0):
+    """Time the CPU oracle on token-row chunks of the workload for ~target_s.
+
+    Each chunk runs A2 + A3 + A4 for all four Linears on 256 token rows (the
+    weights are quantised once beforehand, as on the GPU side).  Returns
+    (TOPS, rows processed, seconds, threads).
+    """
+    import numpy as np
+    from oracle import h3q_oracle as orc
+    rows_done, t_total, chunk, start = 0, 0.0, 256, 0
+    while t_total < target_s and start < M:
+        xb = case.x_bits[start:start + chunk]
+        t0 = time.perf_counter()
+        for (qw, sw), bb in zip(qws, case.bias_bits):
+            orc.linear(xb, qw, sw, bb)
+        t_total += time.perf_counter() - t0
+        rows_done += xb.shape[0]
+        start += chunk
+    ops = 2 * rows_done * N * K * len(LINEARS)
+    return ops / t_total / 1e12, rows_done, t_total, _cpu_threads()
+
+
+def _cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import synth
+    from oracle import h3q_oracle as orc
+    case = synth.attn()
+    qws = [orc.quantize_weights(w) for w in case.w]
+    times = []
+    rows = 0
+    chunk = 128
+    for i in range(args.warmup + args.steps):
+        start = (i * chunk) % M
+        xb = case.x_bits[start:start + chunk]
+        t0 = time.perf_counter()
+        for (qw, sw), bb in zip(qws, case.bias_bits):
+            orc.linear(xb, qw, sw, bb)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            rows += xb.shape[0]
+    t = sum(times)
+    tops = 2 * rows * N * K * len(LINEARS) / t / 1e12
+    sample = (f"{chunk} token rows of the workload per step (all four Linears: A2+A3+A4), "
+              f"{args.steps} steps")
+    line = {"impl": "reference", "metric": METRIC, "value": tops, "unit": "TOPS",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t / len(times), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "s8", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "linears": 4,
+                       "step_rows": chunk},
+            "cpu_baseline": {"value": tops, "unit": "TOPS", "cores": _cpu_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": tops, "unit": "TOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --- the GPU arm -------------------------------------------------------------------
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    import w8a8_int8_linear_h3q_gb300 as h3q
+    import synth
+    h3q.load()
+
+    case = synth.attn()
+    x_host = torch.from_numpy(case.x_bits.view(np.int16)).view(torch.bfloat16)
+    x = x_host.to(dev)
+    wq, wsc, bias = [], [], []
+    for w, b in zip(case.w, case.bias_bits):
+        q, s = h3q.h3q_quantize_weights(torch.from_numpy(w).to(dev))   # offline A1 (untimed)
+        wq.append(q)
+        wsc.append(s)
+        bias.append(torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(dev))
+    xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+    xs = torch.empty((M,), dtype=torch.float32, device=dev)
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in LINEARS]
+    wsb = h3q.h3q_linear_workspace_bytes(M, N, K)
+    workspace = torch.empty((max(wsb, 256),), dtype=torch.uint8, device=dev)
+    flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # per-launch events on the launching stream (the library's kernels run there)
+    def step(ev=None):
+        """One pass of the hot path: A2 once, then four GEMM+epilogue launches."""
+        if ev is not None:
+            ev[0].record(stream)
+        h3q.h3q_quantize_act(x, xq, xs, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        for i in range(len(LINEARS)):
+            h3q.h3q_linear_w8a8(None, wq[i], wsc[i], bias[i], xq=xq, xs=xs, y=ys[i],
+                                workspace=workspace, stream=stream)
+            if ev is not None:
+                ev[2 + i].record(stream)
+
+    launches_per_step = 1 + len(LINEARS) * launches_per_linear(h3q)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2 + len(LINEARS))]
+              for _ in range(args.steps)]
+    clk = ClockSampler(local)
+    clk.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        flush.zero_()                           # L2 flush between timed steps (not timed)
+        step(events[s])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = clk.stop()
+
+    step_ms = [e[0].elapsed_time(e[-1]) for e in events]
+    quant_ms = [e[0].elapsed_time(e[1]) for e in events]
+    gemm_ms = [e[1 + i].elapsed_time(e[2 + i]) for e in events for i in range(len(LINEARS))]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = OPS_PER_STEP * args.steps * world / (total_ms * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers: pinned H2D of X,
+    # the hot path, D2H of the four outputs, all inside the timed region
+    x_pin = x_host.pin_memory()
+    y_pin = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in LINEARS]
+    e2e_steps = 0 if args.no_e2e else max(2, min(args.steps, 5))
+
+    def e2e_step():
+        x.copy_(x_pin, non_blocking=True)
+        step()
+        for i in range(len(LINEARS)):
+            y_pin[i].copy_(ys[i], non_blocking=True)
+
+    if e2e_steps:
+        e2e_step()
+        torch.cuda.synchronize()
+    e_ms = 0.0
+    for _ in range(e2e_steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_ms += a.elapsed_time(b)
+    if world > 1:
+        t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e_ms = float(t.item())
+    e2e_value = OPS_PER_STEP * e2e_steps * world / (e_ms * 1e-3) / 1e12 if e2e_steps else None
+
+    peaks, peak_kind = _peaks()
+    gemm_avg_s = statistics.mean(gemm_ms) * 1e-3
+    gemm_tflops = 2 * M * N * K / gemm_avg_s / 1e12
+    quant_avg_s = statistics.mean(quant_ms) * 1e-3
+    quant_bytes = 2 * M * K + M * K + 4 * M
+    roofline = {"bound": "tensor", "achieved": gemm_tflops, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": gemm_tflops / peaks["bf16_tflops"],
+                "traffic": None,
+                "kernel": gemm_kernel_name(h3q),
+                "peak_source": f"{peak_kind} cuBLAS bf16 burst (MEASURED_PEAKS.json)"
+                               if peak_kind == "measured" else "fallback 1.9 PFLOP/s bf16",
+                "ops_per_launch": 2 * M * N * K}
+    line = {"metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "linears": 4,
+                       "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write)"},
+            "roofline": roofline,
+            "kernels": {"quantize_act_us": quant_avg_s * 1e6,
+                        "quantize_act_gbs": quant_bytes / quant_avg_s / 1e9,
+                        "quantize_act_hbm_frac": quant_bytes / quant_avg_s / 1e9 / peaks["hbm_gbs"],
+                        "gemm_us_per_linear": gemm_avg_s * 1e6,
+                        "gemm_tops": gemm_tflops},
+            "e2e": {"value": e2e_value, "unit": "TOPS", "h2d_bytes_per_step": 2 * M * K,
+                    "d2h_bytes_per_step": 2 * M * N * len(LINEARS)},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        qws = [(q.cpu().numpy(), s.cpu().numpy()) for q, s in zip(wq, wsc)]
+        tops, rows, secs, thr = cpu_oracle_sample(case, qws)
+        line["cpu_baseline"] = {"value": tops, "unit": "TOPS", "cores": thr, "kind": "oracle",
+                                "sample": f"{rows} token rows x 4 Linears (A2+A3+A4), {secs:.1f} s"}
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def launches_per_linear(h3q) -> int:
+    return 1        # one fused GEMM + epilogue launch per pre-quantised Linear
+
+
+def gemm_kernel_name(h3q) -> str:
+    return "gemm_mma_s8_kernel"
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

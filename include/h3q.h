@@ -1,0 +1,147 @@
+/*
+ * h3q.h -- C ABI of the GB300 (sm_103a) W8A8 INT8 projection Linear.
+ *
+ * The operation is the INT8 projection of the MiniMax-H3 DiT: the Q, K, V,
+ * attention-output, FC1 and FC2 Linears at the native hidden width K = 5376
+ * (and the FC2 input width 21504), with no K padding and no weight
+ * dequantisation.  Sources, by page title and section:
+ *   [P1] "feat(mps): support MiniMax-H3 INT8 inference on Apple M5"
+ *        (ModelTC/LightX2V pull request #1672): opening description (the
+ *        300-Linear dit_proj profile, native K = 5376, no K padding, no weight
+ *        dequantisation); Validation (INT8 weights with finite positive FP32
+ *        per-channel scales, CPU INT32 references); Summary by CodeRabbit
+ *        (activation quantiser with masked tails, exact K tiles).
+ *   [P2] "MLX implementation and experiment report" (MiniMax-H3-Image-mlx,
+ *        reports/RESULTS.md): What the default preserves (a biased BF16
+ *        Linear adds the bias before the single rounding of the output).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library allocates no device memory and keeps no per-call state.
+ *   - Layouts are dense and row-major with the last dimension contiguous:
+ *     activations X [M, K] (tokens x in-features), weights W [N, K]
+ *     (out-features x in-features, the nn.Linear layout), outputs [M, N].
+ *   - BF16 tensors are passed as uint16_t bit patterns.
+ *   - Every base pointer must be 16-byte aligned (vector loads and TMA);
+ *     anything else returns H3Q_ERR_MISALIGNED.
+ *   - Shapes: M >= 1, N >= 1, 16 <= K <= 133143 and K % 16 == 0.  The K bound
+ *     keeps K * 127^2 below 2^31, so the INT32 accumulator cannot overflow;
+ *     K % 16 keeps every INT8 row 16-byte aligned.  M and N are otherwise
+ *     arbitrary: ragged tiles are masked.
+ *   - Work is enqueued on `stream` and runs asynchronously, except where an
+ *     entry point says it synchronises.  Argument errors are returned before
+ *     anything is enqueued.  A launch failure returns H3Q_ERR_CUDA; faults of
+ *     already-enqueued work surface at the caller's next synchronisation.
+ *   - Results are bitwise deterministic run to run.
+ */
+#ifndef H3Q_H
+#define H3Q_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum h3q_status {
+  H3Q_OK = 0,
+  H3Q_ERR_INVALID_ARG = 1,       /* null pointer, bad dtype, workspace too small */
+  H3Q_ERR_UNSUPPORTED_SHAPE = 2, /* M, N or K outside the rules above          */
+  H3Q_ERR_MISALIGNED = 3,        /* a base pointer not 16-byte aligned          */
+  H3Q_ERR_NONFINITE = 4,         /* a weight row holds Inf or NaN               */
+  H3Q_ERR_CUDA = 5,              /* a CUDA runtime or launch error              */
+  H3Q_ERR_TIMEOUT = 6,           /* a bounded device-side wait gave up          */
+  H3Q_ERR_NO_DEVICE = 7          /* no sm_103 device is current                 */
+} h3q_status;
+
+typedef enum h3q_dtype {
+  H3Q_DTYPE_F32 = 0,
+  H3Q_DTYPE_BF16 = 1
+} h3q_dtype;
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* h3q_status_string(int status);
+
+/* Library ABI version: major * 10000 + minor * 100 + patch. */
+int h3q_version(void);
+
+/*
+ * A1 -- offline weight quantiser ([P1] Validation; Changes table, "per-row
+ * INT8 conversion").  For each output channel n:
+ *     a = max_k |W[n,k]|,  s = a / 127 (FP32, round to nearest even),
+ *     q[n,k] = clamp(rint(W[n,k] / s), -127, 127)   (FP32 division, ties even),
+ * with s = 1 and q = 0 for an all-zero row and s = 2^-149 for a non-zero row
+ * whose a / 127 underflows to zero.
+ *
+ *   w         [N, K] FP32 (w_dtype = H3Q_DTYPE_F32) or BF16 bits (H3Q_DTYPE_BF16)
+ *   q_out     [N, K] int8, written
+ *   scale_out [N] FP32, written: finite and positive on success
+ *
+ * Returns H3Q_ERR_NONFINITE if any weight is Inf or NaN (q_out and scale_out
+ * are then unspecified).  To check this it copies the N scales to the host and
+ * SYNCHRONISES `stream` before returning; it is an offline call.
+ */
+h3q_status h3q_quantize_weights(const void* w, int w_dtype, int64_t N, int64_t K,
+                                int8_t* q_out, float* scale_out, cudaStream_t stream);
+
+/*
+ * A2 -- per-token activation quantiser ([P1] Summary by CodeRabbit: the
+ * activation quantiser, tails masked).  For each token row m of X, the same
+ * rule as A1 over exactly K elements (a row is never padded).
+ *
+ *   x         [M, K] BF16 bits
+ *   q_out     [M, K] int8, written
+ *   scale_out [M] FP32, written
+ *
+ * Non-finite activations are outside the contract: no check is made and the
+ * affected rows' results are unspecified (no fault).
+ */
+h3q_status h3q_quantize_act(const uint16_t* x, int64_t M, int64_t K,
+                            int8_t* q_out, float* scale_out, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace that h3q_linear_w8a8 needs for this shape.  The
+ * workspace holds the quantised activations re-encoded for the FP16 tensor
+ * cores (exact: every INT8 value is an FP16 value).  The caller allocates it
+ * once and may reuse it across calls that do not overlap on the GPU.
+ */
+size_t h3q_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * A2 + A3 + A4 -- the W8A8 Linear:
+ *     acc[m,n] = sum_k qa[m,k] * qw[n,k]                      (exact INT32)
+ *     y[m,n]   = BF16_RNE(acc[m,n] * xs[m] * ws[n] + bias[n])  (one rounding)
+ * ([P1] Validation, CPU INT32 references; [P2] What the default preserves,
+ * bias added before the rounding).  The BF16 result is within one BF16 ulp
+ * of that value computed exactly (the FP32 operation order is not fixed).
+ *
+ *   x          [M, K] BF16 bits, or NULL when the activations are already
+ *              quantised: then xq and xs are INPUTS.
+ *   xq         [M, K] int8.  With x != NULL: written (the A2 output), or NULL
+ *              to skip writing it.  With x == NULL: read.
+ *   xs         [M] FP32 activation scales.  Written when x != NULL, read when
+ *              x == NULL.  Never NULL.
+ *   wq, ws     [N, K] int8 weights and [N] FP32 per-channel scales (from A1).
+ *   bias       [N] BF16 bits, or NULL for no bias.
+ *   y          [M, N] BF16 bits, written; may be NULL if acc_out is not NULL.
+ *   acc_out    [M, N] int32 raw accumulators, written; NULL to skip (testing).
+ *   workspace  device scratch of at least h3q_linear_workspace_bytes(M, N, K)
+ *              bytes, 16-byte aligned (NULL allowed when that size is 0).
+ *
+ * Everything is enqueued on `stream`; the call does not synchronise.  Calls
+ * sharing a workspace must not overlap on the GPU.
+ */
+h3q_status h3q_linear_w8a8(const uint16_t* x, int8_t* xq, float* xs,
+                           const int8_t* wq, const float* ws, const uint16_t* bias,
+                           int64_t M, int64_t N, int64_t K,
+                           uint16_t* y, int32_t* acc_out,
+                           void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* H3Q_H */

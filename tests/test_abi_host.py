@@ -1,0 +1,103 @@
+"""Host-side checks of the C-ABI library: it loads, exports every entry point
+that include/h3q.h declares, and rejects bad arguments before touching a GPU.
+No compute call is made here (these tests run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"\b(h3q_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def cdll():
+    import w8a8_int8_linear_h3q_gb300 as h3q
+    return h3q.load()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for must in ("h3q_quantize_weights", "h3q_quantize_act", "h3q_linear_w8a8",
+                 "h3q_linear_workspace_bytes", "h3q_status_string", "h3q_version"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(cdll):
+    for name in _declared_functions():
+        assert hasattr(cdll, name), name
+
+
+def test_status_strings(cdll):
+    import w8a8_int8_linear_h3q_gb300 as h3q
+    for code in range(8):
+        s = h3q.h3q_status_string(code)
+        assert s and s != "unknown status"
+    assert h3q.h3q_status_string(99) == "unknown status"
+    assert h3q.h3q_version() >= 100
+
+
+def test_workspace_size(cdll):
+    import w8a8_int8_linear_h3q_gb300 as h3q
+    assert h3q.h3q_linear_workspace_bytes(8192, 5376, 5376) >= 8192 * 5376 * 2
+    assert h3q.h3q_linear_workspace_bytes(1, 1, 16) % 256 == 0
+
+
+# Fake device addresses: aligned and non-null, never dereferenced because every
+# call below is rejected on the host (argument checks come before any CUDA call).
+A = ctypes.c_void_p(0x10000)
+MIS = ctypes.c_void_p(0x10008)
+NUL = None
+
+
+def test_quantize_act_rejects_bad_args(cdll):
+    q = cdll.h3q_quantize_act
+    assert q(NUL, 4, 64, A, A, NUL) == 1                 # null input
+    assert q(A, 4, 64, NUL, A, NUL) == 1                 # null output
+    assert q(A, 0, 64, A, A, NUL) == 2                   # M = 0
+    assert q(A, 4, 8, A, A, NUL) == 2                    # K < 16
+    assert q(A, 4, 72, A, A, NUL) == 2                   # K % 16 != 0
+    assert q(A, 4, 133152, A, A, NUL) == 2               # K past the INT32 bound
+    assert q(MIS, 4, 64, A, A, NUL) == 3                 # misaligned
+    assert q(A, 4, 64, A, MIS, NUL) == 3
+
+
+def test_quantize_weights_rejects_bad_args(cdll):
+    q = cdll.h3q_quantize_weights
+    assert q(A, 2, 4, 64, A, A, NUL) == 1                # bad dtype
+    assert q(NUL, 0, 4, 64, A, A, NUL) == 1
+    assert q(A, 0, -1, 64, A, A, NUL) == 2
+    assert q(A, 1, 4, 40, A, A, NUL) == 2
+    assert q(A, 0, 4, 64, MIS, A, NUL) == 3
+
+
+def test_linear_rejects_bad_args(cdll):
+    f = cdll.h3q_linear_w8a8
+    ws = cdll.h3q_linear_workspace_bytes(4, 8, 64)
+    # x, xq, xs, wq, ws, bias, M, N, K, y, acc, workspace, bytes, stream
+    assert f(A, A, NUL, A, A, NUL, 4, 8, 64, A, NUL, A, ws, NUL) == 1      # no xs
+    assert f(NUL, NUL, A, A, A, NUL, 4, 8, 64, A, NUL, A, ws, NUL) == 1    # no activations
+    assert f(A, A, A, A, A, NUL, 4, 8, 64, NUL, NUL, A, ws, NUL) == 1      # no output
+    assert f(A, NUL, A, A, A, NUL, 4, 8, 64, A, NUL, NUL, 0, NUL) == 1     # no workspace
+    assert f(A, NUL, A, A, A, NUL, 4, 8, 64, A, NUL, A, ws - 256, NUL) == 1
+    assert f(A, A, A, A, A, NUL, 4, 0, 64, A, NUL, A, ws, NUL) == 2        # N = 0
+    assert f(A, A, A, A, A, NUL, 4, 8, 60, A, NUL, A, ws, NUL) == 2        # K % 16
+    assert f(A, A, A, A, A, MIS, 4, 8, 64, A, NUL, A, ws, NUL) == 3        # misaligned bias
+    assert f(A, A, A, A, A, NUL, 4, 8, 64, MIS, NUL, A, ws, NUL) == 3      # misaligned y
+
+
+def test_valid_args_without_a_device_report_no_device(cdll):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: this checks the no-device report only")
+    assert cdll.h3q_quantize_act(A, 4, 64, A, A, NUL) == 7

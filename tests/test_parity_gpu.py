@@ -1,0 +1,249 @@
+"""GPU parity: the CUDA path through the C-ABI against the CPU oracle.
+
+Bar: INT8 activations and weights, FP32 scales and INT32 accumulators
+bit-exact; BF16 outputs within one BF16 ulp of the oracle's float64 epilogue
+value.  Inputs come from the seeded generators in ``synth`` and are the same
+bytes on both sides.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from _parity import check_exact, check_y
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return torch.device("cuda:0")
+
+
+def _bf16_dev(bits, dev):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def _bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _special_rows(K, rng):
+    """Rows that exercise the quantiser's edge cases, as BF16 bits."""
+    rows = [np.zeros(K, np.uint16),                                   # all zero -> s = 1
+            np.full(K, 0x8000, np.uint16),                            # all -0.0
+            np.full(K, 0x3F40, np.uint16),                            # constant 0.75 -> 127
+            np.full(K, 0xBD00, np.uint16)]                            # constant -1/32 -> -127
+    sub = np.zeros(K, np.uint16); sub[::3] = 0x0001; sub[1::3] = 0x8003   # subnormals
+    rows.append(sub)
+    # power-of-two scale (absmax 127 * 2^-3) with exact ties k + 0.5
+    tie = np.array([(k % 60) - 30 + 0.5 for k in range(K)], np.float32) / 8
+    tie[0] = 127.0 / 8
+    rows.append(synth.to_bf16_bits(tie))
+    big = rng.standard_normal(K).astype(np.float32); big[K // 2] = 3.0e38
+    rows.append(synth.to_bf16_bits(big))                              # huge outlier
+    return np.stack(rows)
+
+
+def _act(M, K, seed, special=True):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    m = rng.random((M, K)) < 0.01
+    x[m] *= 25
+    bits = synth.to_bf16_bits(x)
+    if special:
+        sp = _special_rows(K, rng)
+        n = min(len(sp), M)
+        bits[-n:] = sp[:n]
+    return bits
+
+
+@pytest.mark.parametrize("M,K", [(1, 16), (7, 48), (129, 5376), (64, 6144), (33, 6160),
+                                 (300, 21504), (9, 133136)])
+def test_quantize_act_bit_exact(lib, oracle, dev, M, K):
+    xb = _act(M, K, seed=M * 7 + K)
+    q, s = lib.h3q_quantize_act(_bf16_dev(xb, dev))
+    oq, os_ = oracle.quantize_act(xb)
+    check_exact(q.cpu().numpy(), oq, "q_a")
+    check_exact(s.cpu().numpy(), os_, "s_a")
+
+
+@pytest.mark.parametrize("N,K", [(1, 16), (100, 80), (256, 5376), (37, 21504)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_quantize_weights_bit_exact(lib, oracle, dev, N, K, dtype):
+    rng = np.random.default_rng(N + K)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    w[0, :] = 0.0                                   # zero row -> scale 1
+    if N > 2:
+        w[1, :] = np.float32(1e-44)                 # subnormal row
+        w[2, 3] = np.float32(2.0 ** -149)           # smallest subnormal in a row
+    if dtype == "bf16":
+        wb = synth.to_bf16_bits(w)
+        wt = _bf16_dev(wb, dev)
+        oq, os_ = oracle.quantize_weights(wb)
+    else:
+        wt = torch.from_numpy(w).to(dev)
+        oq, os_ = oracle.quantize_weights(w)
+    q, s = lib.h3q_quantize_weights(wt)
+    check_exact(q.cpu().numpy(), oq, "q_w")
+    check_exact(s.cpu().numpy(), os_, "s_w")
+
+
+def test_weight_underflow_scale(lib, oracle, dev):
+    w = np.zeros((2, 32), np.float32)
+    w[0, 5] = np.float32(2.0 ** -149) * 3        # absmax / 127 underflows to 0
+    w[1, 7] = -np.float32(2.0 ** -149) * 63
+    q, s = lib.h3q_quantize_weights(torch.from_numpy(w).to(dev))
+    oq, os_ = oracle.quantize_weights(w)
+    check_exact(q.cpu().numpy(), oq, "q_w")
+    check_exact(s.cpu().numpy(), os_, "s_w")
+    assert float(s[0]) == 2.0 ** -149
+
+
+@pytest.mark.parametrize("bad", [np.inf, -np.inf, np.nan])
+def test_quantize_weights_rejects_non_finite(lib, dev, bad):
+    w = np.ones((8, 64), np.float32)
+    w[5, 9] = bad
+    with pytest.raises(lib.H3QError) as e:
+        lib.h3q_quantize_weights(torch.from_numpy(w).to(dev))
+    assert e.value.status == lib.H3Q_ERR_NONFINITE
+
+
+def _linear_check(lib, oracle, dev, xb, w, bias_bits, rows=None, **kw):
+    wt = torch.from_numpy(w).to(dev)
+    qw, sw = lib.h3q_quantize_weights(wt)
+    oq, osw = oracle.quantize_weights(w)
+    check_exact(qw.cpu().numpy(), oq, "q_w")
+    check_exact(sw.cpu().numpy(), osw, "s_w")
+    bias = None if bias_bits is None else _bf16_dev(bias_bits, dev)
+    out = lib.h3q_linear_w8a8(_bf16_dev(xb, dev), qw, sw, bias, want_acc=True, want_xq=True, **kw)
+    torch.cuda.synchronize()
+    if rows is None:
+        rows = np.arange(xb.shape[0])
+    rt = torch.from_numpy(rows).to(dev)
+    ref = oracle.linear(xb[rows], oq, osw, bias_bits)
+    check_exact(out["xq"][rt].cpu().numpy(), ref["qa"], "q_a")
+    check_exact(out["xs"][rt].cpu().numpy(), ref["sa"], "s_a")
+    check_exact(out["acc"][rt].cpu().numpy(), ref["acc"], "acc")
+    stats = check_y(_bits(out["y"][rt]), ref["v"])
+    return out, stats
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 16), (7, 3, 48), (129, 264, 80), (300, 100, 5376),
+                                   (33, 8, 21504), (130, 257, 64), (5, 131, 1040)])
+def test_linear_parity_ragged(lib, oracle, dev, M, N, K):
+    rng = np.random.default_rng(M * 1000 + N)
+    xb = _act(M, K, seed=M + N + K)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    bias = synth.to_bf16_bits((rng.standard_normal(N) * 0.1).astype(np.float32))
+    _linear_check(lib, oracle, dev, xb, w, bias)
+
+
+def test_linear_tiny_workload(lib, oracle, dev):
+    c = synth.tiny()
+    _, stats = _linear_check(lib, oracle, dev, c.x_bits, c.w[0], c.bias_bits[0])
+    assert stats["max_ulp"] <= 1.0
+
+
+def test_linear_without_bias_and_output_selection(lib, oracle, dev):
+    c = synth.make_linear(70, 136, 5376, seed=21)
+    qw, sw = lib.h3q_quantize_weights(torch.from_numpy(c.w[0]).to(dev))
+    x = _bf16_dev(c.x_bits, dev)
+    ref = oracle.linear(c.x_bits, *oracle.quantize_weights(c.w[0]), None)
+    out = lib.h3q_linear_w8a8(x, qw, sw, None, want_y=True, want_acc=False)
+    check_y(_bits(out["y"]), ref["v"])
+    out = lib.h3q_linear_w8a8(x, qw, sw, None, want_y=False, want_acc=True)
+    check_exact(out["acc"].cpu().numpy(), ref["acc"], "acc")
+
+
+def test_linear_prequantised_input(lib, oracle, dev):
+    c = synth.make_linear(96, 200, 5376, seed=22)
+    qw, sw = lib.h3q_quantize_weights(torch.from_numpy(c.w[0]).to(dev))
+    xq, xs = lib.h3q_quantize_act(_bf16_dev(c.x_bits, dev))
+    bias = _bf16_dev(c.bias_bits[0], dev)
+    out = lib.h3q_linear_w8a8(None, qw, sw, bias, xq=xq, xs=xs, want_acc=True)
+    ref = oracle.linear(c.x_bits, *oracle.quantize_weights(c.w[0]), c.bias_bits[0])
+    check_exact(out["acc"].cpu().numpy(), ref["acc"], "acc")
+    check_y(_bits(out["y"]), ref["v"])
+
+
+@pytest.mark.parametrize("K", [5376, 21504, 133136])
+def test_linear_extreme_accumulators(lib, oracle, dev, K):
+    # constant rows quantise to +-127, so acc = +-127^2 K: the largest
+    # accumulators the shape allows (K = 133136 is the largest legal K)
+    M, N = 3, 4
+    xb = np.zeros((M, K), np.uint16)
+    xb[0] = 0x3F80; xb[1] = 0xBF80                  # +-1.0
+    xb[2, ::2] = 0x3F80; xb[2, 1::2] = 0xBF80       # alternating
+    w = np.ones((N, K), np.float32)
+    w[1] *= -1
+    w[2, : K // 2] = -1
+    w[3, ::3] = 0.5
+    out, _ = _linear_check(lib, oracle, dev, xb, w, None)
+    assert int(out["acc"][0, 0]) == 127 * 127 * K
+    assert int(out["acc"][1, 0]) == -127 * 127 * K
+
+
+def test_linear_partial_sums_cross_2_pow_24(lib, oracle, dev):
+    # running sums exceed 2^24 and come back: exact INT32 required
+    K, M, N = 5376, 4, 8
+    xb = np.full((M, K), 0x3F80, np.uint16)
+    xb[1, K // 3:] = 0xBF80
+    xb[2, ::7] = 0x3F00
+    w = np.ones((N, K), np.float32)
+    w[0, K // 2:] = -1
+    w[1, -1] = 0.5
+    w[2, 1::2] = -1
+    w[3, : 1030] = -1
+    out, _ = _linear_check(lib, oracle, dev, xb, w, None)
+
+
+def test_deterministic(lib, dev):
+    c = synth.make_linear(257, 384, 5376, seed=31)
+    qw, sw = lib.h3q_quantize_weights(torch.from_numpy(c.w[0]).to(dev))
+    x = _bf16_dev(c.x_bits, dev)
+    b = _bf16_dev(c.bias_bits[0], dev)
+    o1 = lib.h3q_linear_w8a8(x, qw, sw, b, want_acc=True)
+    o2 = lib.h3q_linear_w8a8(x, qw, sw, b, want_acc=True)
+    assert torch.equal(o1["y"].view(torch.int16), o2["y"].view(torch.int16))
+    assert torch.equal(o1["acc"], o2["acc"])
+
+
+def test_misaligned_device_pointer_rejected(lib, dev):
+    M, K, N = 4, 64, 8
+    flat = torch.zeros(M * K + 1, dtype=torch.bfloat16, device=dev)
+    x = flat[1:].view(M, K)                       # contiguous, 2 bytes off alignment
+    with pytest.raises(lib.H3QError) as e:
+        lib.h3q_quantize_act(x)
+    assert e.value.status == lib.H3Q_ERR_MISALIGNED
+
+
+# --- the named workloads at full size, sampled rows ---------------------------------
+
+def _sample_rows(M, seed, n_rand=128):
+    rng = np.random.default_rng(seed)
+    head = np.arange(min(128, M))
+    tail = np.arange(max(0, M - 128), M)
+    rand = rng.choice(M, size=min(n_rand, M), replace=False)
+    return np.unique(np.concatenate([head, tail, rand]))
+
+
+@pytest.mark.slow
+def test_attn_workload_sampled(lib, oracle, dev):
+    c = synth.attn()
+    rows = _sample_rows(c.M, 101)
+    for i, nm in enumerate(c.linear_names):
+        _linear_check(lib, oracle, dev, c.x_bits, c.w[i], c.bias_bits[i], rows=rows)
+
+
+@pytest.mark.slow
+def test_fc1_workload_sampled(lib, oracle, dev):
+    c = synth.fc1()
+    _linear_check(lib, oracle, dev, c.x_bits, c.w[0], c.bias_bits[0], rows=_sample_rows(c.M, 102))
+
+
+@pytest.mark.slow
+def test_fc2_workload_sampled(lib, oracle, dev):
+    c = synth.fc2()
+    _linear_check(lib, oracle, dev, c.x_bits, c.w[0], c.bias_bits[0], rows=_sample_rows(c.M, 103))

@@ -1,0 +1,198 @@
+"""Python binding of libh3q.so: the GB300 (sm_103a) W8A8 INT8 projection Linear.
+
+The functions carry the C entry points' names (include/h3q.h) and only
+marshal arguments: torch tensors supply device memory and the current CUDA
+stream, and every step of the computation runs in the library's kernels.
+There is no CPU or library fallback: if libh3q.so cannot be built or loaded,
+``load()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+H3Q_OK = 0
+H3Q_ERR_INVALID_ARG = 1
+H3Q_ERR_UNSUPPORTED_SHAPE = 2
+H3Q_ERR_MISALIGNED = 3
+H3Q_ERR_NONFINITE = 4
+H3Q_ERR_CUDA = 5
+H3Q_ERR_TIMEOUT = 6
+H3Q_ERR_NO_DEVICE = 7
+H3Q_DTYPE_F32 = 0
+H3Q_DTYPE_BF16 = 1
+
+_lib = None
+
+
+class H3QError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {h3q_status_string(status)} (status {status})")
+
+
+def _declare(lib):
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    lib.h3q_status_string.argtypes = [i32]
+    lib.h3q_status_string.restype = ctypes.c_char_p
+    lib.h3q_version.argtypes = []
+    lib.h3q_version.restype = i32
+    lib.h3q_quantize_weights.argtypes = [vp, i32, i64, i64, vp, vp, vp]
+    lib.h3q_quantize_weights.restype = i32
+    lib.h3q_quantize_act.argtypes = [vp, i64, i64, vp, vp, vp]
+    lib.h3q_quantize_act.restype = i32
+    lib.h3q_linear_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.h3q_linear_workspace_bytes.restype = sz
+    lib.h3q_linear_w8a8.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp, sz, vp]
+    lib.h3q_linear_w8a8.restype = i32
+    return lib
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libh3q.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is None:
+        if build_if_missing and _build.stale():
+            _build.build()
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"libh3q.so is missing at {_build.LIB}; build it with "
+                               "python -m w8a8_int8_linear_h3q_gb300._build")
+        _lib = _declare(ctypes.CDLL(_build.LIB))
+    return _lib
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+# --- marshalling helpers ------------------------------------------------------------
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, dtype, shape, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _check(status, where):
+    if status != H3Q_OK:
+        raise H3QError(status, where)
+
+
+# --- the entry points --------------------------------------------------------------
+
+def h3q_status_string(status: int) -> str:
+    return load().h3q_status_string(int(status)).decode()
+
+
+def h3q_version() -> int:
+    return int(load().h3q_version())
+
+
+def h3q_linear_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load().h3q_linear_workspace_bytes(M, N, K))
+
+
+def h3q_quantize_weights(w, q_out=None, scale_out=None, stream=None):
+    """A1: FP32 or BF16 weight [N, K] -> (int8 [N, K], FP32 scale [N]).  Synchronises."""
+    import torch
+    if w.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("weights must be float32 or bfloat16")
+    _need(w, w.dtype, None, "w")
+    N, K = w.shape
+    q_out = torch.empty((N, K), dtype=torch.int8, device=w.device) if q_out is None else q_out
+    scale_out = torch.empty((N,), dtype=torch.float32, device=w.device) if scale_out is None else scale_out
+    _need(q_out, torch.int8, (N, K), "q_out")
+    _need(scale_out, torch.float32, (N,), "scale_out")
+    dt = H3Q_DTYPE_F32 if w.dtype == torch.float32 else H3Q_DTYPE_BF16
+    _check(load().h3q_quantize_weights(_ptr(w), dt, N, K, _ptr(q_out), _ptr(scale_out),
+                                       _stream(stream)), "h3q_quantize_weights")
+    return q_out, scale_out
+
+
+def h3q_quantize_act(x, q_out=None, scale_out=None, stream=None):
+    """A2: BF16 activations [M, K] -> (int8 [M, K], FP32 scale [M])."""
+    import torch
+    _need(x, torch.bfloat16, None, "x")
+    M, K = x.shape
+    q_out = torch.empty((M, K), dtype=torch.int8, device=x.device) if q_out is None else q_out
+    scale_out = torch.empty((M,), dtype=torch.float32, device=x.device) if scale_out is None else scale_out
+    _need(q_out, torch.int8, (M, K), "q_out")
+    _need(scale_out, torch.float32, (M,), "scale_out")
+    _check(load().h3q_quantize_act(_ptr(x), M, K, _ptr(q_out), _ptr(scale_out), _stream(stream)),
+           "h3q_quantize_act")
+    return q_out, scale_out
+
+
+def h3q_linear_w8a8(x, wq, ws, bias=None, *, xq=None, xs=None, y=None, acc_out=None,
+                    want_y=True, want_acc=False, want_xq=False, workspace=None, stream=None):
+    """A2 + A3 + A4.  ``x`` BF16 [M, K] or None (then ``xq``/``xs`` are inputs).
+
+    Returns a dict with whichever of ``y`` (BF16 [M, N]), ``acc`` (int32 [M, N]),
+    ``xq`` (int8 [M, K]) and ``xs`` (FP32 [M]) were produced.  Outputs and the
+    workspace are allocated here when not given (allocation is plumbing; the
+    library itself allocates nothing).
+    """
+    import torch
+    _need(wq, torch.int8, None, "wq")
+    N, K = wq.shape
+    dev = wq.device
+    if x is not None:
+        _need(x, torch.bfloat16, None, "x")
+        M = x.shape[0]
+        if x.shape[1] != K:
+            raise ValueError("x and wq disagree on K")
+        if want_xq and xq is None:
+            xq = torch.empty((M, K), dtype=torch.int8, device=dev)
+        if xs is None:
+            xs = torch.empty((M,), dtype=torch.float32, device=dev)
+    else:
+        if xq is None or xs is None:
+            raise ValueError("pre-quantised call needs xq and xs")
+        M = xq.shape[0]
+    if xq is not None:
+        _need(xq, torch.int8, (M, K), "xq")
+    _need(xs, torch.float32, (M,), "xs")
+    _need(ws, torch.float32, (N,), "ws")
+    if bias is not None:
+        _need(bias, torch.bfloat16, (N,), "bias")
+    if want_y and y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if want_acc and acc_out is None:
+        acc_out = torch.empty((M, N), dtype=torch.int32, device=dev)
+    if y is not None:
+        _need(y, torch.bfloat16, (M, N), "y")
+    if acc_out is not None:
+        _need(acc_out, torch.int32, (M, N), "acc_out")
+    need = h3q_linear_workspace_bytes(M, N, K)
+    if workspace is None and need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().h3q_linear_w8a8(_ptr(x), _ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws), _ptr(bias),
+                                  M, N, K, _ptr(y), _ptr(acc_out), _ptr(workspace), wbytes,
+                                  _stream(stream)), "h3q_linear_w8a8")
+    out = {"xs": xs}
+    if y is not None:
+        out["y"] = y
+    if acc_out is not None:
+        out["acc"] = acc_out
+    if xq is not None:
+        out["xq"] = xq
+    return out

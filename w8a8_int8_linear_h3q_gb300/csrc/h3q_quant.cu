@@ -1,0 +1,230 @@
+// h3q_quant.cu -- A1 (weight) and A2 (activation) symmetric per-row INT8
+// quantisers, and the INT8 -> FP16-coded-integer expansion.
+//
+// Rule (readings of "feat(mps): support MiniMax-H3 INT8 inference on Apple M5",
+// LightX2V #1672, sections Validation and Summary by CodeRabbit):
+//   a = max_k |x[k]|;  s = a / 127 (IEEE FP32 division, round to nearest even);
+//   s = 1 when a == 0;  s = 2^-149 when a > 0 but a / 127 underflows to 0;
+//   q[k] = clamp(rint(x[k] / s), -127, 127) with an IEEE FP32 division.
+// The division is __fdiv_rn so that every q matches an IEEE-754 evaluation
+// bit for bit; the build never uses fast-math or flush-to-zero.
+#include <cuda_fp16.h>
+
+#include "h3q_internal.cuh"
+
+namespace h3q {
+namespace {
+
+constexpr int kWarps = 8;        // rows per block: one warp per row
+constexpr int kRegVecs = 24;     // 16-byte vectors per lane kept in registers
+
+__device__ __forceinline__ float row_scale(float amax) {
+  if (amax == 0.f) return 1.f;
+  const float s = __fdiv_rn(amax, 127.f);
+  return s == 0.f ? __int_as_float(1) : s;   // 2^-149, the smallest positive FP32
+}
+
+__device__ __forceinline__ int quant1(float x, float s) {
+  const int q = __float2int_rn(__fdiv_rn(x, s));
+  return max(-kQMax, min(kQMax, q));
+}
+
+__device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
+  return (uint32_t(a) & 0xFFu) | ((uint32_t(b) & 0xFFu) << 8) | ((uint32_t(c) & 0xFFu) << 16) |
+         (uint32_t(d) << 24);
+}
+
+__device__ __forceinline__ uint32_t pack2_f16(int a, int b) {
+  return uint32_t(__half_as_ushort(__int2half_rn(a))) |
+         (uint32_t(__half_as_ushort(__int2half_rn(b))) << 16);
+}
+
+// |bf16| maximum of the 8 values in a 16-byte vector, as a 16-bit magnitude
+// pattern: for finite BF16 values the order of |x| is the order of (bits & 0x7fff).
+__device__ __forceinline__ uint32_t vec_absmax_bits(uint4 v) {
+  uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                        __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+  return max(m & 0xFFFFu, m >> 16);
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+template <bool kQ8, bool kF16>
+__device__ __forceinline__ void quant_store8(uint4 v, float s, int8_t* q8, uint16_t* qh,
+                                             int64_t elem) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  int q[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    q[2 * j] = quant1(__uint_as_float(w[j] << 16), s);
+    q[2 * j + 1] = quant1(__uint_as_float(w[j] & 0xFFFF0000u), s);
+  }
+  if constexpr (kQ8) {
+    uint2 o;
+    o.x = pack4_s8(q[0], q[1], q[2], q[3]);
+    o.y = pack4_s8(q[4], q[5], q[6], q[7]);
+    *reinterpret_cast<uint2*>(q8 + elem) = o;
+  }
+  if constexpr (kF16) {
+    uint4 o;
+    o.x = pack2_f16(q[0], q[1]);
+    o.y = pack2_f16(q[2], q[3]);
+    o.z = pack2_f16(q[4], q[5]);
+    o.w = pack2_f16(q[6], q[7]);
+    *reinterpret_cast<uint4*>(qh + elem) = o;
+  }
+}
+
+// One warp per token row.  kRegs: the whole row (<= 32 * kRegVecs vectors)
+// stays in registers between the absmax pass and the quantise pass, so X is
+// read from memory once; otherwise the second pass re-reads the row.
+template <bool kRegs, bool kQ8, bool kF16>
+__global__ void __launch_bounds__(kWarps * 32)
+quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int K, int8_t* __restrict__ q8,
+                 float* __restrict__ scale, uint16_t* __restrict__ qh) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const int nvec = K >> 3;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + row * int64_t(K));
+  const int64_t base = row * int64_t(K);
+  uint32_t mbits = 0;
+  if constexpr (kRegs) {
+    uint4 v[kRegVecs];
+#pragma unroll
+    for (int i = 0; i < kRegVecs; ++i) {
+      const int j = lane + 32 * i;
+      if (j < nvec) {
+        v[i] = ld_stream(xr + j);
+        mbits = max(mbits, vec_absmax_bits(v[i]));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mbits = max(mbits, __shfl_xor_sync(0xFFFFFFFFu, mbits, o));
+    const float s = row_scale(__uint_as_float(mbits << 16));
+#pragma unroll
+    for (int i = 0; i < kRegVecs; ++i) {
+      const int j = lane + 32 * i;
+      if (j < nvec) quant_store8<kQ8, kF16>(v[i], s, q8, qh, base + 8 * int64_t(j));
+    }
+    if (lane == 0) scale[row] = s;
+  } else {
+    int j = lane;
+    for (; j + 96 < nvec; j += 128) {
+      const uint4 a = __ldg(xr + j), b = __ldg(xr + j + 32), c = __ldg(xr + j + 64),
+                  d = __ldg(xr + j + 96);
+      mbits = max(max(mbits, vec_absmax_bits(a)), vec_absmax_bits(b));
+      mbits = max(max(mbits, vec_absmax_bits(c)), vec_absmax_bits(d));
+    }
+    for (; j < nvec; j += 32) mbits = max(mbits, vec_absmax_bits(__ldg(xr + j)));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mbits = max(mbits, __shfl_xor_sync(0xFFFFFFFFu, mbits, o));
+    const float s = row_scale(__uint_as_float(mbits << 16));
+    for (j = lane; j < nvec; j += 32)
+      quant_store8<kQ8, kF16>(ld_stream(xr + j), s, q8, qh, base + 8 * int64_t(j));
+    if (lane == 0) scale[row] = s;
+  }
+}
+
+// Weight rows: FP32 or BF16.  Not on the timed path; plain two-pass loops,
+// plus a finiteness check (a row with Inf/NaN gets a NaN scale).
+template <typename T>
+__device__ __forceinline__ float load_w(const T* p, int64_t i);
+template <>
+__device__ __forceinline__ float load_w<float>(const float* p, int64_t i) { return p[i]; }
+template <>
+__device__ __forceinline__ float load_w<uint16_t>(const uint16_t* p, int64_t i) {
+  return __uint_as_float(uint32_t(p[i]) << 16);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32)
+quant_weight_kernel(const T* __restrict__ w, int64_t N, int K, int8_t* __restrict__ q8,
+                    float* __restrict__ scale) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (row >= N) return;
+  const T* wr = w + row * int64_t(K);
+  float amax = 0.f;
+  bool bad = false;
+  for (int k = lane; k < K; k += 32) {
+    const float a = fabsf(load_w<T>(wr, k));
+    bad |= !(a <= 3.4028234663852886e38f);   // Inf or NaN
+    amax = fmaxf(amax, a);
+  }
+  bad = __any_sync(0xFFFFFFFFu, bad);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  const float s = row_scale(amax);
+  int8_t* qr = q8 + row * int64_t(K);
+  for (int k = lane; k < K; k += 32) qr[k] = int8_t(bad ? 0 : quant1(load_w<T>(wr, k), s));
+  if (lane == 0) scale[row] = bad ? __int_as_float(0x7FC00000) : s;
+}
+
+__global__ void int8_to_f16_kernel(const int8_t* __restrict__ q, int64_t n16,
+                                   uint16_t* __restrict__ out) {
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(q) + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int b0 = int(int8_t(w[j])), b1 = int(int8_t(w[j] >> 8));
+      const int b2 = int(int8_t(w[j] >> 16)), b3 = int(int8_t(w[j] >> 24));
+      o[2 * j] = pack2_f16(b0, b1);
+      o[2 * j + 1] = pack2_f16(b2, b3);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out) + 2 * i;
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+template <bool kRegs>
+cudaError_t launch_act(const uint16_t* x, int64_t M, int K, int8_t* q, float* s, uint16_t* qh,
+                       cudaStream_t st) {
+  const dim3 grid(unsigned((M + kWarps - 1) / kWarps)), block(kWarps * 32);
+  if (q && qh)
+    quant_act_kernel<kRegs, true, true><<<grid, block, 0, st>>>(x, M, K, q, s, qh);
+  else if (q)
+    quant_act_kernel<kRegs, true, false><<<grid, block, 0, st>>>(x, M, K, q, s, qh);
+  else
+    quant_act_kernel<kRegs, false, true><<<grid, block, 0, st>>>(x, M, K, q, s, qh);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t* q,
+                                float* scale, uint16_t* q_f16, cudaStream_t s) {
+  if (K / 8 <= 32 * kRegVecs) return launch_act<true>(x, M, int(K), q, scale, q_f16, s);
+  return launch_act<false>(x, M, int(K), q, scale, q_f16, s);
+}
+
+cudaError_t launch_quantize_weights(const void* w, int w_dtype, int64_t N, int64_t K,
+                                    int8_t* q, float* scale, cudaStream_t s) {
+  const dim3 grid(unsigned((N + kWarps - 1) / kWarps)), block(kWarps * 32);
+  if (w_dtype == H3Q_DTYPE_F32)
+    quant_weight_kernel<float><<<grid, block, 0, s>>>(static_cast<const float*>(w), N, int(K),
+                                                      q, scale);
+  else
+    quant_weight_kernel<uint16_t><<<grid, block, 0, s>>>(static_cast<const uint16_t*>(w), N,
+                                                         int(K), q, scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_int8_to_f16(const int8_t* q, int64_t n, uint16_t* out, cudaStream_t s) {
+  const int64_t n16 = n / 16;
+  int64_t blocks = (n16 + 255) / 256;
+  blocks = blocks < 1 ? 1 : (blocks > 152 * 16 ? 152 * 16 : blocks);
+  int8_to_f16_kernel<<<unsigned(blocks), 256, 0, s>>>(q, n16, out);
+  return cudaGetLastError();
+}
+
+}  // namespace h3q
