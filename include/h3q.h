@@ -102,10 +102,11 @@ h3q_status h3q_quantize_act(const uint16_t* x, int64_t M, int64_t K,
                             int8_t* q_out, float* scale_out, cudaStream_t stream);
 
 /*
- * Bytes of device workspace that h3q_linear_w8a8 needs for this shape.  The
- * workspace holds the quantised activations re-encoded for the FP16 tensor
- * cores (exact: every INT8 value is an FP16 value).  The caller allocates it
- * once and may reuse it across calls that do not overlap on the GPU.
+ * Bytes of device workspace that h3q_linear_w8a8 needs for this shape: the
+ * quantised activations re-coded as FP16 (exact: every INT8 value is an FP16
+ * value), read by the tensor cores, followed by a 256-byte block holding a
+ * status word.  The caller allocates it; calls that share a workspace must
+ * not overlap on the GPU.
  */
 size_t h3q_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
@@ -114,24 +115,32 @@ size_t h3q_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
  *     acc[m,n] = sum_k qa[m,k] * qw[n,k]                      (exact INT32)
  *     y[m,n]   = BF16_RNE(acc[m,n] * xs[m] * ws[n] + bias[n])  (one rounding)
  * ([P1] Validation, CPU INT32 references; [P2] What the default preserves,
- * bias added before the rounding).  The BF16 result is within one BF16 ulp
- * of that value computed exactly (the FP32 operation order is not fixed).
+ * bias added before the rounding).  The BF16 result is within one BF16 ulp of
+ * that value computed exactly.  The product runs on the FP16 tensor cores as
+ * exact integer arithmetic (FP32 partial sums drained to INT32 every <= 1024
+ * K), so acc is the exact INT32 sum.
  *
- *   x          [M, K] BF16 bits, or NULL when the activations are already
- *              quantised: then xq and xs are INPUTS.
- *   xq         [M, K] int8.  With x != NULL: written (the A2 output), or NULL
- *              to skip writing it.  With x == NULL: read.
- *   xs         [M] FP32 activation scales.  Written when x != NULL, read when
- *              x == NULL.  Never NULL.
+ * Where the activations come from:
+ *   x != NULL            BF16 [M, K]; quantised here (A2).  xs is written, and
+ *                        xq too unless it is NULL.
+ *   x == NULL, xq != NULL  already quantised: xq [M, K] int8 and xs [M] are read.
+ *   x == NULL, xq == NULL  reuse: the workspace still holds the coded
+ *                        activations of the previous call made with it (same
+ *                        M and K, nothing written to it since); xs is read.
+ *                        This lets Linears that share an input (Q, K, V)
+ *                        quantise it once.
+ *
+ *   xs         [M] FP32 activation scales (never NULL).
  *   wq, ws     [N, K] int8 weights and [N] FP32 per-channel scales (from A1).
  *   bias       [N] BF16 bits, or NULL for no bias.
  *   y          [M, N] BF16 bits, written; may be NULL if acc_out is not NULL.
  *   acc_out    [M, N] int32 raw accumulators, written; NULL to skip (testing).
- *   workspace  device scratch of at least h3q_linear_workspace_bytes(M, N, K)
- *              bytes, 16-byte aligned (NULL allowed when that size is 0).
+ *   workspace  >= h3q_linear_workspace_bytes(M, N, K) bytes, 16-byte aligned.
  *
- * Everything is enqueued on `stream`; the call does not synchronise.  Calls
- * sharing a workspace must not overlap on the GPU.
+ * Everything is enqueued on `stream`; the call does not synchronise.  If a
+ * bounded device-side wait gives up (it cannot on a healthy GPU), the kernel
+ * returns early, leaves the outputs unspecified and sets the workspace's
+ * status word: see h3q_workspace_status.
  */
 h3q_status h3q_linear_w8a8(const uint16_t* x, int8_t* xq, float* xs,
                            const int8_t* wq, const float* ws, const uint16_t* bias,
@@ -139,6 +148,29 @@ h3q_status h3q_linear_w8a8(const uint16_t* x, int8_t* xq, float* xs,
                            uint16_t* y, int32_t* acc_out,
                            void* workspace, size_t workspace_bytes,
                            cudaStream_t stream);
+
+/*
+ * Status of the last h3q_linear_w8a8 that used `workspace` (same M, K):
+ * H3Q_OK, or H3Q_ERR_TIMEOUT if one of its bounded device-side waits gave up.
+ * SYNCHRONISES `stream` to read the status word.
+ */
+h3q_status h3q_workspace_status(const void* workspace, int64_t M, int64_t K,
+                                cudaStream_t stream);
+
+/*
+ * A3 + A4 on the legacy warp-level INT8 tensor instruction (mma.sync
+ * m16n8k32 s8 -> s32), exact by construction; the same arithmetic and output
+ * as h3q_linear_w8a8 from pre-quantised activations.  Kept as the baseline
+ * the tcgen05 path is measured against: on sm_103 this instruction is the
+ * only INT8 tensor path, and it is several times slower.
+ *
+ *   xq [M, K] int8, xs [M] FP32, wq [N, K] int8, ws [N] FP32, bias [N] BF16
+ *   or NULL; y [M, N] BF16 and/or acc_out [M, N] int32.  No workspace.
+ */
+h3q_status h3q_linear_w8a8_mma_sync(const int8_t* xq, const float* xs, const int8_t* wq,
+                                    const float* ws, const uint16_t* bias,
+                                    int64_t M, int64_t N, int64_t K,
+                                    uint16_t* y, int32_t* acc_out, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -29,7 +29,8 @@ def cdll():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for must in ("h3q_quantize_weights", "h3q_quantize_act", "h3q_linear_w8a8",
-                 "h3q_linear_workspace_bytes", "h3q_status_string", "h3q_version"):
+                 "h3q_linear_workspace_bytes", "h3q_status_string", "h3q_version",
+                 "h3q_workspace_status", "h3q_linear_w8a8_mma_sync"):
         assert must in names
 
 
@@ -86,14 +87,25 @@ def test_linear_rejects_bad_args(cdll):
     ws = cdll.h3q_linear_workspace_bytes(4, 8, 64)
     # x, xq, xs, wq, ws, bias, M, N, K, y, acc, workspace, bytes, stream
     assert f(A, A, NUL, A, A, NUL, 4, 8, 64, A, NUL, A, ws, NUL) == 1      # no xs
-    assert f(NUL, NUL, A, A, A, NUL, 4, 8, 64, A, NUL, A, ws, NUL) == 1    # no activations
     assert f(A, A, A, A, A, NUL, 4, 8, 64, NUL, NUL, A, ws, NUL) == 1      # no output
     assert f(A, NUL, A, A, A, NUL, 4, 8, 64, A, NUL, NUL, 0, NUL) == 1     # no workspace
+    assert f(NUL, NUL, A, A, A, NUL, 4, 8, 64, A, NUL, NUL, ws, NUL) == 1  # reuse, no workspace
     assert f(A, NUL, A, A, A, NUL, 4, 8, 64, A, NUL, A, ws - 256, NUL) == 1
     assert f(A, A, A, A, A, NUL, 4, 0, 64, A, NUL, A, ws, NUL) == 2        # N = 0
     assert f(A, A, A, A, A, NUL, 4, 8, 60, A, NUL, A, ws, NUL) == 2        # K % 16
     assert f(A, A, A, A, A, MIS, 4, 8, 64, A, NUL, A, ws, NUL) == 3        # misaligned bias
     assert f(A, A, A, A, A, NUL, 4, 8, 64, MIS, NUL, A, ws, NUL) == 3      # misaligned y
+
+
+def test_status_and_legacy_entry_points_reject_bad_args(cdll):
+    assert cdll.h3q_workspace_status(NUL, 4, 64, NUL) == 1
+    assert cdll.h3q_workspace_status(MIS, 4, 64, NUL) == 3
+    g = cdll.h3q_linear_w8a8_mma_sync
+    # xq, xs, wq, ws, bias, M, N, K, y, acc, stream
+    assert g(NUL, A, A, A, NUL, 4, 8, 64, A, NUL, NUL) == 1
+    assert g(A, A, A, A, NUL, 4, 8, 64, NUL, NUL, NUL) == 1
+    assert g(A, A, A, A, NUL, 4, 8, 24, A, NUL, NUL) == 2
+    assert g(A, A, A, A, NUL, 4, 8, 64, MIS, NUL, NUL) == 3
 
 
 def test_valid_args_without_a_device_report_no_device(cdll):

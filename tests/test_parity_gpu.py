@@ -247,3 +247,87 @@ def test_fc1_workload_sampled(lib, oracle, dev):
 def test_fc2_workload_sampled(lib, oracle, dev):
     c = synth.fc2()
     _linear_check(lib, oracle, dev, c.x_bits, c.w[0], c.bias_bits[0], rows=_sample_rows(c.M, 103))
+
+
+def test_epilogue_deep_cancellation(lib, oracle, dev):
+    # Row 0's bias is -BF16(acc * s_a * s_w), so v there is the small residual
+    # left after cancellation; an FP32 evaluation that rounds the product first
+    # can miss it by many BF16 ulps.  Pre-quantised inputs with full-mantissa
+    # scales make the products carry all 48 bits.
+    rng = np.random.default_rng(77)
+    M, N, K = 64, 256, 64
+    xq = rng.integers(-127, 128, (M, K), dtype=np.int8)
+    wq = rng.integers(-127, 128, (N, K), dtype=np.int8)
+    xs = (rng.uniform(0.5, 1.0, M) * 2.0 ** -6).astype(np.float32)
+    ws = (rng.uniform(0.5, 1.0, N) * 2.0 ** -7).astype(np.float32)
+    acc = oracle.gemm_int32(xq, wq)
+    p0 = oracle.epilogue_value(acc[:1], xs[:1], ws, None)[0]
+    bias = oracle.round_to_bf16(-p0)
+    ref = oracle.epilogue_value(acc, xs, ws, bias)
+    t = lambda a: torch.from_numpy(a).to(dev)
+    out = lib.h3q_linear_w8a8(None, t(wq), t(ws), _bf16_dev(bias, dev), xq=t(xq), xs=t(xs),
+                              want_acc=True)
+    check_exact(out["acc"].cpu().numpy(), acc, "acc")
+    check_y(_bits(out["y"]), ref)
+    assert np.min(np.abs(ref[0]) / np.abs(p0)) < 2.0 ** -16      # the cancellation is deep
+
+
+def test_epilogue_extreme_scales(lib, oracle, dev):
+    # scale products that overflow or underflow FP32 while the exact result
+    # is a finite (or zero) BF16 value, and true overflow to +-inf
+    M, N, K = 4, 8, 16
+    xq = np.full((M, K), 100, np.int8); xq[1] = -100; xq[3, ::2] = 0
+    wq = np.full((N, K), 90, np.int8); wq[:, 1] = -7
+    xs = np.array([2.0 ** 100, 2.0 ** 100, 2.0 ** -100, 3.0e-20], np.float32)
+    ws = np.array([2.0 ** -110, 2.0 ** 20, 2.0 ** -60, 2.0 ** -40, 1.0, 2.0 ** 60,
+                   2.0 ** -126, 5.0e-30], np.float32)
+    acc = oracle.gemm_int32(xq, wq)
+    bias = synth.to_bf16_bits(np.linspace(-1, 1, N).astype(np.float32))
+    ref = oracle.epilogue_value(acc, xs, ws, bias)
+    t = lambda a: torch.from_numpy(a).to(dev)
+    out = lib.h3q_linear_w8a8(None, t(wq), t(ws), _bf16_dev(bias, dev), xq=t(xq), xs=t(xs),
+                              want_acc=True)
+    check_exact(out["acc"].cpu().numpy(), acc, "acc")
+    check_y(_bits(out["y"]), ref)
+
+
+def test_linear_reuse_mode_shares_the_quantised_input(lib, oracle, dev):
+    # Q quantises X into the workspace; K and V reuse it (x = xq = NULL)
+    c = synth.make_linear(200, 136, 5376, seed=23, n_linears=3, outlier_p=0.005, outlier_mul=30)
+    x = _bf16_dev(c.x_bits, dev)
+    outs, refs = [], []
+    ws_buf = None
+    xs = None
+    for i in range(3):
+        qw, sw = lib.h3q_quantize_weights(torch.from_numpy(c.w[i]).to(dev))
+        b = _bf16_dev(c.bias_bits[i], dev)
+        if i == 0:
+            o = lib.h3q_linear_w8a8(x, qw, sw, b, want_acc=True)
+            ws_buf, xs = o["workspace"], o["xs"]
+        else:
+            o = lib.h3q_linear_w8a8(None, qw, sw, b, xs=xs, workspace=ws_buf, want_acc=True)
+        outs.append(o)
+        refs.append(oracle.linear(c.x_bits, *oracle.quantize_weights(c.w[i]), c.bias_bits[i]))
+    assert lib.h3q_workspace_status(ws_buf, 200, 5376) == lib.H3Q_OK
+    for o, r in zip(outs, refs):
+        check_exact(o["acc"].cpu().numpy(), r["acc"], "acc")
+        check_y(_bits(o["y"]), r["v"])
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 16), (130, 257, 64), (300, 100, 5376), (64, 256, 21504)])
+def test_legacy_mma_sync_entry_point(lib, oracle, dev, M, N, K):
+    c = synth.make_linear(M, N, K, seed=M + N, outlier_p=0.01, outlier_mul=20)
+    qw, sw = lib.h3q_quantize_weights(torch.from_numpy(c.w[0]).to(dev))
+    xq, xs = lib.h3q_quantize_act(_bf16_dev(c.x_bits, dev))
+    out = lib.h3q_linear_w8a8_mma_sync(xq, xs, qw, sw, _bf16_dev(c.bias_bits[0], dev),
+                                       want_acc=True)
+    ref = oracle.linear(c.x_bits, *oracle.quantize_weights(c.w[0]), c.bias_bits[0])
+    check_exact(out["acc"].cpu().numpy(), ref["acc"], "acc")
+    check_y(_bits(out["y"]), ref["v"])
+
+
+def test_workspace_status_after_a_normal_call(lib, dev):
+    c = synth.make_linear(300, 400, 2048, seed=41)
+    qw, sw = lib.h3q_quantize_weights(torch.from_numpy(c.w[0]).to(dev))
+    o = lib.h3q_linear_w8a8(_bf16_dev(c.x_bits, dev), qw, sw, None)
+    assert lib.h3q_workspace_status(o["workspace"], 300, 2048) == lib.H3Q_OK

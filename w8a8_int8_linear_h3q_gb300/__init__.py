@@ -47,6 +47,10 @@ def _declare(lib):
     lib.h3q_linear_workspace_bytes.restype = sz
     lib.h3q_linear_w8a8.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp, sz, vp]
     lib.h3q_linear_w8a8.restype = i32
+    lib.h3q_workspace_status.argtypes = [vp, i64, i64, vp]
+    lib.h3q_workspace_status.restype = i32
+    lib.h3q_linear_w8a8_mma_sync.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
+    lib.h3q_linear_w8a8_mma_sync.restype = i32
     return lib
 
 
@@ -142,13 +146,16 @@ def h3q_quantize_act(x, q_out=None, scale_out=None, stream=None):
 
 
 def h3q_linear_w8a8(x, wq, ws, bias=None, *, xq=None, xs=None, y=None, acc_out=None,
-                    want_y=True, want_acc=False, want_xq=False, workspace=None, stream=None):
-    """A2 + A3 + A4.  ``x`` BF16 [M, K] or None (then ``xq``/``xs`` are inputs).
+                    want_y=True, want_acc=False, want_xq=False, workspace=None, M=None,
+                    stream=None):
+    """A2 + A3 + A4.  ``x`` BF16 [M, K]; or None with ``xq``/``xs`` given
+    (pre-quantised); or None with ``xq`` None (reuse: ``workspace`` still holds
+    the coded activations of the previous call on it; pass ``xs`` and ``M``).
 
     Returns a dict with whichever of ``y`` (BF16 [M, N]), ``acc`` (int32 [M, N]),
-    ``xq`` (int8 [M, K]) and ``xs`` (FP32 [M]) were produced.  Outputs and the
-    workspace are allocated here when not given (allocation is plumbing; the
-    library itself allocates nothing).
+    ``xq`` (int8 [M, K]) and ``xs`` (FP32 [M]) were produced, and the
+    ``workspace`` used.  Outputs and the workspace are allocated here when not
+    given (allocation is plumbing; the library itself allocates nothing).
     """
     import torch
     _need(wq, torch.int8, None, "wq")
@@ -163,10 +170,14 @@ def h3q_linear_w8a8(x, wq, ws, bias=None, *, xq=None, xs=None, y=None, acc_out=N
             xq = torch.empty((M, K), dtype=torch.int8, device=dev)
         if xs is None:
             xs = torch.empty((M,), dtype=torch.float32, device=dev)
-    else:
-        if xq is None or xs is None:
-            raise ValueError("pre-quantised call needs xq and xs")
+    elif xq is not None:
+        if xs is None:
+            raise ValueError("pre-quantised call needs xs")
         M = xq.shape[0]
+    else:
+        if xs is None or workspace is None:
+            raise ValueError("reuse call needs xs and the workspace")
+        M = xs.shape[0]
     if xq is not None:
         _need(xq, torch.int8, (M, K), "xq")
     _need(xs, torch.float32, (M,), "xs")
@@ -182,17 +193,52 @@ def h3q_linear_w8a8(x, wq, ws, bias=None, *, xq=None, xs=None, y=None, acc_out=N
     if acc_out is not None:
         _need(acc_out, torch.int32, (M, N), "acc_out")
     need = h3q_linear_workspace_bytes(M, N, K)
-    if workspace is None and need:
+    if workspace is None:
         workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
-    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    wbytes = workspace.numel() * workspace.element_size()
     _check(load().h3q_linear_w8a8(_ptr(x), _ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws), _ptr(bias),
                                   M, N, K, _ptr(y), _ptr(acc_out), _ptr(workspace), wbytes,
                                   _stream(stream)), "h3q_linear_w8a8")
-    out = {"xs": xs}
+    out = {"xs": xs, "workspace": workspace}
     if y is not None:
         out["y"] = y
     if acc_out is not None:
         out["acc"] = acc_out
     if xq is not None:
         out["xq"] = xq
+    return out
+
+
+def h3q_workspace_status(workspace, M: int, K: int, stream=None) -> int:
+    """Status word of the last linear call on ``workspace``: 0 = ok,
+    H3Q_ERR_TIMEOUT if a bounded device-side wait gave up.  Synchronises."""
+    return int(load().h3q_workspace_status(_ptr(workspace), M, K, _stream(stream)))
+
+
+def h3q_linear_w8a8_mma_sync(xq, xs, wq, ws, bias=None, *, y=None, acc_out=None, want_y=True,
+                             want_acc=False, stream=None):
+    """A3 + A4 from pre-quantised activations on the legacy mma.sync INT8 path."""
+    import torch
+    _need(xq, torch.int8, None, "xq")
+    _need(wq, torch.int8, None, "wq")
+    M, K = xq.shape
+    N = wq.shape[0]
+    if wq.shape[1] != K:
+        raise ValueError("xq and wq disagree on K")
+    _need(xs, torch.float32, (M,), "xs")
+    _need(ws, torch.float32, (N,), "ws")
+    if bias is not None:
+        _need(bias, torch.bfloat16, (N,), "bias")
+    if want_y and y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    if want_acc and acc_out is None:
+        acc_out = torch.empty((M, N), dtype=torch.int32, device=xq.device)
+    _check(load().h3q_linear_w8a8_mma_sync(_ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws), _ptr(bias),
+                                           M, N, K, _ptr(y), _ptr(acc_out), _stream(stream)),
+           "h3q_linear_w8a8_mma_sync")
+    out = {}
+    if y is not None:
+        out["y"] = y
+    if acc_out is not None:
+        out["acc"] = acc_out
     return out

@@ -91,34 +91,67 @@ h3q_status h3q_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t* q_o
 size_t h3q_linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   (void)N;
   if (M < 1 || K < 1) return 0;
-  const size_t b = size_t(M) * size_t(K) * 2u;      // FP16-coded activations
-  return (b + 255u) & ~size_t(255);
+  // FP16-coded activations, then one 256-byte block holding the status word
+  return h3q::gemm_tc_status_offset(M, K) + 256u;
 }
 
 h3q_status h3q_linear_w8a8(const uint16_t* x, int8_t* xq, float* xs, const int8_t* wq,
                            const float* ws, const uint16_t* bias, int64_t M, int64_t N,
                            int64_t K, uint16_t* y, int32_t* acc_out, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream) {
-  if (!xs || !wq || !ws) return H3Q_ERR_INVALID_ARG;
-  if (!x && !xq) return H3Q_ERR_INVALID_ARG;       // no activations at all
+  if (!xs || !wq || !ws || !workspace) return H3Q_ERR_INVALID_ARG;
   if (!y && !acc_out) return H3Q_ERR_INVALID_ARG;  // nothing to write
   if (h3q_status st = check_shape(M, N, K)) return st;
-  const size_t need = h3q_linear_workspace_bytes(M, N, K);
-  if (x && !xq && (!workspace || workspace_bytes < need)) return H3Q_ERR_INVALID_ARG;
+  if (workspace_bytes < h3q_linear_workspace_bytes(M, N, K)) return H3Q_ERR_INVALID_ARG;
   const void* ptrs[] = {x, xq, xs, wq, ws, bias, y, acc_out, workspace};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return H3Q_ERR_MISALIGNED;
   if (h3q_status st = check_device()) return st;
 
-  // A2 (unless pre-quantised).  The INT8 activations go to xq, or to the
-  // workspace when the caller does not want them.
-  int8_t* qa = xq ? xq : static_cast<int8_t*>(workspace);
+  uint8_t* wsp = static_cast<uint8_t*>(workspace);
+  uint16_t* act = reinterpret_cast<uint16_t*>(wsp);
+  uint32_t* status = reinterpret_cast<uint32_t*>(wsp + h3q::gemm_tc_status_offset(M, K));
+  // A2, or the FP16 coding of pre-quantised activations, or (x == xq == NULL)
+  // the activations a previous call left coded in this workspace.
   if (x) {
-    if (h3q_status st = from_cuda(h3q::launch_quantize_act(x, M, K, qa, xs, nullptr, stream)))
+    if (h3q_status st = from_cuda(h3q::launch_quantize_act(x, M, K, xq, xs, act, stream)))
       return st;
+  } else if (xq) {
+    if (h3q_status st = from_cuda(h3q::launch_int8_to_f16(xq, M * K, act, stream))) return st;
   }
+  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), stream) != cudaSuccess) return H3Q_ERR_CUDA;
   // A3 + A4.
-  return from_cuda(h3q::launch_gemm_mma_s8(qa, xs, wq, ws, bias, M, N, K, y, acc_out, stream));
+  return from_cuda(h3q::launch_gemm_tc(act, xs, wq, ws, bias, M, N, K, y, acc_out, status,
+                                       stream));
+}
+
+h3q_status h3q_workspace_status(const void* workspace, int64_t M, int64_t K,
+                                cudaStream_t stream) {
+  if (!workspace) return H3Q_ERR_INVALID_ARG;
+  if (M < 1 || K < 1) return H3Q_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(workspace)) return H3Q_ERR_MISALIGNED;
+  if (h3q_status st = check_device()) return st;
+  const uint8_t* wsp = static_cast<const uint8_t*>(workspace);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, wsp + h3q::gemm_tc_status_offset(M, K), sizeof(word),
+                      cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return H3Q_ERR_CUDA;
+  return word ? H3Q_ERR_TIMEOUT : H3Q_OK;
+}
+
+h3q_status h3q_linear_w8a8_mma_sync(const int8_t* xq, const float* xs, const int8_t* wq,
+                                    const float* ws, const uint16_t* bias, int64_t M, int64_t N,
+                                    int64_t K, uint16_t* y, int32_t* acc_out,
+                                    cudaStream_t stream) {
+  if (!xq || !xs || !wq || !ws) return H3Q_ERR_INVALID_ARG;
+  if (!y && !acc_out) return H3Q_ERR_INVALID_ARG;
+  if (h3q_status st = check_shape(M, N, K)) return st;
+  const void* ptrs[] = {xq, xs, wq, ws, bias, y, acc_out};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return H3Q_ERR_MISALIGNED;
+  if (h3q_status st = check_device()) return st;
+  return from_cuda(h3q::launch_gemm_mma_s8(xq, xs, wq, ws, bias, M, N, K, y, acc_out, stream));
 }
 
 }  // extern "C"

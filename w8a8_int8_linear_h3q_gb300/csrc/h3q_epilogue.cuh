@@ -1,0 +1,58 @@
+// h3q_epilogue.cuh -- A4: dequantise, add the bias, round once to BF16.
+//
+//   y = BF16_RNE(acc * s_a * s_w + bias)
+//
+// The bias is added before the single rounding of the output ("MLX
+// implementation and experiment report", What the default preserves: biased
+// BF16 linears use an addmm epilogue).  The value is formed in FP32 with
+// error-free transformations (an FMA-exact two-product for s_a * s_w and for
+// the product with the accumulator, and a two-sum with the bias) so that its
+// error stays far below one BF16 ulp even when the product and the bias
+// nearly cancel, and so that no FP32 intermediate overflows or underflows
+// unless the exact result does.  The result is within one BF16 ulp of the
+// exact value of the expression.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace h3q {
+
+__device__ __forceinline__ float epilogue_value(int acc, float sa, float sw, float bias) {
+  if (acc == 0) return bias;                       // also covers 0 * (huge scale)
+  float sa_ = sa, back = 1.f;
+  float p_hi = __fmul_rn(sa_, sw);
+  if (p_hi < 0x1p-60f) {                           // keep the two-product exact: rescale by 2^64
+    sa_ = __fmul_rn(sa, 0x1p64f);
+    p_hi = __fmul_rn(sa_, sw);
+    back = 0x1p-64f;
+  }
+  if (isinf(p_hi)) return acc > 0 ? p_hi : -p_hi;  // |exact| >= FP32 max > BF16 max
+  const float p_lo = __fmaf_rn(sa_, sw, -p_hi);    // s_a * s_w == p_hi + p_lo exactly
+  const float a_hi = __int2float_rn(acc);
+  const float a_lo = __ll2float_rn(static_cast<long long>(acc) - __float2ll_rz(a_hi));
+  float t_hi = __fmul_rn(a_hi, p_hi);
+  if (isinf(t_hi)) return t_hi;                    // exact result overflows as well
+  float t_lo = __fmaf_rn(a_hi, p_hi, -t_hi);       // exact error of t_hi
+  t_lo = __fmaf_rn(a_hi, p_lo, t_lo);
+  t_lo = __fmaf_rn(a_lo, p_hi, t_lo);              // a_lo * p_lo is below 2^-47 relative
+  if (back != 1.f) {
+    t_hi = __fmul_rn(t_hi, back);
+    t_lo = __fmul_rn(t_lo, back);
+  }
+  // two-sum of t_hi and the bias, then the low parts
+  const float s = __fadd_rn(t_hi, bias);
+  const float bv = __fsub_rn(s, t_hi);
+  const float err = __fadd_rn(__fsub_rn(t_hi, __fsub_rn(s, bv)), __fsub_rn(bias, bv));
+  return __fadd_rn(s, __fadd_rn(err, t_lo));
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(uint32_t(b) << 16);
+}
+
+__device__ __forceinline__ uint16_t float_to_bf16_bits(float v) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+}  // namespace h3q

@@ -1,7 +1,7 @@
 // h3q_gemm_mma.cu -- A3 + A4 on the warp-level INT8 tensor path.
 //
 //   acc[m,n] = sum_k qa[m,k] * qw[n,k]           (mma.sync m16n8k32 s8 -> s32, exact)
-//   y[m,n]   = BF16_RNE(fma(float(acc) * sa[m], sw[n], bias[n]))
+//   y[m,n]   = BF16_RNE(acc * sa[m] * sw[n] + bias[n])       (h3q_epilogue.cuh)
 //
 // Sources: "feat(mps): support MiniMax-H3 INT8 inference on Apple M5"
 // (LightX2V #1672), Validation (INT32 product of INT8 operands) and
@@ -17,6 +17,7 @@
 // kernel is measured against.
 #include <cuda_bf16.h>
 
+#include "h3q_epilogue.cuh"
 #include "h3q_internal.cuh"
 
 namespace h3q {
@@ -56,10 +57,6 @@ __device__ __forceinline__ void mma_s8(int (&d)[4], const uint32_t (&a)[4], uint
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ float epi(int acc, float sa, float sw, float b) {
-  return __fmaf_rn(__fmul_rn(__int2float_rn(acc), sa), sw, b);
 }
 
 __global__ void __launch_bounds__(THREADS)
@@ -160,7 +157,8 @@ gemm_mma_s8_kernel(const int8_t* __restrict__ A, const float* __restrict__ sa,
         }
         if (Y) {
           const float s = sa[m];
-          const __nv_bfloat162 v = __floats2bfloat162_rn(epi(a0, s, sw0, b0), epi(a1, s, sw1, b1));
+          const __nv_bfloat162 v = __floats2bfloat162_rn(epilogue_value(a0, s, sw0, b0),
+                                                         epilogue_value(a1, s, sw1, b1));
           if (two && n_even) {
             *reinterpret_cast<__nv_bfloat162*>(Y + off) = v;
           } else {

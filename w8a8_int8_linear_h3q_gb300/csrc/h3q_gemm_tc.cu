@@ -1,0 +1,411 @@
+// h3q_gemm_tc.cu -- A3 + A4 on the sm_103a 5th-generation tensor cores.
+//
+//   acc[m,n] = sum_k qa[m,k] * qw[n,k]          exact INT32
+//   y[m,n]   = BF16_RNE(acc * sa[m] * sw[n] + bias[n])
+//
+// Sources: "feat(mps): support MiniMax-H3 INT8 inference on Apple M5"
+// (LightX2V #1672) -- Validation (INT8 x INT8 with CPU INT32 references),
+// opening description (native K = 5376, no K padding, no weight
+// dequantisation), Summary by CodeRabbit (exact K tiles); "MLX implementation
+// and experiment report", What the default preserves (bias before the one
+// rounding).
+//
+// sm_103a has no INT8 tcgen05 MMA, so the product runs as exact integer
+// arithmetic on the FP16 MMA (kind::f16, FP32 accumulate):
+//   - every INT8 value is an FP16 value, every product |q_a q_w| <= 127^2 is
+//     exact in FP32, and an FP32 sum of such integers is exact while every
+//     partial sum stays within 2^24, which holds for any 1040 consecutive
+//     K terms (2^24 / 127^2 = 1040.2);
+//   - so K is cut into chunks of at most 1024 (16 k-blocks of 64), each chunk
+//     accumulates into a fresh FP32 TMEM accumulator, and the epilogue warps
+//     fold every chunk into an INT32 running sum kept in TMEM (cvt.rni of an
+//     integer-valued FP32 is exact).  The result is the exact INT32 product.
+// The weights stay INT8 in memory (no dequantisation); converter warps turn
+// each INT8 k-block into FP16 in registers and store it into TMEM, where the
+// MMA reads it as its A operand.  The activations arrive already FP16-coded
+// (written by the activation quantiser) through TMA into 128-byte-swizzled
+// shared memory: the B operand.  Shared memory therefore carries only the
+// activation tiles, and TMEM carries the weights, both accumulators and the
+// running sum.
+//
+// Tile: 128 output channels (MMA M, TMEM lanes) x 128 tokens (MMA N).
+// Persistent CTAs, one per SM, walk the tiles in groups of 16 token blocks so
+// that the concurrently running tiles share weight and activation tiles in L2.
+//
+// Warp roles (576 threads):
+//   warp 0      TMA producer (activation tiles, 8-stage ring)
+//   warp 1      TMEM allocator and MMA issuer (one thread)
+//   warps 2-9   converters: INT8 weights -> FP16 -> TMEM A stages (4-stage ring)
+//   warps 10-17 epilogue: chunk drains into the INT32 running sum, then
+//               dequant + bias + BF16 (and the optional raw INT32 output)
+// Every wait is bounded in time; on a timeout the kernel records an error
+// word, lets every role fall through, drains its in-flight copies and MMAs,
+// frees TMEM and returns.
+#include <cuda.h>
+
+#include "h3q_epilogue.cuh"
+#include "h3q_internal.cuh"
+#include "h3q_tc_ptx.cuh"
+
+namespace h3q {
+namespace {
+
+namespace P = ptx;
+
+constexpr int BM = 128;                 // channels per tile
+constexpr int BN = 128;                 // tokens per tile
+constexpr int BK = 64;                  // K per k-block (128 bytes of FP16)
+constexpr int MAX_KB_PER_CHUNK = 16;    // 1024 K: exact FP32 chunk
+constexpr int B_STAGES = 8;
+constexpr int A_STAGES = 4;
+constexpr int GROUP_M = 16;             // token blocks per raster group
+constexpr int NUM_CONV_WARPS = 8;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int THREADS = 32 * (2 + NUM_CONV_WARPS + NUM_EPI_WARPS);
+constexpr int B_STAGE_BYTES = BN * BK * 2;                 // 16 KB
+constexpr uint32_t TM_D = 0;            // accumulators: cols 0-127 and 128-255
+constexpr uint32_t TM_RS = 256;         // INT32 running sum: cols 256-383
+constexpr uint32_t TM_A = 384;          // A stages: 4 x 32 cols
+constexpr uint32_t TM_COLS = 512;
+constexpr uint32_t IDESC = P::idesc_f16_f32(BM, BN);
+
+// error word bits
+constexpr uint32_t ERR_PRODUCER = 1u, ERR_MMA = 2u, ERR_CONVERT = 4u, ERR_EPILOGUE = 8u,
+                   ERR_TEARDOWN = 16u;
+
+struct __align__(1024) Smem {
+  uint8_t b[B_STAGES][B_STAGE_BYTES];
+  uint64_t full_b[B_STAGES];
+  uint64_t empty_b[B_STAGES];
+  uint64_t full_a[A_STAGES];
+  uint64_t empty_a[A_STAGES];
+  uint64_t dfull[2];
+  uint64_t dempty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;   // + slack for 1024-byte alignment
+
+struct Shape {
+  int M, N, K;
+  int KB;             // k-blocks
+  int nchunks;        // exact-FP32 chunks per tile
+  int kpc;            // k-blocks per chunk (last may be shorter)
+  int mt, nt;         // token blocks, channel blocks
+  int tiles;
+};
+
+__device__ __forceinline__ void tile_coords(const Shape& s, int t, int& mb, int& nb) {
+  const int per_group = GROUP_M * s.nt;
+  const int g = t / per_group;
+  const int first_m = g * GROUP_M;
+  const int gm = min(GROUP_M, s.mt - first_m);
+  const int r = t - g * per_group;
+  mb = first_m + r % gm;
+  nb = r / gm;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const int8_t* __restrict__ wq,
+               const float* __restrict__ sa, const float* __restrict__ sw,
+               const uint16_t* __restrict__ bias, const Shape shp, uint16_t* __restrict__ Y,
+               int32_t* __restrict__ ACC, uint32_t* __restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < B_STAGES; ++i) {
+      P::mbar_init(&sm.full_b[i], 1);
+      P::mbar_init(&sm.empty_b[i], 1);
+    }
+    for (int i = 0; i < A_STAGES; ++i) {
+      P::mbar_init(&sm.full_a[i], NUM_CONV_WARPS * 32);
+      P::mbar_init(&sm.empty_a[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      P::mbar_init(&sm.dfull[i], 1);
+      P::mbar_init(&sm.dempty[i], NUM_EPI_WARPS * 32);
+    }
+    P::mbar_init(&sm.mma_done, 1);
+    sm.abort_flag = 0;
+    P::fence_mbar_init();
+  }
+  if (warp == 1) P::tmem_alloc(&sm.tmem_base, TM_COLS);
+  P::tc_fence_before();
+  __syncthreads();
+  P::tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      P::tma_prefetch_desc(&act_map);
+      uint32_t g = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < shp.tiles; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(shp, t, mb, nb);
+        for (int kb = 0; kb < shp.KB; ++kb, ++g) {
+          const uint32_t s = g % B_STAGES, ph = (g / B_STAGES) & 1u;
+          if (!P::mbar_wait(&sm.empty_b[s], ph ^ 1u, abort_flag, err, ERR_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          P::mbar_arrive_expect_tx(&sm.full_b[s], B_STAGE_BYTES);
+          P::tma_load_2d(P::smem_u32(sm.b[s]), &act_map, &sm.full_b[s], kb * BK, mb * BN);
+        }
+      }
+      // no copy may still be landing in shared memory when the CTA exits
+      const uint32_t issued = g;
+      int no_abort = 0;
+      volatile int* never = &no_abort;   // this drain does not follow the abort flag
+      for (uint32_t i = issued > B_STAGES ? issued - B_STAGES : 0; i < issued; ++i) {
+        const uint32_t s = i % B_STAGES, ph = (i / B_STAGES) & 1u;
+        P::mbar_wait(&sm.full_b[s], ph, never, err, ERR_TEARDOWN);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t g = 0, gc = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < shp.tiles; t += gridDim.x) {
+        for (int c = 0; ok && c < shp.nchunks; ++c, ++gc) {
+          const int kb0 = c * shp.kpc, kb1 = min(shp.KB, kb0 + shp.kpc);
+          const uint32_t buf = gc & 1u;
+          if (!P::mbar_wait(&sm.dempty[buf], ((gc >> 1) & 1u) ^ 1u, abort_flag, err, ERR_MMA)) {
+            ok = false;
+            break;
+          }
+          P::tc_fence_after();
+          const uint32_t d_tmem = tmem + TM_D + buf * BN;
+          for (int kb = kb0; kb < kb1; ++kb, ++g) {
+            const uint32_t sb = g % B_STAGES, pb = (g / B_STAGES) & 1u;
+            const uint32_t sa_ = g % A_STAGES, pa = (g / A_STAGES) & 1u;
+            if (!P::mbar_wait(&sm.full_b[sb], pb, abort_flag, err, ERR_MMA) ||
+                !P::mbar_wait(&sm.full_a[sa_], pa, abort_flag, err, ERR_MMA)) {
+              ok = false;
+              break;
+            }
+            P::tc_fence_after();
+            const uint64_t bdesc = P::smem_desc_sw128(P::smem_u32(sm.b[sb]));
+            const uint32_t a_tmem = tmem + TM_A + sa_ * 32;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              P::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc + uint64_t(kk * 2), IDESC,
+                            (kb > kb0 || kk > 0) ? 1u : 0u);
+            P::mma_commit(&sm.empty_b[sb]);
+            P::mma_commit(&sm.empty_a[sa_]);
+          }
+          if (!ok) break;
+          P::mma_commit(&sm.dfull[buf]);
+        }
+      }
+      // every MMA this thread issued has finished before TMEM is freed
+      P::mma_commit(&sm.mma_done);
+      int no_abort = 0;
+      volatile int* never = &no_abort;
+      P::mbar_wait(&sm.mma_done, 0, never, err, ERR_TEARDOWN);
+    }
+    __syncwarp();
+  } else if (warp < 2 + NUM_CONV_WARPS) {
+    // ---------------- converters: INT8 weights -> FP16 -> TMEM ----------------
+    const int q = warp & 3;                       // TMEM lane quarter of this warp
+    const int half = (warp - 2) >> 2;             // which 32 bytes of a 64-byte k-block
+    const int r = 32 * q + lane;                  // channel row within the tile
+    const uint32_t lane_base = uint32_t(32 * q) << 16;
+    constexpr int PF = 4;                         // k-blocks of loads in flight
+    uint4 buf[PF][2];
+
+    // flat job sequence over (tile, k-block); `ld_*` runs PF jobs ahead
+    int ld_t = blockIdx.x, ld_kb = 0;
+    auto load_job = [&](uint4 (&dst)[2]) {
+      dst[0] = make_uint4(0, 0, 0, 0);
+      dst[1] = make_uint4(0, 0, 0, 0);
+      if (ld_t < shp.tiles) {
+        int mb, nb;
+        tile_coords(shp, ld_t, mb, nb);
+        const int n = nb * BM + r;
+        if (n < shp.N) {
+          const int k0 = ld_kb * BK + half * 32;
+          const int8_t* p = wq + int64_t(n) * shp.K + k0;
+          if (k0 < shp.K) dst[0] = __ldg(reinterpret_cast<const uint4*>(p));
+          if (k0 + 16 < shp.K) dst[1] = __ldg(reinterpret_cast<const uint4*>(p + 16));
+        }
+        if (++ld_kb == shp.KB) {
+          ld_kb = 0;
+          ld_t += gridDim.x;
+        }
+      }
+    };
+#pragma unroll
+    for (int p = 0; p < PF; ++p) load_job(buf[p]);
+
+    uint32_t g = 0;
+    bool ok = true;
+    const uint32_t total = uint32_t((shp.tiles - int(blockIdx.x) + int(gridDim.x) - 1) /
+                                    int(gridDim.x)) * uint32_t(shp.KB);
+    while (ok && g < total) {
+#pragma unroll
+      for (int p = 0; p < PF; ++p) {
+        if (g >= total) break;
+        uint32_t h[16];
+        const uint32_t w[8] = {buf[p][0].x, buf[p][0].y, buf[p][0].z, buf[p][0].w,
+                               buf[p][1].x, buf[p][1].y, buf[p][1].z, buf[p][1].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) P::s8x4_to_f16x4(w[i], h[2 * i], h[2 * i + 1]);
+        load_job(buf[p]);                         // refill this slot PF jobs ahead
+        const uint32_t s = g % A_STAGES, ph = (g / A_STAGES) & 1u;
+        if (!P::mbar_wait_warp(&sm.empty_a[s], ph ^ 1u, abort_flag, err, ERR_CONVERT)) {
+          ok = false;
+          break;
+        }
+        P::tc_fence_after();
+        P::tmem_st16(tmem + lane_base + TM_A + s * 32 + half * 16, h);
+        P::tmem_wait_st();
+        P::tc_fence_before();
+        P::mbar_arrive(&sm.full_a[s]);
+        ++g;
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;
+    const int half = (warp - 2 - NUM_CONV_WARPS) >> 2;   // token columns [64*half, +64)
+    const uint32_t lane_base = uint32_t(32 * q) << 16;
+    uint32_t gc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < shp.tiles; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(shp, t, mb, nb);
+      const int n = nb * BM + 32 * q + lane;
+      const bool n_ok = n < shp.N;
+      const float swn = n_ok ? sw[n] : 0.f;
+      const float bn = (n_ok && bias) ? bf16_bits_to_float(bias[n]) : 0.f;
+      for (int c = 0; c < shp.nchunks; ++c, ++gc) {
+        const uint32_t buf = gc & 1u;
+        if (!P::mbar_wait_warp(&sm.dfull[buf], (gc >> 1) & 1u, abort_flag, err, ERR_EPILOGUE)) {
+          ok = false;
+          break;
+        }
+        P::tc_fence_after();
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          const uint32_t col = 64 * half + 32 * blk;
+          uint32_t d[32], s[32];
+          P::tmem_ld32(tmem + lane_base + TM_D + buf * BN + col, d);
+          if (c > 0) P::tmem_ld32(tmem + lane_base + TM_RS + col, s);
+          P::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int v = __float2int_rn(__uint_as_float(d[j]));
+            s[j] = uint32_t((c > 0 ? int(s[j]) : 0) + v);
+          }
+          P::tmem_st32(tmem + lane_base + TM_RS + col, s);
+        }
+        P::tmem_wait_st();
+        P::tc_fence_before();
+        P::mbar_arrive(&sm.dempty[buf]);
+      }
+      if (!ok) break;
+      // final: dequantise the exact INT32 sums of this tile
+#pragma unroll 1
+      for (int blk = 0; blk < 2; ++blk) {
+        const int col = 64 * half + 32 * blk;
+        const int m0 = mb * BN + col;
+        uint32_t s[32];
+        P::tmem_ld32(tmem + lane_base + TM_RS + uint32_t(col), s);
+        P::tmem_wait_ld();
+        const float sa_l = (m0 + lane < shp.M) ? sa[m0 + lane] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float saj = __shfl_sync(0xFFFFFFFFu, sa_l, j);
+          const int m = m0 + j;
+          if (n_ok && m < shp.M) {
+            const int64_t off = int64_t(m) * shp.N + n;
+            if (ACC) ACC[off] = int32_t(s[j]);
+            if (Y) Y[off] = float_to_bf16_bits(epilogue_value(int(s[j]), saj, swn, bn));
+          }
+        }
+      }
+    }
+  }
+
+  P::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    P::tc_fence_after();
+    P::tmem_dealloc(tmem, TM_COLS);
+  }
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+}  // namespace
+
+size_t gemm_tc_status_offset(int64_t M, int64_t K) {
+  return (size_t(M) * size_t(K) * 2u + 255u) & ~size_t(255);
+}
+
+cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_t* qw,
+                           const float* sw, const uint16_t* bias, int64_t M, int64_t N,
+                           int64_t K, uint16_t* y, int32_t* acc, uint32_t* err, cudaStream_t s) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(M)};
+  const cuuint64_t strides[1] = {cuuint64_t(K) * 2u};
+  const cuuint32_t box[2] = {BK, BN};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(act_f16), dims,
+          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+
+  Shape shp;
+  shp.M = int(M);
+  shp.N = int(N);
+  shp.K = int(K);
+  shp.KB = int((K + BK - 1) / BK);
+  shp.nchunks = (shp.KB + MAX_KB_PER_CHUNK - 1) / MAX_KB_PER_CHUNK;
+  shp.kpc = (shp.KB + shp.nchunks - 1) / shp.nchunks;
+  shp.mt = int((M + BN - 1) / BN);
+  shp.nt = int((N + BM - 1) / BM);
+  shp.tiles = shp.mt * shp.nt;
+
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  const int grid = shp.tiles < sms ? shp.tiles : sms;
+  gemm_tc_kernel<<<grid, THREADS, kSmemBytes, s>>>(map, qw, sa, sw, bias, shp, y, acc, err);
+  return cudaGetLastError();
+}
+
+}  // namespace h3q

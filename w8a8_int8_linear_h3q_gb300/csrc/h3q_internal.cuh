@@ -26,6 +26,16 @@ cudaError_t launch_quantize_weights(const void* w, int w_dtype, int64_t N, int64
 // int8 -> FP16-coded integers (for pre-quantised activations).
 cudaError_t launch_int8_to_f16(const int8_t* q, int64_t n, uint16_t* out, cudaStream_t s);
 
+// A3 + A4 on the tcgen05 tensor cores (exact INT32 via FP16 MMA with chunked
+// FP32 accumulation).  act_f16: [M, K] FP16-coded INT8 activations.
+// err: device status word (0 = ok; bits set when a bounded wait gave up).
+cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_t* qw,
+                           const float* sw, const uint16_t* bias, int64_t M, int64_t N,
+                           int64_t K, uint16_t* y, int32_t* acc, uint32_t* err, cudaStream_t s);
+
+// Byte offset of the status word inside the linear workspace.
+size_t gemm_tc_status_offset(int64_t M, int64_t K);
+
 // A3 + A4 on the legacy warp-level INT8 tensor path (mma.sync m16n8k32 s8).
 cudaError_t launch_gemm_mma_s8(const int8_t* qa, const float* sa, const int8_t* qw,
                                const float* sw, const uint16_t* bias, int64_t M, int64_t N,
