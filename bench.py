@@ -105,6 +105,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# --- cross-rank aggregation (replicas) ---------------------------------------------
+
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time (ms); every rank gets the same value."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tops(total_ms: float, steps: int, world: int) -> float:
+    """All ranks' operations over the slowest rank's time: each replica runs
+    the full workload, so the job does world x steps x OPS_PER_STEP."""
+    return OPS_PER_STEP * steps * world / (total_ms * 1e-3) / 1e12
+
+
 # --- CPU baseline: the oracle, as it stands, on a bounded sample -------------------
 
 def cpu_oracle_sample(case, qws, target_s: float = 12.0):
@@ -249,12 +268,8 @@ def run_gpu(args):
     step_ms = [e[0].elapsed_time(e[-1]) for e in events]
     first_ms = [e[0].elapsed_time(e[1]) for e in events]          # A2 + Q's GEMM
     gemm_ms = [e[i].elapsed_time(e[i + 1]) for e in events for i in range(1, len(LINEARS))]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = OPS_PER_STEP * args.steps * world / (total_ms * 1e-3) / 1e12
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = whole_job_tops(total_ms, args.steps, world)
 
     # end to end through the public API with host buffers: pinned H2D of X,
     # the hot path, D2H of the four outputs, all inside the timed region
@@ -281,11 +296,8 @@ def run_gpu(args):
         b.record(stream)
         torch.cuda.synchronize()
         e_ms += a.elapsed_time(b)
-    if world > 1:
-        t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e_ms = float(t.item())
-    e2e_value = OPS_PER_STEP * e2e_steps * world / (e_ms * 1e-3) / 1e12 if e2e_steps else None
+    e_ms = max_over_ranks(e_ms, world, dev)
+    e2e_value = whole_job_tops(e_ms, e2e_steps, world) if e2e_steps else None
 
     peaks, peak_kind = _peaks()
     gemm_avg_s = statistics.mean(gemm_ms) * 1e-3

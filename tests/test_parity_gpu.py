@@ -255,7 +255,7 @@ def test_epilogue_deep_cancellation(lib, oracle, dev):
     # can miss it by many BF16 ulps.  Pre-quantised inputs with full-mantissa
     # scales make the products carry all 48 bits.
     rng = np.random.default_rng(77)
-    M, N, K = 64, 256, 64
+    M, N, K = 64, 8192, 64
     xq = rng.integers(-127, 128, (M, K), dtype=np.int8)
     wq = rng.integers(-127, 128, (N, K), dtype=np.int8)
     xs = (rng.uniform(0.5, 1.0, M) * 2.0 ** -6).astype(np.float32)
@@ -269,7 +269,8 @@ def test_epilogue_deep_cancellation(lib, oracle, dev):
                               want_acc=True)
     check_exact(out["acc"].cpu().numpy(), acc, "acc")
     check_y(_bits(out["y"]), ref)
-    assert np.min(np.abs(ref[0]) / np.abs(p0)) < 2.0 ** -16      # the cancellation is deep
+    # the construction reaches cancellations deeper than FP32 rounding of the product
+    assert np.sum(np.abs(ref[0]) < 2.0 ** -16 * np.abs(p0)) >= 10
 
 
 def test_epilogue_extreme_scales(lib, oracle, dev):
