@@ -18,7 +18,9 @@
 
 namespace h3q {
 
-__device__ __forceinline__ float epilogue_value(int acc, float sa, float sw, float bias) {
+// Exact-transformation path: used where the cheap path below cannot prove
+// its error small enough.
+static __device__ __noinline__ float epilogue_value_careful(int acc, float sa, float sw, float bias) {
   if (acc == 0) return bias;                       // also covers 0 * (huge scale)
   float sa_ = sa, back = 1.f;
   float p_hi = __fmul_rn(sa_, sw);
@@ -45,6 +47,25 @@ __device__ __forceinline__ float epilogue_value(int acc, float sa, float sw, flo
   const float bv = __fsub_rn(s, t_hi);
   const float err = __fadd_rn(__fsub_rn(t_hi, __fsub_rn(s, bv)), __fsub_rn(bias, bv));
   return __fadd_rn(s, __fadd_rn(err, t_lo));
+}
+
+// Cheap path first.  P = RN(RN(float(acc) * sa) * sw) carries a relative
+// error below 3 * 2^-24 (three roundings, with the intermediate and P both
+// finite and far above the subnormal range), and v = RN(P + bias) adds at most
+// 2^-24 |v|.  When |v| >= 2^-10 |P| the total is below 2^-12 |v|, far under
+// half a BF16 ulp (>= 2^-9 |v|), so one BF16 rounding of v lands within one
+// ulp of the exact value.  Cancellation (|v| < 2^-10 |P|), a non-finite or
+// tiny P, or a tiny v take the exact path.
+__device__ __forceinline__ float epilogue_value(int acc, float sa, float sw, float bias) {
+  const float t = __fmul_rn(__int2float_rn(acc), sa);
+  const float p = __fmul_rn(t, sw);
+  const float v = __fadd_rn(p, bias);
+  const float at = fabsf(t), ap = fabsf(p), av = fabsf(v);
+  if (at <= 3.0e38f && at >= 0x1p-100f && ap <= 3.0e38f && ap >= 0x1p-100f &&
+      av >= 0x1p-110f && av >= ap * 0x1p-10f)
+    return v;
+  if (acc == 0) return bias;
+  return epilogue_value_careful(acc, sa, sw, bias);
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {

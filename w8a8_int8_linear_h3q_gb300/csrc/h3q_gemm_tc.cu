@@ -222,24 +222,35 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const int8_t* __rest
     constexpr int PF = 4;                         // k-blocks of loads in flight
     uint4 buf[PF][2];
 
-    // flat job sequence over (tile, k-block); `ld_*` runs PF jobs ahead
+    // flat job sequence over (tile, k-block); `ld_*` runs PF jobs ahead.  The
+    // weight row of the current tile is found once per tile.
     int ld_t = blockIdx.x, ld_kb = 0;
+    const int8_t* ld_row = wq;
+    bool ld_row_ok = false;
+    auto set_tile = [&](int t) {
+      if (t < shp.tiles) {
+        int mb, nb;
+        tile_coords(shp, t, mb, nb);
+        const int n = nb * BM + r;
+        ld_row_ok = n < shp.N;
+        ld_row = wq + int64_t(ld_row_ok ? n : 0) * shp.K + half * 32;
+      }
+    };
+    set_tile(ld_t);
     auto load_job = [&](uint4 (&dst)[2]) {
       dst[0] = make_uint4(0, 0, 0, 0);
       dst[1] = make_uint4(0, 0, 0, 0);
       if (ld_t < shp.tiles) {
-        int mb, nb;
-        tile_coords(shp, ld_t, mb, nb);
-        const int n = nb * BM + r;
-        if (n < shp.N) {
-          const int k0 = ld_kb * BK + half * 32;
-          const int8_t* p = wq + int64_t(n) * shp.K + k0;
+        const int k0 = ld_kb * BK + half * 32;
+        if (ld_row_ok) {
+          const int8_t* p = ld_row + ld_kb * BK;
           if (k0 < shp.K) dst[0] = __ldg(reinterpret_cast<const uint4*>(p));
           if (k0 + 16 < shp.K) dst[1] = __ldg(reinterpret_cast<const uint4*>(p + 16));
         }
         if (++ld_kb == shp.KB) {
           ld_kb = 0;
           ld_t += gridDim.x;
+          set_tile(ld_t);
         }
       }
     };

@@ -29,6 +29,24 @@ __device__ __forceinline__ int quant1(float x, float s) {
   return max(-kQMax, min(kQMax, q));
 }
 
+// The same value as quant1(x, s), cheaper.  With r = RN(1/s) (s normal) and
+// t = RN(x * r): t = (x/s)(1 + e1)(1 + e2), |e1|, |e2| <= 2^-24, and
+// |x/s| <= 127 (1 + 2^-23), so |t - x/s| < 1.6e-5; the FP32 quotient
+// RN(x/s) is within 2^-18 of x/s.  Hence |t - RN(x/s)| < 2^-15, and unless t
+// lies within 2^-15 of a half-integer, RN(x/s) and t round to the same
+// integer, with no tie.  Near a half-integer (about 6e-5 of inputs) the IEEE
+// division decides.  `fast` is false for rows whose scale is too small for a
+// normal reciprocal; those always divide.
+__device__ __forceinline__ int quant1_fast(float x, float s, float r, bool fast) {
+  if (fast) {
+    const float t = __fmul_rn(x, r);
+    const float n = rintf(t);
+    if (fabsf(__fsub_rn(t, n)) < 0.5f - 0x1p-15f)
+      return max(-kQMax, min(kQMax, int(n)));
+  }
+  return quant1(x, s);
+}
+
 __device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
   return (uint32_t(a) & 0xFFu) | ((uint32_t(b) & 0xFFu) << 8) | ((uint32_t(c) & 0xFFu) << 16) |
          (uint32_t(d) << 24);
@@ -55,14 +73,14 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 }
 
 template <bool kQ8, bool kF16>
-__device__ __forceinline__ void quant_store8(uint4 v, float s, int8_t* q8, uint16_t* qh,
-                                             int64_t elem) {
+__device__ __forceinline__ void quant_store8(uint4 v, float s, float r, bool fast, int8_t* q8,
+                                             uint16_t* qh, int64_t elem) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   int q[8];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    q[2 * j] = quant1(__uint_as_float(w[j] << 16), s);
-    q[2 * j + 1] = quant1(__uint_as_float(w[j] & 0xFFFF0000u), s);
+    q[2 * j] = quant1_fast(__uint_as_float(w[j] << 16), s, r, fast);
+    q[2 * j + 1] = quant1_fast(__uint_as_float(w[j] & 0xFFFF0000u), s, r, fast);
   }
   if constexpr (kQ8) {
     uint2 o;
@@ -107,10 +125,12 @@ quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int K, int8_t* __res
 #pragma unroll
     for (int o = 16; o; o >>= 1) mbits = max(mbits, __shfl_xor_sync(0xFFFFFFFFu, mbits, o));
     const float s = row_scale(__uint_as_float(mbits << 16));
+    const float r = __frcp_rn(s);
+    const bool fast = s >= 0x1p-120f;
 #pragma unroll
     for (int i = 0; i < kRegVecs; ++i) {
       const int j = lane + 32 * i;
-      if (j < nvec) quant_store8<kQ8, kF16>(v[i], s, q8, qh, base + 8 * int64_t(j));
+      if (j < nvec) quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh, base + 8 * int64_t(j));
     }
     if (lane == 0) scale[row] = s;
   } else {
@@ -125,8 +145,10 @@ quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int K, int8_t* __res
 #pragma unroll
     for (int o = 16; o; o >>= 1) mbits = max(mbits, __shfl_xor_sync(0xFFFFFFFFu, mbits, o));
     const float s = row_scale(__uint_as_float(mbits << 16));
+    const float r = __frcp_rn(s);
+    const bool fast = s >= 0x1p-120f;
     for (j = lane; j < nvec; j += 32)
-      quant_store8<kQ8, kF16>(ld_stream(xr + j), s, q8, qh, base + 8 * int64_t(j));
+      quant_store8<kQ8, kF16>(ld_stream(xr + j), s, r, fast, q8, qh, base + 8 * int64_t(j));
     if (lane == 0) scale[row] = s;
   }
 }
