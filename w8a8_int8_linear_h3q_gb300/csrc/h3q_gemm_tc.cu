@@ -20,20 +20,20 @@
 //     accumulates into a fresh FP32 TMEM accumulator, and the epilogue warps
 //     fold every chunk into an INT32 running sum kept in TMEM (cvt.rni of an
 //     integer-valued FP32 is exact).  The result is the exact INT32 product.
-// The weights stay INT8 in memory (no dequantisation); converter warps turn
-// each INT8 k-block into FP16 in registers and store it into TMEM, where the
-// MMA reads it as its A operand.  The activations arrive already FP16-coded
-// (written by the activation quantiser) through TMA into 128-byte-swizzled
-// shared memory: the B operand.  Shared memory therefore carries only the
-// activation tiles, and TMEM carries the weights, both accumulators and the
-// running sum.
+// The weights stay INT8 in memory (no dequantisation).  TMA brings each INT8
+// weight k-block into a 64-byte-swizzled shared-memory ring; converter warps
+// read their row from it, turn it into FP16 in registers and store it into
+// TMEM, where the MMA reads it as its A operand.  The activations arrive
+// already FP16-coded (written by the activation quantiser) through TMA into
+// 128-byte-swizzled shared memory: the B operand.  TMEM carries the FP16
+// weights, both accumulators and the running sum.
 //
 // Tile: 128 output channels (MMA M, TMEM lanes) x 128 tokens (MMA N).
 // Persistent CTAs, one per SM, walk the tiles in groups of 16 token blocks so
 // that the concurrently running tiles share weight and activation tiles in L2.
 //
 // Warp roles (576 threads):
-//   warp 0      TMA producer (activation tiles, 8-stage ring)
+//   warp 0      TMA producer (activation and INT8 weight tiles, 8-stage rings)
 //   warp 1      TMEM allocator and MMA issuer (one thread)
 //   warps 2-9   converters: INT8 weights -> FP16 -> TMEM A stages (4-stage ring)
 //   warps 10-17 epilogue: chunk drains into the INT32 running sum, then
@@ -56,13 +56,15 @@ constexpr int BM = 128;                 // channels per tile
 constexpr int BN = 128;                 // tokens per tile
 constexpr int BK = 64;                  // K per k-block (128 bytes of FP16)
 constexpr int MAX_KB_PER_CHUNK = 16;    // 1024 K: exact FP32 chunk
-constexpr int B_STAGES = 8;
-constexpr int A_STAGES = 4;
+constexpr int B_STAGES = 8;             // activation tiles (SMEM, TMA)
+constexpr int W_STAGES = 8;             // INT8 weight tiles (SMEM, TMA)
+constexpr int A_STAGES = 4;             // FP16 weight tiles (TMEM, converters)
 constexpr int GROUP_M = 16;             // token blocks per raster group
 constexpr int NUM_CONV_WARPS = 8;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int THREADS = 32 * (2 + NUM_CONV_WARPS + NUM_EPI_WARPS);
 constexpr int B_STAGE_BYTES = BN * BK * 2;                 // 16 KB
+constexpr int W_STAGE_BYTES = BM * BK;                     // 8 KB
 constexpr uint32_t TM_D = 0;            // accumulators: cols 0-127 and 128-255
 constexpr uint32_t TM_RS = 256;         // INT32 running sum: cols 256-383
 constexpr uint32_t TM_A = 384;          // A stages: 4 x 32 cols
@@ -75,8 +77,11 @@ constexpr uint32_t ERR_PRODUCER = 1u, ERR_MMA = 2u, ERR_CONVERT = 4u, ERR_EPILOG
 
 struct __align__(1024) Smem {
   uint8_t b[B_STAGES][B_STAGE_BYTES];
+  uint8_t w[W_STAGES][W_STAGE_BYTES];   // 64-byte rows, 64-byte swizzle
   uint64_t full_b[B_STAGES];
   uint64_t empty_b[B_STAGES];
+  uint64_t full_w[W_STAGES];
+  uint64_t empty_w[W_STAGES];
   uint64_t full_a[A_STAGES];
   uint64_t empty_a[A_STAGES];
   uint64_t dfull[2];
@@ -107,7 +112,7 @@ __device__ __forceinline__ void tile_coords(const Shape& s, int t, int& mb, int&
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const int8_t* __restrict__ wq,
+gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constant__ CUtensorMap w_map,
                const float* __restrict__ sa, const float* __restrict__ sw,
                const uint16_t* __restrict__ bias, const Shape shp, uint16_t* __restrict__ Y,
                int32_t* __restrict__ ACC, uint32_t* __restrict__ err) {
@@ -121,6 +126,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const int8_t* __rest
     for (int i = 0; i < B_STAGES; ++i) {
       P::mbar_init(&sm.full_b[i], 1);
       P::mbar_init(&sm.empty_b[i], 1);
+    }
+    for (int i = 0; i < W_STAGES; ++i) {
+      P::mbar_init(&sm.full_w[i], 1);
+      P::mbar_init(&sm.empty_w[i], NUM_CONV_WARPS * 32);
     }
     for (int i = 0; i < A_STAGES; ++i) {
       P::mbar_init(&sm.full_a[i], NUM_CONV_WARPS * 32);
@@ -144,29 +153,38 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const int8_t* __rest
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       P::tma_prefetch_desc(&act_map);
-      uint32_t g = 0;
+      P::tma_prefetch_desc(&w_map);
+      uint32_t g = 0, gw = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < shp.tiles; t += gridDim.x) {
         int mb, nb;
         tile_coords(shp, t, mb, nb);
-        for (int kb = 0; kb < shp.KB; ++kb, ++g) {
+        for (int kb = 0; kb < shp.KB; ++kb) {
           const uint32_t s = g % B_STAGES, ph = (g / B_STAGES) & 1u;
+          const uint32_t sw_ = g % W_STAGES, phw = (g / W_STAGES) & 1u;
+          if (!P::mbar_wait(&sm.empty_w[sw_], phw ^ 1u, abort_flag, err, ERR_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          P::mbar_arrive_expect_tx(&sm.full_w[sw_], W_STAGE_BYTES);
+          P::tma_load_2d(P::smem_u32(sm.w[sw_]), &w_map, &sm.full_w[sw_], kb * BK, nb * BM);
+          gw = g + 1;
           if (!P::mbar_wait(&sm.empty_b[s], ph ^ 1u, abort_flag, err, ERR_PRODUCER)) {
             ok = false;
             break;
           }
           P::mbar_arrive_expect_tx(&sm.full_b[s], B_STAGE_BYTES);
           P::tma_load_2d(P::smem_u32(sm.b[s]), &act_map, &sm.full_b[s], kb * BK, mb * BN);
+          ++g;
         }
       }
       // no copy may still be landing in shared memory when the CTA exits
-      const uint32_t issued = g;
       int no_abort = 0;
-      volatile int* never = &no_abort;   // this drain does not follow the abort flag
-      for (uint32_t i = issued > B_STAGES ? issued - B_STAGES : 0; i < issued; ++i) {
-        const uint32_t s = i % B_STAGES, ph = (i / B_STAGES) & 1u;
-        P::mbar_wait(&sm.full_b[s], ph, never, err, ERR_TEARDOWN);
-      }
+      volatile int* never = &no_abort;   // these drains do not follow the abort flag
+      for (uint32_t i = g > B_STAGES ? g - B_STAGES : 0; i < g; ++i)
+        P::mbar_wait(&sm.full_b[i % B_STAGES], (i / B_STAGES) & 1u, never, err, ERR_TEARDOWN);
+      for (uint32_t i = gw > W_STAGES ? gw - W_STAGES : 0; i < gw; ++i)
+        P::mbar_wait(&sm.full_w[i % W_STAGES], (i / W_STAGES) & 1u, never, err, ERR_TEARDOWN);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -219,70 +237,37 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const int8_t* __rest
     const int half = (warp - 2) >> 2;             // which 32 bytes of a 64-byte k-block
     const int r = 32 * q + lane;                  // channel row within the tile
     const uint32_t lane_base = uint32_t(32 * q) << 16;
-    constexpr int PF = 4;                         // k-blocks of loads in flight
-    uint4 buf[PF][2];
-
-    // flat job sequence over (tile, k-block); `ld_*` runs PF jobs ahead.  The
-    // weight row of the current tile is found once per tile.
-    int ld_t = blockIdx.x, ld_kb = 0;
-    const int8_t* ld_row = wq;
-    bool ld_row_ok = false;
-    auto set_tile = [&](int t) {
-      if (t < shp.tiles) {
-        int mb, nb;
-        tile_coords(shp, t, mb, nb);
-        const int n = nb * BM + r;
-        ld_row_ok = n < shp.N;
-        ld_row = wq + int64_t(ld_row_ok ? n : 0) * shp.K + half * 32;
-      }
-    };
-    set_tile(ld_t);
-    auto load_job = [&](uint4 (&dst)[2]) {
-      dst[0] = make_uint4(0, 0, 0, 0);
-      dst[1] = make_uint4(0, 0, 0, 0);
-      if (ld_t < shp.tiles) {
-        const int k0 = ld_kb * BK + half * 32;
-        if (ld_row_ok) {
-          const int8_t* p = ld_row + ld_kb * BK;
-          if (k0 < shp.K) dst[0] = __ldg(reinterpret_cast<const uint4*>(p));
-          if (k0 + 16 < shp.K) dst[1] = __ldg(reinterpret_cast<const uint4*>(p + 16));
-        }
-        if (++ld_kb == shp.KB) {
-          ld_kb = 0;
-          ld_t += gridDim.x;
-          set_tile(ld_t);
-        }
-      }
-    };
-#pragma unroll
-    for (int p = 0; p < PF; ++p) load_job(buf[p]);
-
+    // this thread's 32 bytes of a 64-byte swizzled row: chunks 2*half, 2*half+1
+    const uint32_t row_off = uint32_t(r) * 64u;
+    const uint32_t c0 = uint32_t((2 * half) ^ ((r >> 1) & 3)) * 16u;
+    const uint32_t c1 = uint32_t((2 * half + 1) ^ ((r >> 1) & 3)) * 16u;
     uint32_t g = 0;
     bool ok = true;
     const uint32_t total = uint32_t((shp.tiles - int(blockIdx.x) + int(gridDim.x) - 1) /
                                     int(gridDim.x)) * uint32_t(shp.KB);
-    while (ok && g < total) {
-#pragma unroll
-      for (int p = 0; p < PF; ++p) {
-        if (g >= total) break;
-        uint32_t h[16];
-        const uint32_t w[8] = {buf[p][0].x, buf[p][0].y, buf[p][0].z, buf[p][0].w,
-                               buf[p][1].x, buf[p][1].y, buf[p][1].z, buf[p][1].w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) P::s8x4_to_f16x4(w[i], h[2 * i], h[2 * i + 1]);
-        load_job(buf[p]);                         // refill this slot PF jobs ahead
-        const uint32_t s = g % A_STAGES, ph = (g / A_STAGES) & 1u;
-        if (!P::mbar_wait_warp(&sm.empty_a[s], ph ^ 1u, abort_flag, err, ERR_CONVERT)) {
-          ok = false;
-          break;
-        }
-        P::tc_fence_after();
-        P::tmem_st16(tmem + lane_base + TM_A + s * 32 + half * 16, h);
-        P::tmem_wait_st();
-        P::tc_fence_before();
-        P::mbar_arrive(&sm.full_a[s]);
-        ++g;
+    for (; ok && g < total; ++g) {
+      const uint32_t sw_ = g % W_STAGES, phw = (g / W_STAGES) & 1u;
+      if (!P::mbar_wait_warp(&sm.full_w[sw_], phw, abort_flag, err, ERR_CONVERT)) {
+        ok = false;
+        break;
       }
+      const uint4 v0 = *reinterpret_cast<const uint4*>(sm.w[sw_] + row_off + c0);
+      const uint4 v1 = *reinterpret_cast<const uint4*>(sm.w[sw_] + row_off + c1);
+      P::mbar_arrive(&sm.empty_w[sw_]);           // the INT8 stage may be refilled
+      uint32_t h[16];
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) P::s8x4_to_f16x4(w[i], h[2 * i], h[2 * i + 1]);
+      const uint32_t s = g % A_STAGES, ph = (g / A_STAGES) & 1u;
+      if (!P::mbar_wait_warp(&sm.empty_a[s], ph ^ 1u, abort_flag, err, ERR_CONVERT)) {
+        ok = false;
+        break;
+      }
+      P::tc_fence_after();
+      P::tmem_st16(tmem + lane_base + TM_A + s * 32 + half * 16, h);
+      P::tmem_wait_st();
+      P::tc_fence_before();
+      P::mbar_arrive(&sm.full_a[s]);
     }
   } else {
     // ---------------- epilogue ----------------
@@ -395,6 +380,15 @@ cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
+  CUtensorMap wmap;
+  const cuuint64_t wdims[2] = {cuuint64_t(K), cuuint64_t(N)};
+  const cuuint64_t wstrides[1] = {cuuint64_t(K)};
+  const cuuint32_t wbox[2] = {BK, BM};
+  if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(qw), wdims, wstrides,
+          wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+
   Shape shp;
   shp.M = int(M);
   shp.N = int(N);
@@ -415,7 +409,7 @@ cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_
                            int(kSmemBytes));
   if (e != cudaSuccess) return e;
   const int grid = shp.tiles < sms ? shp.tiles : sms;
-  gemm_tc_kernel<<<grid, THREADS, kSmemBytes, s>>>(map, qw, sa, sw, bias, shp, y, acc, err);
+  gemm_tc_kernel<<<grid, THREADS, kSmemBytes, s>>>(map, wmap, sa, sw, bias, shp, y, acc, err);
   return cudaGetLastError();
 }
 

@@ -29,22 +29,29 @@ __device__ __forceinline__ int quant1(float x, float s) {
   return max(-kQMax, min(kQMax, q));
 }
 
-// The same value as quant1(x, s), cheaper.  With r = RN(1/s) (s normal) and
-// t = RN(x * r): t = (x/s)(1 + e1)(1 + e2), |e1|, |e2| <= 2^-24, and
-// |x/s| <= 127 (1 + 2^-23), so |t - x/s| < 1.6e-5; the FP32 quotient
-// RN(x/s) is within 2^-18 of x/s.  Hence |t - RN(x/s)| < 2^-15, and unless t
-// lies within 2^-15 of a half-integer, RN(x/s) and t round to the same
-// integer, with no tie.  Near a half-integer (about 6e-5 of inputs) the IEEE
-// division decides.  `fast` is false for rows whose scale is too small for a
-// normal reciprocal; those always divide.
-__device__ __forceinline__ int quant1_fast(float x, float s, float r, bool fast) {
+// The same integer as quant1(x, s), as an integer-valued float, cheaper.
+// With r = RN(1/s) (s normal) and t = RN(x * r): t = (x/s)(1 + e1)(1 + e2),
+// |e1|, |e2| <= 2^-24, and |x/s| <= 127 (1 + 2^-23), so |t - x/s| < 1.6e-5;
+// the FP32 quotient RN(x/s) is within 2^-18 of x/s.  Hence |t - RN(x/s)| <
+// 2^-15, and unless t lies within 2^-15 of a half-integer, RN(x/s) and t
+// round to the same integer, with no tie.  Near a half-integer (about 6e-5 of
+// inputs) the IEEE division decides.  Rounding t to an integer adds and
+// subtracts 1.5 * 2^23: for |t| < 2^22 the sum's last place is 1, so the
+// addition itself rounds t to nearest, ties to even.  `fast` is false for
+// rows whose scale is too small for a normal reciprocal; those always divide.
+// |x| <= absmax makes |q| <= 127 without a clamp.
+__device__ __forceinline__ float quant1_fast(float x, float s, float r, bool fast) {
   if (fast) {
     const float t = __fmul_rn(x, r);
-    const float n = rintf(t);
-    if (fabsf(__fsub_rn(t, n)) < 0.5f - 0x1p-15f)
-      return max(-kQMax, min(kQMax, int(n)));
+    const float n = __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f);
+    if (fabsf(__fsub_rn(t, n)) < 0.5f - 0x1p-15f) return n;
   }
-  return quant1(x, s);
+  return float(quant1(x, s));
+}
+
+// integer-valued float in [-127, 127] -> its two's-complement low byte
+__device__ __forceinline__ uint32_t f2s8_byte(float n) {
+  return uint32_t(__float_as_int(__fadd_rn(n, 12582912.0f)) - 0x4B400000) & 0xFFu;
 }
 
 __device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
@@ -55,6 +62,11 @@ __device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
 __device__ __forceinline__ uint32_t pack2_f16(int a, int b) {
   return uint32_t(__half_as_ushort(__int2half_rn(a))) |
          (uint32_t(__half_as_ushort(__int2half_rn(b))) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack2_f16f(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // |bf16| maximum of the 8 values in a 16-byte vector, as a 16-bit magnitude
@@ -76,7 +88,7 @@ template <bool kQ8, bool kF16>
 __device__ __forceinline__ void quant_store8(uint4 v, float s, float r, bool fast, int8_t* q8,
                                              uint16_t* qh, int64_t elem) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  int q[8];
+  float q[8];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     q[2 * j] = quant1_fast(__uint_as_float(w[j] << 16), s, r, fast);
@@ -84,16 +96,18 @@ __device__ __forceinline__ void quant_store8(uint4 v, float s, float r, bool fas
   }
   if constexpr (kQ8) {
     uint2 o;
-    o.x = pack4_s8(q[0], q[1], q[2], q[3]);
-    o.y = pack4_s8(q[4], q[5], q[6], q[7]);
+    o.x = f2s8_byte(q[0]) | (f2s8_byte(q[1]) << 8) | (f2s8_byte(q[2]) << 16) |
+          (f2s8_byte(q[3]) << 24);
+    o.y = f2s8_byte(q[4]) | (f2s8_byte(q[5]) << 8) | (f2s8_byte(q[6]) << 16) |
+          (f2s8_byte(q[7]) << 24);
     *reinterpret_cast<uint2*>(q8 + elem) = o;
   }
   if constexpr (kF16) {
-    uint4 o;
-    o.x = pack2_f16(q[0], q[1]);
-    o.y = pack2_f16(q[2], q[3]);
-    o.z = pack2_f16(q[4], q[5]);
-    o.w = pack2_f16(q[6], q[7]);
+    uint4 o;   // integers of magnitude <= 127 are exact in FP16
+    o.x = pack2_f16f(q[0], q[1]);
+    o.y = pack2_f16f(q[2], q[3]);
+    o.z = pack2_f16f(q[4], q[5]);
+    o.w = pack2_f16f(q[6], q[7]);
     *reinterpret_cast<uint4*>(qh + elem) = o;
   }
 }
