@@ -167,6 +167,47 @@ quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int K, int8_t* __res
   }
 }
 
+// One 256-thread block per token row, each thread holding kVPT 16-byte vectors
+// of it in registers: X is read once, a row needs only a few registers per
+// thread, so many rows are in flight per SM.
+constexpr int kRowThreads = 256;
+
+template <int kVPT, bool kQ8, bool kF16>
+__global__ void __launch_bounds__(kRowThreads)
+quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__ q8,
+                     float* __restrict__ scale, uint16_t* __restrict__ qh) {
+  __shared__ uint32_t red[kRowThreads / 32];
+  const int64_t row = blockIdx.x;
+  const int nvec = K >> 3;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + row * int64_t(K));
+  const int64_t base = row * int64_t(K);
+  uint4 v[kVPT];
+  uint32_t mbits = 0;
+#pragma unroll
+  for (int i = 0; i < kVPT; ++i) {
+    const int j = threadIdx.x + kRowThreads * i;
+    if (j < nvec) {
+      v[i] = ld_stream(xr + j);
+      mbits = max(mbits, vec_absmax_bits(v[i]));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) mbits = max(mbits, __shfl_xor_sync(0xFFFFFFFFu, mbits, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mbits;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kRowThreads / 32; ++w) mbits = max(mbits, red[w]);
+  const float s = row_scale(__uint_as_float(mbits << 16));
+  const float r = __frcp_rn(s);
+  const bool fast = s >= 0x1p-120f;
+#pragma unroll
+  for (int i = 0; i < kVPT; ++i) {
+    const int j = threadIdx.x + kRowThreads * i;
+    if (j < nvec) quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh, base + 8 * int64_t(j));
+  }
+  if (threadIdx.x == 0) scale[row] = s;
+}
+
 // Weight rows: FP32 or BF16.  Not on the timed path; plain two-pass loops,
 // plus a finiteness check (a row with Inf/NaN gets a NaN scale).
 template <typename T>
@@ -235,11 +276,26 @@ cudaError_t launch_act(const uint16_t* x, int64_t M, int K, int8_t* q, float* s,
   return cudaGetLastError();
 }
 
+template <int kVPT>
+cudaError_t launch_rows(const uint16_t* x, int64_t M, int K, int8_t* q, float* s, uint16_t* qh,
+                        cudaStream_t st) {
+  const dim3 grid(static_cast<unsigned>(M)), block(kRowThreads);
+  if (q && qh)
+    quant_act_row_kernel<kVPT, true, true><<<grid, block, 0, st>>>(x, K, q, s, qh);
+  else if (q)
+    quant_act_row_kernel<kVPT, true, false><<<grid, block, 0, st>>>(x, K, q, s, qh);
+  else
+    quant_act_row_kernel<kVPT, false, true><<<grid, block, 0, st>>>(x, K, q, s, qh);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t* q,
                                 float* scale, uint16_t* q_f16, cudaStream_t s) {
-  if (K / 8 <= 32 * kRegVecs) return launch_act<true>(x, M, int(K), q, scale, q_f16, s);
+  const int64_t nvec = K / 8;
+  if (nvec <= kRowThreads * 3) return launch_rows<3>(x, M, int(K), q, scale, q_f16, s);
+  if (nvec <= kRowThreads * 12) return launch_rows<12>(x, M, int(K), q, scale, q_f16, s);
   return launch_act<false>(x, M, int(K), q, scale, q_f16, s);
 }
 
