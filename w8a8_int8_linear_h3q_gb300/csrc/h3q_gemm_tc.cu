@@ -16,28 +16,36 @@
 //     exact in FP32, and an FP32 sum of such integers is exact while every
 //     partial sum stays within 2^24, which holds for any 1040 consecutive
 //     K terms (2^24 / 127^2 = 1040.2);
-//   - so K is cut into chunks of at most 1024 (16 k-blocks of 64), each chunk
-//     accumulates into a fresh FP32 TMEM accumulator, and the epilogue warps
-//     fold every chunk into an INT32 running sum kept in TMEM (cvt.rni of an
+//   - so K is cut into chunks of at most 1024, each chunk accumulates into a
+//     fresh FP32 TMEM accumulator, and the epilogue warps fold every chunk
+//     into INT32 running sums held in registers (cvt.rni of an
 //     integer-valued FP32 is exact).  The result is the exact INT32 product.
 // The weights stay INT8 in memory (no dequantisation).  TMA brings each INT8
 // weight k-block into a 64-byte-swizzled shared-memory ring; converter warps
 // read their row from it, turn it into FP16 in registers and store it into
 // TMEM, where the MMA reads it as its A operand.  The activations arrive
 // already FP16-coded (written by the activation quantiser) through TMA into
-// 128-byte-swizzled shared memory: the B operand.  TMEM carries the FP16
-// weights, both accumulators and the running sum.
+// 128-byte-swizzled shared memory: the B operand.
+//
+// The MMA issue path is kept bare: on this part every instruction the
+// issuing thread runs between two MMAs (a barrier wait above all) leaves the
+// tensor pipe idle.  So the MMA thread synchronises once per super-stage of
+// four k-blocks (16 MMAs): the converter warps, which see every k-block,
+// also wait for the activation tiles of their super-stage and signal a
+// single barrier when both operands are in place.
 //
 // Tile: 128 output channels (MMA M, TMEM lanes) x 128 tokens (MMA N).
 // Persistent CTAs, one per SM, walk the tiles in groups of 16 token blocks so
 // that the concurrently running tiles share weight and activation tiles in L2.
 //
-// Warp roles (576 threads):
+// Warp roles (448 threads):
 //   warp 0      TMA producer (activation and INT8 weight tiles, 8-stage rings)
 //   warp 1      TMEM allocator and MMA issuer (one thread)
-//   warps 2-9   converters: INT8 weights -> FP16 -> TMEM A stages (4-stage ring)
-//   warps 10-17 epilogue: chunk drains into the INT32 running sum, then
+//   warps 2-5   converters: INT8 weights -> FP16 -> TMEM (2 super-stages)
+//   warps 6-13  epilogue: chunk drains into INT32 running sums, then
 //               dequant + bias + BF16 (and the optional raw INT32 output)
+// TMEM: FP32 accumulators in columns 0-127 and 128-255, A super-stages in
+// 256-383 and 384-511.
 // Every wait is bounded in time; on a timeout the kernel records an error
 // word, lets every role fall through, drains its in-flight copies and MMAs,
 // frees TMEM and returns.
@@ -55,19 +63,21 @@ namespace P = ptx;
 constexpr int BM = 128;                 // channels per tile
 constexpr int BN = 128;                 // tokens per tile
 constexpr int BK = 64;                  // K per k-block (128 bytes of FP16)
-constexpr int MAX_KB_PER_CHUNK = 16;    // 1024 K: exact FP32 chunk
-constexpr int B_STAGES = 8;             // activation tiles (SMEM, TMA)
-constexpr int W_STAGES = 8;             // INT8 weight tiles (SMEM, TMA)
-constexpr int A_STAGES = 4;             // FP16 weight tiles (TMEM, converters)
+constexpr int SS = 4;                   // k-blocks per super-stage (16 MMAs)
+constexpr int MAX_SS_PER_CHUNK = 4;     // 16 k-blocks = 1024 K: exact FP32 chunk
+constexpr int B_STAGES = 8;             // activation tiles (SMEM, TMA), per k-block
+constexpr int W_STAGES = 8;             // INT8 weight tiles (SMEM, TMA), per k-block
+constexpr int A_SUPER = 2;              // FP16 weight super-stages (TMEM)
 constexpr int GROUP_M = 16;             // token blocks per raster group
-constexpr int NUM_CONV_WARPS = 8;
+constexpr int NUM_CONV_WARPS = 4;
 constexpr int NUM_EPI_WARPS = 8;
+constexpr int CONV_WARP0 = 2;
+constexpr int EPI_WARP0 = CONV_WARP0 + NUM_CONV_WARPS;
 constexpr int THREADS = 32 * (2 + NUM_CONV_WARPS + NUM_EPI_WARPS);
 constexpr int B_STAGE_BYTES = BN * BK * 2;                 // 16 KB
 constexpr int W_STAGE_BYTES = BM * BK;                     // 8 KB
 constexpr uint32_t TM_D = 0;            // accumulators: cols 0-127 and 128-255
-constexpr uint32_t TM_RS = 256;         // INT32 running sum: cols 256-383
-constexpr uint32_t TM_A = 384;          // A stages: 4 x 32 cols
+constexpr uint32_t TM_A = 256;          // A super-stages: 2 x (4 k-blocks x 32 cols)
 constexpr uint32_t TM_COLS = 512;
 constexpr uint32_t IDESC = P::idesc_f16_f32(BM, BN);
 
@@ -82,8 +92,8 @@ struct __align__(1024) Smem {
   uint64_t empty_b[B_STAGES];
   uint64_t full_w[W_STAGES];
   uint64_t empty_w[W_STAGES];
-  uint64_t full_a[A_STAGES];
-  uint64_t empty_a[A_STAGES];
+  uint64_t full_a[A_SUPER];             // A converted and B landed for a super-stage
+  uint64_t empty_a[A_SUPER];
   uint64_t dfull[2];
   uint64_t dempty[2];
   uint64_t mma_done;
@@ -95,8 +105,9 @@ constexpr size_t kSmemBytes = sizeof(Smem) + 1024;   // + slack for 1024-byte al
 struct Shape {
   int M, N, K;
   int KB;             // k-blocks
+  int NSS;            // super-stages per tile
   int nchunks;        // exact-FP32 chunks per tile
-  int kpc;            // k-blocks per chunk (last may be shorter)
+  int sspc;           // super-stages per chunk (the last chunk may have fewer)
   int mt, nt;         // token blocks, channel blocks
   int tiles;
 };
@@ -112,10 +123,10 @@ __device__ __forceinline__ void tile_coords(const Shape& s, int t, int& mb, int&
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constant__ CUtensorMap w_map,
-               const float* __restrict__ sa, const float* __restrict__ sw,
-               const uint16_t* __restrict__ bias, const Shape shp, uint16_t* __restrict__ Y,
-               int32_t* __restrict__ ACC, uint32_t* __restrict__ err) {
+gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
+               const __grid_constant__ CUtensorMap w_map, const float* __restrict__ sa,
+               const float* __restrict__ sw, const uint16_t* __restrict__ bias, const Shape shp,
+               uint16_t* __restrict__ Y, int32_t* __restrict__ ACC, uint32_t* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~uintptr_t(1023));
@@ -131,7 +142,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constan
       P::mbar_init(&sm.full_w[i], 1);
       P::mbar_init(&sm.empty_w[i], NUM_CONV_WARPS * 32);
     }
-    for (int i = 0; i < A_STAGES; ++i) {
+    for (int i = 0; i < A_SUPER; ++i) {
       P::mbar_init(&sm.full_a[i], NUM_CONV_WARPS * 32);
       P::mbar_init(&sm.empty_a[i], 1);
     }
@@ -150,7 +161,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constan
   const uint32_t tmem = sm.tmem_base;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer: per k-block, weights then activations ----------------
     if (lane == 0) {
       P::tma_prefetch_desc(&act_map);
       P::tma_prefetch_desc(&w_map);
@@ -188,37 +199,39 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constan
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+    // ---------------- MMA issuer: one wait per 16 MMAs ----------------
     if (lane == 0) {
-      uint32_t g = 0, gc = 0;
+      uint32_t g = 0, gs = 0, gc = 0;     // k-block, super-stage and chunk counters
       bool ok = true;
       for (int t = blockIdx.x; ok && t < shp.tiles; t += gridDim.x) {
         for (int c = 0; ok && c < shp.nchunks; ++c, ++gc) {
-          const int kb0 = c * shp.kpc, kb1 = min(shp.KB, kb0 + shp.kpc);
+          const int ss0 = c * shp.sspc, ss1 = min(shp.NSS, ss0 + shp.sspc);
           const uint32_t buf = gc & 1u;
           if (!P::mbar_wait(&sm.dempty[buf], ((gc >> 1) & 1u) ^ 1u, abort_flag, err, ERR_MMA)) {
             ok = false;
             break;
           }
-          P::tc_fence_after();
           const uint32_t d_tmem = tmem + TM_D + buf * BN;
-          for (int kb = kb0; kb < kb1; ++kb, ++g) {
-            const uint32_t sb = g % B_STAGES, pb = (g / B_STAGES) & 1u;
-            const uint32_t sa_ = g % A_STAGES, pa = (g / A_STAGES) & 1u;
-            if (!P::mbar_wait(&sm.full_b[sb], pb, abort_flag, err, ERR_MMA) ||
-                !P::mbar_wait(&sm.full_a[sa_], pa, abort_flag, err, ERR_MMA)) {
+          for (int ss = ss0; ss < ss1; ++ss, ++gs) {
+            const uint32_t sa_ = gs % A_SUPER;
+            if (!P::mbar_wait(&sm.full_a[sa_], (gs / A_SUPER) & 1u, abort_flag, err, ERR_MMA)) {
               ok = false;
               break;
             }
             P::tc_fence_after();
-            const uint64_t bdesc = P::smem_desc_sw128(P::smem_u32(sm.b[sb]));
-            const uint32_t a_tmem = tmem + TM_A + sa_ * 32;
+            const uint32_t a_tmem = tmem + TM_A + sa_ * (SS * 32);
+            const int nkb = min(SS, shp.KB - ss * SS);
+            for (int j = 0; j < nkb; ++j) {
+              const uint32_t sb = (g + uint32_t(j)) % B_STAGES;
+              const uint64_t bdesc = P::smem_desc_sw128(P::smem_u32(sm.b[sb]));
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              P::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc + uint64_t(kk * 2), IDESC,
-                            (kb > kb0 || kk > 0) ? 1u : 0u);
-            P::mma_commit(&sm.empty_b[sb]);
+              for (int kk = 0; kk < BK / 16; ++kk)
+                P::mma_f16_ts(d_tmem, a_tmem + j * 32 + kk * 8, bdesc + uint64_t(kk * 2), IDESC,
+                              (ss > ss0 || j > 0 || kk > 0) ? 1u : 0u);
+            }
+            for (int j = 0; j < nkb; ++j) P::mma_commit(&sm.empty_b[(g + uint32_t(j)) % B_STAGES]);
             P::mma_commit(&sm.empty_a[sa_]);
+            g += uint32_t(nkb);
           }
           if (!ok) break;
           P::mma_commit(&sm.dfull[buf]);
@@ -231,48 +244,64 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constan
       P::mbar_wait(&sm.mma_done, 0, never, err, ERR_TEARDOWN);
     }
     __syncwarp();
-  } else if (warp < 2 + NUM_CONV_WARPS) {
+  } else if (warp < EPI_WARP0) {
     // ---------------- converters: INT8 weights -> FP16 -> TMEM ----------------
     const int q = warp & 3;                       // TMEM lane quarter of this warp
-    const int half = (warp - 2) >> 2;             // which 32 bytes of a 64-byte k-block
     const int r = 32 * q + lane;                  // channel row within the tile
     const uint32_t lane_base = uint32_t(32 * q) << 16;
-    // this thread's 32 bytes of a 64-byte swizzled row: chunks 2*half, 2*half+1
-    const uint32_t row_off = uint32_t(r) * 64u;
-    const uint32_t c0 = uint32_t((2 * half) ^ ((r >> 1) & 3)) * 16u;
-    const uint32_t c1 = uint32_t((2 * half + 1) ^ ((r >> 1) & 3)) * 16u;
-    uint32_t g = 0;
+    // the four 16-byte chunks of this row in the 64-byte-swizzled INT8 tile
+    const uint32_t row_off = uint32_t(r) * 64u, xr = uint32_t((r >> 1) & 3);
+    uint32_t g = 0, gs = 0;
     bool ok = true;
-    const uint32_t total = uint32_t((shp.tiles - int(blockIdx.x) + int(gridDim.x) - 1) /
-                                    int(gridDim.x)) * uint32_t(shp.KB);
-    for (; ok && g < total; ++g) {
-      const uint32_t sw_ = g % W_STAGES, phw = (g / W_STAGES) & 1u;
-      if (!P::mbar_wait_warp(&sm.full_w[sw_], phw, abort_flag, err, ERR_CONVERT)) {
-        ok = false;
-        break;
-      }
-      const uint4 v0 = *reinterpret_cast<const uint4*>(sm.w[sw_] + row_off + c0);
-      const uint4 v1 = *reinterpret_cast<const uint4*>(sm.w[sw_] + row_off + c1);
-      P::mbar_arrive(&sm.empty_w[sw_]);           // the INT8 stage may be refilled
-      uint32_t h[16];
-      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    for (int t = blockIdx.x; ok && t < shp.tiles; t += gridDim.x) {
+      for (int ss = 0; ok && ss < shp.NSS; ++ss, ++gs) {
+        const uint32_t sa_ = gs % A_SUPER;
+        const int nkb = min(SS, shp.KB - ss * SS);
+        for (int j = 0; j < nkb; ++j, ++g) {
+          const uint32_t sw_ = g % W_STAGES;
+          if (!P::mbar_wait_warp(&sm.full_w[sw_], (g / W_STAGES) & 1u, abort_flag, err,
+                                 ERR_CONVERT)) {
+            ok = false;
+            break;
+          }
+          uint4 v[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) P::s8x4_to_f16x4(w[i], h[2 * i], h[2 * i + 1]);
-      const uint32_t s = g % A_STAGES, ph = (g / A_STAGES) & 1u;
-      if (!P::mbar_wait_warp(&sm.empty_a[s], ph ^ 1u, abort_flag, err, ERR_CONVERT)) {
-        ok = false;
-        break;
+          for (int i = 0; i < 4; ++i)
+            v[i] = *reinterpret_cast<const uint4*>(sm.w[sw_] + row_off + ((uint32_t(i) ^ xr) << 4));
+          P::mbar_arrive(&sm.empty_w[sw_]);       // the INT8 stage may be refilled
+          uint32_t h[32];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            P::s8x4_to_f16x4(v[i].x, h[8 * i + 0], h[8 * i + 1]);
+            P::s8x4_to_f16x4(v[i].y, h[8 * i + 2], h[8 * i + 3]);
+            P::s8x4_to_f16x4(v[i].z, h[8 * i + 4], h[8 * i + 5]);
+            P::s8x4_to_f16x4(v[i].w, h[8 * i + 6], h[8 * i + 7]);
+          }
+          if (j == 0 &&
+              !P::mbar_wait_warp(&sm.empty_a[sa_], ((gs / A_SUPER) & 1u) ^ 1u, abort_flag, err,
+                                 ERR_CONVERT)) {
+            ok = false;
+            break;
+          }
+          P::tc_fence_after();
+          P::tmem_st32(tmem + lane_base + TM_A + sa_ * (SS * 32) + uint32_t(j) * 32, h);
+          // forward the readiness of this k-block's activation tile to the MMA thread
+          if (!P::mbar_wait_warp(&sm.full_b[g % B_STAGES], (g / B_STAGES) & 1u, abort_flag, err,
+                                 ERR_CONVERT)) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
+        P::tmem_wait_st();
+        P::tc_fence_before();
+        P::mbar_arrive(&sm.full_a[sa_]);
       }
-      P::tc_fence_after();
-      P::tmem_st16(tmem + lane_base + TM_A + s * 32 + half * 16, h);
-      P::tmem_wait_st();
-      P::tc_fence_before();
-      P::mbar_arrive(&sm.full_a[s]);
     }
   } else {
     // ---------------- epilogue ----------------
     const int q = warp & 3;
-    const int half = (warp - 2 - NUM_CONV_WARPS) >> 2;   // token columns [64*half, +64)
+    const int half = (warp - EPI_WARP0) >> 2;     // token columns [64*half, +64)
     const uint32_t lane_base = uint32_t(32 * q) << 16;
     uint32_t gc = 0;
     bool ok = true;
@@ -281,8 +310,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constan
       tile_coords(shp, t, mb, nb);
       const int n = nb * BM + 32 * q + lane;
       const bool n_ok = n < shp.N;
-      const float swn = n_ok ? sw[n] : 0.f;
-      const float bn = (n_ok && bias) ? bf16_bits_to_float(bias[n]) : 0.f;
+      int rs[64];                                 // exact INT32 running sums
+#pragma unroll
+      for (int j = 0; j < 64; ++j) rs[j] = 0;
       for (int c = 0; c < shp.nchunks; ++c, ++gc) {
         const uint32_t buf = gc & 1u;
         if (!P::mbar_wait_warp(&sm.dfull[buf], (gc >> 1) & 1u, abort_flag, err, ERR_EPILOGUE)) {
@@ -292,31 +322,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constan
         P::tc_fence_after();
 #pragma unroll
         for (int blk = 0; blk < 2; ++blk) {
-          const uint32_t col = 64 * half + 32 * blk;
-          uint32_t d[32], s[32];
-          P::tmem_ld32(tmem + lane_base + TM_D + buf * BN + col, d);
-          if (c > 0) P::tmem_ld32(tmem + lane_base + TM_RS + col, s);
+          uint32_t d[32];
+          P::tmem_ld32(tmem + lane_base + TM_D + buf * BN + 64 * half + 32 * blk, d);
           P::tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int v = __float2int_rn(__uint_as_float(d[j]));
-            s[j] = uint32_t((c > 0 ? int(s[j]) : 0) + v);
-          }
-          P::tmem_st32(tmem + lane_base + TM_RS + col, s);
+          for (int j = 0; j < 32; ++j) rs[32 * blk + j] += __float2int_rn(__uint_as_float(d[j]));
         }
-        P::tmem_wait_st();
         P::tc_fence_before();
         P::mbar_arrive(&sm.dempty[buf]);
       }
       if (!ok) break;
       // final: dequantise the exact INT32 sums of this tile
-#pragma unroll 1
+      const float swn = n_ok ? sw[n] : 0.f;
+      const float bn = (n_ok && bias) ? bf16_bits_to_float(bias[n]) : 0.f;
+#pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
-        const int col = 64 * half + 32 * blk;
-        const int m0 = mb * BN + col;
-        uint32_t s[32];
-        P::tmem_ld32(tmem + lane_base + TM_RS + uint32_t(col), s);
-        P::tmem_wait_ld();
+        const int m0 = mb * BN + 64 * half + 32 * blk;
         const float sa_l = (m0 + lane < shp.M) ? sa[m0 + lane] : 0.f;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -324,8 +345,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constan
           const int m = m0 + j;
           if (n_ok && m < shp.M) {
             const int64_t off = int64_t(m) * shp.N + n;
-            if (ACC) ACC[off] = int32_t(s[j]);
-            if (Y) Y[off] = float_to_bf16_bits(epilogue_value(int(s[j]), saj, swn, bn));
+            if (ACC) ACC[off] = rs[32 * blk + j];
+            if (Y) Y[off] = float_to_bf16_bits(epilogue_value(rs[32 * blk + j], saj, swn, bn));
           }
         }
       }
@@ -394,8 +415,9 @@ cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_
   shp.N = int(N);
   shp.K = int(K);
   shp.KB = int((K + BK - 1) / BK);
-  shp.nchunks = (shp.KB + MAX_KB_PER_CHUNK - 1) / MAX_KB_PER_CHUNK;
-  shp.kpc = (shp.KB + shp.nchunks - 1) / shp.nchunks;
+  shp.NSS = (shp.KB + SS - 1) / SS;
+  shp.nchunks = (shp.NSS + MAX_SS_PER_CHUNK - 1) / MAX_SS_PER_CHUNK;
+  shp.sspc = (shp.NSS + shp.nchunks - 1) / shp.nchunks;
   shp.mt = int((M + BN - 1) / BN);
   shp.nt = int((N + BM - 1) / BM);
   shp.tiles = shp.mt * shp.nt;
