@@ -35,8 +35,13 @@
 // single barrier when both operands are in place.
 //
 // Tile: 128 output channels (MMA M, TMEM lanes) x 128 tokens (MMA N).
-// Persistent CTAs, one per SM, walk the tiles in groups of 16 token blocks so
-// that the concurrently running tiles share weight and activation tiles in L2.
+// CTAs run in clusters of two that take adjacent channel blocks of the same
+// token block: each loads half of the activation tile and multicasts it to
+// both, which halves the activation bytes fetched from L2, and a k-block's
+// activation stage is refilled only after both CTAs' MMAs have finished with
+// it (their completions are multicast to both producers).  Persistent
+// clusters walk the cluster tiles in groups of 16 token blocks so that the
+// concurrently running tiles share weight and activation tiles in L2.
 //
 // Warp roles (448 threads):
 //   warp 0      TMA producer (activation and INT8 weight tiles, 8-stage rings)
@@ -69,6 +74,8 @@ constexpr int B_STAGES = 8;             // activation tiles (SMEM, TMA), per k-b
 constexpr int W_STAGES = 8;             // INT8 weight tiles (SMEM, TMA), per k-block
 constexpr int A_SUPER = 2;              // FP16 weight super-stages (TMEM)
 constexpr int GROUP_M = 16;             // token blocks per raster group
+constexpr int CLUSTER = 2;              // CTAs sharing one activation tile (multicast)
+constexpr uint16_t CLUSTER_MASK = (1u << CLUSTER) - 1;
 constexpr int NUM_CONV_WARPS = 4;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int CONV_WARP0 = 2;
@@ -109,17 +116,21 @@ struct Shape {
   int nchunks;        // exact-FP32 chunks per tile
   int sspc;           // super-stages per chunk (the last chunk may have fewer)
   int mt, nt;         // token blocks, channel blocks
-  int tiles;
+  int ntc;            // channel-block groups of CLUSTER
+  int tiles;          // cluster tiles: mt * ntc
 };
 
-__device__ __forceinline__ void tile_coords(const Shape& s, int t, int& mb, int& nb) {
-  const int per_group = GROUP_M * s.nt;
+// Cluster tile t -> token block mb and the channel block nb of CTA `rank`
+// (nb >= nt for the spare CTA of an odd channel-block count).
+__device__ __forceinline__ void tile_coords(const Shape& s, int t, uint32_t rank, int& mb,
+                                            int& nb) {
+  const int per_group = GROUP_M * s.ntc;
   const int g = t / per_group;
   const int first_m = g * GROUP_M;
   const int gm = min(GROUP_M, s.mt - first_m);
   const int r = t - g * per_group;
   mb = first_m + r % gm;
-  nb = r / gm;
+  nb = (r / gm) * CLUSTER + int(rank);
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -136,7 +147,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_STAGES; ++i) {
       P::mbar_init(&sm.full_b[i], 1);
-      P::mbar_init(&sm.empty_b[i], 1);
+      P::mbar_init(&sm.empty_b[i], CLUSTER);      // both CTAs' MMAs are done with it
     }
     for (int i = 0; i < W_STAGES; ++i) {
       P::mbar_init(&sm.full_w[i], 1);
@@ -157,8 +168,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
   if (warp == 1) P::tmem_alloc(&sm.tmem_base, TM_COLS);
   P::tc_fence_before();
   __syncthreads();
+  P::cluster_sync();                              // peers' barriers exist before multicasts
   P::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  const uint32_t rank = P::cluster_rank();
+  const int cid = int(P::cluster_id_x()), ncl = int(P::num_clusters_x());
 
   if (warp == 0) {
     // ---------------- TMA producer: per k-block, weights then activations ----------------
@@ -167,9 +181,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
       P::tma_prefetch_desc(&w_map);
       uint32_t g = 0, gw = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < shp.tiles; t += gridDim.x) {
+      for (int t = cid; ok && t < shp.tiles; t += ncl) {
         int mb, nb;
-        tile_coords(shp, t, mb, nb);
+        tile_coords(shp, t, rank, mb, nb);
         for (int kb = 0; kb < shp.KB; ++kb) {
           const uint32_t s = g % B_STAGES, ph = (g / B_STAGES) & 1u;
           const uint32_t sw_ = g % W_STAGES, phw = (g / W_STAGES) & 1u;
@@ -178,14 +192,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
             break;
           }
           P::mbar_arrive_expect_tx(&sm.full_w[sw_], W_STAGE_BYTES);
-          P::tma_load_2d(P::smem_u32(sm.w[sw_]), &w_map, &sm.full_w[sw_], kb * BK, nb * BM);
+          P::tma_load_2d(P::smem_u32(sm.w[sw_]), &w_map, &sm.full_w[sw_], kb * BK,
+                         min(nb, shp.nt - 1) * BM);
           gw = g + 1;
           if (!P::mbar_wait(&sm.empty_b[s], ph ^ 1u, abort_flag, err, ERR_PRODUCER)) {
             ok = false;
             break;
           }
+          // the whole tile lands here: this CTA's half and the peer's
           P::mbar_arrive_expect_tx(&sm.full_b[s], B_STAGE_BYTES);
-          P::tma_load_2d(P::smem_u32(sm.b[s]), &act_map, &sm.full_b[s], kb * BK, mb * BN);
+          P::tma_load_2d_mc(P::smem_u32(sm.b[s]) + rank * (B_STAGE_BYTES / CLUSTER), &act_map,
+                            &sm.full_b[s], kb * BK, mb * BN + int(rank) * (BN / CLUSTER),
+                            CLUSTER_MASK);
           ++g;
         }
       }
@@ -203,7 +221,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
     if (lane == 0) {
       uint32_t g = 0, gs = 0, gc = 0;     // k-block, super-stage and chunk counters
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < shp.tiles; t += gridDim.x) {
+      for (int t = cid; ok && t < shp.tiles; t += ncl) {
         for (int c = 0; ok && c < shp.nchunks; ++c, ++gc) {
           const int ss0 = c * shp.sspc, ss1 = min(shp.NSS, ss0 + shp.sspc);
           const uint32_t buf = gc & 1u;
@@ -229,7 +247,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
                 P::mma_f16_ts(d_tmem, a_tmem + j * 32 + kk * 8, bdesc + uint64_t(kk * 2), IDESC,
                               (ss > ss0 || j > 0 || kk > 0) ? 1u : 0u);
             }
-            for (int j = 0; j < nkb; ++j) P::mma_commit(&sm.empty_b[(g + uint32_t(j)) % B_STAGES]);
+            for (int j = 0; j < nkb; ++j)
+              P::mma_commit_mc(&sm.empty_b[(g + uint32_t(j)) % B_STAGES], CLUSTER_MASK);
             P::mma_commit(&sm.empty_a[sa_]);
             g += uint32_t(nkb);
           }
@@ -253,7 +272,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
     const uint32_t row_off = uint32_t(r) * 64u, xr = uint32_t((r >> 1) & 3);
     uint32_t g = 0, gs = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < shp.tiles; t += gridDim.x) {
+    for (int t = cid; ok && t < shp.tiles; t += ncl) {
       for (int ss = 0; ok && ss < shp.NSS; ++ss, ++gs) {
         const uint32_t sa_ = gs % A_SUPER;
         const int nkb = min(SS, shp.KB - ss * SS);
@@ -305,9 +324,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
     const uint32_t lane_base = uint32_t(32 * q) << 16;
     uint32_t gc = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < shp.tiles; t += gridDim.x) {
+    for (int t = cid; ok && t < shp.tiles; t += ncl) {
       int mb, nb;
-      tile_coords(shp, t, mb, nb);
+      tile_coords(shp, t, rank, mb, nb);
       const int n = nb * BM + 32 * q + lane;
       const bool n_ok = n < shp.N;
       int rs[64];                                 // exact INT32 running sums
@@ -359,6 +378,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
     P::tc_fence_after();
     P::tmem_dealloc(tmem, TM_COLS);
   }
+  P::cluster_sync();                              // no peer still signals or writes here
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
@@ -394,7 +414,7 @@ cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_
   CUtensorMap map;
   const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(M)};
   const cuuint64_t strides[1] = {cuuint64_t(K) * 2u};
-  const cuuint32_t box[2] = {BK, BN};
+  const cuuint32_t box[2] = {BK, BN / CLUSTER};      // each CTA loads half the tile
   const cuuint32_t estr[2] = {1, 1};
   if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(act_f16), dims,
           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -420,7 +440,8 @@ cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_
   shp.sspc = (shp.NSS + shp.nchunks - 1) / shp.nchunks;
   shp.mt = int((M + BN - 1) / BN);
   shp.nt = int((N + BM - 1) / BM);
-  shp.tiles = shp.mt * shp.nt;
+  shp.ntc = (shp.nt + CLUSTER - 1) / CLUSTER;
+  shp.tiles = shp.mt * shp.ntc;
 
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -430,9 +451,20 @@ cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_
   e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(kSmemBytes));
   if (e != cudaSuccess) return e;
-  const int grid = shp.tiles < sms ? shp.tiles : sms;
-  gemm_tc_kernel<<<grid, THREADS, kSmemBytes, s>>>(map, wmap, sa, sw, bias, shp, y, acc, err);
-  return cudaGetLastError();
+  const int clusters = shp.tiles < sms / CLUSTER ? shp.tiles : sms / CLUSTER;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(clusters * CLUSTER));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CLUSTER;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, map, wmap, sa, sw, bias, shp, y, acc, err);
 }
 
 }  // namespace h3q
