@@ -28,11 +28,12 @@
 // 128-byte-swizzled shared memory: the B operand.
 //
 // The MMA issue path is kept bare: on this part every instruction the
-// issuing thread runs between two MMAs (a barrier wait above all) leaves the
+// issuing thread runs between two MMAs (a barrier wait, a commit) leaves the
 // tensor pipe idle.  So the MMA thread synchronises once per super-stage of
-// four k-blocks (16 MMAs): the converter warps, which see every k-block,
-// also wait for the activation tiles of their super-stage and signal a
-// single barrier when both operands are in place.
+// four k-blocks (16 MMAs): one wait on a barrier that the converter warps
+// complete when both operands are in place (they also wait for the
+// activation tiles), and one commit that frees the super-stage's activation
+// and weight slots at once.
 //
 // Tile: 128 output channels (MMA M, TMEM lanes) x 128 tokens (MMA N).
 // CTAs run in clusters of two that take adjacent channel blocks of the same
@@ -44,7 +45,8 @@
 // concurrently running tiles share weight and activation tiles in L2.
 //
 // Warp roles (448 threads):
-//   warp 0      TMA producer (activation and INT8 weight tiles, 8-stage rings)
+//   warp 0      TMA producer (INT8 weight tiles per k-block, 8-stage ring;
+//               activation tiles per super-stage, 2 slots)
 //   warp 1      TMEM allocator and MMA issuer (one thread)
 //   warps 2-5   converters: INT8 weights -> FP16 -> TMEM (2 super-stages)
 //   warps 6-13  epilogue: chunk drains into INT32 running sums, then
@@ -70,9 +72,8 @@ constexpr int BN = 128;                 // tokens per tile
 constexpr int BK = 64;                  // K per k-block (128 bytes of FP16)
 constexpr int SS = 4;                   // k-blocks per super-stage (16 MMAs)
 constexpr int MAX_SS_PER_CHUNK = 4;     // 16 k-blocks = 1024 K: exact FP32 chunk
-constexpr int B_STAGES = 8;             // activation tiles (SMEM, TMA), per k-block
 constexpr int W_STAGES = 8;             // INT8 weight tiles (SMEM, TMA), per k-block
-constexpr int A_SUPER = 2;              // FP16 weight super-stages (TMEM)
+constexpr int SLOTS = 2;                // super-stage slots: activations (SMEM), FP16 weights (TMEM)
 constexpr int GROUP_M = 16;             // token blocks per raster group
 constexpr int CLUSTER = 2;              // CTAs sharing one activation tile (multicast)
 constexpr uint16_t CLUSTER_MASK = (1u << CLUSTER) - 1;
@@ -93,14 +94,13 @@ constexpr uint32_t ERR_PRODUCER = 1u, ERR_MMA = 2u, ERR_CONVERT = 4u, ERR_EPILOG
                    ERR_TEARDOWN = 16u;
 
 struct __align__(1024) Smem {
-  uint8_t b[B_STAGES][B_STAGE_BYTES];
+  uint8_t b[SLOTS][SS][B_STAGE_BYTES];  // activation tiles of a super-stage slot
   uint8_t w[W_STAGES][W_STAGE_BYTES];   // 64-byte rows, 64-byte swizzle
-  uint64_t full_b[B_STAGES];
-  uint64_t empty_b[B_STAGES];
+  uint64_t full_b[SLOTS];               // a slot's activation tiles have landed
   uint64_t full_w[W_STAGES];
   uint64_t empty_w[W_STAGES];
-  uint64_t full_a[A_SUPER];             // A converted and B landed for a super-stage
-  uint64_t empty_a[A_SUPER];
+  uint64_t full_a[SLOTS];               // A converted and B landed for a super-stage
+  uint64_t empty_s[SLOTS];              // both CTAs' MMAs are done with a slot
   uint64_t dfull[2];
   uint64_t dempty[2];
   uint64_t mma_done;
@@ -145,17 +145,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < B_STAGES; ++i) {
-      P::mbar_init(&sm.full_b[i], 1);
-      P::mbar_init(&sm.empty_b[i], CLUSTER);      // both CTAs' MMAs are done with it
-    }
     for (int i = 0; i < W_STAGES; ++i) {
       P::mbar_init(&sm.full_w[i], 1);
       P::mbar_init(&sm.empty_w[i], NUM_CONV_WARPS * 32);
     }
-    for (int i = 0; i < A_SUPER; ++i) {
+    for (int i = 0; i < SLOTS; ++i) {
+      P::mbar_init(&sm.full_b[i], 1);
       P::mbar_init(&sm.full_a[i], NUM_CONV_WARPS * 32);
-      P::mbar_init(&sm.empty_a[i], 1);
+      P::mbar_init(&sm.empty_s[i], CLUSTER);      // one multicast commit per CTA
     }
     for (int i = 0; i < 2; ++i) {
       P::mbar_init(&sm.dfull[i], 1);
@@ -175,51 +172,57 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
   const int cid = int(P::cluster_id_x()), ncl = int(P::num_clusters_x());
 
   if (warp == 0) {
-    // ---------------- TMA producer: per k-block, weights then activations ----------------
+    // ---------------- TMA producer ----------------
     if (lane == 0) {
       P::tma_prefetch_desc(&act_map);
       P::tma_prefetch_desc(&w_map);
-      uint32_t g = 0, gw = 0;
+      uint32_t g = 0, gw = 0, gs = 0, gb = 0;     // k-block, weight issues, super-stage
       bool ok = true;
       for (int t = cid; ok && t < shp.tiles; t += ncl) {
         int mb, nb;
         tile_coords(shp, t, rank, mb, nb);
-        for (int kb = 0; kb < shp.KB; ++kb) {
-          const uint32_t s = g % B_STAGES, ph = (g / B_STAGES) & 1u;
-          const uint32_t sw_ = g % W_STAGES, phw = (g / W_STAGES) & 1u;
-          if (!P::mbar_wait(&sm.empty_w[sw_], phw ^ 1u, abort_flag, err, ERR_PRODUCER)) {
+        for (int ss = 0; ok && ss < shp.NSS; ++ss, ++gs) {
+          const uint32_t slot = gs % SLOTS;
+          const int nkb = min(SS, shp.KB - ss * SS);
+          // the slot is free once both CTAs' MMAs finished its previous use
+          if (!P::mbar_wait(&sm.empty_s[slot], ((gs / SLOTS) & 1u) ^ 1u, abort_flag, err,
+                            ERR_PRODUCER)) {
             ok = false;
             break;
           }
-          P::mbar_arrive_expect_tx(&sm.full_w[sw_], W_STAGE_BYTES);
-          P::tma_load_2d(P::smem_u32(sm.w[sw_]), &w_map, &sm.full_w[sw_], kb * BK,
-                         min(nb, shp.nt - 1) * BM);
-          gw = g + 1;
-          if (!P::mbar_wait(&sm.empty_b[s], ph ^ 1u, abort_flag, err, ERR_PRODUCER)) {
-            ok = false;
-            break;
+          // every activation tile of the slot lands here: this CTA's halves and the peer's
+          P::mbar_arrive_expect_tx(&sm.full_b[slot], uint32_t(nkb) * B_STAGE_BYTES);
+          gb = gs + 1;
+          for (int j = 0; j < nkb; ++j, ++g) {
+            const int kb = ss * SS + j;
+            const uint32_t sw_ = g % W_STAGES, phw = (g / W_STAGES) & 1u;
+            if (!P::mbar_wait(&sm.empty_w[sw_], phw ^ 1u, abort_flag, err, ERR_PRODUCER)) {
+              ok = false;
+              break;
+            }
+            P::mbar_arrive_expect_tx(&sm.full_w[sw_], W_STAGE_BYTES);
+            P::tma_load_2d(P::smem_u32(sm.w[sw_]), &w_map, &sm.full_w[sw_], kb * BK,
+                           min(nb, shp.nt - 1) * BM);
+            gw = g + 1;
+            P::tma_load_2d_mc(P::smem_u32(sm.b[slot][j]) + rank * (B_STAGE_BYTES / CLUSTER),
+                              &act_map, &sm.full_b[slot], kb * BK,
+                              mb * BN + int(rank) * (BN / CLUSTER), CLUSTER_MASK);
           }
-          // the whole tile lands here: this CTA's half and the peer's
-          P::mbar_arrive_expect_tx(&sm.full_b[s], B_STAGE_BYTES);
-          P::tma_load_2d_mc(P::smem_u32(sm.b[s]) + rank * (B_STAGE_BYTES / CLUSTER), &act_map,
-                            &sm.full_b[s], kb * BK, mb * BN + int(rank) * (BN / CLUSTER),
-                            CLUSTER_MASK);
-          ++g;
         }
       }
       // no copy may still be landing in shared memory when the CTA exits
       int no_abort = 0;
       volatile int* never = &no_abort;   // these drains do not follow the abort flag
-      for (uint32_t i = g > B_STAGES ? g - B_STAGES : 0; i < g; ++i)
-        P::mbar_wait(&sm.full_b[i % B_STAGES], (i / B_STAGES) & 1u, never, err, ERR_TEARDOWN);
+      for (uint32_t i = gb > SLOTS ? gb - SLOTS : 0; i < gb; ++i)
+        P::mbar_wait(&sm.full_b[i % SLOTS], (i / SLOTS) & 1u, never, err, ERR_TEARDOWN);
       for (uint32_t i = gw > W_STAGES ? gw - W_STAGES : 0; i < gw; ++i)
         P::mbar_wait(&sm.full_w[i % W_STAGES], (i / W_STAGES) & 1u, never, err, ERR_TEARDOWN);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------- MMA issuer: one wait per 16 MMAs ----------------
+    // ---------------- MMA issuer: one wait and one commit per 16 MMAs ----------------
     if (lane == 0) {
-      uint32_t g = 0, gs = 0, gc = 0;     // k-block, super-stage and chunk counters
+      uint32_t gs = 0, gc = 0;            // super-stage and chunk counters
       bool ok = true;
       for (int t = cid; ok && t < shp.tiles; t += ncl) {
         for (int c = 0; ok && c < shp.nchunks; ++c, ++gc) {
@@ -231,26 +234,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
           }
           const uint32_t d_tmem = tmem + TM_D + buf * BN;
           for (int ss = ss0; ss < ss1; ++ss, ++gs) {
-            const uint32_t sa_ = gs % A_SUPER;
-            if (!P::mbar_wait(&sm.full_a[sa_], (gs / A_SUPER) & 1u, abort_flag, err, ERR_MMA)) {
+            const uint32_t slot = gs % SLOTS;
+            if (!P::mbar_wait(&sm.full_a[slot], (gs / SLOTS) & 1u, abort_flag, err, ERR_MMA)) {
               ok = false;
               break;
             }
             P::tc_fence_after();
-            const uint32_t a_tmem = tmem + TM_A + sa_ * (SS * 32);
+            const uint32_t a_tmem = tmem + TM_A + slot * (SS * 32);
             const int nkb = min(SS, shp.KB - ss * SS);
             for (int j = 0; j < nkb; ++j) {
-              const uint32_t sb = (g + uint32_t(j)) % B_STAGES;
-              const uint64_t bdesc = P::smem_desc_sw128(P::smem_u32(sm.b[sb]));
+              const uint64_t bdesc = P::smem_desc_sw128(P::smem_u32(sm.b[slot][j]));
 #pragma unroll
               for (int kk = 0; kk < BK / 16; ++kk)
                 P::mma_f16_ts(d_tmem, a_tmem + j * 32 + kk * 8, bdesc + uint64_t(kk * 2), IDESC,
                               (ss > ss0 || j > 0 || kk > 0) ? 1u : 0u);
             }
-            for (int j = 0; j < nkb; ++j)
-              P::mma_commit_mc(&sm.empty_b[(g + uint32_t(j)) % B_STAGES], CLUSTER_MASK);
-            P::mma_commit(&sm.empty_a[sa_]);
-            g += uint32_t(nkb);
+            P::mma_commit_mc(&sm.empty_s[slot], CLUSTER_MASK);
           }
           if (!ok) break;
           P::mma_commit(&sm.dfull[buf]);
@@ -274,7 +273,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
     bool ok = true;
     for (int t = cid; ok && t < shp.tiles; t += ncl) {
       for (int ss = 0; ok && ss < shp.NSS; ++ss, ++gs) {
-        const uint32_t sa_ = gs % A_SUPER;
+        const uint32_t slot = gs % SLOTS;
         const int nkb = min(SS, shp.KB - ss * SS);
         for (int j = 0; j < nkb; ++j, ++g) {
           const uint32_t sw_ = g % W_STAGES;
@@ -297,24 +296,24 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
             P::s8x4_to_f16x4(v[i].w, h[8 * i + 6], h[8 * i + 7]);
           }
           if (j == 0 &&
-              !P::mbar_wait_warp(&sm.empty_a[sa_], ((gs / A_SUPER) & 1u) ^ 1u, abort_flag, err,
+              !P::mbar_wait_warp(&sm.empty_s[slot], ((gs / SLOTS) & 1u) ^ 1u, abort_flag, err,
                                  ERR_CONVERT)) {
             ok = false;
             break;
           }
           P::tc_fence_after();
-          P::tmem_st32(tmem + lane_base + TM_A + sa_ * (SS * 32) + uint32_t(j) * 32, h);
-          // forward the readiness of this k-block's activation tile to the MMA thread
-          if (!P::mbar_wait_warp(&sm.full_b[g % B_STAGES], (g / B_STAGES) & 1u, abort_flag, err,
-                                 ERR_CONVERT)) {
-            ok = false;
-            break;
-          }
+          P::tmem_st32(tmem + lane_base + TM_A + slot * (SS * 32) + uint32_t(j) * 32, h);
         }
         if (!ok) break;
+        // forward the readiness of the slot's activation tiles to the MMA thread
+        if (!P::mbar_wait_warp(&sm.full_b[slot], (gs / SLOTS) & 1u, abort_flag, err,
+                               ERR_CONVERT)) {
+          ok = false;
+          break;
+        }
         P::tmem_wait_st();
         P::tc_fence_before();
-        P::mbar_arrive(&sm.full_a[sa_]);
+        P::mbar_arrive(&sm.full_a[slot]);
       }
     }
   } else {
