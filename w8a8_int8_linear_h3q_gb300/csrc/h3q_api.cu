@@ -85,13 +85,14 @@ h3q_status h3q_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t* q_o
   if (h3q_status st = check_shape(M, 1, K)) return st;
   if (!aligned16(x) || !aligned16(q_out) || !aligned16(scale_out)) return H3Q_ERR_MISALIGNED;
   if (h3q_status st = check_device()) return st;
-  return from_cuda(h3q::launch_quantize_act(x, M, K, q_out, scale_out, nullptr, stream));
+  return from_cuda(h3q::launch_quantize_act(x, M, K, q_out, scale_out, nullptr, K, stream));
 }
 
 size_t h3q_linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   (void)N;
   if (M < 1 || K < 1) return 0;
-  // FP16-coded activations, then one 256-byte block holding the status word
+  // FP16-coded activations (rows padded to a multiple of 64), then one
+  // 256-byte block holding the status word
   return h3q::gemm_tc_status_offset(M, K) + 256u;
 }
 
@@ -113,11 +114,13 @@ h3q_status h3q_linear_w8a8(const uint16_t* x, int8_t* xq, float* xs, const int8_
   uint32_t* status = reinterpret_cast<uint32_t*>(wsp + h3q::gemm_tc_status_offset(M, K));
   // A2, or the FP16 coding of pre-quantised activations, or (x == xq == NULL)
   // the activations a previous call left coded in this workspace.
+  const int64_t ldh = h3q::gemm_tc_coded_ld(K);
   if (x) {
-    if (h3q_status st = from_cuda(h3q::launch_quantize_act(x, M, K, xq, xs, act, stream)))
+    if (h3q_status st = from_cuda(h3q::launch_quantize_act(x, M, K, xq, xs, act, ldh, stream)))
       return st;
   } else if (xq) {
-    if (h3q_status st = from_cuda(h3q::launch_int8_to_f16(xq, M * K, act, stream))) return st;
+    if (h3q_status st = from_cuda(h3q::launch_int8_to_f16(xq, M, K, ldh, act, stream)))
+      return st;
   }
   if (cudaMemsetAsync(status, 0, sizeof(uint32_t), stream) != cudaSuccess) return H3Q_ERR_CUDA;
   // A3 + A4.

@@ -20,12 +20,16 @@
 //     fresh FP32 TMEM accumulator, and the epilogue warps fold every chunk
 //     into INT32 running sums held in registers (cvt.rni of an
 //     integer-valued FP32 is exact).  The result is the exact INT32 product.
-// The weights stay INT8 in memory (no dequantisation).  TMA brings each INT8
-// weight k-block into a 64-byte-swizzled shared-memory ring; converter warps
-// read their row from it, turn it into FP16 in registers and store it into
-// TMEM, where the MMA reads it as its A operand.  The activations arrive
-// already FP16-coded (written by the activation quantiser) through TMA into
-// 128-byte-swizzled shared memory: the B operand.
+// The weights stay INT8 in memory (no dequantisation).  TMA brings the INT8
+// weights of a super-stage (two boxes of two k-blocks each) into 128-byte-
+// swizzled shared memory; converter warps read their row from it, turn it
+// into FP16 in registers and store it into TMEM, where the MMA reads it as its
+// A operand.  The activations arrive already FP16-coded (written by the
+// activation quantiser, rows padded with zeros to a multiple of 64) through
+// TMA into 128-byte-swizzled shared memory: the B operand.  Few and large
+// copies keep the single producer thread ahead: per super-stage it issues one
+// 3-D activation load (two whole k-block tiles, viewing a row as chunks of 64)
+// and two weight loads.
 //
 // The MMA issue path is kept bare: on this part every instruction the
 // issuing thread runs between two MMAs (a barrier wait, a commit) leaves the
@@ -37,16 +41,15 @@
 //
 // Tile: 128 output channels (MMA M, TMEM lanes) x 128 tokens (MMA N).
 // CTAs run in clusters of two that take adjacent channel blocks of the same
-// token block: each loads half of the activation tile and multicasts it to
-// both, which halves the activation bytes fetched from L2, and a k-block's
-// activation stage is refilled only after both CTAs' MMAs have finished with
-// it (their completions are multicast to both producers).  Persistent
+// token block: each loads two of a super-stage's four activation tiles and
+// multicasts them to both, which halves the activation bytes fetched from L2,
+// and a slot is refilled only after both CTAs' MMAs have finished with it
+// (their completions are multicast to both producers).  Persistent
 // clusters walk the cluster tiles in groups of 16 token blocks so that the
 // concurrently running tiles share weight and activation tiles in L2.
 //
 // Warp roles (448 threads):
-//   warp 0      TMA producer (INT8 weight tiles per k-block, 8-stage ring;
-//               activation tiles per super-stage, 2 slots)
+//   warp 0      TMA producer (activation and INT8 weight tiles, 2 super-stage slots)
 //   warp 1      TMEM allocator and MMA issuer (one thread)
 //   warps 2-5   converters: INT8 weights -> FP16 -> TMEM (2 super-stages)
 //   warps 6-13  epilogue: chunk drains into INT32 running sums, then
@@ -72,8 +75,8 @@ constexpr int BN = 128;                 // tokens per tile
 constexpr int BK = 64;                  // K per k-block (128 bytes of FP16)
 constexpr int SS = 4;                   // k-blocks per super-stage (16 MMAs)
 constexpr int MAX_SS_PER_CHUNK = 4;     // 16 k-blocks = 1024 K: exact FP32 chunk
-constexpr int W_STAGES = 8;             // INT8 weight tiles (SMEM, TMA), per k-block
-constexpr int SLOTS = 2;                // super-stage slots: activations (SMEM), FP16 weights (TMEM)
+constexpr int SLOTS = 2;                // super-stage slots: activations and INT8 weights
+                                        // (SMEM), FP16 weights (TMEM)
 constexpr int GROUP_M = 16;             // token blocks per raster group
 constexpr int CLUSTER = 2;              // CTAs sharing one activation tile (multicast)
 constexpr uint16_t CLUSTER_MASK = (1u << CLUSTER) - 1;
@@ -83,7 +86,7 @@ constexpr int CONV_WARP0 = 2;
 constexpr int EPI_WARP0 = CONV_WARP0 + NUM_CONV_WARPS;
 constexpr int THREADS = 32 * (2 + NUM_CONV_WARPS + NUM_EPI_WARPS);
 constexpr int B_STAGE_BYTES = BN * BK * 2;                 // 16 KB
-constexpr int W_STAGE_BYTES = BM * BK;                     // 8 KB
+constexpr int W_BOX_BYTES = BM * 2 * BK;                   // 16 KB: 128 rows x 2 k-blocks
 constexpr uint32_t TM_D = 0;            // accumulators: cols 0-127 and 128-255
 constexpr uint32_t TM_A = 256;          // A super-stages: 2 x (4 k-blocks x 32 cols)
 constexpr uint32_t TM_COLS = 512;
@@ -95,10 +98,10 @@ constexpr uint32_t ERR_PRODUCER = 1u, ERR_MMA = 2u, ERR_CONVERT = 4u, ERR_EPILOG
 
 struct __align__(1024) Smem {
   uint8_t b[SLOTS][SS][B_STAGE_BYTES];  // activation tiles of a super-stage slot
-  uint8_t w[W_STAGES][W_STAGE_BYTES];   // 64-byte rows, 64-byte swizzle
+  uint8_t w[SLOTS][SS / 2][W_BOX_BYTES];  // INT8 weights: 128-byte rows, 128-byte swizzle
   uint64_t full_b[SLOTS];               // a slot's activation tiles have landed
-  uint64_t full_w[W_STAGES];
-  uint64_t empty_w[W_STAGES];
+  uint64_t full_w[SLOTS];               // a slot's INT8 weights have landed
+  uint64_t empty_w[SLOTS];              // the converters have read them
   uint64_t full_a[SLOTS];               // A converted and B landed for a super-stage
   uint64_t empty_s[SLOTS];              // both CTAs' MMAs are done with a slot
   uint64_t dfull[2];
@@ -145,11 +148,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < W_STAGES; ++i) {
+    for (int i = 0; i < SLOTS; ++i) {
       P::mbar_init(&sm.full_w[i], 1);
       P::mbar_init(&sm.empty_w[i], NUM_CONV_WARPS * 32);
-    }
-    for (int i = 0; i < SLOTS; ++i) {
       P::mbar_init(&sm.full_b[i], 1);
       P::mbar_init(&sm.full_a[i], NUM_CONV_WARPS * 32);
       P::mbar_init(&sm.empty_s[i], CLUSTER);      // one multicast commit per CTA
@@ -172,42 +173,38 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
   const int cid = int(P::cluster_id_x()), ncl = int(P::num_clusters_x());
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer: three copies per super-stage ----------------
     if (lane == 0) {
       P::tma_prefetch_desc(&act_map);
       P::tma_prefetch_desc(&w_map);
-      uint32_t g = 0, gw = 0, gs = 0, gb = 0;     // k-block, weight issues, super-stage
+      uint32_t gs = 0, gb = 0, gw = 0;     // super-stages seen, B and W slots issued
       bool ok = true;
       for (int t = cid; ok && t < shp.tiles; t += ncl) {
         int mb, nb;
         tile_coords(shp, t, rank, mb, nb);
-        for (int ss = 0; ok && ss < shp.NSS; ++ss, ++gs) {
-          const uint32_t slot = gs % SLOTS;
-          const int nkb = min(SS, shp.KB - ss * SS);
+        const int wrow = min(nb, shp.nt - 1) * BM;
+        for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
+          const uint32_t slot = gs % SLOTS, ph = ((gs / SLOTS) & 1u) ^ 1u;
           // the slot is free once both CTAs' MMAs finished its previous use
-          if (!P::mbar_wait(&sm.empty_s[slot], ((gs / SLOTS) & 1u) ^ 1u, abort_flag, err,
-                            ERR_PRODUCER)) {
+          if (!P::mbar_wait(&sm.empty_s[slot], ph, abort_flag, err, ERR_PRODUCER)) {
             ok = false;
             break;
           }
-          // every activation tile of the slot lands here: this CTA's halves and the peer's
-          P::mbar_arrive_expect_tx(&sm.full_b[slot], uint32_t(nkb) * B_STAGE_BYTES);
+          // all four activation tiles land here: this CTA's two and the peer's two
+          P::mbar_arrive_expect_tx(&sm.full_b[slot], SS * B_STAGE_BYTES);
+          P::tma_load_3d_mc(P::smem_u32(sm.b[slot][2 * rank]), &act_map, &sm.full_b[slot], 0,
+                            mb * BN, ss * SS + 2 * int(rank), CLUSTER_MASK);
           gb = gs + 1;
-          for (int j = 0; j < nkb; ++j, ++g) {
-            const int kb = ss * SS + j;
-            const uint32_t sw_ = g % W_STAGES, phw = (g / W_STAGES) & 1u;
-            if (!P::mbar_wait(&sm.empty_w[sw_], phw ^ 1u, abort_flag, err, ERR_PRODUCER)) {
-              ok = false;
-              break;
-            }
-            P::mbar_arrive_expect_tx(&sm.full_w[sw_], W_STAGE_BYTES);
-            P::tma_load_2d(P::smem_u32(sm.w[sw_]), &w_map, &sm.full_w[sw_], kb * BK,
-                           min(nb, shp.nt - 1) * BM);
-            gw = g + 1;
-            P::tma_load_2d_mc(P::smem_u32(sm.b[slot][j]) + rank * (B_STAGE_BYTES / CLUSTER),
-                              &act_map, &sm.full_b[slot], kb * BK,
-                              mb * BN + int(rank) * (BN / CLUSTER), CLUSTER_MASK);
+          if (!P::mbar_wait(&sm.empty_w[slot], ph, abort_flag, err, ERR_PRODUCER)) {
+            ok = false;
+            break;
           }
+          P::mbar_arrive_expect_tx(&sm.full_w[slot], (SS / 2) * W_BOX_BYTES);
+#pragma unroll
+          for (int p = 0; p < SS / 2; ++p)
+            P::tma_load_2d(P::smem_u32(sm.w[slot][p]), &w_map, &sm.full_w[slot],
+                           (ss * SS + 2 * p) * BK, wrow);
+          gw = gs + 1;
         }
       }
       // no copy may still be landing in shared memory when the CTA exits
@@ -215,8 +212,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
       volatile int* never = &no_abort;   // these drains do not follow the abort flag
       for (uint32_t i = gb > SLOTS ? gb - SLOTS : 0; i < gb; ++i)
         P::mbar_wait(&sm.full_b[i % SLOTS], (i / SLOTS) & 1u, never, err, ERR_TEARDOWN);
-      for (uint32_t i = gw > W_STAGES ? gw - W_STAGES : 0; i < gw; ++i)
-        P::mbar_wait(&sm.full_w[i % W_STAGES], (i / W_STAGES) & 1u, never, err, ERR_TEARDOWN);
+      for (uint32_t i = gw > SLOTS ? gw - SLOTS : 0; i < gw; ++i)
+        P::mbar_wait(&sm.full_w[i % SLOTS], (i / SLOTS) & 1u, never, err, ERR_TEARDOWN);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -267,26 +264,25 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
     const int q = warp & 3;                       // TMEM lane quarter of this warp
     const int r = 32 * q + lane;                  // channel row within the tile
     const uint32_t lane_base = uint32_t(32 * q) << 16;
-    // the four 16-byte chunks of this row in the 64-byte-swizzled INT8 tile
-    const uint32_t row_off = uint32_t(r) * 64u, xr = uint32_t((r >> 1) & 3);
-    uint32_t g = 0, gs = 0;
+    // this row's 16-byte chunks in a 128-byte-swizzled INT8 box (two k-blocks)
+    const uint32_t row_off = uint32_t(r) * 128u, xr = uint32_t(r & 7);
+    uint32_t gs = 0;
     bool ok = true;
     for (int t = cid; ok && t < shp.tiles; t += ncl) {
       for (int ss = 0; ok && ss < shp.NSS; ++ss, ++gs) {
-        const uint32_t slot = gs % SLOTS;
+        const uint32_t slot = gs % SLOTS, ph = (gs / SLOTS) & 1u;
         const int nkb = min(SS, shp.KB - ss * SS);
-        for (int j = 0; j < nkb; ++j, ++g) {
-          const uint32_t sw_ = g % W_STAGES;
-          if (!P::mbar_wait_warp(&sm.full_w[sw_], (g / W_STAGES) & 1u, abort_flag, err,
-                                 ERR_CONVERT)) {
-            ok = false;
-            break;
-          }
+        if (!P::mbar_wait_warp(&sm.full_w[slot], ph, abort_flag, err, ERR_CONVERT)) {
+          ok = false;
+          break;
+        }
+        for (int j = 0; j < nkb; ++j) {
+          const uint8_t* box = sm.w[slot][j >> 1];
+          const uint32_t cb = uint32_t(j & 1) * 4u;
           uint4 v[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            v[i] = *reinterpret_cast<const uint4*>(sm.w[sw_] + row_off + ((uint32_t(i) ^ xr) << 4));
-          P::mbar_arrive(&sm.empty_w[sw_]);       // the INT8 stage may be refilled
+            v[i] = *reinterpret_cast<const uint4*>(box + row_off + (((cb + uint32_t(i)) ^ xr) << 4));
           uint32_t h[32];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -296,8 +292,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
             P::s8x4_to_f16x4(v[i].w, h[8 * i + 6], h[8 * i + 7]);
           }
           if (j == 0 &&
-              !P::mbar_wait_warp(&sm.empty_s[slot], ((gs / SLOTS) & 1u) ^ 1u, abort_flag, err,
-                                 ERR_CONVERT)) {
+              !P::mbar_wait_warp(&sm.empty_s[slot], ph ^ 1u, abort_flag, err, ERR_CONVERT)) {
             ok = false;
             break;
           }
@@ -305,9 +300,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
           P::tmem_st32(tmem + lane_base + TM_A + slot * (SS * 32) + uint32_t(j) * 32, h);
         }
         if (!ok) break;
+        P::mbar_arrive(&sm.empty_w[slot]);        // this slot's INT8 weights may be refilled
         // forward the readiness of the slot's activation tiles to the MMA thread
-        if (!P::mbar_wait_warp(&sm.full_b[slot], (gs / SLOTS) & 1u, abort_flag, err,
-                               ERR_CONVERT)) {
+        if (!P::mbar_wait_warp(&sm.full_b[slot], ph, abort_flag, err, ERR_CONVERT)) {
           ok = false;
           break;
         }
@@ -401,8 +396,10 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
+int64_t gemm_tc_coded_ld(int64_t K) { return (K + BK - 1) / BK * BK; }
+
 size_t gemm_tc_status_offset(int64_t M, int64_t K) {
-  return (size_t(M) * size_t(K) * 2u + 255u) & ~size_t(255);
+  return (size_t(M) * size_t(gemm_tc_coded_ld(K)) * 2u + 255u) & ~size_t(255);
 }
 
 cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_t* qw,
@@ -410,22 +407,25 @@ cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_
                            int64_t K, uint16_t* y, int32_t* acc, uint32_t* err, cudaStream_t s) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
+  // activations: a [M, ld] FP16 matrix viewed as (64-element chunk, row, chunk index),
+  // so one box carries two whole k-block tiles, one after the other
+  const int64_t ld = gemm_tc_coded_ld(K);
   CUtensorMap map;
-  const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(M)};
-  const cuuint64_t strides[1] = {cuuint64_t(K) * 2u};
-  const cuuint32_t box[2] = {BK, BN / CLUSTER};      // each CTA loads half the tile
-  const cuuint32_t estr[2] = {1, 1};
-  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(act_f16), dims,
+  const cuuint64_t dims[3] = {cuuint64_t(BK), cuuint64_t(M), cuuint64_t(ld / BK)};
+  const cuuint64_t strides[2] = {cuuint64_t(ld) * 2u, cuuint64_t(BK) * 2u};
+  const cuuint32_t box[3] = {BK, BN, 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t*>(act_f16), dims,
           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-
+  // weights: [N, K] INT8, boxes of 128 rows x 128 bytes (two k-blocks)
   CUtensorMap wmap;
   const cuuint64_t wdims[2] = {cuuint64_t(K), cuuint64_t(N)};
   const cuuint64_t wstrides[1] = {cuuint64_t(K)};
-  const cuuint32_t wbox[2] = {BK, BM};
+  const cuuint32_t wbox[2] = {2 * BK, BM};
   if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(qw), wdims, wstrides,
-          wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+          wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 

@@ -14,20 +14,26 @@ constexpr int kQMax = 127;
 // Launchers.  Each returns cudaSuccess or the launch error; arguments are
 // already validated by the C-ABI layer.
 
-// A2: BF16 activations -> int8 (optional) + FP32 scale + FP16-coded q (optional).
+// A2: BF16 activations -> int8 (optional) + FP32 scale + FP16-coded q (optional,
+// rows of stride ldh >= K elements, the padding zeroed).
 cudaError_t launch_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t* q,
-                                float* scale, uint16_t* q_f16, cudaStream_t s);
+                                float* scale, uint16_t* q_f16, int64_t ldh, cudaStream_t s);
 
 // A1: FP32 or BF16 weights -> int8 + FP32 scale.  A row with a non-finite
 // element gets a NaN scale, which the caller turns into H3Q_ERR_NONFINITE.
 cudaError_t launch_quantize_weights(const void* w, int w_dtype, int64_t N, int64_t K,
                                     int8_t* q, float* scale, cudaStream_t s);
 
-// int8 -> FP16-coded integers (for pre-quantised activations).
-cudaError_t launch_int8_to_f16(const int8_t* q, int64_t n, uint16_t* out, cudaStream_t s);
+// int8 [M, K] -> FP16-coded integers with row stride ldh (padding zeroed).
+cudaError_t launch_int8_to_f16(const int8_t* q, int64_t M, int64_t K, int64_t ldh,
+                               uint16_t* out, cudaStream_t s);
+
+// Row stride (elements) of the FP16-coded activations in the linear workspace.
+int64_t gemm_tc_coded_ld(int64_t K);
 
 // A3 + A4 on the tcgen05 tensor cores (exact INT32 via FP16 MMA with chunked
-// FP32 accumulation).  act_f16: [M, K] FP16-coded INT8 activations.
+// FP32 accumulation).  act_f16: [M, gemm_tc_coded_ld(K)] FP16-coded INT8
+// activations, the padding beyond K zero.
 // err: device status word (0 = ok; bits set when a bounded wait gave up).
 cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_t* qw,
                            const float* sw, const uint16_t* bias, int64_t M, int64_t N,

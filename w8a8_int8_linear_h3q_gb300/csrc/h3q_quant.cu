@@ -86,7 +86,7 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 
 template <bool kQ8, bool kF16>
 __device__ __forceinline__ void quant_store8(uint4 v, float s, float r, bool fast, int8_t* q8,
-                                             uint16_t* qh, int64_t elem) {
+                                             uint16_t* qh, int64_t elem, int64_t helem) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   float q[8];
 #pragma unroll
@@ -108,7 +108,7 @@ __device__ __forceinline__ void quant_store8(uint4 v, float s, float r, bool fas
     o.y = pack2_f16f(q[2], q[3]);
     o.z = pack2_f16f(q[4], q[5]);
     o.w = pack2_f16f(q[6], q[7]);
-    *reinterpret_cast<uint4*>(qh + elem) = o;
+    *reinterpret_cast<uint4*>(qh + helem) = o;
   }
 }
 
@@ -118,14 +118,18 @@ __device__ __forceinline__ void quant_store8(uint4 v, float s, float r, bool fas
 template <bool kRegs, bool kQ8, bool kF16>
 __global__ void __launch_bounds__(kWarps * 32)
 quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int K, int8_t* __restrict__ q8,
-                 float* __restrict__ scale, uint16_t* __restrict__ qh) {
+                 float* __restrict__ scale, uint16_t* __restrict__ qh, int ldh) {
   const int lane = threadIdx.x & 31;
   const int64_t row = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   if (row >= M) return;
   const int nvec = K >> 3;
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * int64_t(K));
-  const int64_t base = row * int64_t(K);
+  const int64_t base = row * int64_t(K), hbase = row * int64_t(ldh);
   uint32_t mbits = 0;
+  if constexpr (kF16) {   // zero the row's padding up to the coded row stride
+    for (int j = nvec + lane; j < (ldh >> 3); j += 32)
+      *reinterpret_cast<uint4*>(qh + hbase + 8 * int64_t(j)) = make_uint4(0, 0, 0, 0);
+  }
   if constexpr (kRegs) {
     uint4 v[kRegVecs];
 #pragma unroll
@@ -144,7 +148,9 @@ quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int K, int8_t* __res
 #pragma unroll
     for (int i = 0; i < kRegVecs; ++i) {
       const int j = lane + 32 * i;
-      if (j < nvec) quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh, base + 8 * int64_t(j));
+      if (j < nvec)
+        quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh, base + 8 * int64_t(j),
+                                hbase + 8 * int64_t(j));
     }
     if (lane == 0) scale[row] = s;
   } else {
@@ -162,7 +168,8 @@ quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int K, int8_t* __res
     const float r = __frcp_rn(s);
     const bool fast = s >= 0x1p-120f;
     for (j = lane; j < nvec; j += 32)
-      quant_store8<kQ8, kF16>(ld_stream(xr + j), s, r, fast, q8, qh, base + 8 * int64_t(j));
+      quant_store8<kQ8, kF16>(ld_stream(xr + j), s, r, fast, q8, qh, base + 8 * int64_t(j),
+                              hbase + 8 * int64_t(j));
     if (lane == 0) scale[row] = s;
   }
 }
@@ -175,12 +182,16 @@ constexpr int kRowThreads = 256;
 template <int kVPT, bool kQ8, bool kF16>
 __global__ void __launch_bounds__(kRowThreads)
 quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__ q8,
-                     float* __restrict__ scale, uint16_t* __restrict__ qh) {
+                     float* __restrict__ scale, uint16_t* __restrict__ qh, int ldh) {
   __shared__ uint32_t red[kRowThreads / 32];
   const int64_t row = blockIdx.x;
   const int nvec = K >> 3;
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * int64_t(K));
-  const int64_t base = row * int64_t(K);
+  const int64_t base = row * int64_t(K), hbase = row * int64_t(ldh);
+  if constexpr (kF16) {   // zero the row's padding up to the coded row stride
+    for (int j = nvec + int(threadIdx.x); j < (ldh >> 3); j += kRowThreads)
+      *reinterpret_cast<uint4*>(qh + hbase + 8 * int64_t(j)) = make_uint4(0, 0, 0, 0);
+  }
   uint4 v[kVPT];
   uint32_t mbits = 0;
 #pragma unroll
@@ -203,7 +214,9 @@ quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__
 #pragma unroll
   for (int i = 0; i < kVPT; ++i) {
     const int j = threadIdx.x + kRowThreads * i;
-    if (j < nvec) quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh, base + 8 * int64_t(j));
+    if (j < nvec)
+      quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh, base + 8 * int64_t(j),
+                              hbase + 8 * int64_t(j));
   }
   if (threadIdx.x == 0) scale[row] = s;
 }
@@ -243,11 +256,23 @@ quant_weight_kernel(const T* __restrict__ w, int64_t N, int K, int8_t* __restric
   if (lane == 0) scale[row] = bad ? __int_as_float(0x7FC00000) : s;
 }
 
-__global__ void int8_to_f16_kernel(const int8_t* __restrict__ q, int64_t n16,
+// One thread per 16 INT8 values of a row; the coded rows have stride ldh
+// (padding zeroed).
+__global__ void int8_to_f16_kernel(const int8_t* __restrict__ q, int64_t M, int K, int ldh,
                                    uint16_t* __restrict__ out) {
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+  const int per_row = ldh >> 4;                     // 16-element groups per coded row
+  const int64_t total = M * per_row;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += int64_t(gridDim.x) * blockDim.x) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(q) + i);
+    const int64_t row = i / per_row;
+    const int grp = int(i - row * per_row);
+    uint4* dst = reinterpret_cast<uint4*>(out + row * ldh + 16 * int64_t(grp));
+    if (16 * grp >= K) {
+      dst[0] = make_uint4(0, 0, 0, 0);
+      dst[1] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(q + row * K + 16 * int64_t(grp)));
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[8];
 #pragma unroll
@@ -257,7 +282,6 @@ __global__ void int8_to_f16_kernel(const int8_t* __restrict__ q, int64_t n16,
       o[2 * j] = pack2_f16(b0, b1);
       o[2 * j + 1] = pack2_f16(b2, b3);
     }
-    uint4* dst = reinterpret_cast<uint4*>(out) + 2 * i;
     dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
   }
@@ -265,38 +289,39 @@ __global__ void int8_to_f16_kernel(const int8_t* __restrict__ q, int64_t n16,
 
 template <bool kRegs>
 cudaError_t launch_act(const uint16_t* x, int64_t M, int K, int8_t* q, float* s, uint16_t* qh,
-                       cudaStream_t st) {
+                       int ldh, cudaStream_t st) {
   const dim3 grid(unsigned((M + kWarps - 1) / kWarps)), block(kWarps * 32);
   if (q && qh)
-    quant_act_kernel<kRegs, true, true><<<grid, block, 0, st>>>(x, M, K, q, s, qh);
+    quant_act_kernel<kRegs, true, true><<<grid, block, 0, st>>>(x, M, K, q, s, qh, ldh);
   else if (q)
-    quant_act_kernel<kRegs, true, false><<<grid, block, 0, st>>>(x, M, K, q, s, qh);
+    quant_act_kernel<kRegs, true, false><<<grid, block, 0, st>>>(x, M, K, q, s, qh, ldh);
   else
-    quant_act_kernel<kRegs, false, true><<<grid, block, 0, st>>>(x, M, K, q, s, qh);
+    quant_act_kernel<kRegs, false, true><<<grid, block, 0, st>>>(x, M, K, q, s, qh, ldh);
   return cudaGetLastError();
 }
 
 template <int kVPT>
 cudaError_t launch_rows(const uint16_t* x, int64_t M, int K, int8_t* q, float* s, uint16_t* qh,
-                        cudaStream_t st) {
+                        int ldh, cudaStream_t st) {
   const dim3 grid(static_cast<unsigned>(M)), block(kRowThreads);
   if (q && qh)
-    quant_act_row_kernel<kVPT, true, true><<<grid, block, 0, st>>>(x, K, q, s, qh);
+    quant_act_row_kernel<kVPT, true, true><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh);
   else if (q)
-    quant_act_row_kernel<kVPT, true, false><<<grid, block, 0, st>>>(x, K, q, s, qh);
+    quant_act_row_kernel<kVPT, true, false><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh);
   else
-    quant_act_row_kernel<kVPT, false, true><<<grid, block, 0, st>>>(x, K, q, s, qh);
+    quant_act_row_kernel<kVPT, false, true><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t* q,
-                                float* scale, uint16_t* q_f16, cudaStream_t s) {
+                                float* scale, uint16_t* q_f16, int64_t ldh, cudaStream_t s) {
   const int64_t nvec = K / 8;
-  if (nvec <= kRowThreads * 3) return launch_rows<3>(x, M, int(K), q, scale, q_f16, s);
-  if (nvec <= kRowThreads * 12) return launch_rows<12>(x, M, int(K), q, scale, q_f16, s);
-  return launch_act<false>(x, M, int(K), q, scale, q_f16, s);
+  if (nvec <= kRowThreads * 3) return launch_rows<3>(x, M, int(K), q, scale, q_f16, int(ldh), s);
+  if (nvec <= kRowThreads * 12)
+    return launch_rows<12>(x, M, int(K), q, scale, q_f16, int(ldh), s);
+  return launch_act<false>(x, M, int(K), q, scale, q_f16, int(ldh), s);
 }
 
 cudaError_t launch_quantize_weights(const void* w, int w_dtype, int64_t N, int64_t K,
@@ -311,11 +336,12 @@ cudaError_t launch_quantize_weights(const void* w, int w_dtype, int64_t N, int64
   return cudaGetLastError();
 }
 
-cudaError_t launch_int8_to_f16(const int8_t* q, int64_t n, uint16_t* out, cudaStream_t s) {
-  const int64_t n16 = n / 16;
-  int64_t blocks = (n16 + 255) / 256;
+cudaError_t launch_int8_to_f16(const int8_t* q, int64_t M, int64_t K, int64_t ldh,
+                               uint16_t* out, cudaStream_t s) {
+  const int64_t groups = M * (ldh / 16);
+  int64_t blocks = (groups + 255) / 256;
   blocks = blocks < 1 ? 1 : (blocks > 152 * 16 ? 152 * 16 : blocks);
-  int8_to_f16_kernel<<<unsigned(blocks), 256, 0, s>>>(q, n16, out);
+  int8_to_f16_kernel<<<unsigned(blocks), 256, 0, s>>>(q, M, int(K), int(ldh), out);
   return cudaGetLastError();
 }
 

@@ -132,6 +132,16 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* map, ui
       : "memory");
 }
 
+// 3-D tiled load, multicast like tma_load_2d_mc.
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void* map, uint64_t* bar,
+                                               int x, int y, int z, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "h"(mask)
+      : "memory");
+}
+
 // --- clusters -------------------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_rank() {
