@@ -26,10 +26,12 @@
 // into FP16 in registers and store it into TMEM, where the MMA reads it as its
 // A operand.  The activations arrive already FP16-coded (written by the
 // activation quantiser, rows padded with zeros to a multiple of 64) through
-// TMA into 128-byte-swizzled shared memory: the B operand.  Few and large
-// copies keep the single producer thread ahead: per super-stage it issues one
-// 3-D activation load (two whole k-block tiles, viewing a row as chunks of 64)
-// and two weight loads.
+// TMA into 128-byte-swizzled shared memory: the B operand.  Copies are few
+// and large: per super-stage one 3-D activation load per CTA (two whole
+// k-block tiles, viewing a row as chunks of 64) and two weight loads.  The
+// weights have their own producer and a deeper ring (three super-stages), so
+// they are in shared memory before the converters need them; the activation
+// slots are refilled as the MMAs release them.
 //
 // The MMA issue path is kept bare: on this part every instruction the
 // issuing thread runs between two MMAs (a barrier wait, a commit) leaves the
@@ -48,11 +50,12 @@
 // clusters walk the cluster tiles in groups of 16 token blocks so that the
 // concurrently running tiles share weight and activation tiles in L2.
 //
-// Warp roles (448 threads):
-//   warp 0      TMA producer (activation and INT8 weight tiles, 2 super-stage slots)
+// Warp roles (480 threads):
+//   warp 0      TMA producer of the activation tiles (2 super-stage slots)
 //   warp 1      TMEM allocator and MMA issuer (one thread)
-//   warps 2-5   converters: INT8 weights -> FP16 -> TMEM (2 super-stages)
-//   warps 6-13  epilogue: chunk drains into INT32 running sums, then
+//   warp 2      TMA producer of the INT8 weight tiles (3 super-stage slots)
+//   warps 3-6   converters: INT8 weights -> FP16 -> TMEM (2 super-stages)
+//   warps 7-14  epilogue: chunk drains into INT32 running sums, then
 //               dequant + bias + BF16 (and the optional raw INT32 output)
 // TMEM: FP32 accumulators in columns 0-127 and 128-255, A super-stages in
 // 256-383 and 384-511.
@@ -75,16 +78,17 @@ constexpr int BN = 128;                 // tokens per tile
 constexpr int BK = 64;                  // K per k-block (128 bytes of FP16)
 constexpr int SS = 4;                   // k-blocks per super-stage (16 MMAs)
 constexpr int MAX_SS_PER_CHUNK = 4;     // 16 k-blocks = 1024 K: exact FP32 chunk
-constexpr int SLOTS = 2;                // super-stage slots: activations and INT8 weights
-                                        // (SMEM), FP16 weights (TMEM)
+constexpr int SLOTS = 2;                // super-stage slots: activations (SMEM), FP16 weights (TMEM)
+constexpr int W_SLOTS = 3;              // super-stage slots: INT8 weights (SMEM)
 constexpr int GROUP_M = 16;             // token blocks per raster group
 constexpr int CLUSTER = 2;              // CTAs sharing one activation tile (multicast)
 constexpr uint16_t CLUSTER_MASK = (1u << CLUSTER) - 1;
 constexpr int NUM_CONV_WARPS = 4;
 constexpr int NUM_EPI_WARPS = 8;
-constexpr int CONV_WARP0 = 2;
+constexpr int WPROD_WARP = 2;
+constexpr int CONV_WARP0 = 3;
 constexpr int EPI_WARP0 = CONV_WARP0 + NUM_CONV_WARPS;
-constexpr int THREADS = 32 * (2 + NUM_CONV_WARPS + NUM_EPI_WARPS);
+constexpr int THREADS = 32 * (3 + NUM_CONV_WARPS + NUM_EPI_WARPS);
 constexpr int B_STAGE_BYTES = BN * BK * 2;                 // 16 KB
 constexpr int W_BOX_BYTES = BM * 2 * BK;                   // 16 KB: 128 rows x 2 k-blocks
 constexpr uint32_t TM_D = 0;            // accumulators: cols 0-127 and 128-255
@@ -98,10 +102,10 @@ constexpr uint32_t ERR_PRODUCER = 1u, ERR_MMA = 2u, ERR_CONVERT = 4u, ERR_EPILOG
 
 struct __align__(1024) Smem {
   uint8_t b[SLOTS][SS][B_STAGE_BYTES];  // activation tiles of a super-stage slot
-  uint8_t w[SLOTS][SS / 2][W_BOX_BYTES];  // INT8 weights: 128-byte rows, 128-byte swizzle
+  uint8_t w[W_SLOTS][SS / 2][W_BOX_BYTES];  // INT8 weights: 128-byte rows, 128-byte swizzle
   uint64_t full_b[SLOTS];               // a slot's activation tiles have landed
-  uint64_t full_w[SLOTS];               // a slot's INT8 weights have landed
-  uint64_t empty_w[SLOTS];              // the converters have read them
+  uint64_t full_w[W_SLOTS];             // a slot's INT8 weights have landed
+  uint64_t empty_w[W_SLOTS];            // the converters have read them
   uint64_t full_a[SLOTS];               // A converted and B landed for a super-stage
   uint64_t empty_s[SLOTS];              // both CTAs' MMAs are done with a slot
   uint64_t dfull[2];
@@ -148,9 +152,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
   volatile int* abort_flag = &sm.abort_flag;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < SLOTS; ++i) {
+    for (int i = 0; i < W_SLOTS; ++i) {
       P::mbar_init(&sm.full_w[i], 1);
       P::mbar_init(&sm.empty_w[i], NUM_CONV_WARPS * 32);
+    }
+    for (int i = 0; i < SLOTS; ++i) {
       P::mbar_init(&sm.full_b[i], 1);
       P::mbar_init(&sm.full_a[i], NUM_CONV_WARPS * 32);
       P::mbar_init(&sm.empty_s[i], CLUSTER);      // one multicast commit per CTA
@@ -173,20 +179,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
   const int cid = int(P::cluster_id_x()), ncl = int(P::num_clusters_x());
 
   if (warp == 0) {
-    // ---------------- TMA producer: three copies per super-stage ----------------
+    // ---------------- TMA producer: activation tiles ----------------
     if (lane == 0) {
       P::tma_prefetch_desc(&act_map);
-      P::tma_prefetch_desc(&w_map);
-      uint32_t gs = 0, gb = 0, gw = 0;     // super-stages seen, B and W slots issued
+      uint32_t gs = 0, gb = 0;             // super-stages seen, slots issued
       bool ok = true;
       for (int t = cid; ok && t < shp.tiles; t += ncl) {
         int mb, nb;
         tile_coords(shp, t, rank, mb, nb);
-        const int wrow = min(nb, shp.nt - 1) * BM;
         for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
-          const uint32_t slot = gs % SLOTS, ph = ((gs / SLOTS) & 1u) ^ 1u;
+          const uint32_t slot = gs % SLOTS;
           // the slot is free once both CTAs' MMAs finished its previous use
-          if (!P::mbar_wait(&sm.empty_s[slot], ph, abort_flag, err, ERR_PRODUCER)) {
+          if (!P::mbar_wait(&sm.empty_s[slot], ((gs / SLOTS) & 1u) ^ 1u, abort_flag, err,
+                            ERR_PRODUCER)) {
             ok = false;
             break;
           }
@@ -195,7 +200,29 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
           P::tma_load_3d_mc(P::smem_u32(sm.b[slot][2 * rank]), &act_map, &sm.full_b[slot], 0,
                             mb * BN, ss * SS + 2 * int(rank), CLUSTER_MASK);
           gb = gs + 1;
-          if (!P::mbar_wait(&sm.empty_w[slot], ph, abort_flag, err, ERR_PRODUCER)) {
+        }
+      }
+      // no copy may still be landing in shared memory when the CTA exits
+      int no_abort = 0;
+      volatile int* never = &no_abort;   // this drain does not follow the abort flag
+      for (uint32_t i = gb > SLOTS ? gb - SLOTS : 0; i < gb; ++i)
+        P::mbar_wait(&sm.full_b[i % SLOTS], (i / SLOTS) & 1u, never, err, ERR_TEARDOWN);
+    }
+    __syncwarp();
+  } else if (warp == WPROD_WARP) {
+    // ---------------- TMA producer: INT8 weight tiles ----------------
+    if (lane == 0) {
+      P::tma_prefetch_desc(&w_map);
+      uint32_t gs = 0, gw = 0;
+      bool ok = true;
+      for (int t = cid; ok && t < shp.tiles; t += ncl) {
+        int mb, nb;
+        tile_coords(shp, t, rank, mb, nb);
+        const int wrow = min(nb, shp.nt - 1) * BM;
+        for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
+          const uint32_t slot = gs % W_SLOTS;
+          if (!P::mbar_wait(&sm.empty_w[slot], ((gs / W_SLOTS) & 1u) ^ 1u, abort_flag, err,
+                            ERR_PRODUCER)) {
             ok = false;
             break;
           }
@@ -207,13 +234,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
           gw = gs + 1;
         }
       }
-      // no copy may still be landing in shared memory when the CTA exits
       int no_abort = 0;
-      volatile int* never = &no_abort;   // these drains do not follow the abort flag
-      for (uint32_t i = gb > SLOTS ? gb - SLOTS : 0; i < gb; ++i)
-        P::mbar_wait(&sm.full_b[i % SLOTS], (i / SLOTS) & 1u, never, err, ERR_TEARDOWN);
-      for (uint32_t i = gw > SLOTS ? gw - SLOTS : 0; i < gw; ++i)
-        P::mbar_wait(&sm.full_w[i % SLOTS], (i / SLOTS) & 1u, never, err, ERR_TEARDOWN);
+      volatile int* never = &no_abort;
+      for (uint32_t i = gw > W_SLOTS ? gw - W_SLOTS : 0; i < gw; ++i)
+        P::mbar_wait(&sm.full_w[i % W_SLOTS], (i / W_SLOTS) & 1u, never, err, ERR_TEARDOWN);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -271,13 +295,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
     for (int t = cid; ok && t < shp.tiles; t += ncl) {
       for (int ss = 0; ok && ss < shp.NSS; ++ss, ++gs) {
         const uint32_t slot = gs % SLOTS, ph = (gs / SLOTS) & 1u;
+        const uint32_t wslot = gs % W_SLOTS;
         const int nkb = min(SS, shp.KB - ss * SS);
-        if (!P::mbar_wait_warp(&sm.full_w[slot], ph, abort_flag, err, ERR_CONVERT)) {
+        if (!P::mbar_wait_warp(&sm.full_w[wslot], (gs / W_SLOTS) & 1u, abort_flag, err,
+                               ERR_CONVERT)) {
           ok = false;
           break;
         }
         for (int j = 0; j < nkb; ++j) {
-          const uint8_t* box = sm.w[slot][j >> 1];
+          const uint8_t* box = sm.w[wslot][j >> 1];
           const uint32_t cb = uint32_t(j & 1) * 4u;
           uint4 v[4];
 #pragma unroll
@@ -300,7 +326,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
           P::tmem_st32(tmem + lane_base + TM_A + slot * (SS * 32) + uint32_t(j) * 32, h);
         }
         if (!ok) break;
-        P::mbar_arrive(&sm.empty_w[slot]);        // this slot's INT8 weights may be refilled
+        P::mbar_arrive(&sm.empty_w[wslot]);       // this slot's INT8 weights may be refilled
         // forward the readiness of the slot's activation tiles to the MMA thread
         if (!P::mbar_wait_warp(&sm.full_b[slot], ph, abort_flag, err, ERR_CONVERT)) {
           ok = false;
