@@ -172,6 +172,34 @@ h3q_status h3q_linear_w8a8_mma_sync(const int8_t* xq, const float* xs, const int
                                     int64_t M, int64_t N, int64_t K,
                                     uint16_t* y, int32_t* acc_out, cudaStream_t stream);
 
+/*
+ * h3q_linear_w8a8 for callers that cannot allocate device memory (the pages
+ * have no counterpart: this is a convenience of this library).  Some callers
+ * may not call cudaMalloc at call time -- an inference engine's plugin enqueue
+ * that is handed only its input and output buffers, or a serving loop that
+ * must not block on, or fail in, the allocator once warmed up.  This entry
+ * point allocates nothing: its scratch is a 16 MiB array built into the
+ * library, which every GPU that loads the library holds until the process
+ * exits.
+ *
+ * Arguments and results are those of h3q_linear_w8a8, without the workspace,
+ * and with x or xq required (there is no reuse of an earlier call's
+ * activations).  Shapes whose h3q_linear_workspace_bytes(M, N, K) exceeds
+ * 16 MiB (16777216 bytes) are rejected with H3Q_ERR_UNSUPPORTED_SHAPE; at
+ * K = 5376 that allows M up to 1560 tokens.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array and each rewrites what it needs of
+ * it, so calls whose work overlaps on the GPU (different streams, or
+ * concurrent host threads) race and must be serialised by the caller.
+ * Enqueued on `stream`; does not synchronise.
+ */
+h3q_status h3q_linear_w8a8_noalloc(const uint16_t* x, int8_t* xq, float* xs,
+                                   const int8_t* wq, const float* ws, const uint16_t* bias,
+                                   int64_t M, int64_t N, int64_t K,
+                                   uint16_t* y, int32_t* acc_out, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

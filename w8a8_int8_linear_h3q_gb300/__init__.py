@@ -51,6 +51,8 @@ def _declare(lib):
     lib.h3q_workspace_status.restype = i32
     lib.h3q_linear_w8a8_mma_sync.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
     lib.h3q_linear_w8a8_mma_sync.restype = i32
+    lib.h3q_linear_w8a8_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
+    lib.h3q_linear_w8a8_noalloc.restype = i32
     return lib
 
 
@@ -237,6 +239,48 @@ def h3q_linear_w8a8_mma_sync(xq, xs, wq, ws, bias=None, *, y=None, acc_out=None,
                                            M, N, K, _ptr(y), _ptr(acc_out), _stream(stream)),
            "h3q_linear_w8a8_mma_sync")
     out = {}
+    if y is not None:
+        out["y"] = y
+    if acc_out is not None:
+        out["acc"] = acc_out
+    return out
+
+
+def h3q_linear_w8a8_noalloc(x, wq, ws, bias=None, *, xq=None, xs=None, y=None, acc_out=None,
+                            want_y=True, want_acc=False, stream=None):
+    """As h3q_linear_w8a8, with the scratch built into the library (no workspace).
+
+    For callers that cannot allocate device memory at call time; shapes whose
+    workspace would exceed 16 MiB are rejected.  ``x`` BF16 [M, K], or None
+    with ``xq``/``xs`` given.  Output tensors are allocated here when not given.
+    """
+    import torch
+    _need(wq, torch.int8, None, "wq")
+    N, K = wq.shape
+    dev = wq.device
+    if x is not None:
+        _need(x, torch.bfloat16, None, "x")
+        M = x.shape[0]
+        if xs is None:
+            xs = torch.empty((M,), dtype=torch.float32, device=dev)
+    else:
+        if xq is None or xs is None:
+            raise ValueError("without x, both xq and xs are needed")
+        M = xq.shape[0]
+    if xq is not None:
+        _need(xq, torch.int8, (M, K), "xq")
+    _need(xs, torch.float32, (M,), "xs")
+    _need(ws, torch.float32, (N,), "ws")
+    if bias is not None:
+        _need(bias, torch.bfloat16, (N,), "bias")
+    if want_y and y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if want_acc and acc_out is None:
+        acc_out = torch.empty((M, N), dtype=torch.int32, device=dev)
+    _check(load().h3q_linear_w8a8_noalloc(_ptr(x), _ptr(xq), _ptr(xs), _ptr(wq), _ptr(ws),
+                                          _ptr(bias), M, N, K, _ptr(y), _ptr(acc_out),
+                                          _stream(stream)), "h3q_linear_w8a8_noalloc")
+    out = {"xs": xs}
     if y is not None:
         out["y"] = y
     if acc_out is not None:
