@@ -26,7 +26,8 @@
  *     anything else returns H3Q_ERR_MISALIGNED.
  *   - Shapes: M >= 1, N >= 1, 16 <= K <= 133143 and K % 16 == 0.  The K bound
  *     keeps K * 127^2 below 2^31, so the INT32 accumulator cannot overflow;
- *     K % 16 keeps every INT8 row 16-byte aligned.  M and N are otherwise
+ *     K % 16 keeps every INT8 row 16-byte aligned.  M <= 2^31 - 65536 and
+ *     N <= 65535 * 128 (32-bit tile coordinates); within these, M and N are
  *     arbitrary: ragged tiles are masked.
  *   - Work is enqueued on `stream` and runs asynchronously, except where an
  *     entry point says it synchronises.  Argument errors are returned before
@@ -104,9 +105,11 @@ h3q_status h3q_quantize_act(const uint16_t* x, int64_t M, int64_t K,
 /*
  * Bytes of device workspace that h3q_linear_w8a8 needs for this shape: the
  * quantised activations re-coded as FP16 (exact: every INT8 value is an FP16
- * value), read by the tensor cores, followed by a 256-byte block holding a
- * status word.  The caller allocates it; calls that share a workspace must
- * not overlap on the GPU.
+ * value), read by the tensor cores; per 256 tokens the largest sum of squares
+ * of a coded row; a 256-byte status block; per 16 weight rows the largest sum
+ * of squares; and a list of the tiles computed in K chunks (about
+ * M * 2 * K + 8 * M * N / 32768 + N / 4 bytes in all).  The caller allocates
+ * it; calls that share a workspace must not overlap on the GPU.
  */
 size_t h3q_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
@@ -117,8 +120,12 @@ size_t h3q_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * ([P1] Validation, CPU INT32 references; [P2] What the default preserves,
  * bias added before the rounding).  The BF16 result is within one BF16 ulp of
  * that value computed exactly.  The product runs on the FP16 tensor cores as
- * exact integer arithmetic (FP32 partial sums drained to INT32 every <= 1024
- * K), so acc is the exact INT32 sum.
+ * exact integer arithmetic, so acc is the exact INT32 sum: a tile of 256
+ * tokens x 256 channels accumulates all of K in FP32 when the largest
+ * squared row norms of its INT8 activations and weights multiply to at most
+ * 2^48 (every partial sum is then an integer of magnitude <= 2^24, by
+ * Cauchy-Schwarz); any other tile drains its FP32 partial sums into INT32
+ * every <= 1024 K.
  *
  * Where the activations come from:
  *   x != NULL            BF16 [M, K]; quantised here (A2).  xs is written, and
@@ -158,6 +165,17 @@ h3q_status h3q_workspace_status(const void* workspace, int64_t M, int64_t K,
                                 cudaStream_t stream);
 
 /*
+ * Diagnostic: how many tiles of 128 tokens x 256 channels the last
+ * h3q_linear_w8a8 that used `workspace` (same M, K) computed with K cut into
+ * chunks, because the squared-norm bound did not let one FP32 accumulator
+ * hold all of K; the other tiles took the single-accumulator path.  Both
+ * paths give the same exact result; the chunked one is slower.  Written to
+ * *tiles.  SYNCHRONISES `stream`.
+ */
+h3q_status h3q_linear_chunked_tiles(const void* workspace, int64_t M, int64_t K,
+                                    int64_t* tiles, cudaStream_t stream);
+
+/*
  * A3 + A4 on the legacy warp-level INT8 tensor instruction (mma.sync
  * m16n8k32 s8 -> s32), exact by construction; the same arithmetic and output
  * as h3q_linear_w8a8 from pre-quantised activations.  Kept as the baseline
@@ -186,7 +204,7 @@ h3q_status h3q_linear_w8a8_mma_sync(const int8_t* xq, const float* xs, const int
  * and with x or xq required (there is no reuse of an earlier call's
  * activations).  Shapes whose h3q_linear_workspace_bytes(M, N, K) exceeds
  * 16 MiB (16777216 bytes) are rejected with H3Q_ERR_UNSUPPORTED_SHAPE; at
- * K = 5376 that allows M up to 1560 tokens.
+ * N = K = 5376 that allows M up to 1559 tokens.
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream

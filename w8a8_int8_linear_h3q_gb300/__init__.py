@@ -49,6 +49,8 @@ def _declare(lib):
     lib.h3q_linear_w8a8.restype = i32
     lib.h3q_workspace_status.argtypes = [vp, i64, i64, vp]
     lib.h3q_workspace_status.restype = i32
+    lib.h3q_linear_chunked_tiles.argtypes = [vp, i64, i64, ctypes.POINTER(i64), vp]
+    lib.h3q_linear_chunked_tiles.restype = i32
     lib.h3q_linear_w8a8_mma_sync.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
     lib.h3q_linear_w8a8_mma_sync.restype = i32
     lib.h3q_linear_w8a8_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
@@ -215,6 +217,15 @@ def h3q_workspace_status(workspace, M: int, K: int, stream=None) -> int:
     """Status word of the last linear call on ``workspace``: 0 = ok,
     H3Q_ERR_TIMEOUT if a bounded device-side wait gave up.  Synchronises."""
     return int(load().h3q_workspace_status(_ptr(workspace), M, K, _stream(stream)))
+
+
+def h3q_linear_chunked_tiles(workspace, M: int, K: int, stream=None) -> int:
+    """Tiles (128 tokens x 256 channels) that the last linear call on
+    ``workspace`` computed in K chunks.  Synchronises."""
+    n = ctypes.c_int64(-1)
+    _check(load().h3q_linear_chunked_tiles(_ptr(workspace), M, K, ctypes.byref(n),
+                                           _stream(stream)), "h3q_linear_chunked_tiles")
+    return int(n.value)
 
 
 def h3q_linear_w8a8_mma_sync(xq, xs, wq, ws, bias=None, *, y=None, acc_out=None, want_y=True,

@@ -2,6 +2,7 @@
 // device check, and the launch sequence of each entry point.  No entry point
 // allocates device memory; every launch goes on the caller's stream.
 #include <cstdio>
+#include <cstdlib>
 #include <vector>
 
 #include "h3q_internal.cuh"
@@ -9,7 +10,7 @@
 namespace {
 
 constexpr int64_t kMaxK = 133143;            // K * 127^2 < 2^31
-constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 65536;
 constexpr int64_t kMaxN = int64_t(65535) * 128;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -36,7 +37,12 @@ h3q_status check_device() {
   return (major == 10 && minor == 3) ? H3Q_OK : H3Q_ERR_NO_DEVICE;
 }
 
-h3q_status from_cuda(cudaError_t e) { return e == cudaSuccess ? H3Q_OK : H3Q_ERR_CUDA; }
+// With H3Q_VERBOSE set in the environment, CUDA errors are also printed.
+h3q_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return H3Q_OK;
+  if (std::getenv("H3Q_VERBOSE")) std::fprintf(stderr, "h3q: %s\n", cudaGetErrorString(e));
+  return H3Q_ERR_CUDA;
+}
 
 }  // namespace
 
@@ -85,15 +91,13 @@ h3q_status h3q_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t* q_o
   if (h3q_status st = check_shape(M, 1, K)) return st;
   if (!aligned16(x) || !aligned16(q_out) || !aligned16(scale_out)) return H3Q_ERR_MISALIGNED;
   if (h3q_status st = check_device()) return st;
-  return from_cuda(h3q::launch_quantize_act(x, M, K, q_out, scale_out, nullptr, K, stream));
+  return from_cuda(
+      h3q::launch_quantize_act(x, M, K, q_out, scale_out, nullptr, K, nullptr, stream));
 }
 
 size_t h3q_linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  (void)N;
-  if (M < 1 || K < 1) return 0;
-  // FP16-coded activations (rows padded to a multiple of 64), then one
-  // 256-byte block holding the status word
-  return h3q::gemm_tc_status_offset(M, K) + 256u;
+  if (M < 1 || N < 1 || K < 1) return 0;
+  return h3q::workspace_layout(M, N, K).total;
 }
 
 h3q_status h3q_linear_w8a8(const uint16_t* x, int8_t* xq, float* xs, const int8_t* wq,
@@ -109,23 +113,40 @@ h3q_status h3q_linear_w8a8(const uint16_t* x, int8_t* xq, float* xs, const int8_
     if (p && !aligned16(p)) return H3Q_ERR_MISALIGNED;
   if (h3q_status st = check_device()) return st;
 
+  const h3q::WorkspaceLayout lay = h3q::workspace_layout(M, N, K);
   uint8_t* wsp = static_cast<uint8_t*>(workspace);
-  uint16_t* act = reinterpret_cast<uint16_t*>(wsp);
-  uint32_t* status = reinterpret_cast<uint32_t*>(wsp + h3q::gemm_tc_status_offset(M, K));
+  uint16_t* act = reinterpret_cast<uint16_t*>(wsp + lay.act);
+  uint32_t* amax = reinterpret_cast<uint32_t*>(wsp + lay.amax);
+  uint32_t* status = reinterpret_cast<uint32_t*>(wsp + lay.status);
+  uint32_t* nwpart = reinterpret_cast<uint32_t*>(wsp + lay.nwpart);
+  uint2* list = reinterpret_cast<uint2*>(wsp + lay.list);
+  const bool code_acts = x || xq;
+  // Weight norms; zero the status block, and the activation norm maxima when
+  // the activations are coded anew (they sit just before the status block).
+  uint32_t* zero = code_acts ? amax : status;
+  const int64_t nzero = int64_t(lay.status + 256u - (code_acts ? lay.amax : lay.status)) / 4;
+  if (h3q_status st =
+          from_cuda(h3q::launch_weight_norms(wq, N, K, nwpart, zero, nzero, stream)))
+    return st;
   // A2, or the FP16 coding of pre-quantised activations, or (x == xq == NULL)
   // the activations a previous call left coded in this workspace.
   const int64_t ldh = h3q::gemm_tc_coded_ld(K);
   if (x) {
-    if (h3q_status st = from_cuda(h3q::launch_quantize_act(x, M, K, xq, xs, act, ldh, stream)))
+    if (h3q_status st =
+            from_cuda(h3q::launch_quantize_act(x, M, K, xq, xs, act, ldh, amax, stream)))
       return st;
   } else if (xq) {
-    if (h3q_status st = from_cuda(h3q::launch_int8_to_f16(xq, M, K, ldh, act, stream)))
+    if (h3q_status st = from_cuda(h3q::launch_int8_to_f16(xq, M, K, ldh, act, amax, stream)))
       return st;
   }
-  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), stream) != cudaSuccess) return H3Q_ERR_CUDA;
-  // A3 + A4.
+  // A3 + A4: the tiles that are exact over the whole K, then the rest in K
+  // chunks (an empty launch when there are none).
+  if (h3q_status st = from_cuda(h3q::launch_gemm_wide(act, xs, wq, ws, bias, M, N, K, y,
+                                                      acc_out, amax, nwpart, status, list,
+                                                      stream)))
+    return st;
   return from_cuda(h3q::launch_gemm_tc(act, xs, wq, ws, bias, M, N, K, y, acc_out, status,
-                                       stream));
+                                       list, status + 1, stream));
 }
 
 h3q_status h3q_workspace_status(const void* workspace, int64_t M, int64_t K,
@@ -136,11 +157,27 @@ h3q_status h3q_workspace_status(const void* workspace, int64_t M, int64_t K,
   if (h3q_status st = check_device()) return st;
   const uint8_t* wsp = static_cast<const uint8_t*>(workspace);
   uint32_t word = 0;
-  if (cudaMemcpyAsync(&word, wsp + h3q::gemm_tc_status_offset(M, K), sizeof(word),
+  if (cudaMemcpyAsync(&word, wsp + h3q::workspace_layout(M, 1, K).status, sizeof(word),
                       cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
       cudaStreamSynchronize(stream) != cudaSuccess)
     return H3Q_ERR_CUDA;
   return word ? H3Q_ERR_TIMEOUT : H3Q_OK;
+}
+
+h3q_status h3q_linear_chunked_tiles(const void* workspace, int64_t M, int64_t K,
+                                    int64_t* tiles, cudaStream_t stream) {
+  if (!workspace || !tiles) return H3Q_ERR_INVALID_ARG;
+  if (M < 1 || K < 1) return H3Q_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(workspace)) return H3Q_ERR_MISALIGNED;
+  if (h3q_status st = check_device()) return st;
+  const uint8_t* wsp = static_cast<const uint8_t*>(workspace);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, wsp + h3q::workspace_layout(M, 1, K).status + 4, sizeof(word),
+                      cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return H3Q_ERR_CUDA;
+  *tiles = int64_t(word);
+  return H3Q_OK;
 }
 
 h3q_status h3q_linear_w8a8_mma_sync(const int8_t* xq, const float* xs, const int8_t* wq,

@@ -128,9 +128,16 @@ struct Shape {
 };
 
 // Cluster tile t -> token block mb and the channel block nb of CTA `rank`
-// (nb >= nt for the spare CTA of an odd channel-block count).
-__device__ __forceinline__ void tile_coords(const Shape& s, int t, uint32_t rank, int& mb,
-                                            int& nb) {
+// (nb >= nt for the spare CTA of an odd channel-block count).  With a list,
+// entry t names the tile: {token block, channel-block pair}.
+__device__ __forceinline__ void tile_coords(const Shape& s, const uint2* list, int t,
+                                            uint32_t rank, int& mb, int& nb) {
+  if (list) {
+    const uint2 e = list[t];
+    mb = int(e.x);
+    nb = int(e.y) * CLUSTER + int(rank);
+    return;
+  }
   const int per_group = GROUP_M * s.ntc;
   const int g = t / per_group;
   const int first_m = g * GROUP_M;
@@ -144,7 +151,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
                const __grid_constant__ CUtensorMap w_map, const float* __restrict__ sa,
                const float* __restrict__ sw, const uint16_t* __restrict__ bias, const Shape shp,
-               uint16_t* __restrict__ Y, int32_t* __restrict__ ACC, uint32_t* __restrict__ err) {
+               uint16_t* __restrict__ Y, int32_t* __restrict__ ACC, uint32_t* __restrict__ err,
+               const uint2* __restrict__ list, const uint32_t* __restrict__ list_len) {
+  // every CTA of the grid reads the same tile count, so all leave together
+  // (before any cluster barrier) when there is nothing to do
+  const int ntiles = list ? int(*list_len) : shp.tiles;
+  if (ntiles == 0) return;
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~uintptr_t(1023));
@@ -184,9 +196,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
       P::tma_prefetch_desc(&act_map);
       uint32_t gs = 0, gb = 0;             // super-stages seen, slots issued
       bool ok = true;
-      for (int t = cid; ok && t < shp.tiles; t += ncl) {
+      for (int t = cid; ok && t < ntiles; t += ncl) {
         int mb, nb;
-        tile_coords(shp, t, rank, mb, nb);
+        tile_coords(shp, list, t, rank, mb, nb);
         for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
           const uint32_t slot = gs % SLOTS;
           // the slot is free once both CTAs' MMAs finished its previous use
@@ -215,9 +227,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
       P::tma_prefetch_desc(&w_map);
       uint32_t gs = 0, gw = 0;
       bool ok = true;
-      for (int t = cid; ok && t < shp.tiles; t += ncl) {
+      for (int t = cid; ok && t < ntiles; t += ncl) {
         int mb, nb;
-        tile_coords(shp, t, rank, mb, nb);
+        tile_coords(shp, list, t, rank, mb, nb);
         const int wrow = min(nb, shp.nt - 1) * BM;
         for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
           const uint32_t slot = gs % W_SLOTS;
@@ -245,7 +257,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
     if (lane == 0) {
       uint32_t gs = 0, gc = 0;            // super-stage and chunk counters
       bool ok = true;
-      for (int t = cid; ok && t < shp.tiles; t += ncl) {
+      for (int t = cid; ok && t < ntiles; t += ncl) {
         for (int c = 0; ok && c < shp.nchunks; ++c, ++gc) {
           const int ss0 = c * shp.sspc, ss1 = min(shp.NSS, ss0 + shp.sspc);
           const uint32_t buf = gc & 1u;
@@ -292,7 +304,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
     const uint32_t row_off = uint32_t(r) * 128u, xr = uint32_t(r & 7);
     uint32_t gs = 0;
     bool ok = true;
-    for (int t = cid; ok && t < shp.tiles; t += ncl) {
+    for (int t = cid; ok && t < ntiles; t += ncl) {
       for (int ss = 0; ok && ss < shp.NSS; ++ss, ++gs) {
         const uint32_t slot = gs % SLOTS, ph = (gs / SLOTS) & 1u;
         const uint32_t wslot = gs % W_SLOTS;
@@ -344,9 +356,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
     const uint32_t lane_base = uint32_t(32 * q) << 16;
     uint32_t gc = 0;
     bool ok = true;
-    for (int t = cid; ok && t < shp.tiles; t += ncl) {
+    for (int t = cid; ok && t < ntiles; t += ncl) {
       int mb, nb;
-      tile_coords(shp, t, rank, mb, nb);
+      tile_coords(shp, list, t, rank, mb, nb);
       const int n = nb * BM + 32 * q + lane;
       const bool n_ok = n < shp.N;
       int rs[64];                                 // exact INT32 running sums
@@ -401,37 +413,49 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
   P::cluster_sync();                              // no peer still signals or writes here
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = [] {
+}  // namespace
+
+void* tensor_map_encoder() {
+  static void* fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess)
       p = nullptr;
-    return reinterpret_cast<EncodeTiledFn>(p);
+    return p;
   }();
   return fn;
 }
 
-}  // namespace
-
 int64_t gemm_tc_coded_ld(int64_t K) { return (K + BK - 1) / BK * BK; }
 
-size_t gemm_tc_status_offset(int64_t M, int64_t K) {
-  return (size_t(M) * size_t(gemm_tc_coded_ld(K)) * 2u + 255u) & ~size_t(255);
+WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K) {
+  auto up = [](size_t b) { return (b + 255u) & ~size_t(255); };
+  const size_t mt2 = size_t((M + kNormTokens - 1) / kNormTokens);
+  const size_t mt = size_t((M + BN - 1) / BN);
+  const size_t nt = size_t((N + BM - 1) / BM);
+  const size_t ntc = (nt + CLUSTER - 1) / CLUSTER;
+  WorkspaceLayout l;
+  l.act = 0;
+  l.amax = up(size_t(M) * size_t(gemm_tc_coded_ld(K)) * 2u);
+  l.status = l.amax + up(mt2 * 4u);
+  l.nwpart = l.status + 256u;
+  l.list = l.nwpart + up(nt * kNormParts * 4u);
+  l.total = l.list + up(mt * ntc * sizeof(uint2));
+  return l;
 }
 
 cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_t* qw,
                            const float* sw, const uint16_t* bias, int64_t M, int64_t N,
-                           int64_t K, uint16_t* y, int32_t* acc, uint32_t* err, cudaStream_t s) {
-  EncodeTiledFn enc = encode_fn();
+                           int64_t K, uint16_t* y, int32_t* acc, uint32_t* err,
+                           const uint2* list, const uint32_t* list_len, cudaStream_t s) {
+  EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
   if (!enc) return cudaErrorNotSupported;
   // activations: a [M, ld] FP16 matrix viewed as (64-element chunk, row, chunk index),
   // so one box carries two whole k-block tiles, one after the other
@@ -489,7 +513,8 @@ cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, map, wmap, sa, sw, bias, shp, y, acc, err);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, map, wmap, sa, sw, bias, shp, y, acc, err,
+                            list, list_len);
 }
 
 }  // namespace h3q

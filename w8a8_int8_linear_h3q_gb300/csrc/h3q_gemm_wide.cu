@@ -1,0 +1,525 @@
+// h3q_gemm_wide.cu -- A3 + A4 on the sm_103a tensor cores for the tiles whose
+// FP32 sums are exact over the whole K.
+//
+//   acc[m,n] = sum_k qa[m,k] * qw[n,k]          exact INT32
+//   y[m,n]   = BF16_RNE(acc * sa[m] * sw[n] + bias[n])
+//
+// Sources: "feat(mps): support MiniMax-H3 INT8 inference on Apple M5"
+// (LightX2V #1672) -- Validation (INT8 x INT8 with CPU INT32 references),
+// opening description (native K = 5376, no weight dequantisation); "MLX
+// implementation and experiment report", What the default preserves (bias
+// before the one rounding).
+//
+// The arithmetic is the chunked kernel's (INT8 values carried exactly by the
+// FP16 MMA, FP32 accumulation in TMEM); the exactness argument differs.  For
+// a token row a and a channel row w, every partial sum the tensor core can
+// form from the products a_k w_k, in any order and grouping, is at most
+// sum_k |a_k w_k| <= |a|_2 |w|_2 in magnitude (Cauchy-Schwarz).  When
+// |a|_2^2 |w|_2^2 <= 2^48, every partial sum is an integer of magnitude
+// <= 2^24 and hence an FP32 value, so no addition rounds and one FP32
+// accumulator carries the exact dot product over all of K.  The activation
+// quantiser records, per block of 256 tokens, the largest sum of squares of a
+// coded row; a weight pre-pass records the same per 16 channels.  A cluster
+// tile (two 128-channel blocks x 256 tokens) is computed here when the
+// product of its two maxima is at most 2^48, which holds when the codes are
+// mostly well below 127 in magnitude -- the usual case for per-row absmax
+// scaling of K = 5376 rows.  The other tiles go to a list in the workspace
+// that the chunked kernel finishes afterwards.
+//
+// Against the chunked kernel this removes the per-chunk accumulator drains
+// (one drain per tile) and lets each converted weight slice feed 256 tokens
+// (one N = 256 MMA) instead of 128, halving the converter warps' TMEM stores
+// per MMA, which compete with the MMAs for TMEM.
+//
+// Warp roles (736 threads):
+//   warp 0      TMA producer of the activation tiles (2 super-stage slots),
+//               multicast to the cluster peer
+//   warp 1      TMEM allocator and MMA issuer (one thread)
+//   warp 2      tile scheduler (exactness test, fallback list) and TMA
+//               producer of the INT8 weight tiles (4 super-stage slots)
+//   warps 3-6   converters: INT8 weights -> FP16 -> TMEM (2 super-stages)
+//   warps 7-22  epilogue: drain the accumulator to registers, release it,
+//               then dequant + bias + BF16 (and the optional raw INT32)
+// A super-stage is 2 k-blocks of 64 K: 8 MMAs of 128 x 256 x 16.
+// TMEM: the FP32 accumulator in columns 0-255, A super-stages in 256-319 and
+// 320-383.
+// Every wait is bounded in time; on a timeout the kernel records an error
+// bit, lets every role fall through, drains its in-flight copies and MMAs,
+// frees TMEM and returns.
+#include <cuda.h>
+
+#include "h3q_epilogue.cuh"
+#include "h3q_internal.cuh"
+#include "h3q_tc_ptx.cuh"
+
+namespace h3q {
+namespace {
+
+namespace P = ptx;
+
+constexpr int BM = 128;                 // channels per CTA tile (MMA M, TMEM lanes)
+constexpr int BN = kNormTokens;         // tokens per tile (MMA N)
+constexpr int BK = 64;                  // K per k-block (128 bytes of FP16)
+constexpr int SS = 2;                   // k-blocks per super-stage (8 MMAs)
+constexpr int SLOTS = 2;                // super-stage slots: activations (SMEM), FP16 weights (TMEM)
+constexpr int W_SLOTS = 4;              // super-stage slots: INT8 weights (SMEM)
+constexpr int SQ = 4;                   // tile-queue entries
+constexpr int GROUP_M = 8;              // token blocks per raster group
+constexpr int CLUSTER = 2;
+constexpr uint16_t CLUSTER_MASK = (1u << CLUSTER) - 1;
+constexpr int MMA_WARP = 1;
+constexpr int SCHED_WARP = 2;
+constexpr int CONV_WARP0 = 3;
+constexpr int NUM_CONV_WARPS = 4;
+constexpr int EPI_WARP0 = CONV_WARP0 + NUM_CONV_WARPS;
+constexpr int NUM_EPI_WARPS = 16;
+constexpr int THREADS = 32 * (EPI_WARP0 + NUM_EPI_WARPS);
+// every role but the scheduler takes each tile from the queue: one arrival
+// per producer or MMA thread, one per converter or epilogue warp
+constexpr int QUEUE_READERS = 2 + NUM_CONV_WARPS + NUM_EPI_WARPS;
+constexpr int B_KBLOCK_BYTES = BN * BK * 2;                // 32 KB
+constexpr int W_BOX_BYTES = BM * SS * BK;                  // 16 KB: 128 rows x 2 k-blocks
+constexpr uint32_t TM_D = 0;
+constexpr uint32_t TM_A = BN;
+constexpr uint32_t TM_COLS = 512;
+constexpr uint32_t IDESC = P::idesc_f16_f32(BM, BN);
+constexpr uint64_t kExactBound = uint64_t(1) << 48;        // |a|^2 |w|^2 limit
+
+// error bits (the chunked kernel uses the low byte)
+constexpr uint32_t ERR_PRODUCER = 1u << 8, ERR_MMA = 2u << 8, ERR_CONVERT = 4u << 8,
+                   ERR_EPILOGUE = 8u << 8, ERR_TEARDOWN = 16u << 8, ERR_SCHED = 32u << 8;
+
+struct __align__(1024) Smem {
+  uint8_t b[SLOTS][SS][B_KBLOCK_BYTES];  // activation k-blocks of a super-stage slot
+  uint8_t w[W_SLOTS][W_BOX_BYTES];       // INT8 weights: 128-byte rows, 128-byte swizzle
+  uint64_t full_b[SLOTS];                // a slot's activation tiles have landed
+  uint64_t full_w[W_SLOTS];              // a slot's INT8 weights have landed
+  uint64_t empty_w[W_SLOTS];             // the converters have read them
+  uint64_t full_a[SLOTS];                // A converted and B landed for a super-stage
+  uint64_t empty_s[SLOTS];               // both CTAs' MMAs are done with a slot
+  uint64_t dfull, dempty, mma_done;
+  uint64_t q_full[SQ], q_empty[SQ];      // tile queue
+  int q_tile[SQ];                        // cluster tile index, or -1: no more tiles
+  uint32_t tmem_base;
+  int abort_flag;
+};
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;   // + slack for 1024-byte alignment
+
+struct Shape {
+  int M, N, K;
+  int KB;             // k-blocks
+  int NSS;            // super-stages per tile
+  int mt, nt;         // 256-token blocks, 128-channel blocks
+  int mt128;          // 128-token blocks (the chunked kernel's tiles)
+  int ntc;            // channel-block pairs
+  int tiles;          // cluster tiles: mt * ntc
+};
+
+// Cluster tile t -> token block mb (256 tokens) and channel-block pair.
+__device__ __forceinline__ void tile_coords(const Shape& s, int t, int& mb, int& pair) {
+  const int per_group = GROUP_M * s.ntc;
+  const int g = t / per_group;
+  const int first_m = g * GROUP_M;
+  const int gm = min(GROUP_M, s.mt - first_m);
+  const int r = t - g * per_group;
+  mb = first_m + r % gm;
+  pair = r / gm;
+}
+
+// Warp-collective: true when every (token, channel) of the cluster tile has
+// |a|^2 |w|^2 <= 2^48.  Lanes 0-15 read the pair's 16 weight partial maxima.
+__device__ __forceinline__ bool tile_exact(const Shape& s, const uint32_t* amax,
+                                           const uint32_t* nwpart, int mb, int pair, int lane) {
+  const int idx = pair * CLUSTER * kNormParts + lane;
+  uint32_t w = (lane < CLUSTER * kNormParts && idx < s.nt * kNormParts) ? nwpart[idx] : 0u;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) w = max(w, __shfl_xor_sync(0xFFFFFFFFu, w, o));
+  const uint32_t a = amax[mb];
+  return uint64_t(w) * uint64_t(a) <= kExactBound;
+}
+
+// Single-thread take of the next queue entry.  False on a timeout or abort.
+__device__ __forceinline__ bool pop_tile(Smem& sm, uint32_t& nq, volatile int* abort_flag,
+                                         uint32_t* err, uint32_t code, int& t) {
+  const uint32_t q = nq % SQ;
+  if (!P::mbar_wait(&sm.q_full[q], (nq / SQ) & 1u, abort_flag, err, code)) return false;
+  t = sm.q_tile[q];
+  P::mbar_arrive(&sm.q_empty[q]);
+  ++nq;
+  return true;
+}
+
+// Warp-collective take; one arrival for the warp.
+__device__ __forceinline__ bool pop_tile_warp(Smem& sm, uint32_t& nq, volatile int* abort_flag,
+                                              uint32_t* err, uint32_t code, int& t, int lane) {
+  const uint32_t q = nq % SQ;
+  if (!P::mbar_wait_warp(&sm.q_full[q], (nq / SQ) & 1u, abort_flag, err, code)) return false;
+  t = sm.q_tile[q];
+  __syncwarp();
+  if (lane == 0) P::mbar_arrive(&sm.q_empty[q]);
+  ++nq;
+  return true;
+}
+
+__device__ __forceinline__ bool push_tile(Smem& sm, uint32_t& nq, int t, volatile int* abort_flag,
+                                          uint32_t* err) {
+  const uint32_t q = nq % SQ;
+  if (!P::mbar_wait(&sm.q_empty[q], ((nq / SQ) & 1u) ^ 1u, abort_flag, err, ERR_SCHED))
+    return false;
+  sm.q_tile[q] = t;
+  P::mbar_arrive(&sm.q_full[q]);
+  ++nq;
+  return true;
+}
+
+// 23 warps: at most 6 per SM sub-partition, so 80 registers a thread.
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
+                 const __grid_constant__ CUtensorMap w_map, const float* __restrict__ sa,
+                 const float* __restrict__ sw, const uint16_t* __restrict__ bias,
+                 const Shape shp, uint16_t* __restrict__ Y, int32_t* __restrict__ ACC,
+                 const uint32_t* __restrict__ amax, const uint32_t* __restrict__ nwpart,
+                 uint32_t* __restrict__ status, uint2* __restrict__ list) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                      ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = &sm.abort_flag;
+  uint32_t* err = status;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < W_SLOTS; ++i) {
+      P::mbar_init(&sm.full_w[i], 1);
+      P::mbar_init(&sm.empty_w[i], NUM_CONV_WARPS * 32);
+    }
+    for (int i = 0; i < SLOTS; ++i) {
+      P::mbar_init(&sm.full_b[i], 1);
+      P::mbar_init(&sm.full_a[i], NUM_CONV_WARPS * 32);
+      P::mbar_init(&sm.empty_s[i], CLUSTER);      // one multicast commit per CTA
+    }
+    for (int i = 0; i < SQ; ++i) {
+      P::mbar_init(&sm.q_full[i], 1);
+      P::mbar_init(&sm.q_empty[i], QUEUE_READERS);
+    }
+    P::mbar_init(&sm.dfull, 1);
+    P::mbar_init(&sm.dempty, NUM_EPI_WARPS * 32);
+    P::mbar_init(&sm.mma_done, 1);
+    sm.abort_flag = 0;
+    P::fence_mbar_init();
+  }
+  if (warp == MMA_WARP) P::tmem_alloc(&sm.tmem_base, TM_COLS);
+  P::tc_fence_before();
+  __syncthreads();
+  P::cluster_sync();                              // peers' barriers exist before multicasts
+  P::tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const uint32_t rank = P::cluster_rank();
+  const int cid = int(P::cluster_id_x()), ncl = int(P::num_clusters_x());
+
+  if (warp == 0) {
+    // ---------------- TMA producer: activation tiles ----------------
+    if (lane == 0) {
+      P::tma_prefetch_desc(&act_map);
+      uint32_t gs = 0, gb = 0, nq = 0;
+      bool ok = true;
+      for (;;) {
+        int t;
+        if (!pop_tile(sm, nq, abort_flag, err, ERR_PRODUCER, t) || t < 0) break;
+        int mb, pair;
+        tile_coords(shp, t, mb, pair);
+        for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
+          const uint32_t slot = gs % SLOTS;
+          // the slot is free once both CTAs' MMAs finished its previous use
+          if (!P::mbar_wait(&sm.empty_s[slot], ((gs / SLOTS) & 1u) ^ 1u, abort_flag, err,
+                            ERR_PRODUCER)) {
+            ok = false;
+            break;
+          }
+          // both k-blocks land here: this CTA's and the peer's
+          P::mbar_arrive_expect_tx(&sm.full_b[slot], SS * B_KBLOCK_BYTES);
+          P::tma_load_3d_mc(P::smem_u32(sm.b[slot][rank]), &act_map, &sm.full_b[slot], 0,
+                            mb * BN, ss * SS + int(rank), CLUSTER_MASK);
+          gb = gs + 1;
+        }
+        if (!ok) break;
+      }
+      // no copy may still be landing in shared memory when the CTA exits
+      int no_abort = 0;
+      volatile int* never = &no_abort;   // this drain does not follow the abort flag
+      for (uint32_t i = gb > SLOTS ? gb - SLOTS : 0; i < gb; ++i)
+        P::mbar_wait(&sm.full_b[i % SLOTS], (i / SLOTS) & 1u, never, err, ERR_TEARDOWN);
+    }
+    __syncwarp();
+  } else if (warp == SCHED_WARP) {
+    // ---------------- scheduler + TMA producer: INT8 weight tiles ----------------
+    if (lane == 0) P::tma_prefetch_desc(&w_map);
+    uint32_t gs = 0, gw = 0, nq = 0;
+    bool ok = true;
+    for (int t = cid; t < shp.tiles; t += ncl) {
+      int mb, pair;
+      tile_coords(shp, t, mb, pair);
+      if (!tile_exact(shp, amax, nwpart, mb, pair, lane)) {
+        // the chunked kernel takes it, as one or two 128-token tiles
+        if (rank == 0 && lane == 0) {
+          const int n128 = min(2, shp.mt128 - 2 * mb);
+          const uint32_t i = atomicAdd(status + 1, uint32_t(n128));
+          for (int h = 0; h < n128; ++h)
+            list[i + h] = make_uint2(uint32_t(2 * mb + h), uint32_t(pair));
+        }
+        continue;
+      }
+      if (lane == 0) {
+        ok = push_tile(sm, nq, t, abort_flag, err);
+        const int wrow = min(2 * pair + int(rank), shp.nt - 1) * BM;
+        for (int ss = 0; ok && ss < shp.NSS; ++ss, ++gs) {
+          const uint32_t slot = gs % W_SLOTS;
+          if (!P::mbar_wait(&sm.empty_w[slot], ((gs / W_SLOTS) & 1u) ^ 1u, abort_flag, err,
+                            ERR_SCHED)) {
+            ok = false;
+            break;
+          }
+          P::mbar_arrive_expect_tx(&sm.full_w[slot], W_BOX_BYTES);
+          P::tma_load_2d(P::smem_u32(sm.w[slot]), &w_map, &sm.full_w[slot], ss * SS * BK, wrow);
+          gw = gs + 1;
+        }
+      }
+      if (!__shfl_sync(0xFFFFFFFFu, int(ok), 0)) break;
+    }
+    if (lane == 0) {
+      if (ok) push_tile(sm, nq, -1, abort_flag, err);
+      int no_abort = 0;
+      volatile int* never = &no_abort;
+      for (uint32_t i = gw > W_SLOTS ? gw - W_SLOTS : 0; i < gw; ++i)
+        P::mbar_wait(&sm.full_w[i % W_SLOTS], (i / W_SLOTS) & 1u, never, err, ERR_TEARDOWN);
+    }
+    __syncwarp();
+  } else if (warp == MMA_WARP) {
+    // ---------------- MMA issuer: one wait and one commit per 8 MMAs ----------------
+    if (lane == 0) {
+      uint32_t gs = 0, gt = 0, nq = 0;
+      bool ok = true;
+      for (;;) {
+        int t;
+        if (!pop_tile(sm, nq, abort_flag, err, ERR_MMA, t) || t < 0) break;
+        // the epilogue has copied out the previous tile's accumulator
+        if (!P::mbar_wait(&sm.dempty, (gt & 1u) ^ 1u, abort_flag, err, ERR_MMA)) break;
+        for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
+          const uint32_t slot = gs % SLOTS;
+          if (!P::mbar_wait(&sm.full_a[slot], (gs / SLOTS) & 1u, abort_flag, err, ERR_MMA)) {
+            ok = false;
+            break;
+          }
+          P::tc_fence_after();
+          const uint32_t a_tmem = tmem + TM_A + slot * (SS * 32);
+          const int nkb = min(SS, shp.KB - ss * SS);
+          for (int j = 0; j < nkb; ++j) {
+            const uint64_t bdesc = P::smem_desc_sw128(P::smem_u32(sm.b[slot][j]));
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              P::mma_f16_ts(tmem + TM_D, a_tmem + j * 32 + kk * 8, bdesc + uint64_t(kk * 2),
+                            IDESC, (ss > 0 || j > 0 || kk > 0) ? 1u : 0u);
+          }
+          P::mma_commit_mc(&sm.empty_s[slot], CLUSTER_MASK);
+        }
+        if (!ok) break;
+        P::mma_commit(&sm.dfull);
+        ++gt;
+      }
+      // every MMA this thread issued has finished before TMEM is freed
+      P::mma_commit(&sm.mma_done);
+      int no_abort = 0;
+      volatile int* never = &no_abort;
+      P::mbar_wait(&sm.mma_done, 0, never, err, ERR_TEARDOWN);
+    }
+    __syncwarp();
+  } else if (warp < EPI_WARP0) {
+    // ---------------- converters: INT8 weights -> FP16 -> TMEM ----------------
+    const int q = warp & 3;                       // TMEM lane quarter of this warp
+    const int r = 32 * q + lane;                  // channel row within the tile
+    const uint32_t lane_base = uint32_t(32 * q) << 16;
+    // this row's 16-byte chunks in a 128-byte-swizzled INT8 box (two k-blocks)
+    const uint32_t row_off = uint32_t(r) * 128u, xr = uint32_t(r & 7);
+    uint32_t gs = 0, nq = 0;
+    bool ok = true;
+    while (ok) {
+      int t;
+      if (!pop_tile_warp(sm, nq, abort_flag, err, ERR_CONVERT, t, lane) || t < 0) break;
+      for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
+        const uint32_t slot = gs % SLOTS, ph = (gs / SLOTS) & 1u;
+        const uint32_t wslot = gs % W_SLOTS;
+        const int nkb = min(SS, shp.KB - ss * SS);
+        if (!P::mbar_wait_warp(&sm.full_w[wslot], (gs / W_SLOTS) & 1u, abort_flag, err,
+                               ERR_CONVERT)) {
+          ok = false;
+          break;
+        }
+        for (int j = 0; j < nkb; ++j) {
+          const uint8_t* box = sm.w[wslot];
+          const uint32_t cb = uint32_t(j) * 4u;
+          uint4 v[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            v[i] = *reinterpret_cast<const uint4*>(box + row_off + (((cb + uint32_t(i)) ^ xr) << 4));
+          uint32_t h[32];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            P::s8x4_to_f16x4(v[i].x, h[8 * i + 0], h[8 * i + 1]);
+            P::s8x4_to_f16x4(v[i].y, h[8 * i + 2], h[8 * i + 3]);
+            P::s8x4_to_f16x4(v[i].z, h[8 * i + 4], h[8 * i + 5]);
+            P::s8x4_to_f16x4(v[i].w, h[8 * i + 6], h[8 * i + 7]);
+          }
+          if (j == 0 &&
+              !P::mbar_wait_warp(&sm.empty_s[slot], ph ^ 1u, abort_flag, err, ERR_CONVERT)) {
+            ok = false;
+            break;
+          }
+          P::tc_fence_after();
+          P::tmem_st32(tmem + lane_base + TM_A + slot * (SS * 32) + uint32_t(j) * 32, h);
+        }
+        if (!ok) break;
+        P::mbar_arrive(&sm.empty_w[wslot]);       // this slot's INT8 weights may be refilled
+        // forward the readiness of the slot's activation tiles to the MMA thread
+        if (!P::mbar_wait_warp(&sm.full_b[slot], ph, abort_flag, err, ERR_CONVERT)) {
+          ok = false;
+          break;
+        }
+        P::tmem_wait_st();
+        P::tc_fence_before();
+        P::mbar_arrive(&sm.full_a[slot]);
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;                       // TMEM lane quarter
+    const int cq = (warp - EPI_WARP0) >> 2;       // token columns [64*cq, +64)
+    const uint32_t lane_base = uint32_t(32 * q) << 16;
+    uint32_t gt = 0, nq = 0;
+    for (;;) {
+      int t;
+      if (!pop_tile_warp(sm, nq, abort_flag, err, ERR_EPILOGUE, t, lane) || t < 0) break;
+      int mb, pair;
+      tile_coords(shp, t, mb, pair);
+      const int n = (2 * pair + int(rank)) * BM + 32 * q + lane;
+      const bool n_ok = n < shp.N;
+      const float swn = n_ok ? sw[n] : 0.f;
+      const float bn = (n_ok && bias) ? bf16_bits_to_float(bias[n]) : 0.f;
+      const int m0 = mb * BN + 64 * cq;
+      const float sa0 = (m0 + lane < shp.M) ? sa[m0 + lane] : 0.f;
+      const float sa1 = (m0 + 32 + lane < shp.M) ? sa[m0 + 32 + lane] : 0.f;
+      if (!P::mbar_wait_warp(&sm.dfull, gt & 1u, abort_flag, err, ERR_EPILOGUE)) break;
+      P::tc_fence_after();
+      uint32_t d0[32], d1[32];
+      P::tmem_ld32(tmem + lane_base + TM_D + 64 * cq, d0);
+      P::tmem_ld32(tmem + lane_base + TM_D + 64 * cq + 32, d1);
+      P::tmem_wait_ld();
+      P::tc_fence_before();
+      P::mbar_arrive(&sm.dempty);                 // the MMAs of the next tile may start
+      ++gt;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float saj = __shfl_sync(0xFFFFFFFFu, sa0, j);
+        const int m = m0 + j;
+        const int a = __float2int_rn(__uint_as_float(d0[j]));
+        if (n_ok && m < shp.M) {
+          const int64_t off = int64_t(m) * shp.N + n;
+          if (ACC) ACC[off] = a;
+          if (Y) Y[off] = float_to_bf16_bits(epilogue_value(a, saj, swn, bn));
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float saj = __shfl_sync(0xFFFFFFFFu, sa1, j);
+        const int m = m0 + 32 + j;
+        const int a = __float2int_rn(__uint_as_float(d1[j]));
+        if (n_ok && m < shp.M) {
+          const int64_t off = int64_t(m) * shp.N + n;
+          if (ACC) ACC[off] = a;
+          if (Y) Y[off] = float_to_bf16_bits(epilogue_value(a, saj, swn, bn));
+        }
+      }
+    }
+  }
+
+  P::tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    P::tc_fence_after();
+    P::tmem_dealloc(tmem, TM_COLS);
+  }
+  P::cluster_sync();                              // no peer still signals or writes here
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+}  // namespace
+
+cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const int8_t* qw,
+                             const float* sw, const uint16_t* bias, int64_t M, int64_t N,
+                             int64_t K, uint16_t* y, int32_t* acc, const uint32_t* amax,
+                             const uint32_t* nwpart, uint32_t* status, uint2* list,
+                             cudaStream_t s) {
+  EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
+  if (!enc) return cudaErrorNotSupported;
+  // activations: a [M, ld] FP16 matrix viewed as (64-element chunk, row, chunk
+  // index); one box is one k-block of 256 rows
+  const int64_t ld = gemm_tc_coded_ld(K);
+  CUtensorMap map;
+  const cuuint64_t dims[3] = {cuuint64_t(BK), cuuint64_t(M), cuuint64_t(ld / BK)};
+  const cuuint64_t strides[2] = {cuuint64_t(ld) * 2u, cuuint64_t(BK) * 2u};
+  const cuuint32_t box[3] = {BK, BN, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t*>(act_f16), dims,
+          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  // weights: [N, K] INT8, boxes of 128 rows x 128 bytes (two k-blocks)
+  CUtensorMap wmap;
+  const cuuint64_t wdims[2] = {cuuint64_t(K), cuuint64_t(N)};
+  const cuuint64_t wstrides[1] = {cuuint64_t(K)};
+  const cuuint32_t wbox[2] = {SS * BK, BM};
+  if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(qw), wdims, wstrides,
+          wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+
+  Shape shp;
+  shp.M = int(M);
+  shp.N = int(N);
+  shp.K = int(K);
+  shp.KB = int((K + BK - 1) / BK);
+  shp.NSS = (shp.KB + SS - 1) / SS;
+  shp.mt = int((M + BN - 1) / BN);
+  shp.mt128 = int((M + 127) / 128);
+  shp.nt = int((N + BM - 1) / BM);
+  shp.ntc = (shp.nt + CLUSTER - 1) / CLUSTER;
+  shp.tiles = shp.mt * shp.ntc;
+
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(gemm_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  const int clusters = shp.tiles < sms / CLUSTER ? shp.tiles : sms / CLUSTER;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(clusters * CLUSTER));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CLUSTER;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_wide_kernel, map, wmap, sa, sw, bias, shp, y, acc, amax,
+                            nwpart, status, list);
+}
+
+}  // namespace h3q

@@ -15,32 +15,74 @@ constexpr int kQMax = 127;
 // already validated by the C-ABI layer.
 
 // A2: BF16 activations -> int8 (optional) + FP32 scale + FP16-coded q (optional,
-// rows of stride ldh >= K elements, the padding zeroed).
+// rows of stride ldh >= K elements, the padding zeroed).  sq_max (optional):
+// per block of 256 rows, the running maximum of the rows' sums of q^2
+// (atomicMax, so it must start at zero).
 cudaError_t launch_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t* q,
-                                float* scale, uint16_t* q_f16, int64_t ldh, cudaStream_t s);
+                                float* scale, uint16_t* q_f16, int64_t ldh, uint32_t* sq_max,
+                                cudaStream_t s);
 
 // A1: FP32 or BF16 weights -> int8 + FP32 scale.  A row with a non-finite
 // element gets a NaN scale, which the caller turns into H3Q_ERR_NONFINITE.
 cudaError_t launch_quantize_weights(const void* w, int w_dtype, int64_t N, int64_t K,
                                     int8_t* q, float* scale, cudaStream_t s);
 
-// int8 [M, K] -> FP16-coded integers with row stride ldh (padding zeroed).
+// int8 [M, K] -> FP16-coded integers with row stride ldh (padding zeroed),
+// with the per-256-row maxima of sum(q^2) as launch_quantize_act.
 cudaError_t launch_int8_to_f16(const int8_t* q, int64_t M, int64_t K, int64_t ldh,
-                               uint16_t* out, cudaStream_t s);
+                               uint16_t* out, uint32_t* sq_max, cudaStream_t s);
 
 // Row stride (elements) of the FP16-coded activations in the linear workspace.
 int64_t gemm_tc_coded_ld(int64_t K);
+
+// Tokens per block of the activation norm maxima (the wide kernel's tile).
+constexpr int kNormTokens = 256;
+// Weight-norm partial maxima per 128-channel block (16 channels each).
+constexpr int kNormParts = 8;
+
+// The linear workspace, in order (each part 256-byte aligned):
+//   act     [M, gemm_tc_coded_ld(K)] FP16-coded activations
+//   amax    [ceil(M/256)] u32: per 256 tokens, max over rows of sum(qa^2)
+//   status  256 bytes: word 0 error bits, word 1 fallback-list length
+//   nwpart  [ceil(N/128) * 8] u32: per 16 channels, max over rows of sum(qw^2)
+//   list    [ceil(M/128) * ceil(N/256)] uint2 {token block, channel pair}:
+//           the 128 x 256 tiles the chunked kernel must finish
+// act, amax and status depend on M and K only, so a call with another N
+// still finds the coded activations (reuse) and the status word there.
+struct WorkspaceLayout {
+  size_t act, amax, status, nwpart, list, total;
+};
+WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K);
+
+// Weight pre-pass: nwpart as above, and zeroes the u32 words [zero, zero+nzero)
+// (the status block, and the amax maxima when the activations are coded anew).
+cudaError_t launch_weight_norms(const int8_t* qw, int64_t N, int64_t K, uint32_t* nwpart,
+                                uint32_t* zero, int64_t nzero, cudaStream_t s);
+
+// A3 + A4 for the tiles whose FP32 sums are exact over the whole K (checked
+// per tile from amax and nwpart); the others are appended to `list`, and
+// status[1] counts the entries.  status[0]: error bits (bounded waits).
+cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const int8_t* qw,
+                             const float* sw, const uint16_t* bias, int64_t M, int64_t N,
+                             int64_t K, uint16_t* y, int32_t* acc, const uint32_t* amax,
+                             const uint32_t* nwpart, uint32_t* status, uint2* list,
+                             cudaStream_t s);
 
 // A3 + A4 on the tcgen05 tensor cores (exact INT32 via FP16 MMA with chunked
 // FP32 accumulation).  act_f16: [M, gemm_tc_coded_ld(K)] FP16-coded INT8
 // activations, the padding beyond K zero.
 // err: device status word (0 = ok; bits set when a bounded wait gave up).
+// list == NULL: every tile.  Otherwise only the *list_len tiles in `list`
+// (entries written by the wide kernel); the kernel exits at once when the
+// list is empty.
 cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_t* qw,
                            const float* sw, const uint16_t* bias, int64_t M, int64_t N,
-                           int64_t K, uint16_t* y, int32_t* acc, uint32_t* err, cudaStream_t s);
+                           int64_t K, uint16_t* y, int32_t* acc, uint32_t* err,
+                           const uint2* list, const uint32_t* list_len, cudaStream_t s);
 
-// Byte offset of the status word inside the linear workspace.
-size_t gemm_tc_status_offset(int64_t M, int64_t K);
+// cuTensorMapEncodeTiled, looked up through the runtime (no -lcuda); NULL if
+// the driver does not provide it.
+void* tensor_map_encoder();
 
 // A3 + A4 on the legacy warp-level INT8 tensor path (mma.sync m16n8k32 s8).
 cudaError_t launch_gemm_mma_s8(const int8_t* qa, const float* sa, const int8_t* qw,

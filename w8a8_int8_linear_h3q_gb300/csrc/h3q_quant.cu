@@ -54,11 +54,6 @@ __device__ __forceinline__ uint32_t f2s8_byte(float n) {
   return uint32_t(__float_as_int(__fadd_rn(n, 12582912.0f)) - 0x4B400000) & 0xFFu;
 }
 
-__device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
-  return (uint32_t(a) & 0xFFu) | ((uint32_t(b) & 0xFFu) << 8) | ((uint32_t(c) & 0xFFu) << 16) |
-         (uint32_t(d) << 24);
-}
-
 __device__ __forceinline__ uint32_t pack2_f16(int a, int b) {
   return uint32_t(__half_as_ushort(__int2half_rn(a))) |
          (uint32_t(__half_as_ushort(__int2half_rn(b))) << 16);
@@ -84,9 +79,12 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   return r;
 }
 
+// Quantises 8 values, stores them, and returns the sum of their squares
+// (exact: at most 8 * 127^2).
 template <bool kQ8, bool kF16>
-__device__ __forceinline__ void quant_store8(uint4 v, float s, float r, bool fast, int8_t* q8,
-                                             uint16_t* qh, int64_t elem, int64_t helem) {
+__device__ __forceinline__ uint32_t quant_store8(uint4 v, float s, float r, bool fast,
+                                                 int8_t* q8, uint16_t* qh, int64_t elem,
+                                                 int64_t helem) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   float q[8];
 #pragma unroll
@@ -110,6 +108,17 @@ __device__ __forceinline__ void quant_store8(uint4 v, float s, float r, bool fas
     o.w = pack2_f16f(q[6], q[7]);
     *reinterpret_cast<uint4*>(qh + helem) = o;
   }
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) ss = __fmaf_rn(q[j], q[j], ss);
+  return uint32_t(ss);
+}
+
+// Folds a row's sum of squares of q into the running maximum of its block of
+// 256 token rows (read by the GEMM to decide whether a tile's FP32 sums stay
+// exact without splitting K).
+__device__ __forceinline__ void record_row_sq(uint32_t* blk_max, int64_t row, uint32_t sq) {
+  if (blk_max) atomicMax(blk_max + (row >> 8), sq);
 }
 
 // One warp per token row.  kRegs: the whole row (<= 32 * kRegVecs vectors)
@@ -118,7 +127,8 @@ __device__ __forceinline__ void quant_store8(uint4 v, float s, float r, bool fas
 template <bool kRegs, bool kQ8, bool kF16>
 __global__ void __launch_bounds__(kWarps * 32)
 quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int K, int8_t* __restrict__ q8,
-                 float* __restrict__ scale, uint16_t* __restrict__ qh, int ldh) {
+                 float* __restrict__ scale, uint16_t* __restrict__ qh, int ldh,
+                 uint32_t* __restrict__ sq_max) {
   const int lane = threadIdx.x & 31;
   const int64_t row = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -145,14 +155,20 @@ quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int K, int8_t* __res
     const float s = row_scale(__uint_as_float(mbits << 16));
     const float r = __frcp_rn(s);
     const bool fast = s >= 0x1p-120f;
+    uint32_t sq = 0;
 #pragma unroll
     for (int i = 0; i < kRegVecs; ++i) {
       const int j = lane + 32 * i;
       if (j < nvec)
-        quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh, base + 8 * int64_t(j),
-                                hbase + 8 * int64_t(j));
+        sq += quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh, base + 8 * int64_t(j),
+                                      hbase + 8 * int64_t(j));
     }
-    if (lane == 0) scale[row] = s;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+    if (lane == 0) {
+      scale[row] = s;
+      record_row_sq(sq_max, row, sq);
+    }
   } else {
     int j = lane;
     for (; j + 96 < nvec; j += 128) {
@@ -167,10 +183,16 @@ quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int K, int8_t* __res
     const float s = row_scale(__uint_as_float(mbits << 16));
     const float r = __frcp_rn(s);
     const bool fast = s >= 0x1p-120f;
+    uint32_t sq = 0;
     for (j = lane; j < nvec; j += 32)
-      quant_store8<kQ8, kF16>(ld_stream(xr + j), s, r, fast, q8, qh, base + 8 * int64_t(j),
-                              hbase + 8 * int64_t(j));
-    if (lane == 0) scale[row] = s;
+      sq += quant_store8<kQ8, kF16>(ld_stream(xr + j), s, r, fast, q8, qh,
+                                    base + 8 * int64_t(j), hbase + 8 * int64_t(j));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+    if (lane == 0) {
+      scale[row] = s;
+      record_row_sq(sq_max, row, sq);
+    }
   }
 }
 
@@ -182,8 +204,10 @@ constexpr int kRowThreads = 256;
 template <int kVPT, bool kQ8, bool kF16>
 __global__ void __launch_bounds__(kRowThreads)
 quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__ q8,
-                     float* __restrict__ scale, uint16_t* __restrict__ qh, int ldh) {
+                     float* __restrict__ scale, uint16_t* __restrict__ qh, int ldh,
+                     uint32_t* __restrict__ sq_max) {
   __shared__ uint32_t red[kRowThreads / 32];
+  __shared__ uint32_t red_sq[kRowThreads / 32];
   const int64_t row = blockIdx.x;
   const int nvec = K >> 3;
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * int64_t(K));
@@ -211,14 +235,27 @@ quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__
   const float s = row_scale(__uint_as_float(mbits << 16));
   const float r = __frcp_rn(s);
   const bool fast = s >= 0x1p-120f;
+  uint32_t sq = 0;
 #pragma unroll
   for (int i = 0; i < kVPT; ++i) {
     const int j = threadIdx.x + kRowThreads * i;
     if (j < nvec)
-      quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh, base + 8 * int64_t(j),
-                              hbase + 8 * int64_t(j));
+      sq += quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh, base + 8 * int64_t(j),
+                                    hbase + 8 * int64_t(j));
   }
   if (threadIdx.x == 0) scale[row] = s;
+  if (sq_max) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+    if ((threadIdx.x & 31) == 0) red_sq[threadIdx.x >> 5] = sq;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t t = 0;
+#pragma unroll
+      for (int w = 0; w < kRowThreads / 32; ++w) t += red_sq[w];
+      record_row_sq(sq_max, row, t);
+    }
+  }
 }
 
 // Weight rows: FP32 or BF16.  Not on the timed path; plain two-pass loops,
@@ -256,16 +293,16 @@ quant_weight_kernel(const T* __restrict__ w, int64_t N, int K, int8_t* __restric
   if (lane == 0) scale[row] = bad ? __int_as_float(0x7FC00000) : s;
 }
 
-// One thread per 16 INT8 values of a row; the coded rows have stride ldh
-// (padding zeroed).
-__global__ void int8_to_f16_kernel(const int8_t* __restrict__ q, int64_t M, int K, int ldh,
-                                   uint16_t* __restrict__ out) {
-  const int per_row = ldh >> 4;                     // 16-element groups per coded row
-  const int64_t total = M * per_row;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t row = i / per_row;
-    const int grp = int(i - row * per_row);
+// One 256-thread block per row: INT8 -> FP16-coded integers, rows of stride
+// ldh with the padding zeroed, and the row's sum of squares.
+__global__ void __launch_bounds__(256)
+int8_to_f16_kernel(const int8_t* __restrict__ q, int K, int ldh, uint16_t* __restrict__ out,
+                   uint32_t* __restrict__ sq_max) {
+  __shared__ uint32_t red[8];
+  const int64_t row = blockIdx.x;
+  const int groups = ldh >> 4;                      // 16-element groups of a coded row
+  uint32_t sq = 0;
+  for (int grp = threadIdx.x; grp < groups; grp += 256) {
     uint4* dst = reinterpret_cast<uint4*>(out + row * ldh + 16 * int64_t(grp));
     if (16 * grp >= K) {
       dst[0] = make_uint4(0, 0, 0, 0);
@@ -281,47 +318,115 @@ __global__ void int8_to_f16_kernel(const int8_t* __restrict__ q, int64_t M, int 
       const int b2 = int(int8_t(w[j] >> 16)), b3 = int(int8_t(w[j] >> 24));
       o[2 * j] = pack2_f16(b0, b1);
       o[2 * j + 1] = pack2_f16(b2, b3);
+      sq = uint32_t(__dp4a(int(w[j]), int(w[j]), int(sq)));
     }
     dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+  if (sq_max) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sq;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t t = 0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) t += red[w];
+      record_row_sq(sq_max, row, t);
+    }
+  }
+}
+
+// One block of 16 warps per 16 weight rows (block b: rows 16b .. 16b+15):
+// each warp sums q^2 over its row with DP4A on 16-byte loads, and the block
+// writes the largest row sum to part[b].  The sums are taken modulo 2^32,
+// which is exact: K * 128^2 < 2^32 for every supported K.  All blocks also
+// zero the words [zero, zero + nzero).
+constexpr int kNormRows = 16;
+
+__global__ void __launch_bounds__(32 * kNormRows)
+weight_norm_kernel(const int8_t* __restrict__ wq, int64_t N, int K, uint32_t* __restrict__ part,
+                   uint32_t* __restrict__ zero, int64_t nzero) {
+  __shared__ uint32_t red[kNormRows];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < nzero; i += stride)
+    zero[i] = 0u;
+  const int64_t n = int64_t(blockIdx.x) * kNormRows + warp;
+  uint32_t sq = 0;
+  if (n < N) {
+    const uint4* row = reinterpret_cast<const uint4*>(wq + n * K);
+    const int nv = K >> 4;
+    int i = lane;
+    for (; i + 96 < nv; i += 128) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldg(row + i + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        sq = uint32_t(__dp4a(int(v[u].x), int(v[u].x), int(sq)));
+        sq = uint32_t(__dp4a(int(v[u].y), int(v[u].y), int(sq)));
+        sq = uint32_t(__dp4a(int(v[u].z), int(v[u].z), int(sq)));
+        sq = uint32_t(__dp4a(int(v[u].w), int(v[u].w), int(sq)));
+      }
+    }
+    for (; i < nv; i += 32) {
+      const uint4 v = __ldg(row + i);
+      sq = uint32_t(__dp4a(int(v.x), int(v.x), int(sq)));
+      sq = uint32_t(__dp4a(int(v.y), int(v.y), int(sq)));
+      sq = uint32_t(__dp4a(int(v.z), int(v.z), int(sq)));
+      sq = uint32_t(__dp4a(int(v.w), int(v.w), int(sq)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+  if (lane == 0) red[warp] = sq;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int w = 0; w < kNormRows; ++w) m = max(m, red[w]);
+    part[blockIdx.x] = m;
   }
 }
 
 template <bool kRegs>
 cudaError_t launch_act(const uint16_t* x, int64_t M, int K, int8_t* q, float* s, uint16_t* qh,
-                       int ldh, cudaStream_t st) {
+                       int ldh, uint32_t* sqm, cudaStream_t st) {
   const dim3 grid(unsigned((M + kWarps - 1) / kWarps)), block(kWarps * 32);
   if (q && qh)
-    quant_act_kernel<kRegs, true, true><<<grid, block, 0, st>>>(x, M, K, q, s, qh, ldh);
+    quant_act_kernel<kRegs, true, true><<<grid, block, 0, st>>>(x, M, K, q, s, qh, ldh, sqm);
   else if (q)
-    quant_act_kernel<kRegs, true, false><<<grid, block, 0, st>>>(x, M, K, q, s, qh, ldh);
+    quant_act_kernel<kRegs, true, false><<<grid, block, 0, st>>>(x, M, K, q, s, qh, ldh, sqm);
   else
-    quant_act_kernel<kRegs, false, true><<<grid, block, 0, st>>>(x, M, K, q, s, qh, ldh);
+    quant_act_kernel<kRegs, false, true><<<grid, block, 0, st>>>(x, M, K, q, s, qh, ldh, sqm);
   return cudaGetLastError();
 }
 
 template <int kVPT>
 cudaError_t launch_rows(const uint16_t* x, int64_t M, int K, int8_t* q, float* s, uint16_t* qh,
-                        int ldh, cudaStream_t st) {
+                        int ldh, uint32_t* sqm, cudaStream_t st) {
   const dim3 grid(static_cast<unsigned>(M)), block(kRowThreads);
   if (q && qh)
-    quant_act_row_kernel<kVPT, true, true><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh);
+    quant_act_row_kernel<kVPT, true, true><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh, sqm);
   else if (q)
-    quant_act_row_kernel<kVPT, true, false><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh);
+    quant_act_row_kernel<kVPT, true, false><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh, sqm);
   else
-    quant_act_row_kernel<kVPT, false, true><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh);
+    quant_act_row_kernel<kVPT, false, true><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh, sqm);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t* q,
-                                float* scale, uint16_t* q_f16, int64_t ldh, cudaStream_t s) {
+                                float* scale, uint16_t* q_f16, int64_t ldh, uint32_t* sq_max,
+                                cudaStream_t s) {
   const int64_t nvec = K / 8;
-  if (nvec <= kRowThreads * 3) return launch_rows<3>(x, M, int(K), q, scale, q_f16, int(ldh), s);
+  if (nvec <= kRowThreads * 3)
+    return launch_rows<3>(x, M, int(K), q, scale, q_f16, int(ldh), sq_max, s);
   if (nvec <= kRowThreads * 12)
-    return launch_rows<12>(x, M, int(K), q, scale, q_f16, int(ldh), s);
-  return launch_act<false>(x, M, int(K), q, scale, q_f16, int(ldh), s);
+    return launch_rows<12>(x, M, int(K), q, scale, q_f16, int(ldh), sq_max, s);
+  return launch_act<false>(x, M, int(K), q, scale, q_f16, int(ldh), sq_max, s);
 }
 
 cudaError_t launch_quantize_weights(const void* w, int w_dtype, int64_t N, int64_t K,
@@ -336,12 +441,18 @@ cudaError_t launch_quantize_weights(const void* w, int w_dtype, int64_t N, int64
   return cudaGetLastError();
 }
 
+cudaError_t launch_weight_norms(const int8_t* qw, int64_t N, int64_t K, uint32_t* nwpart,
+                                uint32_t* zero, int64_t nzero, cudaStream_t s) {
+  static_assert(128 / kNormRows == kNormParts, "partial maxima per 128-channel block");
+  const int64_t blocks = (N + 127) / 128 * kNormParts;
+  weight_norm_kernel<<<static_cast<unsigned>(blocks), 32 * kNormRows, 0, s>>>(
+      qw, N, int(K), nwpart, zero, nzero);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_int8_to_f16(const int8_t* q, int64_t M, int64_t K, int64_t ldh,
-                               uint16_t* out, cudaStream_t s) {
-  const int64_t groups = M * (ldh / 16);
-  int64_t blocks = (groups + 255) / 256;
-  blocks = blocks < 1 ? 1 : (blocks > 152 * 16 ? 152 * 16 : blocks);
-  int8_to_f16_kernel<<<unsigned(blocks), 256, 0, s>>>(q, M, int(K), int(ldh), out);
+                               uint16_t* out, uint32_t* sq_max, cudaStream_t s) {
+  int8_to_f16_kernel<<<static_cast<unsigned>(M), 256, 0, s>>>(q, int(K), int(ldh), out, sq_max);
   return cudaGetLastError();
 }
 
