@@ -118,16 +118,14 @@ h3q_status h3q_linear_w8a8(const uint16_t* x, int8_t* xq, float* xs, const int8_
   uint16_t* act = reinterpret_cast<uint16_t*>(wsp + lay.act);
   uint32_t* amax = reinterpret_cast<uint32_t*>(wsp + lay.amax);
   uint32_t* status = reinterpret_cast<uint32_t*>(wsp + lay.status);
-  uint32_t* nwpart = reinterpret_cast<uint32_t*>(wsp + lay.nwpart);
+  uint32_t* flags = reinterpret_cast<uint32_t*>(wsp + lay.flags);
   uint2* list = reinterpret_cast<uint2*>(wsp + lay.list);
   const bool code_acts = x || xq;
-  // Weight norms; zero the status block, and the activation norm maxima when
-  // the activations are coded anew (they sit just before the status block).
-  uint32_t* zero = code_acts ? amax : status;
-  const int64_t nzero = int64_t(lay.status + 256u - (code_acts ? lay.amax : lay.status)) / 4;
-  if (h3q_status st =
-          from_cuda(h3q::launch_weight_norms(wq, N, K, nwpart, zero, nzero, stream)))
-    return st;
+  // Zero the status block and the tile flags, and the activation norm maxima
+  // when the activations are coded anew (they sit just before the status block).
+  const size_t zero_from = code_acts ? lay.amax : lay.status;
+  if (cudaMemsetAsync(wsp + zero_from, 0, lay.list - zero_from, stream) != cudaSuccess)
+    return H3Q_ERR_CUDA;
   // A2, or the FP16 coding of pre-quantised activations, or (x == xq == NULL)
   // the activations a previous call left coded in this workspace.
   const int64_t ldh = h3q::gemm_tc_coded_ld(K);
@@ -142,7 +140,7 @@ h3q_status h3q_linear_w8a8(const uint16_t* x, int8_t* xq, float* xs, const int8_
   // A3 + A4: the tiles that are exact over the whole K, then the rest in K
   // chunks (an empty launch when there are none).
   if (h3q_status st = from_cuda(h3q::launch_gemm_wide(act, xs, wq, ws, bias, M, N, K, y,
-                                                      acc_out, amax, nwpart, status, list,
+                                                      acc_out, amax, status, flags, list,
                                                       stream)))
     return st;
   return from_cuda(h3q::launch_gemm_tc(act, xs, wq, ws, bias, M, N, K, y, acc_out, status,

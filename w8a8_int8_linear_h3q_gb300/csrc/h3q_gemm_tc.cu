@@ -153,8 +153,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
                const float* __restrict__ sw, const uint16_t* __restrict__ bias, const Shape shp,
                uint16_t* __restrict__ Y, int32_t* __restrict__ ACC, uint32_t* __restrict__ err,
                const uint2* __restrict__ list, const uint32_t* __restrict__ list_len) {
-  // every CTA of the grid reads the same tile count, so all leave together
-  // (before any cluster barrier) when there is nothing to do
+  // With a list this grid may be scheduled before the kernel that writes the
+  // list has finished (programmatic dependent launch): wait for it first.
+  // Every CTA then reads the same tile count, so all leave together (before
+  // any cluster barrier) when there is nothing to do.
+  if (list) ptx::grid_dependency_wait();
   const int ntiles = list ? int(*list_len) : shp.tiles;
   if (ntiles == 0) return;
   extern __shared__ uint8_t smem_raw[];
@@ -445,8 +448,8 @@ WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K) {
   l.act = 0;
   l.amax = up(size_t(M) * size_t(gemm_tc_coded_ld(K)) * 2u);
   l.status = l.amax + up(mt2 * 4u);
-  l.nwpart = l.status + 256u;
-  l.list = l.nwpart + up(nt * kNormParts * 4u);
+  l.flags = l.status + 256u;
+  l.list = l.flags + up(mt2 * ntc * 4u);
   l.total = l.list + up(mt * ntc * sizeof(uint2));
   return l;
 }
@@ -506,13 +509,15 @@ cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CLUSTER;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = list ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, map, wmap, sa, sw, bias, shp, y, acc, err,
                             list, list_len);
 }

@@ -19,30 +19,44 @@
 // <= 2^24 and hence an FP32 value, so no addition rounds and one FP32
 // accumulator carries the exact dot product over all of K.  The activation
 // quantiser records, per block of 256 tokens, the largest sum of squares of a
-// coded row; a weight pre-pass records the same per 16 channels.  A cluster
-// tile (two 128-channel blocks x 256 tokens) is computed here when the
-// product of its two maxima is at most 2^48, which holds when the codes are
-// mostly well below 127 in magnitude -- the usual case for per-row absmax
-// scaling of K = 5376 rows.  The other tiles go to a list in the workspace
-// that the chunked kernel finishes afterwards.
+// coded row; the converter warps sum the squares of each weight row as they
+// convert it.  Every tile is computed here; the epilogue stores a channel row
+// of a tile only when that row's |w|^2 times its token block's largest |a|^2
+// is at most 2^48, which holds when the codes are mostly well below 127 in
+// magnitude -- the usual case for per-row absmax scaling of K = 5376 rows.
+// A tile with a row that fails is put (once) on a list in the workspace, and
+// the chunked kernel recomputes it afterwards.
 //
 // Against the chunked kernel this removes the per-chunk accumulator drains
 // (one drain per tile) and lets each converted weight slice feed 256 tokens
-// (one N = 256 MMA) instead of 128, halving the converter warps' TMEM stores
-// per MMA, which compete with the MMAs for TMEM.
+// instead of 128, halving the converter warps' TMEM stores per MMA, which
+// compete with the MMAs for TMEM.
 //
-// Warp roles (736 threads):
-//   warp 0      TMA producer of the activation tiles (2 super-stage slots),
-//               multicast to the cluster peer
-//   warp 1      TMEM allocator and MMA issuer (one thread)
-//   warp 2      tile scheduler (exactness test, fallback list) and TMA
-//               producer of the INT8 weight tiles (4 super-stage slots)
-//   warps 3-6   converters: INT8 weights -> FP16 -> TMEM (2 super-stages)
+// The two CTAs of a cluster work as a pair on one tile of 256 channels x 256
+// tokens with the paired MMA (cta_group::2, M = 256): each CTA converts the
+// weights of its own 128 channels into its own TMEM and holds the
+// accumulator for them, and each CTA's shared memory holds only its half of
+// the tile's tokens (128), which the pair MMA reads from both.  Half-size
+// activation stages let the activation ring be four super-stages deep, and
+// each CTA refills its own stages with no wait on the other.  One thread of
+// the even CTA issues every MMA; it waits on barriers that both CTAs'
+// converter and epilogue threads arrive on, and its commits arrive in both
+// CTAs.
+//
+// Warp roles (736 threads per CTA):
+//   warp 0      TMA producer of this CTA's activation half (4 super-stages)
+//   warp 1      TMEM allocator; MMA issuer (one thread, even CTA only)
+//   warp 2      tile scheduler and TMA producer of this CTA's INT8 weight
+//               tiles (4 super-stages)
+//   warps 3-6   converters: INT8 weights -> FP16 -> TMEM (2 super-stages),
+//               and each weight row's sum of squares
 //   warps 7-22  epilogue: drain the accumulator to registers, release it,
-//               then dequant + bias + BF16 (and the optional raw INT32)
-// A super-stage is 2 k-blocks of 64 K: 8 MMAs of 128 x 256 x 16.
-// TMEM: the FP32 accumulator in columns 0-255, A super-stages in 256-319 and
-// 320-383.
+//               then check the bound per row, dequant + bias + BF16 (and
+//               the optional raw INT32)
+// A super-stage is 2 k-blocks of 64 K: 8 pair MMAs of 256 x 256 x 16.
+// TMEM (each CTA): the FP32 accumulator in columns 0-255, A super-stages in
+// 256-319 and 320-383.  (Four A super-stages fit, but measured slower: the
+// converters then run ahead into activation tiles that have not landed.)
 // Every wait is bounded in time; on a timeout the kernel records an error
 // bit, lets every role fall through, drains its in-flight copies and MMAs,
 // frees TMEM and returns.
@@ -57,11 +71,13 @@ namespace {
 
 namespace P = ptx;
 
-constexpr int BM = 128;                 // channels per CTA tile (MMA M, TMEM lanes)
+constexpr int BM = 128;                 // channels per CTA (TMEM lanes); the pair MMA has M = 256
 constexpr int BN = kNormTokens;         // tokens per tile (MMA N)
+constexpr int BNH = BN / 2;             // tokens held by each CTA of the pair
 constexpr int BK = 64;                  // K per k-block (128 bytes of FP16)
 constexpr int SS = 2;                   // k-blocks per super-stage (8 MMAs)
-constexpr int SLOTS = 2;                // super-stage slots: activations (SMEM), FP16 weights (TMEM)
+constexpr int B_SLOTS = 4;              // super-stage slots: activation halves (SMEM)
+constexpr int A_SLOTS = 2;              // super-stage slots: FP16 weights (TMEM)
 constexpr int W_SLOTS = 4;              // super-stage slots: INT8 weights (SMEM)
 constexpr int SQ = 4;                   // tile-queue entries
 constexpr int GROUP_M = 8;              // token blocks per raster group
@@ -77,12 +93,16 @@ constexpr int THREADS = 32 * (EPI_WARP0 + NUM_EPI_WARPS);
 // every role but the scheduler takes each tile from the queue: one arrival
 // per producer or MMA thread, one per converter or epilogue warp
 constexpr int QUEUE_READERS = 2 + NUM_CONV_WARPS + NUM_EPI_WARPS;
-constexpr int B_KBLOCK_BYTES = BN * BK * 2;                // 32 KB
+constexpr int B_KBLOCK_BYTES = BNH * BK * 2;               // 16 KB
 constexpr int W_BOX_BYTES = BM * SS * BK;                  // 16 KB: 128 rows x 2 k-blocks
 constexpr uint32_t TM_D = 0;
 constexpr uint32_t TM_A = BN;
 constexpr uint32_t TM_COLS = 512;
-constexpr uint32_t IDESC = P::idesc_f16_f32(BM, BN);
+static_assert(TM_A + A_SLOTS * SS * 32 <= TM_COLS, "TMEM columns");
+// the converters find an A slot free through the super-stage barriers of the
+// activation ring, so the A ring may not be deeper than that ring
+static_assert(A_SLOTS <= B_SLOTS, "A ring deeper than the activation ring");
+constexpr uint32_t IDESC = P::idesc_f16_f32(2 * BM, BN);
 constexpr uint64_t kExactBound = uint64_t(1) << 48;        // |a|^2 |w|^2 limit
 
 // error bits (the chunked kernel uses the low byte)
@@ -90,15 +110,19 @@ constexpr uint32_t ERR_PRODUCER = 1u << 8, ERR_MMA = 2u << 8, ERR_CONVERT = 4u <
                    ERR_EPILOGUE = 8u << 8, ERR_TEARDOWN = 16u << 8, ERR_SCHED = 32u << 8;
 
 struct __align__(1024) Smem {
-  uint8_t b[SLOTS][SS][B_KBLOCK_BYTES];  // activation k-blocks of a super-stage slot
+  uint8_t b[B_SLOTS][SS][B_KBLOCK_BYTES];  // this CTA's activation half, per k-block
   uint8_t w[W_SLOTS][W_BOX_BYTES];       // INT8 weights: 128-byte rows, 128-byte swizzle
-  uint64_t full_b[SLOTS];                // a slot's activation tiles have landed
+  uint64_t full_b[B_SLOTS];              // a slot's activation half has landed
   uint64_t full_w[W_SLOTS];              // a slot's INT8 weights have landed
   uint64_t empty_w[W_SLOTS];             // the converters have read them
-  uint64_t full_a[SLOTS];                // A converted and B landed for a super-stage
-  uint64_t empty_s[SLOTS];               // both CTAs' MMAs are done with a slot
-  uint64_t dfull, dempty, mma_done;
+  uint64_t full_a[A_SLOTS];              // (even CTA) both CTAs' A and B are in place
+  uint64_t empty_ss[B_SLOTS];            // the pair MMAs of super-stage s are done
+  uint64_t dfull;                        // the tile's accumulator is complete
+  uint64_t dempty;                       // (even CTA) both epilogues have copied it out
+  uint64_t mma_done;
   uint64_t q_full[SQ], q_empty[SQ];      // tile queue
+  uint64_t wn_full[2];                   // a tile's weight-row norms are in wn2
+  uint32_t wn2[2][BM];                   // per tile (alternating): sum of q^2 per channel row
   int q_tile[SQ];                        // cluster tile index, or -1: no more tiles
   uint32_t tmem_base;
   int abort_flag;
@@ -124,18 +148,6 @@ __device__ __forceinline__ void tile_coords(const Shape& s, int t, int& mb, int&
   const int r = t - g * per_group;
   mb = first_m + r % gm;
   pair = r / gm;
-}
-
-// Warp-collective: true when every (token, channel) of the cluster tile has
-// |a|^2 |w|^2 <= 2^48.  Lanes 0-15 read the pair's 16 weight partial maxima.
-__device__ __forceinline__ bool tile_exact(const Shape& s, const uint32_t* amax,
-                                           const uint32_t* nwpart, int mb, int pair, int lane) {
-  const int idx = pair * CLUSTER * kNormParts + lane;
-  uint32_t w = (lane < CLUSTER * kNormParts && idx < s.nt * kNormParts) ? nwpart[idx] : 0u;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) w = max(w, __shfl_xor_sync(0xFFFFFFFFu, w, o));
-  const uint32_t a = amax[mb];
-  return uint64_t(w) * uint64_t(a) <= kExactBound;
 }
 
 // Single-thread take of the next queue entry.  False on a timeout or abort.
@@ -178,8 +190,8 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
                  const __grid_constant__ CUtensorMap w_map, const float* __restrict__ sa,
                  const float* __restrict__ sw, const uint16_t* __restrict__ bias,
                  const Shape shp, uint16_t* __restrict__ Y, int32_t* __restrict__ ACC,
-                 const uint32_t* __restrict__ amax, const uint32_t* __restrict__ nwpart,
-                 uint32_t* __restrict__ status, uint2* __restrict__ list) {
+                 const uint32_t* __restrict__ amax, uint32_t* __restrict__ status,
+                 uint32_t* __restrict__ flags, uint2* __restrict__ list) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~uintptr_t(1023));
@@ -192,29 +204,38 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
       P::mbar_init(&sm.full_w[i], 1);
       P::mbar_init(&sm.empty_w[i], NUM_CONV_WARPS * 32);
     }
-    for (int i = 0; i < SLOTS; ++i) {
+    for (int i = 0; i < B_SLOTS; ++i) {
       P::mbar_init(&sm.full_b[i], 1);
-      P::mbar_init(&sm.full_a[i], NUM_CONV_WARPS * 32);
-      P::mbar_init(&sm.empty_s[i], CLUSTER);      // one multicast commit per CTA
+      P::mbar_init(&sm.empty_ss[i], 1);           // the pair's commit
     }
+    for (int i = 0; i < A_SLOTS; ++i)
+      P::mbar_init(&sm.full_a[i], CLUSTER * NUM_CONV_WARPS * 32);
     for (int i = 0; i < SQ; ++i) {
       P::mbar_init(&sm.q_full[i], 1);
       P::mbar_init(&sm.q_empty[i], QUEUE_READERS);
     }
+    for (int i = 0; i < 2; ++i) P::mbar_init(&sm.wn_full[i], NUM_CONV_WARPS * 32);
     P::mbar_init(&sm.dfull, 1);
-    P::mbar_init(&sm.dempty, NUM_EPI_WARPS * 32);
+    P::mbar_init(&sm.dempty, CLUSTER * NUM_EPI_WARPS * 32);
     P::mbar_init(&sm.mma_done, 1);
     sm.abort_flag = 0;
     P::fence_mbar_init();
   }
-  if (warp == MMA_WARP) P::tmem_alloc(&sm.tmem_base, TM_COLS);
+  if (warp == MMA_WARP) P::tmem_alloc_pair(&sm.tmem_base, TM_COLS);   // one warp per CTA
   P::tc_fence_before();
   __syncthreads();
-  P::cluster_sync();                              // peers' barriers exist before multicasts
+  P::cluster_sync();                              // the peer's barriers exist before any arrive
   P::tc_fence_after();
+  // The set-up above overlaps the tail of the previous kernel on the stream
+  // (programmatic dependent launch); nothing it wrote is read before here.
+  P::grid_dependency_wait();
+  P::allow_dependent_launch();
   const uint32_t tmem = sm.tmem_base;
   const uint32_t rank = P::cluster_rank();
   const int cid = int(P::cluster_id_x()), ncl = int(P::num_clusters_x());
+  // the even CTA's barriers that both CTAs arrive on
+  const uint32_t full_a_pair = P::mapa_shared(P::smem_u32(&sm.full_a[0]), 0);
+  const uint32_t dempty_pair = P::mapa_shared(P::smem_u32(&sm.dempty), 0);
 
   if (warp == 0) {
     // ---------------- TMA producer: activation tiles ----------------
@@ -227,18 +248,18 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
         if (!pop_tile(sm, nq, abort_flag, err, ERR_PRODUCER, t) || t < 0) break;
         int mb, pair;
         tile_coords(shp, t, mb, pair);
+        const int row0 = mb * BN + int(rank) * BNH;
         for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
-          const uint32_t slot = gs % SLOTS;
-          // the slot is free once both CTAs' MMAs finished its previous use
-          if (!P::mbar_wait(&sm.empty_s[slot], ((gs / SLOTS) & 1u) ^ 1u, abort_flag, err,
+          const uint32_t slot = gs % B_SLOTS;
+          // the slot is free once the pair MMAs of its previous super-stage are done
+          if (!P::mbar_wait(&sm.empty_ss[slot], ((gs / B_SLOTS) & 1u) ^ 1u, abort_flag, err,
                             ERR_PRODUCER)) {
             ok = false;
             break;
           }
-          // both k-blocks land here: this CTA's and the peer's
+          // this CTA's 128 tokens of the super-stage's two k-blocks
           P::mbar_arrive_expect_tx(&sm.full_b[slot], SS * B_KBLOCK_BYTES);
-          P::tma_load_3d_mc(P::smem_u32(sm.b[slot][rank]), &act_map, &sm.full_b[slot], 0,
-                            mb * BN, ss * SS + int(rank), CLUSTER_MASK);
+          P::tma_load_3d(P::smem_u32(sm.b[slot][0]), &act_map, &sm.full_b[slot], 0, row0, ss * SS);
           gb = gs + 1;
         }
         if (!ok) break;
@@ -246,8 +267,8 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
       // no copy may still be landing in shared memory when the CTA exits
       int no_abort = 0;
       volatile int* never = &no_abort;   // this drain does not follow the abort flag
-      for (uint32_t i = gb > SLOTS ? gb - SLOTS : 0; i < gb; ++i)
-        P::mbar_wait(&sm.full_b[i % SLOTS], (i / SLOTS) & 1u, never, err, ERR_TEARDOWN);
+      for (uint32_t i = gb > B_SLOTS ? gb - B_SLOTS : 0; i < gb; ++i)
+        P::mbar_wait(&sm.full_b[i % B_SLOTS], (i / B_SLOTS) & 1u, never, err, ERR_TEARDOWN);
     }
     __syncwarp();
   } else if (warp == SCHED_WARP) {
@@ -256,19 +277,9 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
     uint32_t gs = 0, gw = 0, nq = 0;
     bool ok = true;
     for (int t = cid; t < shp.tiles; t += ncl) {
-      int mb, pair;
-      tile_coords(shp, t, mb, pair);
-      if (!tile_exact(shp, amax, nwpart, mb, pair, lane)) {
-        // the chunked kernel takes it, as one or two 128-token tiles
-        if (rank == 0 && lane == 0) {
-          const int n128 = min(2, shp.mt128 - 2 * mb);
-          const uint32_t i = atomicAdd(status + 1, uint32_t(n128));
-          for (int h = 0; h < n128; ++h)
-            list[i + h] = make_uint2(uint32_t(2 * mb + h), uint32_t(pair));
-        }
-        continue;
-      }
       if (lane == 0) {
+        int mb, pair;
+        tile_coords(shp, t, mb, pair);
         ok = push_tile(sm, nq, t, abort_flag, err);
         const int wrow = min(2 * pair + int(rank), shp.nt - 1) * BM;
         for (int ss = 0; ok && ss < shp.NSS; ++ss, ++gs) {
@@ -294,42 +305,51 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
-    // ---------------- MMA issuer: one wait and one commit per 8 MMAs ----------------
-    if (lane == 0) {
+    // ---------------- MMA issuer (even CTA): one wait and one commit per 8 MMAs ----------------
+    if (lane == 0 && rank == 0) {
       uint32_t gs = 0, gt = 0, nq = 0;
       bool ok = true;
       for (;;) {
         int t;
         if (!pop_tile(sm, nq, abort_flag, err, ERR_MMA, t) || t < 0) break;
-        // the epilogue has copied out the previous tile's accumulator
+        // both epilogues have copied out the previous tile's accumulator
         if (!P::mbar_wait(&sm.dempty, (gt & 1u) ^ 1u, abort_flag, err, ERR_MMA)) break;
         for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
-          const uint32_t slot = gs % SLOTS;
-          if (!P::mbar_wait(&sm.full_a[slot], (gs / SLOTS) & 1u, abort_flag, err, ERR_MMA)) {
+          const uint32_t slot = gs % B_SLOTS, aslot = gs % A_SLOTS;
+          if (!P::mbar_wait(&sm.full_a[aslot], (gs / A_SLOTS) & 1u, abort_flag, err, ERR_MMA)) {
             ok = false;
             break;
           }
           P::tc_fence_after();
-          const uint32_t a_tmem = tmem + TM_A + slot * (SS * 32);
+          const uint32_t a_tmem = tmem + TM_A + aslot * (SS * 32);
           const int nkb = min(SS, shp.KB - ss * SS);
           for (int j = 0; j < nkb; ++j) {
             const uint64_t bdesc = P::smem_desc_sw128(P::smem_u32(sm.b[slot][j]));
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
-              P::mma_f16_ts(tmem + TM_D, a_tmem + j * 32 + kk * 8, bdesc + uint64_t(kk * 2),
-                            IDESC, (ss > 0 || j > 0 || kk > 0) ? 1u : 0u);
+              P::mma_f16_ts_pair(tmem + TM_D, a_tmem + j * 32 + kk * 8,
+                                 bdesc + uint64_t(kk * 2), IDESC,
+                                 (ss > 0 || j > 0 || kk > 0) ? 1u : 0u);
           }
-          P::mma_commit_mc(&sm.empty_s[slot], CLUSTER_MASK);
+          P::mma_commit_pair_mc(&sm.empty_ss[slot], CLUSTER_MASK);
         }
         if (!ok) break;
-        P::mma_commit(&sm.dfull);
+        P::mma_commit_pair_mc(&sm.dfull, CLUSTER_MASK);
         ++gt;
       }
       // every MMA this thread issued has finished before TMEM is freed
-      P::mma_commit(&sm.mma_done);
+      P::mma_commit_pair_mc(&sm.mma_done, 1);
       int no_abort = 0;
       volatile int* never = &no_abort;
       P::mbar_wait(&sm.mma_done, 0, never, err, ERR_TEARDOWN);
+    } else if (lane == 0) {
+      // the odd CTA issues nothing; it takes the tiles from the queue like
+      // every other role so that the queue slots are released
+      uint32_t nq = 0;
+      for (;;) {
+        int t;
+        if (!pop_tile(sm, nq, abort_flag, err, ERR_MMA, t) || t < 0) break;
+      }
     }
     __syncwarp();
   } else if (warp < EPI_WARP0) {
@@ -339,13 +359,14 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
     const uint32_t lane_base = uint32_t(32 * q) << 16;
     // this row's 16-byte chunks in a 128-byte-swizzled INT8 box (two k-blocks)
     const uint32_t row_off = uint32_t(r) * 128u, xr = uint32_t(r & 7);
-    uint32_t gs = 0, nq = 0;
+    uint32_t gs = 0, nq = 0, gt = 0;
     bool ok = true;
     while (ok) {
       int t;
       if (!pop_tile_warp(sm, nq, abort_flag, err, ERR_CONVERT, t, lane) || t < 0) break;
+      uint32_t sq = 0;                            // this row's sum of q^2 (exact mod 2^32)
       for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
-        const uint32_t slot = gs % SLOTS, ph = (gs / SLOTS) & 1u;
+        const uint32_t slot = gs % B_SLOTS, aslot = gs % A_SLOTS;
         const uint32_t wslot = gs % W_SLOTS;
         const int nkb = min(SS, shp.KB - ss * SS);
         if (!P::mbar_wait_warp(&sm.full_w[wslot], (gs / W_SLOTS) & 1u, abort_flag, err,
@@ -360,6 +381,13 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             v[i] = *reinterpret_cast<const uint4*>(box + row_off + (((cb + uint32_t(i)) ^ xr) << 4));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            sq = uint32_t(__dp4a(int(v[i].x), int(v[i].x), int(sq)));
+            sq = uint32_t(__dp4a(int(v[i].y), int(v[i].y), int(sq)));
+            sq = uint32_t(__dp4a(int(v[i].z), int(v[i].z), int(sq)));
+            sq = uint32_t(__dp4a(int(v[i].w), int(v[i].w), int(sq)));
+          }
           uint32_t h[32];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -368,26 +396,37 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
             P::s8x4_to_f16x4(v[i].z, h[8 * i + 4], h[8 * i + 5]);
             P::s8x4_to_f16x4(v[i].w, h[8 * i + 6], h[8 * i + 7]);
           }
-          if (j == 0 &&
-              !P::mbar_wait_warp(&sm.empty_s[slot], ph ^ 1u, abort_flag, err, ERR_CONVERT)) {
-            ok = false;
-            break;
+          // the A slot is free once the pair MMAs of super-stage gs - A_SLOTS are done
+          if (j == 0 && gs >= A_SLOTS) {
+            const uint32_t prev = gs - A_SLOTS;
+            if (!P::mbar_wait_warp(&sm.empty_ss[prev % B_SLOTS], (prev / B_SLOTS) & 1u,
+                                   abort_flag, err, ERR_CONVERT)) {
+              ok = false;
+              break;
+            }
           }
           P::tc_fence_after();
-          P::tmem_st32(tmem + lane_base + TM_A + slot * (SS * 32) + uint32_t(j) * 32, h);
+          P::tmem_st32(tmem + lane_base + TM_A + aslot * (SS * 32) + uint32_t(j) * 32, h);
         }
         if (!ok) break;
         P::mbar_arrive(&sm.empty_w[wslot]);       // this slot's INT8 weights may be refilled
-        // forward the readiness of the slot's activation tiles to the MMA thread
-        if (!P::mbar_wait_warp(&sm.full_b[slot], ph, abort_flag, err, ERR_CONVERT)) {
+        // forward the readiness of this CTA's activation half to the MMA thread
+        if (!P::mbar_wait_warp(&sm.full_b[slot], (gs / B_SLOTS) & 1u, abort_flag, err,
+                               ERR_CONVERT)) {
           ok = false;
           break;
         }
         P::tmem_wait_st();
         P::tc_fence_before();
-        P::mbar_arrive(&sm.full_a[slot]);
+        P::mbar_arrive_cluster(full_a_pair + aslot * 8u);
       }
+      if (!ok) break;
+      // the row norms of this tile, for the epilogue's bound check
+      sm.wn2[gt & 1u][r] = sq;
+      P::mbar_arrive(&sm.wn_full[gt & 1u]);
+      ++gt;
     }
+    P::tmem_wait_st();
   } else {
     // ---------------- epilogue ----------------
     const int q = warp & 3;                       // TMEM lane quarter
@@ -406,21 +445,37 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
       const int m0 = mb * BN + 64 * cq;
       const float sa0 = (m0 + lane < shp.M) ? sa[m0 + lane] : 0.f;
       const float sa1 = (m0 + 32 + lane < shp.M) ? sa[m0 + 32 + lane] : 0.f;
+      const uint32_t amb = amax[mb];
       if (!P::mbar_wait_warp(&sm.dfull, gt & 1u, abort_flag, err, ERR_EPILOGUE)) break;
+      if (!P::mbar_wait_warp(&sm.wn_full[gt & 1u], (gt >> 1) & 1u, abort_flag, err,
+                             ERR_EPILOGUE))
+        break;
+      // this row's FP32 sums were exact over all of K if |w|^2 max|a|^2 <= 2^48
+      const bool keep = n_ok && uint64_t(sm.wn2[gt & 1u][32 * q + lane]) * amb <= kExactBound;
+      if (!__all_sync(0xFFFFFFFFu, keep || !n_ok) && lane == 0) {
+        // the chunked kernel recomputes this tile, as one or two 128-token tiles;
+        // the flag keeps the warps of both CTAs from listing it twice
+        if (atomicExch(flags + mb * shp.ntc + pair, 1u) == 0u) {
+          const int n128 = min(2, shp.mt128 - 2 * mb);
+          const uint32_t i = atomicAdd(status + 1, uint32_t(n128));
+          for (int h = 0; h < n128; ++h)
+            list[i + h] = make_uint2(uint32_t(2 * mb + h), uint32_t(pair));
+        }
+      }
       P::tc_fence_after();
       uint32_t d0[32], d1[32];
       P::tmem_ld32(tmem + lane_base + TM_D + 64 * cq, d0);
       P::tmem_ld32(tmem + lane_base + TM_D + 64 * cq + 32, d1);
       P::tmem_wait_ld();
       P::tc_fence_before();
-      P::mbar_arrive(&sm.dempty);                 // the MMAs of the next tile may start
+      P::mbar_arrive_cluster(dempty_pair);        // the MMAs of the next tile may start
       ++gt;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float saj = __shfl_sync(0xFFFFFFFFu, sa0, j);
         const int m = m0 + j;
         const int a = __float2int_rn(__uint_as_float(d0[j]));
-        if (n_ok && m < shp.M) {
+        if (keep && m < shp.M) {
           const int64_t off = int64_t(m) * shp.N + n;
           if (ACC) ACC[off] = a;
           if (Y) Y[off] = float_to_bf16_bits(epilogue_value(a, saj, swn, bn));
@@ -431,7 +486,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
         const float saj = __shfl_sync(0xFFFFFFFFu, sa1, j);
         const int m = m0 + 32 + j;
         const int a = __float2int_rn(__uint_as_float(d1[j]));
-        if (n_ok && m < shp.M) {
+        if (keep && m < shp.M) {
           const int64_t off = int64_t(m) * shp.N + n;
           if (ACC) ACC[off] = a;
           if (Y) Y[off] = float_to_bf16_bits(epilogue_value(a, saj, swn, bn));
@@ -442,9 +497,10 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
 
   P::tc_fence_before();
   __syncthreads();
+  P::cluster_sync();                              // both CTAs are done with TMEM
   if (warp == MMA_WARP) {
     P::tc_fence_after();
-    P::tmem_dealloc(tmem, TM_COLS);
+    P::tmem_dealloc_pair(tmem, TM_COLS);
   }
   P::cluster_sync();                              // no peer still signals or writes here
 }
@@ -459,17 +515,16 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const int8_t* qw,
                              const float* sw, const uint16_t* bias, int64_t M, int64_t N,
                              int64_t K, uint16_t* y, int32_t* acc, const uint32_t* amax,
-                             const uint32_t* nwpart, uint32_t* status, uint2* list,
-                             cudaStream_t s) {
+                             uint32_t* status, uint32_t* flags, uint2* list, cudaStream_t s) {
   EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
   if (!enc) return cudaErrorNotSupported;
   // activations: a [M, ld] FP16 matrix viewed as (64-element chunk, row, chunk
-  // index); one box is one k-block of 256 rows
+  // index); one box is two k-blocks of 128 rows
   const int64_t ld = gemm_tc_coded_ld(K);
   CUtensorMap map;
   const cuuint64_t dims[3] = {cuuint64_t(BK), cuuint64_t(M), cuuint64_t(ld / BK)};
   const cuuint64_t strides[2] = {cuuint64_t(ld) * 2u, cuuint64_t(BK) * 2u};
-  const cuuint32_t box[3] = {BK, BN, 1};
+  const cuuint32_t box[3] = {BK, BNH, SS};
   const cuuint32_t estr[3] = {1, 1, 1};
   if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t*>(act_f16), dims,
           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -511,15 +566,18 @@ cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const int
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CLUSTER;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may start while the previous kernel (the quantiser) finishes
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, gemm_wide_kernel, map, wmap, sa, sw, bias, shp, y, acc, amax,
-                            nwpart, status, list);
+                            status, flags, list);
 }
 
 }  // namespace h3q

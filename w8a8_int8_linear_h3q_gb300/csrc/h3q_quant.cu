@@ -337,59 +337,6 @@ int8_to_f16_kernel(const int8_t* __restrict__ q, int K, int ldh, uint16_t* __res
   }
 }
 
-// One block of 16 warps per 16 weight rows (block b: rows 16b .. 16b+15):
-// each warp sums q^2 over its row with DP4A on 16-byte loads, and the block
-// writes the largest row sum to part[b].  The sums are taken modulo 2^32,
-// which is exact: K * 128^2 < 2^32 for every supported K.  All blocks also
-// zero the words [zero, zero + nzero).
-constexpr int kNormRows = 16;
-
-__global__ void __launch_bounds__(32 * kNormRows)
-weight_norm_kernel(const int8_t* __restrict__ wq, int64_t N, int K, uint32_t* __restrict__ part,
-                   uint32_t* __restrict__ zero, int64_t nzero) {
-  __shared__ uint32_t red[kNormRows];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < nzero; i += stride)
-    zero[i] = 0u;
-  const int64_t n = int64_t(blockIdx.x) * kNormRows + warp;
-  uint32_t sq = 0;
-  if (n < N) {
-    const uint4* row = reinterpret_cast<const uint4*>(wq + n * K);
-    const int nv = K >> 4;
-    int i = lane;
-    for (; i + 96 < nv; i += 128) {
-      uint4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = __ldg(row + i + 32 * u);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        sq = uint32_t(__dp4a(int(v[u].x), int(v[u].x), int(sq)));
-        sq = uint32_t(__dp4a(int(v[u].y), int(v[u].y), int(sq)));
-        sq = uint32_t(__dp4a(int(v[u].z), int(v[u].z), int(sq)));
-        sq = uint32_t(__dp4a(int(v[u].w), int(v[u].w), int(sq)));
-      }
-    }
-    for (; i < nv; i += 32) {
-      const uint4 v = __ldg(row + i);
-      sq = uint32_t(__dp4a(int(v.x), int(v.x), int(sq)));
-      sq = uint32_t(__dp4a(int(v.y), int(v.y), int(sq)));
-      sq = uint32_t(__dp4a(int(v.z), int(v.z), int(sq)));
-      sq = uint32_t(__dp4a(int(v.w), int(v.w), int(sq)));
-    }
-  }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
-  if (lane == 0) red[warp] = sq;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t m = 0;
-#pragma unroll
-    for (int w = 0; w < kNormRows; ++w) m = max(m, red[w]);
-    part[blockIdx.x] = m;
-  }
-}
-
 template <bool kRegs>
 cudaError_t launch_act(const uint16_t* x, int64_t M, int K, int8_t* q, float* s, uint16_t* qh,
                        int ldh, uint32_t* sqm, cudaStream_t st) {
@@ -438,15 +385,6 @@ cudaError_t launch_quantize_weights(const void* w, int w_dtype, int64_t N, int64
   else
     quant_weight_kernel<uint16_t><<<grid, block, 0, s>>>(static_cast<const uint16_t*>(w), N,
                                                          int(K), q, scale);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_weight_norms(const int8_t* qw, int64_t N, int64_t K, uint32_t* nwpart,
-                                uint32_t* zero, int64_t nzero, cudaStream_t s) {
-  static_assert(128 / kNormRows == kNormParts, "partial maxima per 128-channel block");
-  const int64_t blocks = (N + 127) / 128 * kNormParts;
-  weight_norm_kernel<<<static_cast<unsigned>(blocks), 32 * kNormRows, 0, s>>>(
-      qw, N, int(K), nwpart, zero, nzero);
   return cudaGetLastError();
 }
 
