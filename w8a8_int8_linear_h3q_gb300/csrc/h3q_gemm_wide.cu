@@ -137,6 +137,7 @@ struct Shape {
   int mt128;          // 128-token blocks (the chunked kernel's tiles)
   int ntc;            // channel-block pairs
   int tiles;          // cluster tiles: mt * ntc
+  uint64_t wmax2;     // 128^2 K: no weight row's sum of squares exceeds it
 };
 
 // Cluster tile t -> token block mb (256 tokens) and channel-block pair.
@@ -364,6 +365,11 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
     while (ok) {
       int t;
       if (!pop_tile_warp(sm, nq, abort_flag, err, ERR_CONVERT, t, lane) || t < 0) break;
+      int mb, pair;
+      tile_coords(shp, t, mb, pair);
+      // the row norms matter only if the token block fails the bound with the
+      // largest possible weight row (|w|^2 <= 128^2 K)
+      const bool need_norm = uint64_t(amax[mb]) * shp.wmax2 > kExactBound;
       uint32_t sq = 0;                            // this row's sum of q^2 (exact mod 2^32)
       for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
         const uint32_t slot = gs % B_SLOTS, aslot = gs % A_SLOTS;
@@ -381,12 +387,14 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             v[i] = *reinterpret_cast<const uint4*>(box + row_off + (((cb + uint32_t(i)) ^ xr) << 4));
+          if (need_norm) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            sq = uint32_t(__dp4a(int(v[i].x), int(v[i].x), int(sq)));
-            sq = uint32_t(__dp4a(int(v[i].y), int(v[i].y), int(sq)));
-            sq = uint32_t(__dp4a(int(v[i].z), int(v[i].z), int(sq)));
-            sq = uint32_t(__dp4a(int(v[i].w), int(v[i].w), int(sq)));
+            for (int i = 0; i < 4; ++i) {
+              sq = uint32_t(__dp4a(int(v[i].x), int(v[i].x), int(sq)));
+              sq = uint32_t(__dp4a(int(v[i].y), int(v[i].y), int(sq)));
+              sq = uint32_t(__dp4a(int(v[i].z), int(v[i].z), int(sq)));
+              sq = uint32_t(__dp4a(int(v[i].w), int(v[i].w), int(sq)));
+            }
           }
           uint32_t h[32];
 #pragma unroll
@@ -451,7 +459,9 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
                              ERR_EPILOGUE))
         break;
       // this row's FP32 sums were exact over all of K if |w|^2 max|a|^2 <= 2^48
-      const bool keep = n_ok && uint64_t(sm.wn2[gt & 1u][32 * q + lane]) * amb <= kExactBound;
+      const bool keep =
+          n_ok && (uint64_t(amb) * shp.wmax2 <= kExactBound ||
+                   uint64_t(sm.wn2[gt & 1u][32 * q + lane]) * amb <= kExactBound);
       if (!__all_sync(0xFFFFFFFFu, keep || !n_ok) && lane == 0) {
         // the chunked kernel recomputes this tile, as one or two 128-token tiles;
         // the flag keeps the warps of both CTAs from listing it twice
@@ -551,6 +561,7 @@ cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const int
   shp.nt = int((N + BM - 1) / BM);
   shp.ntc = (shp.nt + CLUSTER - 1) / CLUSTER;
   shp.tiles = shp.mt * shp.ntc;
+  shp.wmax2 = uint64_t(128 * 128) * uint64_t(K);
 
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
