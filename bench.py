@@ -243,10 +243,11 @@ def run_gpu(args):
             if ev is not None:
                 ev[1 + i].record(stream)
 
-    # A2 once; per Linear the single-accumulator GEMM and the chunked GEMM
-    # (which exits at once when no tile needs it), after a memset of the
-    # workspace's status words
-    launches_per_step = 1 + 2 * len(LINEARS)
+    # A2 once; per Linear the weight-norm pre-pass (which returns at once when
+    # the activations alone settle exactness), the single-accumulator GEMM and
+    # the chunked GEMM (which exits at once when no tile needs it), after a
+    # memset of the workspace's status words
+    launches_per_step = 1 + 3 * len(LINEARS)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -319,8 +320,8 @@ def run_gpu(args):
                 "unit": "TFLOP/s", "frac": gemm_tflops / peaks["bf16_tflops"],
                 "traffic": None,
                 "kernel": gemm_kernel_name(h3q),
-                "timed_as": "whole reuse-mode Linear call: status memset + "
-                            "gemm_wide_kernel + the chunked kernel's launch",
+                "timed_as": "whole reuse-mode Linear call: status memset + weight-norm "
+                            "pre-pass + gemm_wide_kernel + the chunked kernel's launch",
                 "peak_source": f"{peak_kind} cuBLAS bf16 burst (MEASURED_PEAKS.json)"
                                if peak_kind == "measured" else "fallback 1.9 PFLOP/s bf16",
                 "ops_per_launch": 2 * M * N * K}

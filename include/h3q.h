@@ -106,10 +106,10 @@ h3q_status h3q_quantize_act(const uint16_t* x, int64_t M, int64_t K,
  * Bytes of device workspace that h3q_linear_w8a8 needs for this shape: the
  * quantised activations re-coded as FP16 (exact: every INT8 value is an FP16
  * value), read by the tensor cores; per 256 tokens the largest sum of squares
- * of a coded row; a 256-byte status block; and a flag per tile and a list of
- * the tiles computed in K chunks (about M * 2 * K + 12 * M * N / 65536 bytes
- * in all).  The caller allocates it; calls that share a workspace must not
- * overlap on the GPU.
+ * of a coded row; a 256-byte status block; per 16 weight rows the largest sum
+ * of squares; and a list of the tiles computed in K chunks (about
+ * M * 2 * K + 8 * M * N / 32768 + N / 4 bytes in all).  The caller allocates
+ * it; calls that share a workspace must not overlap on the GPU.
  */
 size_t h3q_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
@@ -204,7 +204,7 @@ h3q_status h3q_linear_w8a8_mma_sync(const int8_t* xq, const float* xs, const int
  * and with x or xq required (there is no reuse of an earlier call's
  * activations).  Shapes whose h3q_linear_workspace_bytes(M, N, K) exceeds
  * 16 MiB (16777216 bytes) are rejected with H3Q_ERR_UNSUPPORTED_SHAPE; at
- * N = K = 5376 that allows M up to 1560 tokens.
+ * N = K = 5376 that allows M up to 1559 tokens.
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream

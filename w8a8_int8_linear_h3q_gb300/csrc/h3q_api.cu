@@ -118,13 +118,13 @@ h3q_status h3q_linear_w8a8(const uint16_t* x, int8_t* xq, float* xs, const int8_
   uint16_t* act = reinterpret_cast<uint16_t*>(wsp + lay.act);
   uint32_t* amax = reinterpret_cast<uint32_t*>(wsp + lay.amax);
   uint32_t* status = reinterpret_cast<uint32_t*>(wsp + lay.status);
-  uint32_t* flags = reinterpret_cast<uint32_t*>(wsp + lay.flags);
+  uint32_t* nwpart = reinterpret_cast<uint32_t*>(wsp + lay.nwpart);
   uint2* list = reinterpret_cast<uint2*>(wsp + lay.list);
   const bool code_acts = x || xq;
-  // Zero the status block and the tile flags, and the activation norm maxima
-  // when the activations are coded anew (they sit just before the status block).
+  // Zero the status block, and the activation norm maxima when the
+  // activations are coded anew (they sit just before the status block).
   const size_t zero_from = code_acts ? lay.amax : lay.status;
-  if (cudaMemsetAsync(wsp + zero_from, 0, lay.list - zero_from, stream) != cudaSuccess)
+  if (cudaMemsetAsync(wsp + zero_from, 0, lay.nwpart - zero_from, stream) != cudaSuccess)
     return H3Q_ERR_CUDA;
   // A2, or the FP16 coding of pre-quantised activations, or (x == xq == NULL)
   // the activations a previous call left coded in this workspace.
@@ -137,10 +137,14 @@ h3q_status h3q_linear_w8a8(const uint16_t* x, int8_t* xq, float* xs, const int8_
     if (h3q_status st = from_cuda(h3q::launch_int8_to_f16(xq, M, K, ldh, act, amax, stream)))
       return st;
   }
+  // Weight-row norms, where the activations alone do not settle exactness.
+  if (h3q_status st =
+          from_cuda(h3q::launch_weight_norms(wq, N, K, amax, M, nwpart, stream)))
+    return st;
   // A3 + A4: the tiles that are exact over the whole K, then the rest in K
   // chunks (an empty launch when there are none).
   if (h3q_status st = from_cuda(h3q::launch_gemm_wide(act, xs, wq, ws, bias, M, N, K, y,
-                                                      acc_out, amax, status, flags, list,
+                                                      acc_out, amax, nwpart, status, list,
                                                       stream)))
     return st;
   return from_cuda(h3q::launch_gemm_tc(act, xs, wq, ws, bias, M, N, K, y, acc_out, status,

@@ -448,8 +448,8 @@ WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K) {
   l.act = 0;
   l.amax = up(size_t(M) * size_t(gemm_tc_coded_ld(K)) * 2u);
   l.status = l.amax + up(mt2 * 4u);
-  l.flags = l.status + 256u;
-  l.list = l.flags + up(mt2 * ntc * 4u);
+  l.nwpart = l.status + 256u;
+  l.list = l.nwpart + up(nt * kNormParts * 4u);
   l.total = l.list + up(mt * ntc * sizeof(uint2));
   return l;
 }

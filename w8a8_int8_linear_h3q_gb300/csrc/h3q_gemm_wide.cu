@@ -19,13 +19,13 @@
 // <= 2^24 and hence an FP32 value, so no addition rounds and one FP32
 // accumulator carries the exact dot product over all of K.  The activation
 // quantiser records, per block of 256 tokens, the largest sum of squares of a
-// coded row; the converter warps sum the squares of each weight row as they
-// convert it.  Every tile is computed here; the epilogue stores a channel row
-// of a tile only when that row's |w|^2 times its token block's largest |a|^2
-// is at most 2^48, which holds when the codes are mostly well below 127 in
-// magnitude -- the usual case for per-row absmax scaling of K = 5376 rows.
-// A tile with a row that fails is put (once) on a list in the workspace, and
-// the chunked kernel recomputes it afterwards.
+// coded row.  A tile (256 channels x 256 tokens) is computed here when that
+// maximum times the largest possible weight row (128^2 K) is at most 2^48 --
+// which holds for activations whose codes are mostly small, as per-row absmax
+// scaling of K = 5376 rows with outliers gives -- or, failing that, when it
+// times the tile's largest weight-row sum of squares (from a pre-pass that
+// runs only when some tile needs it) is.  The other tiles go to a list in the
+// workspace that the chunked kernel finishes afterwards.
 //
 // Against the chunked kernel this removes the per-chunk accumulator drains
 // (one drain per tile) and lets each converted weight slice feed 256 tokens
@@ -46,13 +46,11 @@
 // Warp roles (736 threads per CTA):
 //   warp 0      TMA producer of this CTA's activation half (4 super-stages)
 //   warp 1      TMEM allocator; MMA issuer (one thread, even CTA only)
-//   warp 2      tile scheduler and TMA producer of this CTA's INT8 weight
-//               tiles (4 super-stages)
-//   warps 3-6   converters: INT8 weights -> FP16 -> TMEM (2 super-stages),
-//               and each weight row's sum of squares
+//   warp 2      tile scheduler (exactness test, fallback list) and TMA
+//               producer of this CTA's INT8 weight tiles (4 super-stages)
+//   warps 3-6   converters: INT8 weights -> FP16 -> TMEM (2 super-stages)
 //   warps 7-22  epilogue: drain the accumulator to registers, release it,
-//               then check the bound per row, dequant + bias + BF16 (and
-//               the optional raw INT32)
+//               then dequant + bias + BF16 (and the optional raw INT32)
 // A super-stage is 2 k-blocks of 64 K: 8 pair MMAs of 256 x 256 x 16.
 // TMEM (each CTA): the FP32 accumulator in columns 0-255, A super-stages in
 // 256-319 and 320-383.  (Four A super-stages fit, but measured slower: the
@@ -121,8 +119,6 @@ struct __align__(1024) Smem {
   uint64_t dempty;                       // (even CTA) both epilogues have copied it out
   uint64_t mma_done;
   uint64_t q_full[SQ], q_empty[SQ];      // tile queue
-  uint64_t wn_full[2];                   // a tile's weight-row norms are in wn2
-  uint32_t wn2[2][BM];                   // per tile (alternating): sum of q^2 per channel row
   int q_tile[SQ];                        // cluster tile index, or -1: no more tiles
   uint32_t tmem_base;
   int abort_flag;
@@ -149,6 +145,21 @@ __device__ __forceinline__ void tile_coords(const Shape& s, int t, int& mb, int&
   const int r = t - g * per_group;
   mb = first_m + r % gm;
   pair = r / gm;
+}
+
+// Warp-collective: true when every (token, channel) of the cluster tile has
+// |a|^2 |w|^2 <= 2^48.  The token block's maximum against the largest possible
+// weight row settles most tiles; otherwise lanes 0-15 read the pair's 16
+// weight partial maxima.
+__device__ __forceinline__ bool tile_exact(const Shape& s, const uint32_t* amax,
+                                           const uint32_t* nwpart, int mb, int pair, int lane) {
+  const uint64_t a = amax[mb];
+  if (a * s.wmax2 <= kExactBound) return true;
+  const int idx = pair * CLUSTER * kNormParts + lane;
+  uint32_t w = (lane < CLUSTER * kNormParts && idx < s.nt * kNormParts) ? nwpart[idx] : 0u;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) w = max(w, __shfl_xor_sync(0xFFFFFFFFu, w, o));
+  return uint64_t(w) * a <= kExactBound;
 }
 
 // Single-thread take of the next queue entry.  False on a timeout or abort.
@@ -191,8 +202,8 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
                  const __grid_constant__ CUtensorMap w_map, const float* __restrict__ sa,
                  const float* __restrict__ sw, const uint16_t* __restrict__ bias,
                  const Shape shp, uint16_t* __restrict__ Y, int32_t* __restrict__ ACC,
-                 const uint32_t* __restrict__ amax, uint32_t* __restrict__ status,
-                 uint32_t* __restrict__ flags, uint2* __restrict__ list) {
+                 const uint32_t* __restrict__ amax, const uint32_t* __restrict__ nwpart,
+                 uint32_t* __restrict__ status, uint2* __restrict__ list) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~uintptr_t(1023));
@@ -215,7 +226,6 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
       P::mbar_init(&sm.q_full[i], 1);
       P::mbar_init(&sm.q_empty[i], QUEUE_READERS);
     }
-    for (int i = 0; i < 2; ++i) P::mbar_init(&sm.wn_full[i], NUM_CONV_WARPS * 32);
     P::mbar_init(&sm.dfull, 1);
     P::mbar_init(&sm.dempty, CLUSTER * NUM_EPI_WARPS * 32);
     P::mbar_init(&sm.mma_done, 1);
@@ -278,9 +288,20 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
     uint32_t gs = 0, gw = 0, nq = 0;
     bool ok = true;
     for (int t = cid; t < shp.tiles; t += ncl) {
+      int mb, pair;
+      tile_coords(shp, t, mb, pair);
+      if (!tile_exact(shp, amax, nwpart, mb, pair, lane)) {
+        // the chunked kernel takes it, as one or two 128-token tiles (both
+        // CTAs reach the same verdict; the even one lists it)
+        if (rank == 0 && lane == 0) {
+          const int n128 = min(2, shp.mt128 - 2 * mb);
+          const uint32_t i = atomicAdd(status + 1, uint32_t(n128));
+          for (int h = 0; h < n128; ++h)
+            list[i + h] = make_uint2(uint32_t(2 * mb + h), uint32_t(pair));
+        }
+        continue;
+      }
       if (lane == 0) {
-        int mb, pair;
-        tile_coords(shp, t, mb, pair);
         ok = push_tile(sm, nq, t, abort_flag, err);
         const int wrow = min(2 * pair + int(rank), shp.nt - 1) * BM;
         for (int ss = 0; ok && ss < shp.NSS; ++ss, ++gs) {
@@ -360,17 +381,11 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
     const uint32_t lane_base = uint32_t(32 * q) << 16;
     // this row's 16-byte chunks in a 128-byte-swizzled INT8 box (two k-blocks)
     const uint32_t row_off = uint32_t(r) * 128u, xr = uint32_t(r & 7);
-    uint32_t gs = 0, nq = 0, gt = 0;
+    uint32_t gs = 0, nq = 0;
     bool ok = true;
     while (ok) {
       int t;
       if (!pop_tile_warp(sm, nq, abort_flag, err, ERR_CONVERT, t, lane) || t < 0) break;
-      int mb, pair;
-      tile_coords(shp, t, mb, pair);
-      // the row norms matter only if the token block fails the bound with the
-      // largest possible weight row (|w|^2 <= 128^2 K)
-      const bool need_norm = uint64_t(amax[mb]) * shp.wmax2 > kExactBound;
-      uint32_t sq = 0;                            // this row's sum of q^2 (exact mod 2^32)
       for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
         const uint32_t slot = gs % B_SLOTS, aslot = gs % A_SLOTS;
         const uint32_t wslot = gs % W_SLOTS;
@@ -387,15 +402,6 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             v[i] = *reinterpret_cast<const uint4*>(box + row_off + (((cb + uint32_t(i)) ^ xr) << 4));
-          if (need_norm) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              sq = uint32_t(__dp4a(int(v[i].x), int(v[i].x), int(sq)));
-              sq = uint32_t(__dp4a(int(v[i].y), int(v[i].y), int(sq)));
-              sq = uint32_t(__dp4a(int(v[i].z), int(v[i].z), int(sq)));
-              sq = uint32_t(__dp4a(int(v[i].w), int(v[i].w), int(sq)));
-            }
-          }
           uint32_t h[32];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -428,11 +434,6 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
         P::tc_fence_before();
         P::mbar_arrive_cluster(full_a_pair + aslot * 8u);
       }
-      if (!ok) break;
-      // the row norms of this tile, for the epilogue's bound check
-      sm.wn2[gt & 1u][r] = sq;
-      P::mbar_arrive(&sm.wn_full[gt & 1u]);
-      ++gt;
     }
     P::tmem_wait_st();
   } else {
@@ -453,25 +454,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
       const int m0 = mb * BN + 64 * cq;
       const float sa0 = (m0 + lane < shp.M) ? sa[m0 + lane] : 0.f;
       const float sa1 = (m0 + 32 + lane < shp.M) ? sa[m0 + 32 + lane] : 0.f;
-      const uint32_t amb = amax[mb];
       if (!P::mbar_wait_warp(&sm.dfull, gt & 1u, abort_flag, err, ERR_EPILOGUE)) break;
-      if (!P::mbar_wait_warp(&sm.wn_full[gt & 1u], (gt >> 1) & 1u, abort_flag, err,
-                             ERR_EPILOGUE))
-        break;
-      // this row's FP32 sums were exact over all of K if |w|^2 max|a|^2 <= 2^48
-      const bool keep =
-          n_ok && (uint64_t(amb) * shp.wmax2 <= kExactBound ||
-                   uint64_t(sm.wn2[gt & 1u][32 * q + lane]) * amb <= kExactBound);
-      if (!__all_sync(0xFFFFFFFFu, keep || !n_ok) && lane == 0) {
-        // the chunked kernel recomputes this tile, as one or two 128-token tiles;
-        // the flag keeps the warps of both CTAs from listing it twice
-        if (atomicExch(flags + mb * shp.ntc + pair, 1u) == 0u) {
-          const int n128 = min(2, shp.mt128 - 2 * mb);
-          const uint32_t i = atomicAdd(status + 1, uint32_t(n128));
-          for (int h = 0; h < n128; ++h)
-            list[i + h] = make_uint2(uint32_t(2 * mb + h), uint32_t(pair));
-        }
-      }
       P::tc_fence_after();
       uint32_t d0[32], d1[32];
       P::tmem_ld32(tmem + lane_base + TM_D + 64 * cq, d0);
@@ -485,7 +468,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
         const float saj = __shfl_sync(0xFFFFFFFFu, sa0, j);
         const int m = m0 + j;
         const int a = __float2int_rn(__uint_as_float(d0[j]));
-        if (keep && m < shp.M) {
+        if (n_ok && m < shp.M) {
           const int64_t off = int64_t(m) * shp.N + n;
           if (ACC) ACC[off] = a;
           if (Y) Y[off] = float_to_bf16_bits(epilogue_value(a, saj, swn, bn));
@@ -496,7 +479,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
         const float saj = __shfl_sync(0xFFFFFFFFu, sa1, j);
         const int m = m0 + 32 + j;
         const int a = __float2int_rn(__uint_as_float(d1[j]));
-        if (keep && m < shp.M) {
+        if (n_ok && m < shp.M) {
           const int64_t off = int64_t(m) * shp.N + n;
           if (ACC) ACC[off] = a;
           if (Y) Y[off] = float_to_bf16_bits(epilogue_value(a, saj, swn, bn));
@@ -525,7 +508,8 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const int8_t* qw,
                              const float* sw, const uint16_t* bias, int64_t M, int64_t N,
                              int64_t K, uint16_t* y, int32_t* acc, const uint32_t* amax,
-                             uint32_t* status, uint32_t* flags, uint2* list, cudaStream_t s) {
+                             const uint32_t* nwpart, uint32_t* status, uint2* list,
+                             cudaStream_t s) {
   EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
   if (!enc) return cudaErrorNotSupported;
   // activations: a [M, ld] FP16 matrix viewed as (64-element chunk, row, chunk
@@ -582,13 +566,13 @@ cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const int
   attr[0].val.clusterDim.x = CLUSTER;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  // may start while the previous kernel (the quantiser) finishes
+  // may start while the weight-norm pre-pass finishes
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, gemm_wide_kernel, map, wmap, sa, sw, bias, shp, y, acc, amax,
-                            status, flags, list);
+                            nwpart, status, list);
 }
 
 }  // namespace h3q

@@ -37,31 +37,39 @@ int64_t gemm_tc_coded_ld(int64_t K);
 
 // Tokens per block of the activation norm maxima (the wide kernel's tile).
 constexpr int kNormTokens = 256;
+// Weight-norm partial maxima per 128-channel block (16 channels each).
+constexpr int kNormParts = 8;
 
 // The linear workspace, in order (each part 256-byte aligned):
 //   act     [M, gemm_tc_coded_ld(K)] FP16-coded activations
 //   amax    [ceil(M/256)] u32: per 256 tokens, max over rows of sum(qa^2)
 //   status  256 bytes: word 0 error bits, word 1 fallback-list length
-//   flags   [ceil(M/256) * ceil(N/256)] u32: a 256 x 256 tile is on the list
+//   nwpart  [ceil(N/128) * 8] u32: per 16 channels, max over rows of sum(qw^2)
 //   list    [ceil(M/128) * ceil(N/256)] uint2 {token block, channel pair}:
 //           the 128 x 256 tiles the chunked kernel must finish
 // act, amax and status depend on M and K only, so a call with another N
 // still finds the coded activations (reuse) and the status word there.
-// status and flags start each call at zero, amax too when the activations
-// are coded anew; they are contiguous so that one memset clears them.
+// status starts each call at zero, amax too when the activations are coded
+// anew; they are contiguous so that one memset clears them.
 struct WorkspaceLayout {
-  size_t act, amax, status, flags, list, total;
+  size_t act, amax, status, nwpart, list, total;
 };
 WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K);
 
-// A3 + A4 on every tile with one FP32 accumulator over the whole K; a tile
-// row whose squared-norm bound fails is not stored, and its tile is
-// appended (once, through flags) to `list`, status[1] counting the entries.
-// status[0]: error bits (bounded waits).
+// Weight pre-pass: nwpart as above, left unwritten when amax shows that no
+// tile can need it (programmatic dependent launch after the quantiser).
+cudaError_t launch_weight_norms(const int8_t* qw, int64_t N, int64_t K, const uint32_t* amax,
+                                int64_t M, uint32_t* nwpart, cudaStream_t s);
+
+// A3 + A4 for the tiles whose FP32 sums are exact over the whole K (checked
+// per tile from amax and, where that is not enough, nwpart); the others are
+// appended to `list`, status[1] counting the entries.  status[0]: error bits
+// (bounded waits).
 cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const int8_t* qw,
                              const float* sw, const uint16_t* bias, int64_t M, int64_t N,
                              int64_t K, uint16_t* y, int32_t* acc, const uint32_t* amax,
-                             uint32_t* status, uint32_t* flags, uint2* list, cudaStream_t s);
+                             const uint32_t* nwpart, uint32_t* status, uint2* list,
+                             cudaStream_t s);
 
 // A3 + A4 on the tcgen05 tensor cores (exact INT32 via FP16 MMA with chunked
 // FP32 accumulation).  act_f16: [M, gemm_tc_coded_ld(K)] FP16-coded INT8

@@ -337,6 +337,70 @@ int8_to_f16_kernel(const int8_t* __restrict__ q, int K, int ldh, uint16_t* __res
   }
 }
 
+// Weight-row norms for the GEMM's exactness test.  Every block first checks
+// whether any block of 256 tokens could fail the test against the largest
+// possible weight row (sum q^2 <= 128^2 K); if none can, the GEMM never reads
+// the norms and the block returns at once.  Otherwise block b (16 warps) sums
+// q^2 over weight rows 16b .. 16b+15 with DP4A on 16-byte loads and writes the
+// largest to part[b].  The sums are taken modulo 2^32, which is exact:
+// K * 128^2 < 2^32 for every supported K.
+constexpr int kNormRows = 16;
+
+__global__ void __launch_bounds__(32 * kNormRows)
+weight_norm_kernel(const int8_t* __restrict__ wq, int64_t N, int K,
+                   const uint32_t* __restrict__ amax, int mt2, uint32_t* __restrict__ part) {
+  // the quantiser that wrote amax may still be finishing (programmatic
+  // dependent launch): wait for it, then let the GEMM be scheduled
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ uint32_t red[kNormRows];
+  __shared__ int needed;
+  if (threadIdx.x == 0) needed = 0;
+  __syncthreads();
+  const uint64_t wmax2 = uint64_t(128 * 128) * uint64_t(K);
+  for (int i = threadIdx.x; i < mt2; i += blockDim.x)
+    if (uint64_t(amax[i]) * wmax2 > (uint64_t(1) << 48)) needed = 1;
+  __syncthreads();
+  if (!needed) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t n = int64_t(blockIdx.x) * kNormRows + warp;
+  uint32_t sq = 0;
+  if (n < N) {
+    const uint4* row = reinterpret_cast<const uint4*>(wq + n * K);
+    const int nv = K >> 4;
+    int i = lane;
+    for (; i + 96 < nv; i += 128) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldg(row + i + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        sq = uint32_t(__dp4a(int(v[u].x), int(v[u].x), int(sq)));
+        sq = uint32_t(__dp4a(int(v[u].y), int(v[u].y), int(sq)));
+        sq = uint32_t(__dp4a(int(v[u].z), int(v[u].z), int(sq)));
+        sq = uint32_t(__dp4a(int(v[u].w), int(v[u].w), int(sq)));
+      }
+    }
+    for (; i < nv; i += 32) {
+      const uint4 v = __ldg(row + i);
+      sq = uint32_t(__dp4a(int(v.x), int(v.x), int(sq)));
+      sq = uint32_t(__dp4a(int(v.y), int(v.y), int(sq)));
+      sq = uint32_t(__dp4a(int(v.z), int(v.z), int(sq)));
+      sq = uint32_t(__dp4a(int(v.w), int(v.w), int(sq)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+  if (lane == 0) red[warp] = sq;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int w = 0; w < kNormRows; ++w) m = max(m, red[w]);
+    part[blockIdx.x] = m;
+  }
+}
+
 template <bool kRegs>
 cudaError_t launch_act(const uint16_t* x, int64_t M, int K, int8_t* q, float* s, uint16_t* qh,
                        int ldh, uint32_t* sqm, cudaStream_t st) {
@@ -386,6 +450,23 @@ cudaError_t launch_quantize_weights(const void* w, int w_dtype, int64_t N, int64
     quant_weight_kernel<uint16_t><<<grid, block, 0, s>>>(static_cast<const uint16_t*>(w), N,
                                                          int(K), q, scale);
   return cudaGetLastError();
+}
+
+cudaError_t launch_weight_norms(const int8_t* qw, int64_t N, int64_t K, const uint32_t* amax,
+                                int64_t M, uint32_t* nwpart, cudaStream_t s) {
+  static_assert(128 / kNormRows == kNormParts, "partial maxima per 128-channel block");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((N + 127) / 128 * kNormParts));
+  cfg.blockDim = dim3(32 * kNormRows);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int mt2 = static_cast<int>((M + kNormTokens - 1) / kNormTokens);
+  return cudaLaunchKernelEx(&cfg, weight_norm_kernel, qw, N, static_cast<int>(K), amax, mt2,
+                            nwpart);
 }
 
 cudaError_t launch_int8_to_f16(const int8_t* q, int64_t M, int64_t K, int64_t ldh,
