@@ -316,9 +316,11 @@ def run_gpu(args):
     gemm_tflops = 2 * M * N * K / gemm_avg_s / 1e12
     quant_avg_s = time_quantize_act(h3q, x, flush)
     quant_bytes = 2 * M * K + M * K + 4 * M       # BF16 in, INT8 out, FP32 scales
+    traffic, traffic_note = profiled_traffic()
     roofline = {"bound": "tensor", "achieved": gemm_tflops, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": gemm_tflops / peaks["bf16_tflops"],
-                "traffic": None,
+                "traffic": traffic, "traffic_source": traffic_note,
+                "algorithmic_bytes_per_launch": 2 * M * K + N * K + 2 * M * N + 4 * M + 6 * N,
                 "kernel": gemm_kernel_name(h3q),
                 "timed_as": "whole reuse-mode Linear call: status memset + weight-norm "
                             "pre-pass + gemm_wide_kernel + the chunked kernel's launch",
@@ -359,6 +361,46 @@ def run_gpu(args):
 
 def gemm_kernel_name(h3q) -> str:
     return "gemm_wide_kernel"
+
+
+# The dominant kernel's DRAM traffic comes from an ncu capture summarised in
+# profiles/; it is reported only while the kernel's sources are the ones that
+# were captured (their SHA-256 is recorded beside the figure).
+WIDE_SOURCES = ["w8a8_int8_linear_h3q_gb300/csrc/h3q_gemm_wide.cu",
+                "w8a8_int8_linear_h3q_gb300/csrc/h3q_tc_ptx.cuh",
+                "w8a8_int8_linear_h3q_gb300/csrc/h3q_epilogue.cuh",
+                "w8a8_int8_linear_h3q_gb300/csrc/h3q_internal.cuh",
+                "include/h3q.h"]
+WIDE_PROFILE = "profiles/gemm_wide_attn_8192x5376x5376.md"
+
+
+def wide_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in WIDE_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic():
+    """(bytes per launch, note) from the committed ncu summary, or (None, why)."""
+    try:
+        text = open(os.path.join(ROOT, WIDE_PROFILE)).read()
+    except OSError:
+        return None, "no ncu summary"
+    fields = {}
+    for line in text.splitlines():
+        line = line.strip().lstrip("-* ").strip("`")
+        for key in ("traffic_bytes_per_launch:", "source_sha256:"):
+            if line.startswith(key):
+                fields[key[:-1]] = line[len(key):].strip()
+    if fields.get("source_sha256") != wide_sources_sha256():
+        return None, "kernel changed since the ncu capture"
+    try:
+        return int(fields["traffic_bytes_per_launch"]), f"ncu capture, {WIDE_PROFILE}"
+    except (KeyError, ValueError):
+        return None, "no traffic figure in the ncu summary"
 
 
 def time_quantize_act(h3q, x, flush, reps=10):
