@@ -196,6 +196,55 @@ __device__ __forceinline__ bool push_tile(Smem& sm, uint32_t& nq, int t, volatil
   return true;
 }
 
+// A4 for 32 consecutive tokens of this lane's channel row n: lane l holds the
+// scale of token mbase + l in sa_l, and d[j] the accumulator of token
+// mbase + j, an exact integer |t| <= 2^24 as an FP32 value.
+//
+// The epilogue's instructions compete for issue slots with the converter
+// warps, which are on the critical path right after a tile's accumulator is
+// released, so the common case is kept short.  Per element: c = RN(s_a s_w),
+// P = RN(t c) (relative error below 2^-23) and v = RN(P + bias) (at most
+// 2^-24 |v| more).  Whenever |v| >= 2^-10 |P| the total is below 2^-12 |v|,
+// under half a BF16 ulp, so one BF16 rounding of v is within one ulp of the
+// exact value.  Scales in the checked ranges keep c in [2^-100, 2^90], so for
+// t != 0 P is a finite normal number and the check also keeps v far above
+// the subnormal range; t = 0 gives v = bias exactly.  An element that fails
+// the check (deep cancellation with the bias) takes the error-free path.
+// Blocks with scales outside those ranges, ragged token tails and the raw
+// INT32 output take the general per-element path.
+__device__ __forceinline__ void emit_block(const uint32_t (&d)[32], float sa_l, int mbase,
+                                           float swn, float bn, int n, bool n_ok,
+                                           const Shape& shp, uint16_t* __restrict__ Y,
+                                           int32_t* __restrict__ ACC) {
+  const bool s_in = (sa_l == 0.f || (sa_l >= 0x1p-60f && sa_l <= 0x1p45f)) &&
+                    (swn >= 0x1p-40f && swn <= 0x1p45f);
+  if (__all_sync(0xFFFFFFFFu, s_in) && !ACC && Y && mbase + 32 <= shp.M) {
+    uint16_t* yp = Y + int64_t(mbase) * shp.N + n;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float saj = __shfl_sync(0xFFFFFFFFu, sa_l, j);
+      const float t = __uint_as_float(d[j]);
+      const float p = __fmul_rn(t, __fmul_rn(saj, swn));
+      float v = __fadd_rn(p, bn);
+      if (!(fabsf(v) >= fabsf(p) * 0x1p-10f))
+        v = epilogue_value_careful(__float2int_rn(t), saj, swn, bn);
+      if (n_ok) yp[int64_t(j) * shp.N] = float_to_bf16_bits(v);
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float saj = __shfl_sync(0xFFFFFFFFu, sa_l, j);
+    const int m = mbase + j;
+    const int a = __float2int_rn(__uint_as_float(d[j]));
+    if (n_ok && m < shp.M) {
+      const int64_t off = int64_t(m) * shp.N + n;
+      if (ACC) ACC[off] = a;
+      if (Y) Y[off] = float_to_bf16_bits(epilogue_value(a, saj, swn, bn));
+    }
+  }
+}
+
 // 23 warps: at most 6 per SM sub-partition, so 80 registers a thread.
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
@@ -463,28 +512,8 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
       P::tc_fence_before();
       P::mbar_arrive_cluster(dempty_pair);        // the MMAs of the next tile may start
       ++gt;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float saj = __shfl_sync(0xFFFFFFFFu, sa0, j);
-        const int m = m0 + j;
-        const int a = __float2int_rn(__uint_as_float(d0[j]));
-        if (n_ok && m < shp.M) {
-          const int64_t off = int64_t(m) * shp.N + n;
-          if (ACC) ACC[off] = a;
-          if (Y) Y[off] = float_to_bf16_bits(epilogue_value(a, saj, swn, bn));
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float saj = __shfl_sync(0xFFFFFFFFu, sa1, j);
-        const int m = m0 + 32 + j;
-        const int a = __float2int_rn(__uint_as_float(d1[j]));
-        if (n_ok && m < shp.M) {
-          const int64_t off = int64_t(m) * shp.N + n;
-          if (ACC) ACC[off] = a;
-          if (Y) Y[off] = float_to_bf16_bits(epilogue_value(a, saj, swn, bn));
-        }
-      }
+      emit_block(d0, sa0, m0, swn, bn, n, n_ok, shp, Y, ACC);
+      emit_block(d1, sa1, m0 + 32, swn, bn, n, n_ok, shp, Y, ACC);
     }
   }
 
