@@ -202,7 +202,8 @@ __device__ __forceinline__ bool push_tile(Smem& sm, uint32_t& nq, int t, volatil
 //
 // The epilogue's instructions compete for issue slots with the converter
 // warps, which are on the critical path right after a tile's accumulator is
-// released, so the common case is kept short.  Per element: c = RN(s_a s_w),
+// released, so the common case is kept short (and runs two tokens per
+// instruction where it can).  Per element: c = RN(s_a s_w),
 // P = RN(t c) (relative error below 2^-23) and v = RN(P + bias) (at most
 // 2^-24 |v| more).  Whenever |v| >= 2^-10 |P| the total is below 2^-12 |v|,
 // under half a BF16 ulp, so one BF16 rounding of v is within one ulp of the
@@ -220,15 +221,32 @@ __device__ __forceinline__ void emit_block(const uint32_t (&d)[32], float sa_l, 
                     (swn >= 0x1p-40f && swn <= 0x1p45f);
   if (__all_sync(0xFFFFFFFFu, s_in) && !ACC && Y && mbase + 32 <= shp.M) {
     uint16_t* yp = Y + int64_t(mbase) * shp.N + n;
+    // two tokens at a time with the paired FP32 instructions (the same IEEE
+    // operations as the scalar ones, half the instructions)
+    const uint64_t sw2 = (uint64_t(__float_as_uint(swn)) << 32) | __float_as_uint(swn);
+    const uint64_t b2 = (uint64_t(__float_as_uint(bn)) << 32) | __float_as_uint(bn);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float saj = __shfl_sync(0xFFFFFFFFu, sa_l, j);
-      const float t = __uint_as_float(d[j]);
-      const float p = __fmul_rn(t, __fmul_rn(saj, swn));
-      float v = __fadd_rn(p, bn);
-      if (!(fabsf(v) >= fabsf(p) * 0x1p-10f))
-        v = epilogue_value_careful(__float2int_rn(t), saj, swn, bn);
-      if (n_ok) yp[int64_t(j) * shp.N] = float_to_bf16_bits(v);
+    for (int j = 0; j < 32; j += 2) {
+      const float sa_a = __shfl_sync(0xFFFFFFFFu, sa_l, j);
+      const float sa_b = __shfl_sync(0xFFFFFFFFu, sa_l, j + 1);
+      const uint64_t sa2 = (uint64_t(__float_as_uint(sa_b)) << 32) | __float_as_uint(sa_a);
+      const uint64_t t2 = (uint64_t(d[j + 1]) << 32) | d[j];
+      uint64_t c2, p2, v2;
+      asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(c2) : "l"(sa2), "l"(sw2));
+      asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p2) : "l"(t2), "l"(c2));
+      asm("add.rn.f32x2 %0, %1, %2;" : "=l"(v2) : "l"(p2), "l"(b2));
+      const float pa = __uint_as_float(uint32_t(p2)), pb = __uint_as_float(uint32_t(p2 >> 32));
+      float va = __uint_as_float(uint32_t(v2)), vb = __uint_as_float(uint32_t(v2 >> 32));
+      if (!(fabsf(va) >= fabsf(pa) * 0x1p-10f))
+        va = epilogue_value_careful(__float2int_rn(__uint_as_float(d[j])), sa_a, swn, bn);
+      if (!(fabsf(vb) >= fabsf(pb) * 0x1p-10f))
+        vb = epilogue_value_careful(__float2int_rn(__uint_as_float(d[j + 1])), sa_b, swn, bn);
+      uint32_t h2;
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h2) : "f"(vb), "f"(va));
+      if (n_ok) {
+        yp[int64_t(j) * shp.N] = uint16_t(h2);
+        yp[int64_t(j + 1) * shp.N] = uint16_t(h2 >> 16);
+      }
     }
     return;
   }
