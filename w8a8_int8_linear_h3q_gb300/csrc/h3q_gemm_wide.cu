@@ -197,8 +197,9 @@ __device__ __forceinline__ bool push_tile(Smem& sm, uint32_t& nq, int t, volatil
 }
 
 // A4 for 32 consecutive tokens of this lane's channel row n: lane l holds the
-// scale of token mbase + l in sa_l, and d[j] the accumulator of token
-// mbase + j, an exact integer |t| <= 2^24 as an FP32 value.
+// scale of token mbase + l in sa_l (sa_all is the whole scale vector), and d[j]
+// the accumulator of token mbase + j, an exact integer |t| <= 2^24 as an FP32
+// value.
 //
 // The epilogue's instructions compete for issue slots with the converter
 // warps, which are on the critical path right after a tile's accumulator is
@@ -216,19 +217,21 @@ __device__ __forceinline__ bool push_tile(Smem& sm, uint32_t& nq, int t, volatil
 __device__ __forceinline__ void emit_block(const uint32_t (&d)[32], float sa_l, int mbase,
                                            float swn, float bn, int n, bool n_ok,
                                            const Shape& shp, uint16_t* __restrict__ Y,
-                                           int32_t* __restrict__ ACC) {
+                                           int32_t* __restrict__ ACC, const float* __restrict__ sa_all) {
   const bool s_in = (sa_l == 0.f || (sa_l >= 0x1p-60f && sa_l <= 0x1p45f)) &&
                     (swn >= 0x1p-40f && swn <= 0x1p45f);
   if (__all_sync(0xFFFFFFFFu, s_in) && !ACC && Y && mbase + 32 <= shp.M) {
     uint16_t* yp = Y + int64_t(mbase) * shp.N + n;
+    const float* sa_ptr = sa_all + mbase;
     // two tokens at a time with the paired FP32 instructions (the same IEEE
     // operations as the scalar ones, half the instructions)
     const uint64_t sw2 = (uint64_t(__float_as_uint(swn)) << 32) | __float_as_uint(swn);
     const uint64_t b2 = (uint64_t(__float_as_uint(bn)) << 32) | __float_as_uint(bn);
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
-      const float sa_a = __shfl_sync(0xFFFFFFFFu, sa_l, j);
-      const float sa_b = __shfl_sync(0xFFFFFFFFu, sa_l, j + 1);
+      // both tokens' scales in one broadcast load (every lane reads the same 8 bytes)
+      const float2 sab = __ldg(reinterpret_cast<const float2*>(sa_ptr + j));
+      const float sa_a = sab.x, sa_b = sab.y;
       const uint64_t sa2 = (uint64_t(__float_as_uint(sa_b)) << 32) | __float_as_uint(sa_a);
       const uint64_t t2 = (uint64_t(d[j + 1]) << 32) | d[j];
       uint64_t c2, p2, v2;
@@ -446,8 +449,12 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
     const int q = warp & 3;                       // TMEM lane quarter of this warp
     const int r = 32 * q + lane;                  // channel row within the tile
     const uint32_t lane_base = uint32_t(32 * q) << 16;
-    // this row's 16-byte chunks in a 128-byte-swizzled INT8 box (two k-blocks)
+    // this row's 16-byte chunks in a 128-byte-swizzled INT8 box (two k-blocks),
+    // precomputed: the converters' instructions are on the critical path
     const uint32_t row_off = uint32_t(r) * 128u, xr = uint32_t(r & 7);
+    uint32_t coff[4 * SS];
+#pragma unroll
+    for (int k = 0; k < 4 * SS; ++k) coff[k] = row_off + ((uint32_t(k) ^ xr) << 4);
     uint32_t gs = 0, nq = 0;
     bool ok = true;
     while (ok) {
@@ -462,13 +469,14 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
           ok = false;
           break;
         }
-        for (int j = 0; j < nkb; ++j) {
+#pragma unroll
+        for (int j = 0; j < SS; ++j) {
+          if (j >= nkb) break;
           const uint8_t* box = sm.w[wslot];
-          const uint32_t cb = uint32_t(j) * 4u;
           uint4 v[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            v[i] = *reinterpret_cast<const uint4*>(box + row_off + (((cb + uint32_t(i)) ^ xr) << 4));
+            v[i] = *reinterpret_cast<const uint4*>(box + coff[4 * j + i]);
           uint32_t h[32];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -485,8 +493,8 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
               ok = false;
               break;
             }
+            P::tc_fence_after();
           }
-          P::tc_fence_after();
           P::tmem_st32(tmem + lane_base + TM_A + aslot * (SS * 32) + uint32_t(j) * 32, h);
         }
         if (!ok) break;
@@ -530,8 +538,8 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
       P::tc_fence_before();
       P::mbar_arrive_cluster(dempty_pair);        // the MMAs of the next tile may start
       ++gt;
-      emit_block(d0, sa0, m0, swn, bn, n, n_ok, shp, Y, ACC);
-      emit_block(d1, sa1, m0 + 32, swn, bn, n, n_ok, shp, Y, ACC);
+      emit_block(d0, sa0, m0, swn, bn, n, n_ok, shp, Y, ACC, sa);
+      emit_block(d1, sa1, m0 + 32, swn, bn, n, n_ok, shp, Y, ACC, sa);
     }
   }
 
