@@ -231,10 +231,25 @@ def run_gpu(args):
     flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    # per-launch events on the launching stream (the library's kernels run there)
+    gws = torch.empty((h3q.h3q_linear_grouped_workspace_bytes(len(LINEARS), M, N, K),),
+                      dtype=torch.uint8, device=dev)
+
+    # events on the launching stream (the library's kernels run there)
     def step(ev=None):
-        """One pass of the hot path: Q quantises X (A2) into the workspace and
-        runs its GEMM; K, V and O reuse the coded activations."""
+        """One pass of the hot path: the four Linears share X, so one grouped
+        call quantises X once (A2) and computes all four outputs in one GEMM
+        launch."""
+        if ev is not None:
+            ev[0].record(stream)
+        h3q.h3q_linear_w8a8_grouped(x, wq, wsc, bias, xs=xs, ys=ys, workspace=gws,
+                                    stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def step_per_linear(ev=None):
+        """The same pass as four calls: Q quantises X into the workspace and runs
+        its GEMM; K, V and O reuse the coded activations.  Events between the
+        calls time each reuse-mode GEMM call on its own."""
         if ev is not None:
             ev[0].record(stream)
         for i in range(len(LINEARS)):
@@ -243,18 +258,20 @@ def run_gpu(args):
             if ev is not None:
                 ev[1 + i].record(stream)
 
-    # A2 once; per Linear the weight-norm pre-pass (which returns at once when
-    # the activations alone settle exactness), the single-accumulator GEMM and
-    # the chunked GEMM (which exits at once when no tile needs it), after a
-    # memset of the workspace's status words
-    launches_per_step = 1 + 3 * len(LINEARS)
+    # A2, the weight-norm pre-pass (which returns at once when the activations
+    # alone settle exactness), one single-accumulator GEMM launch for all four
+    # Linears and per Linear the chunked GEMM (which exits at once when no
+    # tile needs it), after a memset of the workspace's status words
+    launches_per_step = 3 + len(LINEARS)
 
     for _ in range(args.warmup):
         flush.zero_()
         step()
+        flush.zero_()
+        step_per_linear()
     torch.cuda.synchronize()
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(1 + len(LINEARS))]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
               for _ in range(args.steps)]
     clk = ClockSampler(local)
     clk.start()
@@ -271,10 +288,21 @@ def run_gpu(args):
     clocks = clk.stop()
 
     step_ms = [e[0].elapsed_time(e[-1]) for e in events]
-    first_ms = [e[0].elapsed_time(e[1]) for e in events]          # A2 + Q's GEMM
-    gemm_ms = [e[i].elapsed_time(e[i + 1]) for e in events for i in range(1, len(LINEARS))]
     total_ms = max_over_ranks(sum(step_ms), world, dev)
     value = whole_job_tops(total_ms, args.steps, world)
+
+    # the per-Linear form of the step (untimed for the headline): its calls
+    # give the single GEMM call's time for the roofline
+    pl_steps = min(args.steps, 50)
+    pl_events = [[torch.cuda.Event(enable_timing=True) for _ in range(1 + len(LINEARS))]
+                 for _ in range(pl_steps)]
+    for s in range(pl_steps):
+        flush.zero_()
+        step_per_linear(pl_events[s])
+    torch.cuda.synchronize()
+    pl_ms = max_over_ranks(sum(e[0].elapsed_time(e[-1]) for e in pl_events), world, dev)
+    per_linear_tops = whole_job_tops(pl_ms, pl_steps, world)
+    gemm_ms = [e[i].elapsed_time(e[i + 1]) for e in pl_events for i in range(1, len(LINEARS))]
 
     # end to end through the public API with host buffers: pinned H2D of X,
     # the hot path, D2H of the four outputs, all inside the timed region.  Each
@@ -344,6 +372,7 @@ def run_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
             "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "linears": 4,
                        "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "step": "h3q_linear_w8a8_grouped: A2 once, one GEMM launch for Q, K, V, O",
                        "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MB write)",
                        "chunked_tiles_per_linear": chunked,
                        "tiles_per_linear": -(-M // 128) * -(-N // 256)},
@@ -353,6 +382,8 @@ def run_gpu(args):
                         "quantize_act_gbs": quant_bytes / quant_avg_s / 1e9,
                         "quantize_act_hbm_frac": quant_bytes / quant_avg_s / 1e9 / peaks["hbm_gbs"],
                         "gemm_us_per_linear": gemm_avg_s * 1e6,
+                        "per_linear_step_tops": per_linear_tops,
+                        "per_linear_step_ms": pl_ms / pl_steps,
                         "gemm_tops": gemm_tflops},
             "e2e": {"value": e2e_value, "unit": "TOPS", "ms_per_step":
                     e_ms / e2e_steps if e2e_steps else None,

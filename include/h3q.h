@@ -157,6 +157,40 @@ h3q_status h3q_linear_w8a8(const uint16_t* x, int8_t* xq, float* xs,
                            cudaStream_t stream);
 
 /*
+ * Bytes of device workspace for h3q_linear_w8a8_grouped with G Linears of
+ * this shape (as h3q_linear_workspace_bytes, with the weight norms and the
+ * fallback lists once per Linear).  0 if G is outside 1..4.
+ */
+size_t h3q_linear_grouped_workspace_bytes(int G, int64_t M, int64_t N, int64_t K);
+
+/*
+ * A2 + A3 + A4 for G Linears that read the same activations -- the Q, K and
+ * V projections of a DiT block ([P1] opening description: the per-block
+ * projections of the 300-Linear dit_proj profile, quantised separately, never
+ * fused) -- in one pass: A2 once, then the output tiles of all G Linears from
+ * one persistent GEMM launch.  Each result is that of h3q_linear_w8a8 with
+ * the same operands, bit for bit.
+ *
+ *   x, xq, xs  as in h3q_linear_w8a8 (quantise, pre-quantised, or reuse).
+ *   G          1..4 Linears, all of shape [N, K].
+ *   wq, ws, bias, y
+ *              host arrays of G device pointers: INT8 weights [N, K], FP32
+ *              scales [N], BF16 bias [N] (bias itself, or any entry, may be
+ *              NULL), BF16 outputs [M, N] (never NULL).
+ *   workspace  >= h3q_linear_grouped_workspace_bytes(G, M, N, K) bytes.
+ *
+ * Errors as h3q_linear_w8a8; G outside 1..4 or a NULL array or required
+ * entry gives H3Q_ERR_INVALID_ARG.  The pointer arrays are read during the
+ * call only.  Enqueued on `stream`; does not synchronise.
+ */
+h3q_status h3q_linear_w8a8_grouped(const uint16_t* x, int8_t* xq, float* xs, int G,
+                                   const int8_t* const* wq, const float* const* ws,
+                                   const uint16_t* const* bias,
+                                   int64_t M, int64_t N, int64_t K,
+                                   uint16_t* const* y, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream);
+
+/*
  * Status of the last h3q_linear_w8a8 that used `workspace` (same M, K):
  * H3Q_OK, or H3Q_ERR_TIMEOUT if one of its bounded device-side waits gave up.
  * SYNCHRONISES `stream` to read the status word.
@@ -166,7 +200,8 @@ h3q_status h3q_workspace_status(const void* workspace, int64_t M, int64_t K,
 
 /*
  * Diagnostic: how many tiles of 128 tokens x 256 channels the last
- * h3q_linear_w8a8 that used `workspace` (same M, K) computed with K cut into
+ * h3q_linear_w8a8 (or, summed over its Linears, h3q_linear_w8a8_grouped)
+ * that used `workspace` (same M, K) computed with K cut into
  * chunks, because the squared-norm bound did not let one FP32 accumulator
  * hold all of K; the other tiles took the single-accumulator path.  Both
  * paths give the same exact result; the chunked one is slower.  Written to

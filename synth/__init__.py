@@ -141,6 +141,36 @@ def fc2(M: int = 32768) -> LinearCase:
     return c
 
 
+# --- H3-Image operator shapes at 4096 tokens (a secondary workload) ----------------
+# "MLX implementation and experiment report" (MiniMax-H3-Image-mlx), Operator
+# tuning: the QKV GEMM 5376 -> 21504, the fused gate/up GEMM 5376 -> 28672 and
+# the down GEMM 14336 -> 5376, timed there at 4096 tokens on synthetic BF16
+# inputs.  Here: X ~ N(0,1), W ~ N(0, 0.02), bias ~ N(0, 0.1).
+
+IMAGE_TOKENS = 4096
+
+
+def image_qkv(M: int = IMAGE_TOKENS) -> LinearCase:
+    """X [4096, 5376] N(0,1); W [21504, 5376] N(0, 0.02); seed 5."""
+    c = make_linear(M, 21504, H3_WIDTH, seed=5, w_std=0.02, names=["qkv"])
+    c.name = "image_qkv"
+    return c
+
+
+def image_gate_up(M: int = IMAGE_TOKENS) -> LinearCase:
+    """X [4096, 5376] N(0,1); W [28672, 5376] N(0, 0.02); seed 6."""
+    c = make_linear(M, 28672, H3_WIDTH, seed=6, w_std=0.02, names=["gate_up"])
+    c.name = "image_gate_up"
+    return c
+
+
+def image_down(M: int = IMAGE_TOKENS) -> LinearCase:
+    """X [4096, 14336] N(0,1); W [5376, 14336] N(0, 0.02); seed 7."""
+    c = make_linear(M, H3_WIDTH, 14336, seed=7, w_std=0.02, names=["down"])
+    c.name = "image_down"
+    return c
+
+
 # --- the 300-Linear sweep (device-generated) -------------------------------------
 
 SWEEP_M = 75647
@@ -180,4 +210,5 @@ def sweep_weight(block: int, j: int, device):
     return w, b
 
 
-WORKLOADS = {"tiny": tiny, "attn": attn, "fc1": fc1, "fc2": fc2}
+WORKLOADS = {"tiny": tiny, "attn": attn, "fc1": fc1, "fc2": fc2, "image_qkv": image_qkv,
+             "image_gate_up": image_gate_up, "image_down": image_down}

@@ -113,3 +113,27 @@ def test_valid_args_without_a_device_report_no_device(cdll):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present: this checks the no-device report only")
     assert cdll.h3q_quantize_act(A, 4, 64, A, A, NUL) == 7
+
+
+def test_grouped_linear_rejects_bad_args(cdll):
+    f = cdll.h3q_linear_w8a8_grouped
+    ws = cdll.h3q_linear_grouped_workspace_bytes(3, 4, 8, 64)
+    assert cdll.h3q_linear_grouped_workspace_bytes(0, 4, 8, 64) == 0
+    assert cdll.h3q_linear_grouped_workspace_bytes(5, 4, 8, 64) == 0
+    assert (cdll.h3q_linear_grouped_workspace_bytes(3, 4096, 5376, 64)
+            > cdll.h3q_linear_workspace_bytes(4096, 5376, 64))
+    arr = lambda *p: (ctypes.c_void_p * len(p))(*p)
+    P3 = arr(0x10000, 0x20000, 0x30000)
+    one_null = arr(0x10000, None, 0x30000)
+    one_mis = arr(0x10000, 0x10008, 0x30000)
+    # x, xq, xs, G, wq, ws, bias, M, N, K, y, workspace, bytes, stream
+    assert f(A, NUL, A, 0, P3, P3, NUL, 4, 8, 64, P3, A, ws, NUL) == 1         # G = 0
+    assert f(A, NUL, A, 5, P3, P3, NUL, 4, 8, 64, P3, A, ws, NUL) == 1         # G = 5
+    assert f(A, NUL, A, 3, NUL, P3, NUL, 4, 8, 64, P3, A, ws, NUL) == 1        # no weight array
+    assert f(A, NUL, A, 3, one_null, P3, NUL, 4, 8, 64, P3, A, ws, NUL) == 1   # a NULL weight
+    assert f(A, NUL, A, 3, P3, P3, NUL, 4, 8, 64, one_null, A, ws, NUL) == 1   # a NULL output
+    assert f(A, NUL, NUL, 3, P3, P3, NUL, 4, 8, 64, P3, A, ws, NUL) == 1       # no xs
+    assert f(A, NUL, A, 3, P3, P3, NUL, 4, 8, 64, P3, A, ws - 256, NUL) == 1   # workspace too small
+    assert f(A, NUL, A, 3, P3, P3, NUL, 4, 8, 60, P3, A, ws, NUL) == 2         # K % 16
+    assert f(A, NUL, A, 3, P3, one_mis, NUL, 4, 8, 64, P3, A, ws, NUL) == 3    # misaligned scale
+    assert f(A, NUL, A, 3, P3, P3, one_mis, 4, 8, 64, P3, A, ws, NUL) == 3     # misaligned bias

@@ -244,6 +244,15 @@ def test_fc1_workload_sampled(lib, oracle, dev):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("name", ["image_qkv", "image_gate_up", "image_down"])
+def test_image_operator_shapes_sampled(lib, oracle, dev, name):
+    # the H3-Image operator shapes at 4096 tokens (secondary workload)
+    c = synth.WORKLOADS[name]()
+    _linear_check(lib, oracle, dev, c.x_bits, c.w[0], c.bias_bits[0],
+                  rows=_sample_rows(c.M, 105 + len(name)))
+
+
+@pytest.mark.slow
 def test_fc2_workload_sampled(lib, oracle, dev):
     c = synth.fc2()
     _linear_check(lib, oracle, dev, c.x_bits, c.w[0], c.bias_bits[0], rows=_sample_rows(c.M, 103))

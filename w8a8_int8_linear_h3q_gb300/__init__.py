@@ -49,6 +49,12 @@ def _declare(lib):
     lib.h3q_linear_w8a8.restype = i32
     lib.h3q_workspace_status.argtypes = [vp, i64, i64, vp]
     lib.h3q_workspace_status.restype = i32
+    lib.h3q_linear_grouped_workspace_bytes.argtypes = [i32, i64, i64, i64]
+    lib.h3q_linear_grouped_workspace_bytes.restype = sz
+    lib.h3q_linear_w8a8_grouped.argtypes = [vp, vp, vp, i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                            ctypes.POINTER(vp), i64, i64, i64, ctypes.POINTER(vp),
+                                            vp, sz, vp]
+    lib.h3q_linear_w8a8_grouped.restype = i32
     lib.h3q_linear_chunked_tiles.argtypes = [vp, i64, i64, ctypes.POINTER(i64), vp]
     lib.h3q_linear_chunked_tiles.restype = i32
     lib.h3q_linear_w8a8_mma_sync.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
@@ -217,6 +223,62 @@ def h3q_workspace_status(workspace, M: int, K: int, stream=None) -> int:
     """Status word of the last linear call on ``workspace``: 0 = ok,
     H3Q_ERR_TIMEOUT if a bounded device-side wait gave up.  Synchronises."""
     return int(load().h3q_workspace_status(_ptr(workspace), M, K, _stream(stream)))
+
+
+def h3q_linear_grouped_workspace_bytes(G: int, M: int, N: int, K: int) -> int:
+    return int(load().h3q_linear_grouped_workspace_bytes(G, M, N, K))
+
+
+def h3q_linear_w8a8_grouped(x, wqs, wss, biases=None, *, xq=None, xs=None, ys=None,
+                            workspace=None, M=None, stream=None):
+    """A2 once + A3 + A4 for the Linears (wqs[g], wss[g], biases[g]) that share
+    the input, in one GEMM launch.  ``x`` BF16 [M, K], or None with ``xq``/``xs``
+    (pre-quantised), or None with ``xq`` None (reuse: pass ``xs``, ``M`` and the
+    ``workspace`` of an earlier call).  Returns a dict with the outputs ``ys``
+    (BF16 [M, N] each), ``xs`` and the ``workspace``."""
+    import torch
+    G = len(wqs)
+    if not 1 <= G <= 4 or len(wss) != G or (biases is not None and len(biases) != G):
+        raise ValueError("1..4 Linears, with one scale vector (and bias) each")
+    for w in wqs:
+        _need(w, torch.int8, tuple(wqs[0].shape), "wq")
+    N, K = wqs[0].shape
+    dev = wqs[0].device
+    if x is not None:
+        _need(x, torch.bfloat16, None, "x")
+        M = x.shape[0]
+        if xs is None:
+            xs = torch.empty((M,), dtype=torch.float32, device=dev)
+    elif xq is not None:
+        if xs is None:
+            raise ValueError("pre-quantised call needs xs")
+        M = xq.shape[0]
+        _need(xq, torch.int8, (M, K), "xq")
+    else:
+        if xs is None or workspace is None:
+            raise ValueError("reuse call needs xs and the workspace")
+        M = xs.shape[0]
+    _need(xs, torch.float32, (M,), "xs")
+    for s in wss:
+        _need(s, torch.float32, (N,), "ws")
+    if biases is not None:
+        for b in biases:
+            if b is not None:
+                _need(b, torch.bfloat16, (N,), "bias")
+    if ys is None:
+        ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(G)]
+    for y in ys:
+        _need(y, torch.bfloat16, (M, N), "y")
+    need = h3q_linear_grouped_workspace_bytes(G, M, N, K)
+    if workspace is None:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=dev)
+    wbytes = workspace.numel() * workspace.element_size()
+    arr = lambda ts: (ctypes.c_void_p * G)(*[None if t is None else t.data_ptr() for t in ts])
+    _check(load().h3q_linear_w8a8_grouped(
+        _ptr(x), _ptr(xq), _ptr(xs), G, arr(wqs), arr(wss),
+        None if biases is None else arr(biases), M, N, K, arr(ys), _ptr(workspace), wbytes,
+        _stream(stream)), "h3q_linear_w8a8_grouped")
+    return {"ys": ys, "xs": xs, "workspace": workspace}
 
 
 def h3q_linear_chunked_tiles(workspace, M: int, K: int, stream=None) -> int:

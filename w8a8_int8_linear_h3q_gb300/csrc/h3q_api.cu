@@ -44,6 +44,62 @@ h3q_status from_cuda(cudaError_t e) {
   return H3Q_ERR_CUDA;
 }
 
+// The launch sequence of a (grouped) Linear call; the per-Linear pointers are
+// already checked.
+h3q_status run_linear(const uint16_t* x, int8_t* xq, float* xs, const h3q::LinearGroup& grp,
+                      int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+  if (!xs || !workspace) return H3Q_ERR_INVALID_ARG;
+  if (h3q_status st = check_shape(M, N, K)) return st;
+  const h3q::WorkspaceLayout lay = h3q::workspace_layout(M, N, K, grp.G);
+  if (workspace_bytes < lay.total) return H3Q_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, xq, xs, workspace};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return H3Q_ERR_MISALIGNED;
+  if (h3q_status st = check_device()) return st;
+
+  uint8_t* wsp = static_cast<uint8_t*>(workspace);
+  uint16_t* act = reinterpret_cast<uint16_t*>(wsp + lay.act);
+  uint32_t* amax = reinterpret_cast<uint32_t*>(wsp + lay.amax);
+  uint32_t* status = reinterpret_cast<uint32_t*>(wsp + lay.status);
+  uint32_t* nwpart = reinterpret_cast<uint32_t*>(wsp + lay.nwpart);
+  uint2* list = reinterpret_cast<uint2*>(wsp + lay.list);
+  const bool code_acts = x || xq;
+  // Zero the status block, and the activation norm maxima when the
+  // activations are coded anew (they sit just before the status block).
+  const size_t zero_from = code_acts ? lay.amax : lay.status;
+  if (cudaMemsetAsync(wsp + zero_from, 0, lay.nwpart - zero_from, stream) != cudaSuccess)
+    return H3Q_ERR_CUDA;
+  // A2, or the FP16 coding of pre-quantised activations, or (x == xq == NULL)
+  // the activations a previous call left coded in this workspace.
+  const int64_t ldh = h3q::gemm_tc_coded_ld(K);
+  if (x) {
+    if (h3q_status st =
+            from_cuda(h3q::launch_quantize_act(x, M, K, xq, xs, act, ldh, amax, stream)))
+      return st;
+  } else if (xq) {
+    if (h3q_status st = from_cuda(h3q::launch_int8_to_f16(xq, M, K, ldh, act, amax, stream)))
+      return st;
+  }
+  // Weight-row norms, where the activations alone do not settle exactness.
+  if (h3q_status st =
+          from_cuda(h3q::launch_weight_norms(grp, N, K, amax, M, nwpart, stream)))
+    return st;
+  // A3 + A4: the tiles that are exact over the whole K, of every Linear in
+  // one launch; then, per Linear, the rest in K chunks (an empty launch when
+  // there are none).
+  if (h3q_status st = from_cuda(h3q::launch_gemm_wide(act, xs, grp, M, N, K, amax, nwpart,
+                                                      status, list, stream)))
+    return st;
+  const size_t cap = h3q::fallback_list_capacity(M, N);
+  for (int g = 0; g < grp.G; ++g)
+    if (h3q_status st = from_cuda(h3q::launch_gemm_tc(act, xs, grp.wq[g], grp.ws[g], grp.bias[g],
+                                                      M, N, K, grp.y[g], grp.acc[g], status,
+                                                      list + g * cap, status + 2 + g, stream)))
+      return st;
+  return H3Q_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -104,51 +160,47 @@ h3q_status h3q_linear_w8a8(const uint16_t* x, int8_t* xq, float* xs, const int8_
                            const float* ws, const uint16_t* bias, int64_t M, int64_t N,
                            int64_t K, uint16_t* y, int32_t* acc_out, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream) {
-  if (!xs || !wq || !ws || !workspace) return H3Q_ERR_INVALID_ARG;
+  if (!wq || !ws) return H3Q_ERR_INVALID_ARG;
   if (!y && !acc_out) return H3Q_ERR_INVALID_ARG;  // nothing to write
-  if (h3q_status st = check_shape(M, N, K)) return st;
-  if (workspace_bytes < h3q_linear_workspace_bytes(M, N, K)) return H3Q_ERR_INVALID_ARG;
-  const void* ptrs[] = {x, xq, xs, wq, ws, bias, y, acc_out, workspace};
+  const void* ptrs[] = {wq, ws, bias, y, acc_out};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return H3Q_ERR_MISALIGNED;
-  if (h3q_status st = check_device()) return st;
+  h3q::LinearGroup grp = {};
+  grp.G = 1;
+  grp.wq[0] = wq;
+  grp.ws[0] = ws;
+  grp.bias[0] = bias;
+  grp.y[0] = y;
+  grp.acc[0] = acc_out;
+  return run_linear(x, xq, xs, grp, M, N, K, workspace, workspace_bytes, stream);
+}
 
-  const h3q::WorkspaceLayout lay = h3q::workspace_layout(M, N, K);
-  uint8_t* wsp = static_cast<uint8_t*>(workspace);
-  uint16_t* act = reinterpret_cast<uint16_t*>(wsp + lay.act);
-  uint32_t* amax = reinterpret_cast<uint32_t*>(wsp + lay.amax);
-  uint32_t* status = reinterpret_cast<uint32_t*>(wsp + lay.status);
-  uint32_t* nwpart = reinterpret_cast<uint32_t*>(wsp + lay.nwpart);
-  uint2* list = reinterpret_cast<uint2*>(wsp + lay.list);
-  const bool code_acts = x || xq;
-  // Zero the status block, and the activation norm maxima when the
-  // activations are coded anew (they sit just before the status block).
-  const size_t zero_from = code_acts ? lay.amax : lay.status;
-  if (cudaMemsetAsync(wsp + zero_from, 0, lay.nwpart - zero_from, stream) != cudaSuccess)
-    return H3Q_ERR_CUDA;
-  // A2, or the FP16 coding of pre-quantised activations, or (x == xq == NULL)
-  // the activations a previous call left coded in this workspace.
-  const int64_t ldh = h3q::gemm_tc_coded_ld(K);
-  if (x) {
-    if (h3q_status st =
-            from_cuda(h3q::launch_quantize_act(x, M, K, xq, xs, act, ldh, amax, stream)))
-      return st;
-  } else if (xq) {
-    if (h3q_status st = from_cuda(h3q::launch_int8_to_f16(xq, M, K, ldh, act, amax, stream)))
-      return st;
+size_t h3q_linear_grouped_workspace_bytes(int G, int64_t M, int64_t N, int64_t K) {
+  if (G < 1 || G > h3q::kMaxGroup || M < 1 || N < 1 || K < 1) return 0;
+  return h3q::workspace_layout(M, N, K, G).total;
+}
+
+h3q_status h3q_linear_w8a8_grouped(const uint16_t* x, int8_t* xq, float* xs, int G,
+                                   const int8_t* const* wq, const float* const* ws,
+                                   const uint16_t* const* bias, int64_t M, int64_t N, int64_t K,
+                                   uint16_t* const* y, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream) {
+  if (G < 1 || G > h3q::kMaxGroup) return H3Q_ERR_INVALID_ARG;
+  if (!wq || !ws || !y) return H3Q_ERR_INVALID_ARG;
+  h3q::LinearGroup grp = {};
+  grp.G = G;
+  for (int g = 0; g < G; ++g) {
+    if (!wq[g] || !ws[g] || !y[g]) return H3Q_ERR_INVALID_ARG;
+    const void* ptrs[] = {wq[g], ws[g], bias ? bias[g] : nullptr, y[g]};
+    for (const void* p : ptrs)
+      if (p && !aligned16(p)) return H3Q_ERR_MISALIGNED;
+    grp.wq[g] = wq[g];
+    grp.ws[g] = ws[g];
+    grp.bias[g] = bias ? bias[g] : nullptr;
+    grp.y[g] = y[g];
+    grp.acc[g] = nullptr;
   }
-  // Weight-row norms, where the activations alone do not settle exactness.
-  if (h3q_status st =
-          from_cuda(h3q::launch_weight_norms(wq, N, K, amax, M, nwpart, stream)))
-    return st;
-  // A3 + A4: the tiles that are exact over the whole K, then the rest in K
-  // chunks (an empty launch when there are none).
-  if (h3q_status st = from_cuda(h3q::launch_gemm_wide(act, xs, wq, ws, bias, M, N, K, y,
-                                                      acc_out, amax, nwpart, status, list,
-                                                      stream)))
-    return st;
-  return from_cuda(h3q::launch_gemm_tc(act, xs, wq, ws, bias, M, N, K, y, acc_out, status,
-                                       list, status + 1, stream));
+  return run_linear(x, xq, xs, grp, M, N, K, workspace, workspace_bytes, stream);
 }
 
 h3q_status h3q_workspace_status(const void* workspace, int64_t M, int64_t K,

@@ -438,19 +438,23 @@ void* tensor_map_encoder() {
 
 int64_t gemm_tc_coded_ld(int64_t K) { return (K + BK - 1) / BK * BK; }
 
-WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K) {
-  auto up = [](size_t b) { return (b + 255u) & ~size_t(255); };
-  const size_t mt2 = size_t((M + kNormTokens - 1) / kNormTokens);
+size_t fallback_list_capacity(int64_t M, int64_t N) {
   const size_t mt = size_t((M + BN - 1) / BN);
   const size_t nt = size_t((N + BM - 1) / BM);
-  const size_t ntc = (nt + CLUSTER - 1) / CLUSTER;
+  return mt * ((nt + CLUSTER - 1) / CLUSTER);
+}
+
+WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K, int G) {
+  auto up = [](size_t b) { return (b + 255u) & ~size_t(255); };
+  const size_t mt2 = size_t((M + kNormTokens - 1) / kNormTokens);
+  const size_t nt = size_t((N + BM - 1) / BM);
   WorkspaceLayout l;
   l.act = 0;
   l.amax = up(size_t(M) * size_t(gemm_tc_coded_ld(K)) * 2u);
   l.status = l.amax + up(mt2 * 4u);
   l.nwpart = l.status + 256u;
-  l.list = l.nwpart + up(nt * kNormParts * 4u);
-  l.total = l.list + up(mt * ntc * sizeof(uint2));
+  l.list = l.nwpart + up(size_t(G) * nt * kNormParts * 4u);
+  l.total = l.list + up(size_t(G) * fallback_list_capacity(M, N) * sizeof(uint2));
   return l;
 }
 

@@ -125,24 +125,42 @@ struct __align__(1024) Smem {
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;   // + slack for 1024-byte alignment
 
+// The weight maps and output pointers of the Linears of a call (they share
+// the activations).
+struct WMaps {
+  CUtensorMap m[kMaxGroup];
+};
+struct Outs {
+  const float* sw[kMaxGroup];
+  const uint16_t* bias[kMaxGroup];
+  uint16_t* y[kMaxGroup];
+  int32_t* acc[kMaxGroup];
+};
+
 struct Shape {
+  int G;              // Linears
   int M, N, K;
   int KB;             // k-blocks
   int NSS;            // super-stages per tile
   int mt, nt;         // 256-token blocks, 128-channel blocks
   int mt128;          // 128-token blocks (the chunked kernel's tiles)
   int ntc;            // channel-block pairs
-  int tiles;          // cluster tiles: mt * ntc
+  int tiles;          // cluster tiles: G * mt * ntc
+  int list_cap;       // entries of one Linear's fallback list
   uint64_t wmax2;     // 128^2 K: no weight row's sum of squares exceeds it
 };
 
-// Cluster tile t -> token block mb (256 tokens) and channel-block pair.
-__device__ __forceinline__ void tile_coords(const Shape& s, int t, int& mb, int& pair) {
+// Cluster tile t -> Linear g, token block mb (256 tokens) and channel-block
+// pair.  The Linears alternate fastest, so concurrent tiles of different
+// Linears read the same activation tiles.
+__device__ __forceinline__ void tile_coords(const Shape& s, int t, int& g, int& mb, int& pair) {
+  g = t % s.G;
+  t /= s.G;
   const int per_group = GROUP_M * s.ntc;
-  const int g = t / per_group;
-  const int first_m = g * GROUP_M;
+  const int grp = t / per_group;               // raster group of GROUP_M token blocks
+  const int first_m = grp * GROUP_M;
   const int gm = min(GROUP_M, s.mt - first_m);
-  const int r = t - g * per_group;
+  const int r = t - grp * per_group;
   mb = first_m + r % gm;
   pair = r / gm;
 }
@@ -268,10 +286,8 @@ __device__ __forceinline__ void emit_block(const uint32_t (&d)[32], float sa_l, 
 
 // 23 warps: at most 6 per SM sub-partition, so 80 registers a thread.
 __global__ void __launch_bounds__(THREADS, 1)
-gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
-                 const __grid_constant__ CUtensorMap w_map, const float* __restrict__ sa,
-                 const float* __restrict__ sw, const uint16_t* __restrict__ bias,
-                 const Shape shp, uint16_t* __restrict__ Y, int32_t* __restrict__ ACC,
+gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constant__ WMaps wmaps,
+                 const float* __restrict__ sa, const __grid_constant__ Outs outs, const Shape shp,
                  const uint32_t* __restrict__ amax, const uint32_t* __restrict__ nwpart,
                  uint32_t* __restrict__ status, uint2* __restrict__ list) {
   extern __shared__ uint8_t smem_raw[];
@@ -327,8 +343,8 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
       for (;;) {
         int t;
         if (!pop_tile(sm, nq, abort_flag, err, ERR_PRODUCER, t) || t < 0) break;
-        int mb, pair;
-        tile_coords(shp, t, mb, pair);
+        int g, mb, pair;
+        tile_coords(shp, t, g, mb, pair);
         const int row0 = mb * BN + int(rank) * BNH;
         for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
           const uint32_t slot = gs % B_SLOTS;
@@ -354,20 +370,21 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
     __syncwarp();
   } else if (warp == SCHED_WARP) {
     // ---------------- scheduler + TMA producer: INT8 weight tiles ----------------
-    if (lane == 0) P::tma_prefetch_desc(&w_map);
+    if (lane < shp.G) P::tma_prefetch_desc(&wmaps.m[lane]);
     uint32_t gs = 0, gw = 0, nq = 0;
     bool ok = true;
     for (int t = cid; t < shp.tiles; t += ncl) {
-      int mb, pair;
-      tile_coords(shp, t, mb, pair);
-      if (!tile_exact(shp, amax, nwpart, mb, pair, lane)) {
+      int g, mb, pair;
+      tile_coords(shp, t, g, mb, pair);
+      if (!tile_exact(shp, amax, nwpart + g * shp.nt * kNormParts, mb, pair, lane)) {
         // the chunked kernel takes it, as one or two 128-token tiles (both
         // CTAs reach the same verdict; the even one lists it)
         if (rank == 0 && lane == 0) {
           const int n128 = min(2, shp.mt128 - 2 * mb);
-          const uint32_t i = atomicAdd(status + 1, uint32_t(n128));
+          const uint32_t i = atomicAdd(status + 2 + g, uint32_t(n128));
+          atomicAdd(status + 1, uint32_t(n128));
           for (int h = 0; h < n128; ++h)
-            list[i + h] = make_uint2(uint32_t(2 * mb + h), uint32_t(pair));
+            list[g * shp.list_cap + i + h] = make_uint2(uint32_t(2 * mb + h), uint32_t(pair));
         }
         continue;
       }
@@ -382,7 +399,8 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
             break;
           }
           P::mbar_arrive_expect_tx(&sm.full_w[slot], W_BOX_BYTES);
-          P::tma_load_2d(P::smem_u32(sm.w[slot]), &w_map, &sm.full_w[slot], ss * SS * BK, wrow);
+          P::tma_load_2d(P::smem_u32(sm.w[slot]), &wmaps.m[g], &sm.full_w[slot], ss * SS * BK,
+                         wrow);
           gw = gs + 1;
         }
       }
@@ -520,11 +538,12 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
     for (;;) {
       int t;
       if (!pop_tile_warp(sm, nq, abort_flag, err, ERR_EPILOGUE, t, lane) || t < 0) break;
-      int mb, pair;
-      tile_coords(shp, t, mb, pair);
+      int g, mb, pair;
+      tile_coords(shp, t, g, mb, pair);
       const int n = (2 * pair + int(rank)) * BM + 32 * q + lane;
       const bool n_ok = n < shp.N;
-      const float swn = n_ok ? sw[n] : 0.f;
+      const float swn = n_ok ? outs.sw[g][n] : 0.f;
+      const uint16_t* bias = outs.bias[g];
       const float bn = (n_ok && bias) ? bf16_bits_to_float(bias[n]) : 0.f;
       const int m0 = mb * BN + 64 * cq;
       const float sa0 = (m0 + lane < shp.M) ? sa[m0 + lane] : 0.f;
@@ -538,8 +557,8 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map,
       P::tc_fence_before();
       P::mbar_arrive_cluster(dempty_pair);        // the MMAs of the next tile may start
       ++gt;
-      emit_block(d0, sa0, m0, swn, bn, n, n_ok, shp, Y, ACC, sa);
-      emit_block(d1, sa1, m0 + 32, swn, bn, n, n_ok, shp, Y, ACC, sa);
+      emit_block(d0, sa0, m0, swn, bn, n, n_ok, shp, outs.y[g], outs.acc[g], sa);
+      emit_block(d1, sa1, m0 + 32, swn, bn, n, n_ok, shp, outs.y[g], outs.acc[g], sa);
     }
   }
 
@@ -560,9 +579,8 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 
 }  // namespace
 
-cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const int8_t* qw,
-                             const float* sw, const uint16_t* bias, int64_t M, int64_t N,
-                             int64_t K, uint16_t* y, int32_t* acc, const uint32_t* amax,
+cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const LinearGroup& grp,
+                             int64_t M, int64_t N, int64_t K, const uint32_t* amax,
                              const uint32_t* nwpart, uint32_t* status, uint2* list,
                              cudaStream_t s) {
   EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
@@ -579,17 +597,28 @@ cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const int
           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  // weights: [N, K] INT8, boxes of 128 rows x 128 bytes (two k-blocks)
-  CUtensorMap wmap;
+  // weights: [N, K] INT8 per Linear, boxes of 128 rows x 128 bytes (two k-blocks)
+  WMaps wmaps;
+  Outs outs = {};
   const cuuint64_t wdims[2] = {cuuint64_t(K), cuuint64_t(N)};
   const cuuint64_t wstrides[1] = {cuuint64_t(K)};
   const cuuint32_t wbox[2] = {SS * BK, BM};
-  if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(qw), wdims, wstrides,
-          wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+  for (int g = 0; g < kMaxGroup; ++g) {
+    // unused entries repeat the first Linear's map (never read)
+    const int src = g < grp.G ? g : 0;
+    if (enc(&wmaps.m[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(grp.wq[src]),
+            wdims, wstrides, wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    outs.sw[g] = grp.ws[src];
+    outs.bias[g] = grp.bias[src];
+    outs.y[g] = grp.y[src];
+    outs.acc[g] = grp.acc[src];
+  }
 
   Shape shp;
+  shp.G = grp.G;
   shp.M = int(M);
   shp.N = int(N);
   shp.K = int(K);
@@ -599,7 +628,8 @@ cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const int
   shp.mt128 = int((M + 127) / 128);
   shp.nt = int((N + BM - 1) / BM);
   shp.ntc = (shp.nt + CLUSTER - 1) / CLUSTER;
-  shp.tiles = shp.mt * shp.ntc;
+  shp.tiles = shp.G * shp.mt * shp.ntc;
+  shp.list_cap = int(fallback_list_capacity(M, N));
   shp.wmax2 = uint64_t(128 * 128) * uint64_t(K);
 
   int dev = 0, sms = 0;
@@ -626,8 +656,8 @@ cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const int
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemm_wide_kernel, map, wmap, sa, sw, bias, shp, y, acc, amax,
-                            nwpart, status, list);
+  return cudaLaunchKernelEx(&cfg, gemm_wide_kernel, map, wmaps, sa, outs, shp, amax, nwpart,
+                            status, list);
 }
 
 }  // namespace h3q

@@ -39,13 +39,27 @@ int64_t gemm_tc_coded_ld(int64_t K);
 constexpr int kNormTokens = 256;
 // Weight-norm partial maxima per 128-channel block (16 channels each).
 constexpr int kNormParts = 8;
+// Linears of one grouped call (they share the input).
+constexpr int kMaxGroup = 4;
+
+// The per-Linear operands of a call: G Linears with the same N and K that read
+// the same activations (G = 1 for a single Linear).
+struct LinearGroup {
+  int G;
+  const int8_t* wq[kMaxGroup];
+  const float* ws[kMaxGroup];
+  const uint16_t* bias[kMaxGroup];
+  uint16_t* y[kMaxGroup];
+  int32_t* acc[kMaxGroup];
+};
 
 // The linear workspace, in order (each part 256-byte aligned):
 //   act     [M, gemm_tc_coded_ld(K)] FP16-coded activations
 //   amax    [ceil(M/256)] u32: per 256 tokens, max over rows of sum(qa^2)
-//   status  256 bytes: word 0 error bits, word 1 fallback-list length
-//   nwpart  [ceil(N/128) * 8] u32: per 16 channels, max over rows of sum(qw^2)
-//   list    [ceil(M/128) * ceil(N/256)] uint2 {token block, channel pair}:
+//   status  256 bytes: word 0 error bits, word 1 fallback-list length over
+//           all Linears, word 2 + g the length of Linear g's list
+//   nwpart  G x [ceil(N/128) * 8] u32: per 16 channels, max over rows of sum(qw^2)
+//   list    G x [ceil(M/128) * ceil(N/256)] uint2 {token block, channel pair}:
 //           the 128 x 256 tiles the chunked kernel must finish
 // act, amax and status depend on M and K only, so a call with another N
 // still finds the coded activations (reuse) and the status word there.
@@ -54,20 +68,22 @@ constexpr int kNormParts = 8;
 struct WorkspaceLayout {
   size_t act, amax, status, nwpart, list, total;
 };
-WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K);
+WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K, int G = 1);
+// Entries of one Linear's fallback list.
+size_t fallback_list_capacity(int64_t M, int64_t N);
 
 // Weight pre-pass: nwpart as above, left unwritten when amax shows that no
 // tile can need it (programmatic dependent launch after the quantiser).
-cudaError_t launch_weight_norms(const int8_t* qw, int64_t N, int64_t K, const uint32_t* amax,
-                                int64_t M, uint32_t* nwpart, cudaStream_t s);
+cudaError_t launch_weight_norms(const LinearGroup& grp, int64_t N, int64_t K,
+                                const uint32_t* amax, int64_t M, uint32_t* nwpart,
+                                cudaStream_t s);
 
 // A3 + A4 for the tiles whose FP32 sums are exact over the whole K (checked
 // per tile from amax and, where that is not enough, nwpart); the others are
 // appended to `list`, status[1] counting the entries.  status[0]: error bits
 // (bounded waits).
-cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const int8_t* qw,
-                             const float* sw, const uint16_t* bias, int64_t M, int64_t N,
-                             int64_t K, uint16_t* y, int32_t* acc, const uint32_t* amax,
+cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const LinearGroup& grp,
+                             int64_t M, int64_t N, int64_t K, const uint32_t* amax,
                              const uint32_t* nwpart, uint32_t* status, uint2* list,
                              cudaStream_t s);
 

@@ -346,8 +346,12 @@ int8_to_f16_kernel(const int8_t* __restrict__ q, int K, int ldh, uint16_t* __res
 // K * 128^2 < 2^32 for every supported K.
 constexpr int kNormRows = 16;
 
+struct WeightPtrs {
+  const int8_t* w[kMaxGroup];
+};
+
 __global__ void __launch_bounds__(32 * kNormRows)
-weight_norm_kernel(const int8_t* __restrict__ wq, int64_t N, int K,
+weight_norm_kernel(const WeightPtrs wqs, int64_t N, int K, int blocks_per_linear,
                    const uint32_t* __restrict__ amax, int mt2, uint32_t* __restrict__ part) {
   // the quantiser that wrote amax may still be finishing (programmatic
   // dependent launch): wait for it, then let the GEMM be scheduled
@@ -363,7 +367,10 @@ weight_norm_kernel(const int8_t* __restrict__ wq, int64_t N, int K,
   __syncthreads();
   if (!needed) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t n = int64_t(blockIdx.x) * kNormRows + warp;
+  // block b covers rows 16 (b mod blocks_per_linear) .. + 15 of Linear b / blocks_per_linear
+  const int g = int(blockIdx.x) / blocks_per_linear;
+  const int8_t* __restrict__ wq = wqs.w[g];
+  const int64_t n = int64_t(int(blockIdx.x) - g * blocks_per_linear) * kNormRows + warp;
   uint32_t sq = 0;
   if (n < N) {
     const uint4* row = reinterpret_cast<const uint4*>(wq + n * K);
@@ -452,11 +459,15 @@ cudaError_t launch_quantize_weights(const void* w, int w_dtype, int64_t N, int64
   return cudaGetLastError();
 }
 
-cudaError_t launch_weight_norms(const int8_t* qw, int64_t N, int64_t K, const uint32_t* amax,
-                                int64_t M, uint32_t* nwpart, cudaStream_t s) {
+cudaError_t launch_weight_norms(const LinearGroup& grp, int64_t N, int64_t K,
+                                const uint32_t* amax, int64_t M, uint32_t* nwpart,
+                                cudaStream_t s) {
   static_assert(128 / kNormRows == kNormParts, "partial maxima per 128-channel block");
+  WeightPtrs wqs = {};
+  for (int g = 0; g < grp.G; ++g) wqs.w[g] = grp.wq[g];
+  const int per = static_cast<int>((N + 127) / 128 * kNormParts);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((N + 127) / 128 * kNormParts));
+  cfg.gridDim = dim3(static_cast<unsigned>(per) * static_cast<unsigned>(grp.G));
   cfg.blockDim = dim3(32 * kNormRows);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -465,8 +476,8 @@ cudaError_t launch_weight_norms(const int8_t* qw, int64_t N, int64_t K, const ui
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const int mt2 = static_cast<int>((M + kNormTokens - 1) / kNormTokens);
-  return cudaLaunchKernelEx(&cfg, weight_norm_kernel, qw, N, static_cast<int>(K), amax, mt2,
-                            nwpart);
+  return cudaLaunchKernelEx(&cfg, weight_norm_kernel, wqs, N, static_cast<int>(K), per, amax,
+                            mt2, nwpart);
 }
 
 cudaError_t launch_int8_to_f16(const int8_t* q, int64_t M, int64_t K, int64_t ldh,
