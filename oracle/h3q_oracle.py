@@ -182,6 +182,32 @@ def linear(x_bits, qw, sw, bias_bits=None) -> dict:
     return {"qa": qa, "sa": sa, "acc": acc, "v": v, "y": round_to_bf16(v)}
 
 
+# --- accuracy of the quantised Linear against the unquantised one --------------------
+# [P4] review notes, test coverage: an INT8 SNR check.  The pages give no
+# formula; the plain reading: the unquantised Linear y_ref = X W^T + bias
+# (BF16 X and bias widened exactly, FP32 W) evaluated in float64, and
+#   SNR = 10 log10( sum y_ref^2 / sum (y - y_ref)^2 )  dB
+# for the quantised outputs y over the same elements.
+
+def reference_linear(x_bits, w, bias_bits=None) -> np.ndarray:
+    """The unquantised Linear in float64: widen(X) @ W^T + widen(bias)."""
+    y = widen_bf16(x_bits).astype(np.float64) @ np.asarray(w, dtype=np.float64).T
+    if bias_bits is not None:
+        y = y + widen_bf16(bias_bits).astype(np.float64)
+    return y
+
+
+def snr_db(y, y_ref) -> float:
+    """Signal-to-noise ratio of y against y_ref, in dB (inf when equal)."""
+    y = np.asarray(y, dtype=np.float64)
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    noise = float(np.sum((y - y_ref) ** 2))
+    signal = float(np.sum(y_ref ** 2))
+    if noise == 0.0:
+        return float("inf")
+    return 10.0 * np.log10(signal / noise)
+
+
 # --- the converter's scope rule (passthrough) -------------------------------------
 
 # Per-block projection names of the dit_proj profile: Q, K, V, attention output,

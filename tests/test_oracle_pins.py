@@ -324,3 +324,37 @@ def test_converter_passthrough_is_byte_identical(oracle):
                 assert hashlib.sha256(out[k].tobytes()).hexdigest() == h[k]
                 assert out[k].dtype == v.dtype and out[k].shape == v.shape
         assert len(out) == len(tensors) + n_quant
+
+
+# --- accuracy report: the unquantised reference Linear and the SNR ----------------
+
+def test_reference_linear_brute_force(oracle):
+    rng = np.random.default_rng(90)
+    M, N, K = 3, 4, 5
+    xb = oracle.round_to_bf16(rng.standard_normal((M, K)))
+    w = rng.standard_normal((N, K)).astype(np.float32)
+    bb = oracle.round_to_bf16(rng.standard_normal(N))
+    x = oracle.widen_bf16(xb)
+    b = oracle.widen_bf16(bb)
+    ref = oracle.reference_linear(xb, w, bb)
+    for m in range(M):
+        for n in range(N):
+            # exact rational sum of products of the FP32 values, then the bias
+            exact = sum(Fraction(float(x[m, k])) * Fraction(float(w[n, k])) for k in range(K))
+            exact += Fraction(float(b[n]))
+            assert abs(ref[m, n] - float(exact)) <= 1e-12 * max(1.0, abs(float(exact)))
+    assert np.array_equal(oracle.reference_linear(xb, w), ref - b)
+
+
+def test_snr_closed_forms(oracle):
+    rng = np.random.default_rng(91)
+    ref = rng.standard_normal(1000)
+    assert oracle.snr_db(ref, ref) == float("inf")
+    assert abs(oracle.snr_db(np.zeros_like(ref), ref) - 0.0) < 1e-12
+    # a uniform 1 % relative error is 40 dB; a 10 % one is 20 dB
+    assert abs(oracle.snr_db(ref * 1.01, ref) - 40.0) < 1e-9
+    assert abs(oracle.snr_db(ref * 0.9, ref) - 20.0) < 1e-9
+    # halving the noise amplitude gains 20 log10(2) dB
+    noise = rng.standard_normal(1000) * 1e-3
+    d = oracle.snr_db(ref + noise / 2, ref) - oracle.snr_db(ref + noise, ref)
+    assert abs(d - 20 * np.log10(2)) < 1e-9
