@@ -500,6 +500,76 @@ def legacy_tops(h3q, x, wq, wsc, bias, dev, reps=5):
     return 2 * M * N * K * reps / (a.elapsed_time(b) * 1e-3) / 1e12
 
 
+CONFIG_TABLE = ("tiny", "attn", "fc1", "fc2", "image_qkv", "image_gate_up", "image_down")
+
+
+def run_configs(args):
+    """Per-workload table (not the contract line): for each seeded workload,
+    one Linear timed two ways with CUDA events, L2 flushed before each rep:
+    GEMM + epilogue on activations already coded in the workspace (reuse
+    mode), and the whole call from BF16 X (A2 + A3 + A4).  Prints one JSON
+    object per workload."""
+    import numpy as np
+    import torch
+    import w8a8_int8_linear_h3q_gb300 as h3q
+    import synth
+    h3q.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, peak_kind = _peaks()
+    flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+    names = args.configs.split(",") if args.configs != "all" else CONFIG_TABLE
+    for name in names:
+        case = synth.WORKLOADS[name]()
+        x = torch.from_numpy(case.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        wq, wsc = h3q.h3q_quantize_weights(torch.from_numpy(case.w[0]).to(dev))
+        bias = torch.from_numpy(case.bias_bits[0].view(np.int16)).view(torch.bfloat16).to(dev)
+        del case
+        Mc, Kc = x.shape
+        Nc = wq.shape[0]
+        xs = torch.empty((Mc,), dtype=torch.float32, device=dev)
+        y = torch.empty((Mc, Nc), dtype=torch.bfloat16, device=dev)
+        ws_buf = torch.empty((h3q.h3q_linear_workspace_bytes(Mc, Nc, Kc),), dtype=torch.uint8,
+                             device=dev)
+
+        def full():
+            h3q.h3q_linear_w8a8(x, wq, wsc, bias, xs=xs, y=y, workspace=ws_buf)
+
+        def reuse():
+            h3q.h3q_linear_w8a8(None, wq, wsc, bias, xs=xs, y=y, workspace=ws_buf)
+
+        def med_us(fn, reps):
+            ts = []
+            for _ in range(reps):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b) * 1e3)
+            return statistics.median(ts)
+
+        for _ in range(args.warmup):
+            full()
+        torch.cuda.synchronize()
+        t_full = med_us(full, args.steps)
+        full()
+        t_gemm = med_us(reuse, args.steps)
+        chunked = h3q.h3q_linear_chunked_tiles(ws_buf, Mc, Kc)
+        ops = 2 * Mc * Nc * Kc
+        print(json.dumps({
+            "workload": name, "M": Mc, "N": Nc, "K": Kc, "reps": args.steps,
+            "gemm_us": t_gemm, "gemm_tops": ops / t_gemm / 1e6,
+            "gemm_frac_of_bf16_peak": ops / t_gemm / 1e6 / peaks["bf16_tflops"],
+            "call_us": t_full, "call_tops": ops / t_full / 1e6,
+            "chunked_tiles": chunked, "tiles": -(-Mc // 128) * -(-Nc // 256),
+            "peak": f"{peaks['bf16_tflops']} TFLOP/s bf16 burst ({peak_kind})"}), flush=True)
+        del x, wq, wsc, bias, xs, y, ws_buf
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -508,11 +578,16 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--configs", default=None,
+                    help="instead of the contract line, print a per-workload table: 'all' or "
+                         "a comma list of " + ",".join(CONFIG_TABLE))
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.configs:
+        return run_configs(args)
     return run_gpu(args)
 
 

@@ -106,10 +106,11 @@ h3q_status h3q_quantize_act(const uint16_t* x, int64_t M, int64_t K,
  * Bytes of device workspace that h3q_linear_w8a8 needs for this shape: the
  * quantised activations re-coded as FP16 (exact: every INT8 value is an FP16
  * value), read by the tensor cores; per 256 tokens the largest sum of squares
- * of a coded row; a 256-byte status block; per 16 weight rows the largest sum
- * of squares; and a list of the tiles computed in K chunks (about
- * M * 2 * K + 8 * M * N / 32768 + N / 4 bytes in all).  The caller allocates
- * it; calls that share a workspace must not overlap on the GPU.
+ * of a coded row, whole and per quarter of K; a 256-byte status block; per 16
+ * weight rows the largest sum of squares, whole and per quarter of K; and a
+ * list of the tiles computed in K chunks (about
+ * M * 2 * K + 8 * M * N / 32768 + 5 * N / 4 bytes in all).  The caller
+ * allocates it; calls that share a workspace must not overlap on the GPU.
  */
 size_t h3q_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
@@ -202,13 +203,26 @@ h3q_status h3q_workspace_status(const void* workspace, int64_t M, int64_t K,
  * Diagnostic: how many tiles of 128 tokens x 256 channels the last
  * h3q_linear_w8a8 (or, summed over its Linears, h3q_linear_w8a8_grouped)
  * that used `workspace` (same M, K) computed with K cut into
- * chunks, because the squared-norm bound did not let one FP32 accumulator
+ * chunks, because the squared-norm bounds did not let one FP32 accumulator
  * hold all of K; the other tiles took the single-accumulator path.  Both
  * paths give the same exact result; the chunked one is slower.  Written to
  * *tiles.  SYNCHRONISES `stream`.
  */
 h3q_status h3q_linear_chunked_tiles(const void* workspace, int64_t M, int64_t K,
                                     int64_t* tiles, cudaStream_t stream);
+
+/*
+ * Diagnostic: how many tiles of 256 tokens x 256 channels the same call
+ * computed with one FP32 accumulator over all of K by way of checkpoints:
+ * the whole-K norm bound failed, but the bounds of the four quarters of K
+ * ("norm segments") held, and between runs of segments the kernel read the
+ * accumulator's largest magnitude and proved that the next run could not
+ * carry a partial sum past 2^24.  A tile whose proof fails is also counted
+ * by h3q_linear_chunked_tiles (as one or two 128-token tiles): the chunked
+ * kernel recomputes it.  Written to *tiles.  SYNCHRONISES `stream`.
+ */
+h3q_status h3q_linear_checkpointed_tiles(const void* workspace, int64_t M, int64_t K,
+                                         int64_t* tiles, cudaStream_t stream);
 
 /*
  * A3 + A4 on the legacy warp-level INT8 tensor instruction (mma.sync

@@ -1,11 +1,16 @@
-"""GPU parity of the two ways h3q_linear_w8a8 accumulates a tile.
+"""GPU parity of the ways h3q_linear_w8a8 accumulates a tile.
 
 A tile whose INT8 rows satisfy |a|^2 |w|^2 <= 2^48 (largest squared row norms
-of its 256 tokens and 256 channels) keeps all of K in one FP32 accumulator;
-any other tile cuts K into chunks of at most 1024.  Both must give the exact
-INT32 sum.  These tests drive each path on its own, the boundary case, and a
-mix, and check that the split is the one the norms dictate (the expected
-split is computed here from the INT8 codes, independently of the library).
+of its 256 tokens and 256 channels) keeps all of K in one FP32 accumulator.
+A tile that fails that test can still keep one accumulator by checkpoints:
+K is cut into four norm segments, runs of segments are bounded by
+Cauchy-Schwarz on the per-segment norms, and between runs the kernel reads
+the accumulator's largest magnitude and proves that the next run stays
+within 2^24.  Any other tile, or a checkpointed one whose proof fails, is
+recomputed with K cut into chunks of at most 1024.  All must give the exact
+INT32 sum.  These tests drive each path, the boundary case, and mixes, and
+check that the split is the one the rules dictate: `tile_paths` below
+computes it from the INT8 codes with numpy, independently of the library.
 """
 import math
 
@@ -18,6 +23,9 @@ from _parity import check_exact, check_y
 pytestmark = pytest.mark.gpu
 
 BOUND = 1 << 48
+EXACT = 1 << 24                  # FP32 holds every integer up to this
+RUN_LIMIT = EXACT - (1 << 21)    # a planned run's bound leaves room for the start value
+SEGS = 4
 
 
 @pytest.fixture(scope="module")
@@ -34,21 +42,72 @@ def _bits(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def expected_chunked_tiles(qa, qw):
-    """128-token x 256-channel tiles that fail the squared-norm bound: per
-    256-token block and 256-channel block, max |a|^2 * max |w|^2 > 2^48."""
-    M, N = qa.shape[0], qw.shape[0]
-    a2 = (qa.astype(np.int64) ** 2).sum(1)
-    w2 = (qw.astype(np.int64) ** 2).sum(1)
+def segment_len(K):
+    """Norm segment length: a quarter of the 128-element super-stages, rounded up."""
+    return math.ceil(math.ceil(K / 128) / SEGS) * 128
+
+
+def tile_paths(qa, qw):
+    """(chunked 128 x 256 tiles, checkpointed 256 x 256 tiles) under the rules:
+    a 256-token x 256-channel tile is exact on one accumulator if
+    max|a|^2 * 128^2 K or max|a|^2 * max|w|^2 is <= 2^48; otherwise runs of
+    norm segments grow while (sum of the tile's per-segment token maxima) x
+    (sum of its channel maxima) <= RUN_LIMIT^2, a checkpoint starting each new
+    run, and a segment that alone exceeds it (or the first) sends the tile to
+    the chunked path; at each checkpoint the exact partial sums so far give
+    obs = max |S| over the tile, and the tile falls back to the chunked path
+    unless (2^24 - obs)^2 >= (the next run's norm sums product)."""
+    M, K = qa.shape
+    N = qw.shape[0]
+    sl, nss = segment_len(K), math.ceil(K / 128)
+    a2 = qa.astype(np.int64) ** 2
+    w2 = qw.astype(np.int64) ** 2
+    a_full, w_full = a2.sum(1), w2.sum(1)
+    a_seg = np.stack([a2[:, s * sl:(s + 1) * sl].sum(1) for s in range(SEGS)], 1)
+    w_seg = np.stack([w2[:, s * sl:(s + 1) * sl].sum(1) for s in range(SEGS)], 1)
+    qa64, qw64 = qa.astype(np.float64), qw.astype(np.float64)
     mt128 = math.ceil(M / 128)
-    count = 0
+    chunked = ckpt = 0
     for b in range(math.ceil(M / 256)):
-        amax = int(a2[256 * b: 256 * b + 256].max())
+        rows = slice(256 * b, 256 * b + 256)
+        A = int(a_full[rows].max())
+        As = [int(v) for v in a_seg[rows].max(0)]
         for p in range(math.ceil(N / 256)):
-            wmax = int(w2[256 * p: 256 * p + 256].max())
-            if amax * wmax > BOUND:
-                count += min(2, mt128 - 2 * b)
-    return count
+            cols = slice(256 * p, 256 * p + 256)
+            if A * 128 * 128 * K <= BOUND or A * int(w_full[cols].max()) <= BOUND:
+                continue
+            Ws = [int(v) for v in w_seg[cols].max(0)]
+            ra = rw = 0
+            plan, to_chunked = [], False
+            for i in range(SEGS):
+                if i * (sl // 128) >= nss:
+                    break
+                na, nw = ra + As[i], rw + Ws[i]
+                if na * nw <= RUN_LIMIT ** 2:
+                    ra, rw = na, nw
+                    continue
+                if i == 0 or As[i] * Ws[i] > RUN_LIMIT ** 2:
+                    to_chunked = True
+                    break
+                plan.append(i)
+                ra, rw = As[i], Ws[i]
+            if to_chunked:
+                chunked += min(2, mt128 - 2 * b)
+                continue
+            if not plan:
+                continue
+            ckpt += 1
+            failed = False
+            for j, s in enumerate(plan):
+                S = qa64[rows, :s * sl] @ qw64[cols, :s * sl].T     # exact: < 2^53
+                obs = int(np.abs(S).max())
+                end = plan[j + 1] if j + 1 < len(plan) else SEGS
+                ar, wr = sum(As[s:end]), sum(Ws[s:end])
+                if obs > EXACT or (EXACT - obs) ** 2 < ar * wr:
+                    failed = True
+            if failed:
+                chunked += min(2, mt128 - 2 * b)
+    return chunked, ckpt
 
 
 def _run(lib, oracle, dev, xq, wq, xs, ws, bias):
@@ -61,7 +120,10 @@ def _run(lib, oracle, dev, xq, wq, xs, ws, bias):
     check_y(_bits(out["y"]), ref)
     M, K = xq.shape
     assert lib.h3q_workspace_status(out["workspace"], M, K) == lib.H3Q_OK
-    return acc, lib.h3q_linear_chunked_tiles(out["workspace"], M, K)
+    got = (lib.h3q_linear_chunked_tiles(out["workspace"], M, K),
+           lib.h3q_linear_checkpointed_tiles(out["workspace"], M, K))
+    assert got == tile_paths(xq, wq)
+    return acc, got
 
 
 def _odd_vector_with_square_norm(K, target, seed):
@@ -107,16 +169,17 @@ def test_bound_reached_exactly_takes_the_single_accumulator(lib, oracle, dev):
     wq = (sw * v).astype(np.int8)
     xs = rng.uniform(2.0 ** -9, 2.0 ** -8, M).astype(np.float32)
     ws = rng.uniform(2.0 ** -9, 2.0 ** -8, N).astype(np.float32)
-    acc, chunked = _run(lib, oracle, dev, xq, wq, xs, ws, None)
+    acc, paths = _run(lib, oracle, dev, xq, wq, xs, ws, None)
     assert acc[0, 0] == 1 << 24 and acc[7, 3] == 1 << 24
-    assert expected_chunked_tiles(xq, wq) == 0
-    assert chunked == 0
+    assert paths == (0, 0)
 
 
 def test_bound_exceeded_by_one_row_takes_the_chunked_path(lib, oracle, dev):
     # the same rows, with one token row of the first 256-token block raised
-    # above the bound: that block (two 128-token tiles) goes to the chunked
-    # path, the ragged second block stays on the single accumulator
+    # above the bound: that block's tile takes checkpoints, but its partial
+    # sums (all of one sign) do reach past 2^24, so the proof fails and the
+    # chunked path recomputes it (two 128-token tiles); the ragged second
+    # block stays on the single accumulator
     K, M, N = 4096, 293, 200
     v = _odd_vector_with_square_norm(K, 1 << 24, seed=5)
     xq = np.tile(v, (M, 1)).astype(np.int8)
@@ -127,39 +190,77 @@ def test_bound_exceeded_by_one_row_takes_the_chunked_path(lib, oracle, dev):
     xs = rng.uniform(0.5, 1.0, M).astype(np.float32) * 2.0 ** -10
     ws = rng.uniform(0.5, 1.0, N).astype(np.float32) * 2.0 ** -10
     bias = (rng.integers(0, 2 ** 15, N) & 0x7F7F).astype(np.uint16)
-    acc, chunked = _run(lib, oracle, dev, xq, wq, xs, ws, bias)
-    assert expected_chunked_tiles(xq, wq) == 2
-    assert chunked == 2
+    acc, paths = _run(lib, oracle, dev, xq, wq, xs, ws, bias)
+    assert paths == (2, 1)
     assert acc[0, 0] == 1 << 24 and acc[100, 0] > 1 << 24
 
 
 def test_mixed_tiles(lib, oracle, dev):
-    # per-block amplitudes put some tiles above the bound and some below:
-    # token blocks of 256 with |q| up to {20, 127, 40, 127, 90}, channel
-    # blocks of 256 with |q| up to {30, 127, 60}; the last of each is ragged
+    # per-block amplitudes put some tiles within the whole-K bound, some
+    # within reach of checkpoints and some beyond: token blocks of 256 with
+    # |q| up to {20, 127, 40, 127, 90}, the second of them made of rows of
+    # one sign and full magnitude; channel blocks of 256 with |q| up to
+    # {30, 127, 60}; the last of each is ragged
     K, M, N = 8192, 1100, 700
     rng = np.random.default_rng(9)
     amp_m = np.repeat([20, 127, 40, 127, 90], 256)[:M]
     amp_n = np.repeat([30, 127, 60], 256)[:N]
     xq = np.round(rng.uniform(-1, 1, (M, K)) * amp_m[:, None]).astype(np.int8)
     wq = np.round(rng.uniform(-1, 1, (N, K)) * amp_n[:, None]).astype(np.int8)
+    xq[256:512] = (np.where(rng.random(256) < 0.5, -127, 127)[:, None] *
+                   np.ones(K, np.int64)).astype(np.int8)
     xs = rng.uniform(2.0 ** -12, 2.0 ** -11, M).astype(np.float32)
     ws = rng.uniform(2.0 ** -12, 2.0 ** -11, N).astype(np.float32)
     bias = (rng.integers(0, 2 ** 15, N) & 0xBF7F).astype(np.uint16)
-    exp = expected_chunked_tiles(xq, wq)
+    chunked, ckpt = tile_paths(xq, wq)
     total = math.ceil(M / 128) * math.ceil(N / 256)
-    assert 0 < exp < total
-    _, chunked = _run(lib, oracle, dev, xq, wq, xs, ws, bias)
-    assert chunked == exp
+    assert 0 < chunked < total and ckpt > 0
+    _run(lib, oracle, dev, xq, wq, xs, ws, bias)
 
 
 def test_every_tile_chunked(lib, oracle, dev):
-    # constant +-127 rows: |a|^2 |w|^2 = (127^2 K)^2 > 2^48 everywhere
-    K, M, N = 2048, 300, 520
+    # constant +-127 rows with K = 8192: each quarter of K alone has
+    # |a|^2 |w|^2 = (127^2 2048)^2 above the run limit, so no tile can take
+    # checkpoints and every tile goes straight to the chunked path
+    K, M, N = 8192, 300, 520
     rng = np.random.default_rng(10)
     xq = np.where(rng.random((M, K)) < 0.5, -127, 127).astype(np.int8)
     wq = np.where(rng.random((N, K)) < 0.5, -127, 127).astype(np.int8)
     xs = np.full(M, 2.0 ** -7, np.float32)
     ws = np.full(N, 2.0 ** -7, np.float32)
-    _, chunked = _run(lib, oracle, dev, xq, wq, xs, ws, None)
-    assert chunked == math.ceil(M / 128) * math.ceil(N / 256)
+    _, paths = _run(lib, oracle, dev, xq, wq, xs, ws, None)
+    assert paths == (math.ceil(M / 128) * math.ceil(N / 256), 0)
+
+
+def test_uniform_codes_take_checkpoints(lib, oracle, dev):
+    # codes uniform in [-127, 127] with K = 4096: |a|^2 |w|^2 is about 1.7 x
+    # 2^48, so no tile passes the whole-K test, but half of K stays within
+    # the run limit and the random-walk partial sums stay far below 2^24:
+    # every tile keeps one accumulator with one checkpoint
+    K, M, N = 4096, 600, 520
+    rng = np.random.default_rng(11)
+    xq = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    wq = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    xs = rng.uniform(2.0 ** -12, 2.0 ** -11, M).astype(np.float32)
+    ws = rng.uniform(2.0 ** -12, 2.0 ** -11, N).astype(np.float32)
+    bias = (rng.integers(0, 2 ** 15, N) & 0xBF7F).astype(np.uint16)
+    _, paths = _run(lib, oracle, dev, xq, wq, xs, ws, bias)
+    assert paths == (0, math.ceil(M / 256) * math.ceil(N / 256))
+
+
+def test_failed_checkpoints_fall_back(lib, oracle, dev):
+    # rows of one sign and magnitude (+-127 times a per-row sign) with
+    # K = 2048: every quarter of K passes the run limit, so every tile takes
+    # checkpoints, but the partial sums grow linearly to 127^2 K > 2^24, the
+    # second checkpoint's proof fails, and the chunked path recomputes every
+    # tile
+    K, M, N = 2048, 300, 520
+    rng = np.random.default_rng(12)
+    xq = (np.where(rng.random(M) < 0.5, -127, 127)[:, None] * np.ones(K, np.int64)).astype(np.int8)
+    wq = (np.where(rng.random(N) < 0.5, -127, 127)[:, None] * np.ones(K, np.int64)).astype(np.int8)
+    xs = np.full(M, 2.0 ** -9, np.float32)
+    ws = np.full(N, 2.0 ** -9, np.float32)
+    acc, paths = _run(lib, oracle, dev, xq, wq, xs, ws, None)
+    assert paths == (math.ceil(M / 128) * math.ceil(N / 256),
+                     math.ceil(M / 256) * math.ceil(N / 256))
+    assert abs(int(acc[0, 0])) == 127 * 127 * K

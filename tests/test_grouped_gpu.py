@@ -69,12 +69,15 @@ def test_grouped_prequantised_and_reuse_modes(lib, dev):
 
 
 def test_grouped_with_chunked_tiles(lib, oracle, dev):
-    # Linear 0's weights keep every tile on the single accumulator, Linear 1's
-    # send the large-activation token block to the chunked path
+    # Linear 0's weights keep every tile on the single accumulator; Linear 1's
+    # send the token block of full-magnitude one-sign rows to the chunked
+    # path and keep the uniform-code block on one accumulator by checkpoints
     K, M, N = 8192, 600, 300
     rng = np.random.default_rng(62)
     amp_m = np.repeat([20, 127, 40], 256)[:M]
     xq = np.round(rng.uniform(-1, 1, (M, K)) * amp_m[:, None]).astype(np.int8)
+    xq[:128] = (np.where(rng.random(128) < 0.5, -127, 127)[:, None] *
+                np.ones(K, np.int64)).astype(np.int8)
     wq0 = np.round(rng.uniform(-1, 1, (N, K)) * 10).astype(np.int8)
     wq1 = np.round(rng.uniform(-1, 1, (N, K)) * 127).astype(np.int8)
     xs = rng.uniform(2.0 ** -12, 2.0 ** -11, M).astype(np.float32)
@@ -86,11 +89,13 @@ def test_grouped_with_chunked_tiles(lib, oracle, dev):
     for g, wq in enumerate((wq0, wq1)):
         one = lib.h3q_linear_w8a8(None, t(wq), t(ws[g]), None, xq=t(xq), xs=t(xs))
         assert _same(grp["ys"][g], one["y"])
-        counts.append(lib.h3q_linear_chunked_tiles(one["workspace"], M, K))
+        counts.append((lib.h3q_linear_chunked_tiles(one["workspace"], M, K),
+                       lib.h3q_linear_checkpointed_tiles(one["workspace"], M, K)))
         ref = oracle.epilogue_value(oracle.gemm_int32(xq, wq), xs, ws[g], None)
         check_y(_bits(grp["ys"][g]), ref)
-    assert counts[0] == 0 and counts[1] > 0
-    assert lib.h3q_linear_chunked_tiles(grp["workspace"], M, K) == sum(counts)
+    assert counts[0] == (0, 0) and counts[1][0] > 0 and counts[1][1] > 0
+    assert lib.h3q_linear_chunked_tiles(grp["workspace"], M, K) == sum(c[0] for c in counts)
+    assert lib.h3q_linear_checkpointed_tiles(grp["workspace"], M, K) == sum(c[1] for c in counts)
 
 
 @pytest.mark.slow

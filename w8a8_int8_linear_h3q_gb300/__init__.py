@@ -57,6 +57,8 @@ def _declare(lib):
     lib.h3q_linear_w8a8_grouped.restype = i32
     lib.h3q_linear_chunked_tiles.argtypes = [vp, i64, i64, ctypes.POINTER(i64), vp]
     lib.h3q_linear_chunked_tiles.restype = i32
+    lib.h3q_linear_checkpointed_tiles.argtypes = [vp, i64, i64, ctypes.POINTER(i64), vp]
+    lib.h3q_linear_checkpointed_tiles.restype = i32
     lib.h3q_linear_w8a8_mma_sync.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
     lib.h3q_linear_w8a8_mma_sync.restype = i32
     lib.h3q_linear_w8a8_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
@@ -287,6 +289,15 @@ def h3q_linear_chunked_tiles(workspace, M: int, K: int, stream=None) -> int:
     n = ctypes.c_int64(-1)
     _check(load().h3q_linear_chunked_tiles(_ptr(workspace), M, K, ctypes.byref(n),
                                            _stream(stream)), "h3q_linear_chunked_tiles")
+    return int(n.value)
+
+
+def h3q_linear_checkpointed_tiles(workspace, M: int, K: int, stream=None) -> int:
+    """Tiles (256 tokens x 256 channels) that the last linear call on
+    ``workspace`` kept on one accumulator by way of checkpoints.  Synchronises."""
+    n = ctypes.c_int64(-1)
+    _check(load().h3q_linear_checkpointed_tiles(_ptr(workspace), M, K, ctypes.byref(n),
+                                                _stream(stream)), "h3q_linear_checkpointed_tiles")
     return int(n.value)
 
 

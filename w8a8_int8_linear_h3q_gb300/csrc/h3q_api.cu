@@ -46,6 +46,23 @@ h3q_status from_cuda(cudaError_t e) {
 
 // The launch sequence of a (grouped) Linear call; the per-Linear pointers are
 // already checked.
+// Word `index` of the status block of a workspace last used with (M, K).
+h3q_status read_status_word(const void* workspace, int64_t M, int64_t K, int index,
+                            int64_t* value, cudaStream_t stream) {
+  if (!workspace || !value) return H3Q_ERR_INVALID_ARG;
+  if (M < 1 || K < 1) return H3Q_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(workspace)) return H3Q_ERR_MISALIGNED;
+  if (h3q_status st = check_device()) return st;
+  const uint8_t* wsp = static_cast<const uint8_t*>(workspace);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, wsp + h3q::workspace_layout(M, 1, K).status + 4 * index,
+                      sizeof(word), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return H3Q_ERR_CUDA;
+  *value = int64_t(word);
+  return H3Q_OK;
+}
+
 h3q_status run_linear(const uint16_t* x, int8_t* xq, float* xs, const h3q::LinearGroup& grp,
                       int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream) {
@@ -220,18 +237,12 @@ h3q_status h3q_workspace_status(const void* workspace, int64_t M, int64_t K,
 
 h3q_status h3q_linear_chunked_tiles(const void* workspace, int64_t M, int64_t K,
                                     int64_t* tiles, cudaStream_t stream) {
-  if (!workspace || !tiles) return H3Q_ERR_INVALID_ARG;
-  if (M < 1 || K < 1) return H3Q_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned16(workspace)) return H3Q_ERR_MISALIGNED;
-  if (h3q_status st = check_device()) return st;
-  const uint8_t* wsp = static_cast<const uint8_t*>(workspace);
-  uint32_t word = 0;
-  if (cudaMemcpyAsync(&word, wsp + h3q::workspace_layout(M, 1, K).status + 4, sizeof(word),
-                      cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
-      cudaStreamSynchronize(stream) != cudaSuccess)
-    return H3Q_ERR_CUDA;
-  *tiles = int64_t(word);
-  return H3Q_OK;
+  return read_status_word(workspace, M, K, 1, tiles, stream);
+}
+
+h3q_status h3q_linear_checkpointed_tiles(const void* workspace, int64_t M, int64_t K,
+                                         int64_t* tiles, cudaStream_t stream) {
+  return read_status_word(workspace, M, K, 6, tiles, stream);
 }
 
 h3q_status h3q_linear_w8a8_mma_sync(const int8_t* xq, const float* xs, const int8_t* wq,

@@ -451,9 +451,9 @@ WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K, int G) {
   WorkspaceLayout l;
   l.act = 0;
   l.amax = up(size_t(M) * size_t(gemm_tc_coded_ld(K)) * 2u);
-  l.status = l.amax + up(mt2 * 4u);
+  l.status = l.amax + up(mt2 * (1u + kNormSegs) * 4u);
   l.nwpart = l.status + 256u;
-  l.list = l.nwpart + up(size_t(G) * nt * kNormParts * 4u);
+  l.list = l.nwpart + up(size_t(G) * nt * kNormParts * (1u + kNormSegs) * 4u);
   l.total = l.list + up(size_t(G) * fallback_list_capacity(M, N) * sizeof(uint2));
   return l;
 }

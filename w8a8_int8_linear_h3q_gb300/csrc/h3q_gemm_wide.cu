@@ -24,8 +24,25 @@
 // which holds for activations whose codes are mostly small, as per-row absmax
 // scaling of K = 5376 rows with outliers gives -- or, failing that, when it
 // times the tile's largest weight-row sum of squares (from a pre-pass that
-// runs only when some tile needs it) is.  The other tiles go to a list in the
-// workspace that the chunked kernel finishes afterwards.
+// runs only when some tile needs it) is.
+//
+// A tile that fails this test by a little (long K with Gaussian-like codes,
+// where the tile's largest token and channel norms just cross the bound,
+// although nearly every actual partial sum stays far below 2^24) can still
+// keep one accumulator, with checkpoints.  K is cut into four norm segments;
+// the quantiser and the pre-pass also record the largest sums of squares per
+// segment.  Over a run of segments r the partial sums of the run move the
+// accumulator by at most sqrt(A_r W_r) (Cauchy-Schwarz over the run, A_r and
+// W_r the sums of the tile's per-segment maxima), so an accumulator that
+// holds exactly S at the run's start stays exact through the run when
+// max|S| + sqrt(A_r W_r) <= 2^24.  The scheduler plans the runs (greedily,
+// each with sqrt(A_r W_r) <= 2^24 - 2^21); before each later run the MMA
+// issuer stops, the epilogue warps read the accumulator (exact so far) and
+// report max|S| over the tile, and the issuer checks the inequality with that
+// value.  Should a check fail, the tile still runs to its end, but it is put
+// on the fallback list, and the chunked kernel, which runs afterwards,
+// overwrites its outputs.  The remaining tiles go to that list from the
+// start.
 //
 // Against the chunked kernel this removes the per-chunk accumulator drains
 // (one drain per tile) and lets each converted weight slice feed 256 tokens
@@ -102,6 +119,14 @@ static_assert(TM_A + A_SLOTS * SS * 32 <= TM_COLS, "TMEM columns");
 static_assert(A_SLOTS <= B_SLOTS, "A ring deeper than the activation ring");
 constexpr uint32_t IDESC = P::idesc_f16_f32(2 * BM, BN);
 constexpr uint64_t kExactBound = uint64_t(1) << 48;        // |a|^2 |w|^2 limit
+constexpr int NSEG = kNormSegs;
+static_assert(SS * BK == kSegQuantum, "norm segments are whole super-stages");
+constexpr uint32_t kAccExact = 1u << 24;   // FP32 holds every integer up to this
+// a planned run's bound leaves this much room for the accumulator's value at
+// the run's start
+constexpr uint32_t kRunLimit = kAccExact - (1u << 21);
+// ways through the kernel of a cluster tile
+constexpr int TILE_WIDE = 0, TILE_CKPT = 1, TILE_CHUNKED = 2;
 
 // error bits (the chunked kernel uses the low byte)
 constexpr uint32_t ERR_PRODUCER = 1u << 8, ERR_MMA = 2u << 8, ERR_CONVERT = 4u << 8,
@@ -119,7 +144,11 @@ struct __align__(1024) Smem {
   uint64_t dempty;                       // (even CTA) both epilogues have copied it out
   uint64_t mma_done;
   uint64_t q_full[SQ], q_empty[SQ];      // tile queue
+  uint64_t cp_slot[CLUSTER * NUM_EPI_WARPS];  // (even CTA) per epilogue warp at a checkpoint:
+                                             // event tag << 32 | max |accumulator| of its block
   int q_tile[SQ];                        // cluster tile index, or -1: no more tiles
+  uint32_t q_ckpt[SQ];                   // bit s: the accumulator is checked before segment s
+  uint32_t q_aw[SQ][2 * NSEG];           // the tile's per-segment norm maxima (tokens, channels)
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -147,7 +176,16 @@ struct Shape {
   int ntc;            // channel-block pairs
   int tiles;          // cluster tiles: G * mt * ntc
   int list_cap;       // entries of one Linear's fallback list
+  int seg_ss;         // super-stages per norm segment
   uint64_t wmax2;     // 128^2 K: no weight row's sum of squares exceeds it
+};
+
+// A TILE_CKPT tile's plan: where the accumulator is checked, and the largest
+// per-segment sums of squares of its token rows (aw[0..3]) and channel rows
+// (aw[4..7]).
+struct TilePlan {
+  uint32_t ckpt;
+  uint32_t aw[2 * NSEG];
 };
 
 // Cluster tile t -> Linear g, token block mb (256 tokens) and channel-block
@@ -165,53 +203,129 @@ __device__ __forceinline__ void tile_coords(const Shape& s, int t, int& g, int& 
   pair = r / gm;
 }
 
-// Warp-collective: true when every (token, channel) of the cluster tile has
-// |a|^2 |w|^2 <= 2^48.  The token block's maximum against the largest possible
-// weight row settles most tiles; otherwise lanes 0-15 read the pair's 16
-// weight partial maxima.
-__device__ __forceinline__ bool tile_exact(const Shape& s, const uint32_t* amax,
-                                           const uint32_t* nwpart, int mb, int pair, int lane) {
-  const uint64_t a = amax[mb];
-  if (a * s.wmax2 <= kExactBound) return true;
-  const int idx = pair * CLUSTER * kNormParts + lane;
-  uint32_t w = (lane < CLUSTER * kNormParts && idx < s.nt * kNormParts) ? nwpart[idx] : 0u;
+// Warp-collective: tile_path past its first test.  Lanes 0-15 read the pair's 16
+// weight partial maxima; failing the whole-K test, the per-segment maxima
+// (lanes 0-15 segments 0-1, lanes 16-31 segments 2-3 of the same partial
+// maxima) give the checkpoint plan: runs of segments grow while
+// sqrt(A_r W_r) <= kRunLimit, and a segment that alone exceeds it sends the
+// tile to the chunked kernel.  Every lane returns the same plan.
+__device__ __forceinline__ int tile_path_norms(const Shape& s, uint64_t a, const uint32_t* aseg,
+                                            const uint32_t* nwpart, const uint32_t* nwseg, int mb,
+                                            int pair, int lane, TilePlan& plan) {
+  const int p = pair * CLUSTER * kNormParts + (lane & (CLUSTER * kNormParts - 1));
+  const bool p_ok = p < s.nt * kNormParts;
+  uint32_t w = (lane < CLUSTER * kNormParts && p_ok) ? nwpart[p] : 0u;
 #pragma unroll
   for (int o = 16; o; o >>= 1) w = max(w, __shfl_xor_sync(0xFFFFFFFFu, w, o));
-  return uint64_t(w) * a <= kExactBound;
+  if (uint64_t(w) * a <= kExactBound) return TILE_WIDE;
+  static_assert(CLUSTER * kNormParts == 16 && NSEG == 4, "two segments per half-warp");
+  const int sg = 2 * (lane >> 4);
+  uint32_t w0 = p_ok ? nwseg[p * NSEG + sg] : 0u, w1 = p_ok ? nwseg[p * NSEG + sg + 1] : 0u;
+#pragma unroll
+  for (int o = 8; o; o >>= 1) {
+    w0 = max(w0, __shfl_xor_sync(0xFFFFFFFFu, w0, o));
+    w1 = max(w1, __shfl_xor_sync(0xFFFFFFFFu, w1, o));
+  }
+  plan.aw[NSEG + 0] = __shfl_sync(0xFFFFFFFFu, w0, 0);
+  plan.aw[NSEG + 1] = __shfl_sync(0xFFFFFFFFu, w1, 0);
+  plan.aw[NSEG + 2] = __shfl_sync(0xFFFFFFFFu, w0, 16);
+  plan.aw[NSEG + 3] = __shfl_sync(0xFFFFFFFFu, w1, 16);
+#pragma unroll
+  for (int i = 0; i < NSEG; ++i) plan.aw[i] = aseg[mb * NSEG + i];
+  // every sum below is at most 127^2 K < 2^32 and every product < 2^64
+  const uint64_t lim2 = uint64_t(kRunLimit) * kRunLimit;
+  uint64_t ra = 0, rw = 0;
+  uint32_t ck = 0;
+#pragma unroll
+  for (int i = 0; i < NSEG; ++i) {
+    if (i * s.seg_ss >= s.NSS) break;               // empty trailing segments
+    const uint64_t na = ra + plan.aw[i], nw = rw + plan.aw[NSEG + i];
+    if (na * nw <= lim2) {
+      ra = na;
+      rw = nw;
+      continue;
+    }
+    if (i == 0 || uint64_t(plan.aw[i]) * plan.aw[NSEG + i] > lim2) return TILE_CHUNKED;
+    ck |= 1u << i;
+    ra = plan.aw[i];
+    rw = plan.aw[NSEG + i];
+  }
+  plan.ckpt = ck;
+  // no checkpoint: the segment maxima bound the whole K within 2^24 after all
+  return ck ? TILE_CKPT : TILE_WIDE;
 }
 
-// Single-thread take of the next queue entry.  False on a timeout or abort.
+// Warp-collective: how a cluster tile is computed.  TILE_WIDE when every
+// (token, channel) of the tile has |a|^2 |w|^2 <= 2^48: the token block's
+// maximum against the largest possible weight row settles most tiles;
+// otherwise tile_path_norms decides, from the weight norms.
+__device__ __forceinline__ int tile_path(const Shape& s, const uint32_t* amax,
+                                         const uint32_t* aseg, const uint32_t* nwpart,
+                                         const uint32_t* nwseg, int mb, int pair, int lane,
+                                         TilePlan& plan) {
+  const uint64_t a = amax[mb];
+  if (a * s.wmax2 <= kExactBound) return TILE_WIDE;
+  return tile_path_norms(s, a, aseg, nwpart, nwseg, mb, pair, lane, plan);
+}
+
+// Single-thread take of the next queue entry (and, if `plan` is given, its
+// checkpoint plan).  False on a timeout or abort.
 __device__ __forceinline__ bool pop_tile(Smem& sm, uint32_t& nq, volatile int* abort_flag,
-                                         uint32_t* err, uint32_t code, int& t) {
+                                         uint32_t* err, uint32_t code, int& t,
+                                         TilePlan* plan = nullptr) {
   const uint32_t q = nq % SQ;
   if (!P::mbar_wait(&sm.q_full[q], (nq / SQ) & 1u, abort_flag, err, code)) return false;
   t = sm.q_tile[q];
+  if (plan) {
+    plan->ckpt = sm.q_ckpt[q];
+    if (plan->ckpt)
+      for (int i = 0; i < 2 * NSEG; ++i) plan->aw[i] = sm.q_aw[q][i];
+  }
   P::mbar_arrive(&sm.q_empty[q]);
   ++nq;
   return true;
 }
 
-// Warp-collective take; one arrival for the warp.
+// Warp-collective take (with the entry's checkpoint bits); one arrival for
+// the warp.
 __device__ __forceinline__ bool pop_tile_warp(Smem& sm, uint32_t& nq, volatile int* abort_flag,
-                                              uint32_t* err, uint32_t code, int& t, int lane) {
+                                              uint32_t* err, uint32_t code, int& t, int lane,
+                                              uint32_t* ckpt = nullptr) {
   const uint32_t q = nq % SQ;
   if (!P::mbar_wait_warp(&sm.q_full[q], (nq / SQ) & 1u, abort_flag, err, code)) return false;
   t = sm.q_tile[q];
+  if (ckpt) *ckpt = sm.q_ckpt[q];
   __syncwarp();
   if (lane == 0) P::mbar_arrive(&sm.q_empty[q]);
   ++nq;
   return true;
 }
 
-__device__ __forceinline__ bool push_tile(Smem& sm, uint32_t& nq, int t, volatile int* abort_flag,
-                                          uint32_t* err) {
+__device__ __forceinline__ bool push_tile(Smem& sm, uint32_t& nq, int t, const TilePlan* plan,
+                                          volatile int* abort_flag, uint32_t* err) {
   const uint32_t q = nq % SQ;
   if (!P::mbar_wait(&sm.q_empty[q], ((nq / SQ) & 1u) ^ 1u, abort_flag, err, ERR_SCHED))
     return false;
   sm.q_tile[q] = t;
+  sm.q_ckpt[q] = plan ? plan->ckpt : 0u;
+  if (plan) {
+#pragma unroll
+    for (int i = 0; i < 2 * NSEG; ++i) sm.q_aw[q][i] = plan->aw[i];
+  }
   P::mbar_arrive(&sm.q_full[q]);
   ++nq;
   return true;
+}
+
+// Lists a 256 x 256 cluster tile for the chunked kernel, as one or two
+// 128-token tiles.
+__device__ __forceinline__ void list_for_chunked(const Shape& shp, uint32_t* status, uint2* list,
+                                                 int g, int mb, int pair) {
+  const int n128 = min(2, shp.mt128 - 2 * mb);
+  const uint32_t i = atomicAdd(status + 2 + g, uint32_t(n128));
+  atomicAdd(status + 1, uint32_t(n128));
+  for (int h = 0; h < n128; ++h)
+    list[g * shp.list_cap + i + h] = make_uint2(uint32_t(2 * mb + h), uint32_t(pair));
 }
 
 // A4 for 32 consecutive tokens of this lane's channel row n: lane l holds the
@@ -284,6 +398,80 @@ __device__ __forceinline__ void emit_block(const uint32_t (&d)[32], float sa_l, 
   }
 }
 
+// The MMA issuer's checkpoint before norm segment `seg` (out of line and
+// outside the issue loop, whose speed it would otherwise cost).  The MMAs
+// issued so far complete into the accumulator, the
+// epilogues read it (exact so far) and each reports the largest magnitude of
+// its block, tagged with this event's number (gt + 1); then the run that
+// starts here (segments up to the next checkpoint) is checked against 2^24.
+// Returns 0 if it holds, 1 if not (or a report is missing), -1 if a wait
+// gave up.
+__device__ __noinline__ int mma_checkpoint(Smem& sm, const TilePlan& pl, int seg, uint32_t gt,
+                                           volatile int* abort_flag, uint32_t* err) {
+  P::mma_commit_pair_mc(&sm.dfull, CLUSTER_MASK);
+  if (!P::mbar_wait_cluster(&sm.dempty, ((gt + 1) & 1u) ^ 1u, abort_flag, err, ERR_MMA))
+    return -1;
+  P::tc_fence_after();
+  uint32_t obs = 0;
+  for (int i = 0; i < CLUSTER * NUM_EPI_WARPS; ++i) {
+    const uint64_t word = *reinterpret_cast<volatile uint64_t*>(&sm.cp_slot[i]);
+    if (uint32_t(word >> 32) != gt + 1) return 1;
+    obs = max(obs, uint32_t(word));
+  }
+  uint64_t ra = 0, rw = 0;
+  bool in_run = true;
+#pragma unroll
+  for (int i = 0; i < NSEG; ++i) {
+    if (i > seg && ((pl.ckpt >> i) & 1u)) in_run = false;
+    if (i >= seg && in_run) {
+      ra += pl.aw[i];
+      rw += pl.aw[NSEG + i];
+    }
+  }
+  return (obs > kAccExact || uint64_t(kAccExact - obs) * (kAccExact - obs) < ra * rw) ? 1 : 0;
+}
+
+constexpr uint32_t kNoEvent = 0xFFFFFFFFu;
+
+// An epilogue warp's part of a tile's checkpoints (warp-collective): at each,
+// the largest |accumulator| of the warp's 32 x 64 block (TMEM address d_tmem)
+// goes into the warp's own slot in the even CTA, tagged with the event's
+// number, and lane 0 arrives with a cluster-scope release (the MMA issuer
+// waits with a cluster-scope acquire).  (A single word updated by 64-bit
+// atomic maxima from both CTAs was seen to lose updates, hence one slot per
+// warp.)  Returns the event count after them, or kNoEvent when a wait gave
+// up.
+__device__ __forceinline__ uint32_t epilogue_checkpoints(Smem& sm, uint32_t ckpt, uint32_t gt,
+                                                         volatile int* abort_flag, uint32_t* err,
+                                                         uint32_t d_tmem, uint32_t slot_pair,
+                                                         uint32_t dempty_pair, int lane) {
+  for (; ckpt; ckpt &= ckpt - 1u) {
+    if (!P::mbar_wait_warp(&sm.dfull, gt & 1u, abort_flag, err, ERR_EPILOGUE)) return kNoEvent;
+    P::tc_fence_after();
+    uint32_t d0[32], d1[32];
+    P::tmem_ld32(d_tmem, d0);
+    P::tmem_ld32(d_tmem + 32, d1);
+    P::tmem_wait_ld();
+    P::tc_fence_before();
+    float mx = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(d0[j])), fabsf(__uint_as_float(d1[j]))));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    if (lane == 0) {
+      // float -> unsigned conversion saturates
+      P::st_cluster_u64(slot_pair, (uint64_t(gt + 1) << 32) | __float2uint_ru(mx));
+      P::fence_acq_rel_cluster();
+      P::mbar_arrive_cluster_release(dempty_pair);
+    } else {
+      P::mbar_arrive_cluster(dempty_pair);
+    }
+    ++gt;
+  }
+  return gt;
+}
+
 // 23 warps: at most 6 per SM sub-partition, so 80 registers a thread.
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constant__ WMaps wmaps,
@@ -315,6 +503,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
     P::mbar_init(&sm.dfull, 1);
     P::mbar_init(&sm.dempty, CLUSTER * NUM_EPI_WARPS * 32);
     P::mbar_init(&sm.mma_done, 1);
+    for (int i = 0; i < CLUSTER * NUM_EPI_WARPS; ++i) sm.cp_slot[i] = 0;
     sm.abort_flag = 0;
     P::fence_mbar_init();
   }
@@ -333,6 +522,9 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
   // the even CTA's barriers that both CTAs arrive on
   const uint32_t full_a_pair = P::mapa_shared(P::smem_u32(&sm.full_a[0]), 0);
   const uint32_t dempty_pair = P::mapa_shared(P::smem_u32(&sm.dempty), 0);
+  // the norm maxima per segment follow the whole-row ones
+  const uint32_t* aseg = amax + shp.mt;
+  const uint32_t* nwseg = nwpart + shp.G * shp.nt * kNormParts;
 
   if (warp == 0) {
     // ---------------- TMA producer: activation tiles ----------------
@@ -376,20 +568,18 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
     for (int t = cid; t < shp.tiles; t += ncl) {
       int g, mb, pair;
       tile_coords(shp, t, g, mb, pair);
-      if (!tile_exact(shp, amax, nwpart + g * shp.nt * kNormParts, mb, pair, lane)) {
-        // the chunked kernel takes it, as one or two 128-token tiles (both
-        // CTAs reach the same verdict; the even one lists it)
-        if (rank == 0 && lane == 0) {
-          const int n128 = min(2, shp.mt128 - 2 * mb);
-          const uint32_t i = atomicAdd(status + 2 + g, uint32_t(n128));
-          atomicAdd(status + 1, uint32_t(n128));
-          for (int h = 0; h < n128; ++h)
-            list[g * shp.list_cap + i + h] = make_uint2(uint32_t(2 * mb + h), uint32_t(pair));
-        }
+      TilePlan plan;
+      const int path = tile_path(shp, amax, aseg, nwpart + g * shp.nt * kNormParts,
+                                 nwseg + g * shp.nt * kNormParts * NSEG, mb, pair, lane, plan);
+      if (path == TILE_CHUNKED) {
+        // the chunked kernel takes it (both CTAs reach the same verdict; the
+        // even one lists it)
+        if (rank == 0 && lane == 0) list_for_chunked(shp, status, list, g, mb, pair);
         continue;
       }
       if (lane == 0) {
-        ok = push_tile(sm, nq, t, abort_flag, err);
+        ok = push_tile(sm, nq, t, path == TILE_CKPT ? &plan : nullptr, abort_flag, err);
+        if (ok && path == TILE_CKPT && rank == 0) atomicAdd(status + 6, 1u);
         const int wrow = min(2 * pair + int(rank), shp.nt - 1) * BM;
         for (int ss = 0; ok && ss < shp.NSS; ++ss, ++gs) {
           const uint32_t slot = gs % W_SLOTS;
@@ -407,7 +597,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
       if (!__shfl_sync(0xFFFFFFFFu, int(ok), 0)) break;
     }
     if (lane == 0) {
-      if (ok) push_tile(sm, nq, -1, abort_flag, err);
+      if (ok) push_tile(sm, nq, -1, nullptr, abort_flag, err);
       int no_abort = 0;
       volatile int* never = &no_abort;
       for (uint32_t i = gw > W_SLOTS ? gw - W_SLOTS : 0; i < gw; ++i)
@@ -421,31 +611,58 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
       bool ok = true;
       for (;;) {
         int t;
-        if (!pop_tile(sm, nq, abort_flag, err, ERR_MMA, t) || t < 0) break;
+        TilePlan pl;
+        if (!pop_tile(sm, nq, abort_flag, err, ERR_MMA, t, &pl) || t < 0) break;
         // both epilogues have copied out the previous tile's accumulator
         if (!P::mbar_wait(&sm.dempty, (gt & 1u) ^ 1u, abort_flag, err, ERR_MMA)) break;
-        for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
-          const uint32_t slot = gs % B_SLOTS, aslot = gs % A_SLOTS;
-          if (!P::mbar_wait(&sm.full_a[aslot], (gs / A_SLOTS) & 1u, abort_flag, err, ERR_MMA)) {
+        bool check_failed = false;
+        uint32_t pending = pl.ckpt;                 // checkpoints still ahead
+        // the super-stages run by run, a checkpoint between runs (the inner
+        // loop is kept free of the checkpoint code)
+        for (int ss = 0;;) {
+          const int ss_end = pending ? (__ffs(pending) - 1) * shp.seg_ss : shp.NSS;
+          for (; ss < ss_end; ++ss, ++gs) {
+            const uint32_t slot = gs % B_SLOTS, aslot = gs % A_SLOTS;
+            if (!P::mbar_wait(&sm.full_a[aslot], (gs / A_SLOTS) & 1u, abort_flag, err,
+                              ERR_MMA)) {
+              ok = false;
+              break;
+            }
+            P::tc_fence_after();
+            const uint32_t a_tmem = tmem + TM_A + aslot * (SS * 32);
+            const int nkb = min(SS, shp.KB - ss * SS);
+            for (int j = 0; j < nkb; ++j) {
+              const uint64_t bdesc = P::smem_desc_sw128(P::smem_u32(sm.b[slot][j]));
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk)
+                P::mma_f16_ts_pair(tmem + TM_D, a_tmem + j * 32 + kk * 8,
+                                   bdesc + uint64_t(kk * 2), IDESC,
+                                   (ss > 0 || j > 0 || kk > 0) ? 1u : 0u);
+            }
+            P::mma_commit_pair_mc(&sm.empty_ss[slot], CLUSTER_MASK);
+          }
+          if (!ok || !pending) break;
+          const int seg = __ffs(pending) - 1;
+          pending &= pending - 1u;
+          const int r = mma_checkpoint(sm, pl, seg, gt, abort_flag, err);
+          ++gt;
+          if (r < 0) {
             ok = false;
             break;
           }
-          P::tc_fence_after();
-          const uint32_t a_tmem = tmem + TM_A + aslot * (SS * 32);
-          const int nkb = min(SS, shp.KB - ss * SS);
-          for (int j = 0; j < nkb; ++j) {
-            const uint64_t bdesc = P::smem_desc_sw128(P::smem_u32(sm.b[slot][j]));
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              P::mma_f16_ts_pair(tmem + TM_D, a_tmem + j * 32 + kk * 8,
-                                 bdesc + uint64_t(kk * 2), IDESC,
-                                 (ss > 0 || j > 0 || kk > 0) ? 1u : 0u);
-          }
-          P::mma_commit_pair_mc(&sm.empty_ss[slot], CLUSTER_MASK);
+          check_failed = check_failed || r > 0;
         }
         if (!ok) break;
         P::mma_commit_pair_mc(&sm.dfull, CLUSTER_MASK);
         ++gt;
+        if (check_failed) {
+          // its outputs are rewritten by the chunked kernel, which runs after
+          // this grid has completed
+          int g, mb, pair;
+          tile_coords(shp, t, g, mb, pair);
+          list_for_chunked(shp, status, list, g, mb, pair);
+          atomicAdd(status + 7, 1u);
+        }
       }
       // every MMA this thread issued has finished before TMEM is freed
       P::mma_commit_pair_mc(&sm.mma_done, 1);
@@ -534,10 +751,18 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
     const int q = warp & 3;                       // TMEM lane quarter
     const int cq = (warp - EPI_WARP0) >> 2;       // token columns [64*cq, +64)
     const uint32_t lane_base = uint32_t(32 * q) << 16;
+    const uint32_t cp_slot_pair = P::mapa_shared(
+        P::smem_u32(&sm.cp_slot[int(rank) * NUM_EPI_WARPS + (warp - EPI_WARP0)]), 0);
     uint32_t gt = 0, nq = 0;
     for (;;) {
       int t;
-      if (!pop_tile_warp(sm, nq, abort_flag, err, ERR_EPILOGUE, t, lane) || t < 0) break;
+      uint32_t ckpt;
+      if (!pop_tile_warp(sm, nq, abort_flag, err, ERR_EPILOGUE, t, lane, &ckpt) || t < 0) break;
+      if (ckpt) {
+        gt = epilogue_checkpoints(sm, ckpt, gt, abort_flag, err, tmem + lane_base + TM_D + 64 * cq,
+                                  cp_slot_pair, dempty_pair, lane);
+        if (gt == kNoEvent) break;
+      }
       int g, mb, pair;
       tile_coords(shp, t, g, mb, pair);
       const int n = (2 * pair + int(rank)) * BM + 32 * q + lane;
@@ -630,6 +855,7 @@ cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const Lin
   shp.ntc = (shp.nt + CLUSTER - 1) / CLUSTER;
   shp.tiles = shp.G * shp.mt * shp.ntc;
   shp.list_cap = int(fallback_list_capacity(M, N));
+  shp.seg_ss = norm_segment_len(K) / kSegQuantum;
   shp.wmax2 = uint64_t(128 * 128) * uint64_t(K);
 
   int dev = 0, sms = 0;

@@ -14,10 +14,22 @@ constexpr int kQMax = 127;
 // Launchers.  Each returns cudaSuccess or the launch error; arguments are
 // already validated by the C-ABI layer.
 
+// Norm segments: the K range of a row is cut into kNormSegs segments of
+// norm_segment_len(K) elements (the last ones shorter or empty), each a whole
+// number of the GEMM's 128-element super-stages.  The GEMM may check its
+// accumulator between segments.
+constexpr int kNormSegs = 4;
+constexpr int kSegQuantum = 128;
+__host__ __device__ constexpr int norm_segment_len(int64_t K) {
+  return int(((K + kSegQuantum - 1) / kSegQuantum + kNormSegs - 1) / kNormSegs) * kSegQuantum;
+}
+
 // A2: BF16 activations -> int8 (optional) + FP32 scale + FP16-coded q (optional,
 // rows of stride ldh >= K elements, the padding zeroed).  sq_max (optional):
-// per block of 256 rows, the running maximum of the rows' sums of q^2
-// (atomicMax, so it must start at zero).
+// the activation norm maxima, ceil(M/256) * (1 + kNormSegs) words: per block
+// of 256 rows the running maximum of the rows' sums of q^2, then per block
+// and segment the maximum of the rows' sums over that segment (atomicMax, so
+// the region must start at zero).
 cudaError_t launch_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t* q,
                                 float* scale, uint16_t* q_f16, int64_t ldh, uint32_t* sq_max,
                                 cudaStream_t s);
@@ -28,7 +40,7 @@ cudaError_t launch_quantize_weights(const void* w, int w_dtype, int64_t N, int64
                                     int8_t* q, float* scale, cudaStream_t s);
 
 // int8 [M, K] -> FP16-coded integers with row stride ldh (padding zeroed),
-// with the per-256-row maxima of sum(q^2) as launch_quantize_act.
+// with the activation norm maxima as launch_quantize_act.
 cudaError_t launch_int8_to_f16(const int8_t* q, int64_t M, int64_t K, int64_t ldh,
                                uint16_t* out, uint32_t* sq_max, cudaStream_t s);
 
@@ -55,10 +67,14 @@ struct LinearGroup {
 
 // The linear workspace, in order (each part 256-byte aligned):
 //   act     [M, gemm_tc_coded_ld(K)] FP16-coded activations
-//   amax    [ceil(M/256)] u32: per 256 tokens, max over rows of sum(qa^2)
+//   amax    [ceil(M/256)] u32: per 256 tokens, max over rows of sum(qa^2);
+//           then [ceil(M/256)][kNormSegs] u32, the same per norm segment
 //   status  256 bytes: word 0 error bits, word 1 fallback-list length over
-//           all Linears, word 2 + g the length of Linear g's list
-//   nwpart  G x [ceil(N/128) * 8] u32: per 16 channels, max over rows of sum(qw^2)
+//           all Linears, word 2 + g the length of Linear g's list, word 6
+//           the tiles that took accumulator checkpoints, word 7 those of
+//           them whose check failed (they are on the fallback list too)
+//   nwpart  G x [ceil(N/128) * 8] u32: per 16 channels, max over rows of
+//           sum(qw^2); then G x [ceil(N/128) * 8][kNormSegs], per segment
 //   list    G x [ceil(M/128) * ceil(N/256)] uint2 {token block, channel pair}:
 //           the 128 x 256 tiles the chunked kernel must finish
 // act, amax and status depend on M and K only, so a call with another N
@@ -79,9 +95,10 @@ cudaError_t launch_weight_norms(const LinearGroup& grp, int64_t N, int64_t K,
                                 cudaStream_t s);
 
 // A3 + A4 for the tiles whose FP32 sums are exact over the whole K (checked
-// per tile from amax and, where that is not enough, nwpart); the others are
-// appended to `list`, status[1] counting the entries.  status[0]: error bits
-// (bounded waits).
+// per tile from amax and, where that is not enough, nwpart), or provably
+// exact with checks of the accumulator between norm segments; the others
+// are appended to `list`, status[1] counting the entries.  status[0]: error
+// bits (bounded waits).
 cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const LinearGroup& grp,
                              int64_t M, int64_t N, int64_t K, const uint32_t* amax,
                              const uint32_t* nwpart, uint32_t* status, uint2* list,

@@ -114,11 +114,51 @@ __device__ __forceinline__ uint32_t quant_store8(uint4 v, float s, float r, bool
   return uint32_t(ss);
 }
 
-// Folds a row's sum of squares of q into the running maximum of its block of
-// 256 token rows (read by the GEMM to decide whether a tile's FP32 sums stay
-// exact without splitting K).
-__device__ __forceinline__ void record_row_sq(uint32_t* blk_max, int64_t row, uint32_t sq) {
-  if (blk_max) atomicMax(blk_max + (row >> 8), sq);
+// A row's sums of q^2, one per norm segment.  Every sum is exact: it is at
+// most 127^2 K < 2^32 for every supported K.
+static_assert(kNormSegs == 4, "the segment selects below are written out for four");
+struct SegSq {
+  uint32_t s0 = 0, s1 = 0, s2 = 0, s3 = 0;
+  // v into the segment of element k (selects, so no register is indexed)
+  __device__ __forceinline__ void add(int k, int seg_len, uint32_t v) {
+    const int g = int(k >= seg_len) + int(k >= 2 * seg_len) + int(k >= 3 * seg_len);
+    s0 += g == 0 ? v : 0u;
+    s1 += g == 1 ? v : 0u;
+    s2 += g == 2 ? v : 0u;
+    s3 += g == 3 ? v : 0u;
+  }
+  __device__ __forceinline__ void warp_sum() {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      s0 += __shfl_xor_sync(0xFFFFFFFFu, s0, o);
+      s1 += __shfl_xor_sync(0xFFFFFFFFu, s1, o);
+      s2 += __shfl_xor_sync(0xFFFFFFFFu, s2, o);
+      s3 += __shfl_xor_sync(0xFFFFFFFFu, s3, o);
+    }
+  }
+  __device__ __forceinline__ void store(uint4* p) const { *p = make_uint4(s0, s1, s2, s3); }
+  __device__ __forceinline__ void add(const uint4& v) {
+    s0 += v.x;
+    s1 += v.y;
+    s2 += v.z;
+    s3 += v.w;
+  }
+};
+
+// Folds a row's sums of squares of q into the running maxima of its block of
+// 256 token rows: the whole row's sum into blk_max[block], each segment's
+// into seg_max[block][segment] (read by the GEMM to decide whether a tile's
+// FP32 sums stay exact without splitting K).
+__device__ __forceinline__ void record_row_sq(uint32_t* blk_max, uint32_t* seg_max, int64_t row,
+                                              const SegSq& q) {
+  if (!blk_max) return;
+  const int64_t b = row >> 8;
+  atomicMax(blk_max + b, q.s0 + q.s1 + q.s2 + q.s3);
+  uint32_t* sm = seg_max + b * kNormSegs;
+  if (q.s0) atomicMax(sm + 0, q.s0);
+  if (q.s1) atomicMax(sm + 1, q.s1);
+  if (q.s2) atomicMax(sm + 2, q.s2);
+  if (q.s3) atomicMax(sm + 3, q.s3);
 }
 
 // One warp per token row.  kRegs: the whole row (<= 32 * kRegVecs vectors)
@@ -128,7 +168,7 @@ template <bool kRegs, bool kQ8, bool kF16>
 __global__ void __launch_bounds__(kWarps * 32)
 quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int K, int8_t* __restrict__ q8,
                  float* __restrict__ scale, uint16_t* __restrict__ qh, int ldh,
-                 uint32_t* __restrict__ sq_max) {
+                 uint32_t* __restrict__ sq_max, uint32_t* __restrict__ seg_max, int seg_len) {
   const int lane = threadIdx.x & 31;
   const int64_t row = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -155,19 +195,19 @@ quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int K, int8_t* __res
     const float s = row_scale(__uint_as_float(mbits << 16));
     const float r = __frcp_rn(s);
     const bool fast = s >= 0x1p-120f;
-    uint32_t sq = 0;
+    SegSq sq;
 #pragma unroll
     for (int i = 0; i < kRegVecs; ++i) {
       const int j = lane + 32 * i;
       if (j < nvec)
-        sq += quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh, base + 8 * int64_t(j),
-                                      hbase + 8 * int64_t(j));
+        sq.add(8 * j, seg_len,
+               quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh, base + 8 * int64_t(j),
+                                       hbase + 8 * int64_t(j)));
     }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+    sq.warp_sum();
     if (lane == 0) {
       scale[row] = s;
-      record_row_sq(sq_max, row, sq);
+      record_row_sq(sq_max, seg_max, row, sq);
     }
   } else {
     int j = lane;
@@ -183,15 +223,15 @@ quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int K, int8_t* __res
     const float s = row_scale(__uint_as_float(mbits << 16));
     const float r = __frcp_rn(s);
     const bool fast = s >= 0x1p-120f;
-    uint32_t sq = 0;
+    SegSq sq;
     for (j = lane; j < nvec; j += 32)
-      sq += quant_store8<kQ8, kF16>(ld_stream(xr + j), s, r, fast, q8, qh,
-                                    base + 8 * int64_t(j), hbase + 8 * int64_t(j));
-#pragma unroll
-    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+      sq.add(8 * j, seg_len,
+             quant_store8<kQ8, kF16>(ld_stream(xr + j), s, r, fast, q8, qh,
+                                     base + 8 * int64_t(j), hbase + 8 * int64_t(j)));
+    sq.warp_sum();
     if (lane == 0) {
       scale[row] = s;
-      record_row_sq(sq_max, row, sq);
+      record_row_sq(sq_max, seg_max, row, sq);
     }
   }
 }
@@ -205,9 +245,10 @@ template <int kVPT, bool kQ8, bool kF16>
 __global__ void __launch_bounds__(kRowThreads)
 quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__ q8,
                      float* __restrict__ scale, uint16_t* __restrict__ qh, int ldh,
-                     uint32_t* __restrict__ sq_max) {
+                     uint32_t* __restrict__ sq_max, uint32_t* __restrict__ seg_max,
+                     int seg_len) {
   __shared__ uint32_t red[kRowThreads / 32];
-  __shared__ uint32_t red_sq[kRowThreads / 32];
+  __shared__ uint4 red_sq[kRowThreads / 32];
   const int64_t row = blockIdx.x;
   const int nvec = K >> 3;
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * int64_t(K));
@@ -235,25 +276,25 @@ quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__
   const float s = row_scale(__uint_as_float(mbits << 16));
   const float r = __frcp_rn(s);
   const bool fast = s >= 0x1p-120f;
-  uint32_t sq = 0;
+  SegSq sq;
 #pragma unroll
   for (int i = 0; i < kVPT; ++i) {
     const int j = threadIdx.x + kRowThreads * i;
     if (j < nvec)
-      sq += quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh, base + 8 * int64_t(j),
-                                    hbase + 8 * int64_t(j));
+      sq.add(8 * j, seg_len,
+             quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh, base + 8 * int64_t(j),
+                                     hbase + 8 * int64_t(j)));
   }
   if (threadIdx.x == 0) scale[row] = s;
   if (sq_max) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
-    if ((threadIdx.x & 31) == 0) red_sq[threadIdx.x >> 5] = sq;
+    sq.warp_sum();
+    if ((threadIdx.x & 31) == 0) sq.store(&red_sq[threadIdx.x >> 5]);
     __syncthreads();
     if (threadIdx.x == 0) {
-      uint32_t t = 0;
+      SegSq t;
 #pragma unroll
-      for (int w = 0; w < kRowThreads / 32; ++w) t += red_sq[w];
-      record_row_sq(sq_max, row, t);
+      for (int w = 0; w < kRowThreads / 32; ++w) t.add(red_sq[w]);
+      record_row_sq(sq_max, seg_max, row, t);
     }
   }
 }
@@ -297,11 +338,11 @@ quant_weight_kernel(const T* __restrict__ w, int64_t N, int K, int8_t* __restric
 // ldh with the padding zeroed, and the row's sum of squares.
 __global__ void __launch_bounds__(256)
 int8_to_f16_kernel(const int8_t* __restrict__ q, int K, int ldh, uint16_t* __restrict__ out,
-                   uint32_t* __restrict__ sq_max) {
-  __shared__ uint32_t red[8];
+                   uint32_t* __restrict__ sq_max, uint32_t* __restrict__ seg_max, int seg_len) {
+  __shared__ uint4 red[8];
   const int64_t row = blockIdx.x;
   const int groups = ldh >> 4;                      // 16-element groups of a coded row
-  uint32_t sq = 0;
+  SegSq sq;
   for (int grp = threadIdx.x; grp < groups; grp += 256) {
     uint4* dst = reinterpret_cast<uint4*>(out + row * ldh + 16 * int64_t(grp));
     if (16 * grp >= K) {
@@ -312,27 +353,28 @@ int8_to_f16_kernel(const int8_t* __restrict__ q, int K, int ldh, uint16_t* __res
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(q + row * K + 16 * int64_t(grp)));
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[8];
+    uint32_t g2 = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int b0 = int(int8_t(w[j])), b1 = int(int8_t(w[j] >> 8));
       const int b2 = int(int8_t(w[j] >> 16)), b3 = int(int8_t(w[j] >> 24));
       o[2 * j] = pack2_f16(b0, b1);
       o[2 * j + 1] = pack2_f16(b2, b3);
-      sq = uint32_t(__dp4a(int(w[j]), int(w[j]), int(sq)));
+      g2 = uint32_t(__dp4a(int(w[j]), int(w[j]), int(g2)));
     }
+    sq.add(16 * grp, seg_len, g2);
     dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
   }
   if (sq_max) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sq;
+    sq.warp_sum();
+    if ((threadIdx.x & 31) == 0) sq.store(&red[threadIdx.x >> 5]);
     __syncthreads();
     if (threadIdx.x == 0) {
-      uint32_t t = 0;
+      SegSq t;
 #pragma unroll
-      for (int w = 0; w < 8; ++w) t += red[w];
-      record_row_sq(sq_max, row, t);
+      for (int w = 0; w < 8; ++w) t.add(red[w]);
+      record_row_sq(sq_max, seg_max, row, t);
     }
   }
 }
@@ -341,9 +383,10 @@ int8_to_f16_kernel(const int8_t* __restrict__ q, int K, int ldh, uint16_t* __res
 // whether any block of 256 tokens could fail the test against the largest
 // possible weight row (sum q^2 <= 128^2 K); if none can, the GEMM never reads
 // the norms and the block returns at once.  Otherwise block b (16 warps) sums
-// q^2 over weight rows 16b .. 16b+15 with DP4A on 16-byte loads and writes the
-// largest to part[b].  The sums are taken modulo 2^32, which is exact:
-// K * 128^2 < 2^32 for every supported K.
+// q^2 over weight rows 16b .. 16b+15 with DP4A on 16-byte loads, per norm
+// segment, and writes the largest whole-row sum to part[b] and the largest
+// sum of each segment s to part[nblocks + b * kNormSegs + s].  The sums are
+// taken modulo 2^32, which is exact: K * 128^2 < 2^32 for every supported K.
 constexpr int kNormRows = 16;
 
 struct WeightPtrs {
@@ -352,12 +395,13 @@ struct WeightPtrs {
 
 __global__ void __launch_bounds__(32 * kNormRows)
 weight_norm_kernel(const WeightPtrs wqs, int64_t N, int K, int blocks_per_linear,
-                   const uint32_t* __restrict__ amax, int mt2, uint32_t* __restrict__ part) {
+                   const uint32_t* __restrict__ amax, int mt2, uint32_t* __restrict__ part,
+                   int seg_len) {
   // the quantiser that wrote amax may still be finishing (programmatic
   // dependent launch): wait for it, then let the GEMM be scheduled
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  __shared__ uint32_t red[kNormRows];
+  __shared__ uint4 red[kNormRows];
   __shared__ int needed;
   if (threadIdx.x == 0) needed = 0;
   __syncthreads();
@@ -371,8 +415,9 @@ weight_norm_kernel(const WeightPtrs wqs, int64_t N, int K, int blocks_per_linear
   const int g = int(blockIdx.x) / blocks_per_linear;
   const int8_t* __restrict__ wq = wqs.w[g];
   const int64_t n = int64_t(int(blockIdx.x) - g * blocks_per_linear) * kNormRows + warp;
-  uint32_t sq = 0;
+  SegSq sq;
   if (n < N) {
+    // a 16-byte vector never straddles two segments (they are multiples of 128)
     const uint4* row = reinterpret_cast<const uint4*>(wq + n * K);
     const int nv = K >> 4;
     int i = lane;
@@ -382,42 +427,59 @@ weight_norm_kernel(const WeightPtrs wqs, int64_t N, int K, int blocks_per_linear
       for (int u = 0; u < 4; ++u) v[u] = __ldg(row + i + 32 * u);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        sq = uint32_t(__dp4a(int(v[u].x), int(v[u].x), int(sq)));
-        sq = uint32_t(__dp4a(int(v[u].y), int(v[u].y), int(sq)));
-        sq = uint32_t(__dp4a(int(v[u].z), int(v[u].z), int(sq)));
-        sq = uint32_t(__dp4a(int(v[u].w), int(v[u].w), int(sq)));
+        uint32_t t = uint32_t(__dp4a(int(v[u].x), int(v[u].x), 0));
+        t = uint32_t(__dp4a(int(v[u].y), int(v[u].y), int(t)));
+        t = uint32_t(__dp4a(int(v[u].z), int(v[u].z), int(t)));
+        t = uint32_t(__dp4a(int(v[u].w), int(v[u].w), int(t)));
+        sq.add(16 * (i + 32 * u), seg_len, t);
       }
     }
     for (; i < nv; i += 32) {
       const uint4 v = __ldg(row + i);
-      sq = uint32_t(__dp4a(int(v.x), int(v.x), int(sq)));
-      sq = uint32_t(__dp4a(int(v.y), int(v.y), int(sq)));
-      sq = uint32_t(__dp4a(int(v.z), int(v.z), int(sq)));
-      sq = uint32_t(__dp4a(int(v.w), int(v.w), int(sq)));
+      uint32_t t = uint32_t(__dp4a(int(v.x), int(v.x), 0));
+      t = uint32_t(__dp4a(int(v.y), int(v.y), int(t)));
+      t = uint32_t(__dp4a(int(v.z), int(v.z), int(t)));
+      t = uint32_t(__dp4a(int(v.w), int(v.w), int(t)));
+      sq.add(16 * i, seg_len, t);
     }
   }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
-  if (lane == 0) red[warp] = sq;
+  sq.warp_sum();
+  if (lane == 0) sq.store(&red[warp]);
   __syncthreads();
   if (threadIdx.x == 0) {
     uint32_t m = 0;
+    uint4 ms = make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int w = 0; w < kNormRows; ++w) m = max(m, red[w]);
+    for (int w = 0; w < kNormRows; ++w) {
+      const uint4 r = red[w];
+      m = max(m, r.x + r.y + r.z + r.w);
+      ms = make_uint4(max(ms.x, r.x), max(ms.y, r.y), max(ms.z, r.z), max(ms.w, r.w));
+    }
     part[blockIdx.x] = m;
+    reinterpret_cast<uint4*>(part + gridDim.x)[blockIdx.x] = ms;
   }
+}
+
+// The per-segment activation norm maxima follow the per-block ones.
+uint32_t* seg_maxima(uint32_t* sq_max, int64_t M) {
+  return sq_max ? sq_max + (M + kNormTokens - 1) / kNormTokens : nullptr;
 }
 
 template <bool kRegs>
 cudaError_t launch_act(const uint16_t* x, int64_t M, int K, int8_t* q, float* s, uint16_t* qh,
                        int ldh, uint32_t* sqm, cudaStream_t st) {
   const dim3 grid(unsigned((M + kWarps - 1) / kWarps)), block(kWarps * 32);
+  uint32_t* sgm = seg_maxima(sqm, M);
+  const int sl = norm_segment_len(K);
   if (q && qh)
-    quant_act_kernel<kRegs, true, true><<<grid, block, 0, st>>>(x, M, K, q, s, qh, ldh, sqm);
+    quant_act_kernel<kRegs, true, true><<<grid, block, 0, st>>>(x, M, K, q, s, qh, ldh, sqm,
+                                                                sgm, sl);
   else if (q)
-    quant_act_kernel<kRegs, true, false><<<grid, block, 0, st>>>(x, M, K, q, s, qh, ldh, sqm);
+    quant_act_kernel<kRegs, true, false><<<grid, block, 0, st>>>(x, M, K, q, s, qh, ldh, sqm,
+                                                                 sgm, sl);
   else
-    quant_act_kernel<kRegs, false, true><<<grid, block, 0, st>>>(x, M, K, q, s, qh, ldh, sqm);
+    quant_act_kernel<kRegs, false, true><<<grid, block, 0, st>>>(x, M, K, q, s, qh, ldh, sqm,
+                                                                 sgm, sl);
   return cudaGetLastError();
 }
 
@@ -425,12 +487,17 @@ template <int kVPT>
 cudaError_t launch_rows(const uint16_t* x, int64_t M, int K, int8_t* q, float* s, uint16_t* qh,
                         int ldh, uint32_t* sqm, cudaStream_t st) {
   const dim3 grid(static_cast<unsigned>(M)), block(kRowThreads);
+  uint32_t* sgm = seg_maxima(sqm, M);
+  const int sl = norm_segment_len(K);
   if (q && qh)
-    quant_act_row_kernel<kVPT, true, true><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh, sqm);
+    quant_act_row_kernel<kVPT, true, true><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh, sqm,
+                                                                   sgm, sl);
   else if (q)
-    quant_act_row_kernel<kVPT, true, false><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh, sqm);
+    quant_act_row_kernel<kVPT, true, false><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh, sqm,
+                                                                    sgm, sl);
   else
-    quant_act_row_kernel<kVPT, false, true><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh, sqm);
+    quant_act_row_kernel<kVPT, false, true><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh, sqm,
+                                                                    sgm, sl);
   return cudaGetLastError();
 }
 
@@ -477,12 +544,13 @@ cudaError_t launch_weight_norms(const LinearGroup& grp, int64_t N, int64_t K,
   cfg.numAttrs = 1;
   const int mt2 = static_cast<int>((M + kNormTokens - 1) / kNormTokens);
   return cudaLaunchKernelEx(&cfg, weight_norm_kernel, wqs, N, static_cast<int>(K), per, amax,
-                            mt2, nwpart);
+                            mt2, nwpart, norm_segment_len(K));
 }
 
 cudaError_t launch_int8_to_f16(const int8_t* q, int64_t M, int64_t K, int64_t ldh,
                                uint16_t* out, uint32_t* sq_max, cudaStream_t s) {
-  int8_to_f16_kernel<<<static_cast<unsigned>(M), 256, 0, s>>>(q, int(K), int(ldh), out, sq_max);
+  int8_to_f16_kernel<<<static_cast<unsigned>(M), 256, 0, s>>>(
+      q, int(K), int(ldh), out, sq_max, seg_maxima(sq_max, M), norm_segment_len(K));
   return cudaGetLastError();
 }
 

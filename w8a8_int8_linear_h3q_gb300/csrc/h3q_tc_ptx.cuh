@@ -155,6 +155,24 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   }
 }
 
+// Store to a 64-bit word in the shared memory of any CTA of the cluster
+// (address from mapa_shared).
+__device__ __forceinline__ void st_cluster_u64(uint32_t cluster_addr, uint64_t v) {
+  asm volatile("st.relaxed.cluster.shared::cluster.u64 [%0], %1;" ::"r"(cluster_addr), "l"(v)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+
+// mbar_arrive_cluster with a cluster-scope release: publishes this thread's
+// generic-memory writes to a waiter in another CTA (about a microsecond).
+__device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
 // --- programmatic dependent launch ----------------------------------------------------
 
 // Wait until the grids this one depends on have completed and their memory
