@@ -303,6 +303,8 @@ def run_gpu(args):
     pl_ms = max_over_ranks(sum(e[0].elapsed_time(e[-1]) for e in pl_events), world, dev)
     per_linear_tops = whole_job_tops(pl_ms, pl_steps, world)
     gemm_ms = [e[i].elapsed_time(e[i + 1]) for e in pl_events for i in range(1, len(LINEARS))]
+    # A2 inside the call: the Q call (A2 + GEMM) less a reuse-mode call (GEMM)
+    q_call_ms = [e[0].elapsed_time(e[1]) for e in pl_events]
 
     # end to end through the public API with host buffers: pinned H2D of X,
     # the hot path, D2H of the four outputs, all inside the timed region.  Each
@@ -355,6 +357,8 @@ def run_gpu(args):
     gemm_tflops = 2 * M * N * K / gemm_avg_s / 1e12
     quant_avg_s = time_quantize_act(h3q, x, flush)
     quant_bytes = 2 * M * K + M * K + 4 * M       # BF16 in, INT8 out, FP32 scales
+    a2_call_s = (statistics.median(q_call_ms) - statistics.median(gemm_ms)) * 1e-3
+    a2_call_bytes = 2 * M * K + 2 * M * K + 4 * M  # BF16 in, FP16-coded out, FP32 scales
     traffic, traffic_note = profiled_traffic()
     roofline = {"bound": "tensor", "achieved": gemm_tflops, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": gemm_tflops / peaks["bf16_tflops"],
@@ -381,6 +385,10 @@ def run_gpu(args):
                         "quantize_act_us": quant_avg_s * 1e6,
                         "quantize_act_gbs": quant_bytes / quant_avg_s / 1e9,
                         "quantize_act_hbm_frac": quant_bytes / quant_avg_s / 1e9 / peaks["hbm_gbs"],
+                        "quantize_act_in_call_us": a2_call_s * 1e6,
+                        "quantize_act_in_call_hbm_frac":
+                            a2_call_bytes / a2_call_s / 1e9 / peaks["hbm_gbs"] if a2_call_s > 0
+                            else None,
                         "gemm_us_per_linear": gemm_avg_s * 1e6,
                         "per_linear_step_tops": per_linear_tops,
                         "per_linear_step_ms": pl_ms / pl_steps,

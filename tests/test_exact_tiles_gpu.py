@@ -264,3 +264,40 @@ def test_failed_checkpoints_fall_back(lib, oracle, dev):
     assert paths == (math.ceil(M / 128) * math.ceil(N / 256),
                      math.ceil(M / 256) * math.ceil(N / 256))
     assert abs(int(acc[0, 0])) == 127 * 127 * K
+
+
+def _workspace_norms(ws, M, K):
+    """The activation norm maxima a Linear call leaves in its workspace: per
+    256-token block the largest sum of q^2 of a row, then per block and norm
+    segment (the workspace starts with the FP16-coded activations, rows of
+    ceil(K / 64) * 64 elements, each part 256-byte aligned)."""
+    up = lambda b: (b + 255) // 256 * 256
+    mt = math.ceil(M / 256)
+    off = up(M * math.ceil(K / 64) * 64 * 2)
+    w = ws.cpu().numpy()[off:off + 4 * mt * (1 + SEGS)].view(np.uint32)
+    return w[:mt], w[mt:].reshape(mt, SEGS)
+
+
+@pytest.mark.parametrize("M,K", [(700, 5376), (300, 14336), (37, 2064)])
+def test_norm_maxima_from_bf16_input(lib, oracle, dev, M, K):
+    # the quantiser inside the call records, besides the codes and scales, the
+    # per-block and per-segment maxima of the rows' sums of q^2 that decide the
+    # tile paths; compare them with the oracle's codes
+    rng = np.random.default_rng(13 + K)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x[rng.random((M, K)) < 0.003] *= 25.0
+    x[5] = 0.0                                    # an all-zero row
+    xb = oracle.round_to_bf16(x)
+    w = (rng.standard_normal((40, K)) * 0.02).astype(np.float32)
+    qw, sw = lib.h3q_quantize_weights(torch.from_numpy(w).to(dev))
+    out = lib.h3q_linear_w8a8(_bf16_dev(xb, dev), qw, sw, None)
+    torch.cuda.synchronize()
+    qa, _ = oracle.quantize_act(xb)
+    a2 = qa.astype(np.int64) ** 2
+    sl = segment_len(K)
+    full, seg = _workspace_norms(out["workspace"], M, K)
+    for b in range(math.ceil(M / 256)):
+        rows = slice(256 * b, 256 * b + 256)
+        assert int(full[b]) == int(a2[rows].sum(1).max())
+        for s in range(SEGS):
+            assert int(seg[b, s]) == int(a2[rows, s * sl:(s + 1) * sl].sum(1).max())

@@ -92,7 +92,7 @@ h3q_status run_linear(const uint16_t* x, int8_t* xq, float* xs, const h3q::Linea
   const int64_t ldh = h3q::gemm_tc_coded_ld(K);
   if (x) {
     if (h3q_status st =
-            from_cuda(h3q::launch_quantize_act(x, M, K, xq, xs, act, ldh, amax, stream)))
+            from_cuda(h3q::launch_quantize_act(x, M, K, xq, xs, act, ldh, amax, stream, status)))
       return st;
   } else if (xq) {
     if (h3q_status st = from_cuda(h3q::launch_int8_to_f16(xq, M, K, ldh, act, amax, stream)))

@@ -29,10 +29,12 @@ __host__ __device__ constexpr int norm_segment_len(int64_t K) {
 // the activation norm maxima, ceil(M/256) * (1 + kNormSegs) words: per block
 // of 256 rows the running maximum of the rows' sums of q^2, then per block
 // and segment the maximum of the rows' sums over that segment (atomicMax, so
-// the region must start at zero).
+// the region must start at zero).  err (optional, a status word): with it,
+// rows of 6144 < K <= 24576 take the kernel that stages them in shared
+// memory, whose bounded waits report a timeout there.
 cudaError_t launch_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t* q,
                                 float* scale, uint16_t* q_f16, int64_t ldh, uint32_t* sq_max,
-                                cudaStream_t s);
+                                cudaStream_t s, uint32_t* err = nullptr);
 
 // A1: FP32 or BF16 weights -> int8 + FP32 scale.  A row with a non-finite
 // element gets a NaN scale, which the caller turns into H3Q_ERR_NONFINITE.

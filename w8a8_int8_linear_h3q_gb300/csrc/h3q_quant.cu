@@ -11,6 +11,7 @@
 #include <cuda_fp16.h>
 
 #include "h3q_internal.cuh"
+#include "h3q_tc_ptx.cuh"
 
 namespace h3q {
 namespace {
@@ -27,26 +28,6 @@ __device__ __forceinline__ float row_scale(float amax) {
 __device__ __forceinline__ int quant1(float x, float s) {
   const int q = __float2int_rn(__fdiv_rn(x, s));
   return max(-kQMax, min(kQMax, q));
-}
-
-// The same integer as quant1(x, s), as an integer-valued float, cheaper.
-// With r = RN(1/s) (s normal) and t = RN(x * r): t = (x/s)(1 + e1)(1 + e2),
-// |e1|, |e2| <= 2^-24, and |x/s| <= 127 (1 + 2^-23), so |t - x/s| < 1.6e-5;
-// the FP32 quotient RN(x/s) is within 2^-18 of x/s.  Hence |t - RN(x/s)| <
-// 2^-15, and unless t lies within 2^-15 of a half-integer, RN(x/s) and t
-// round to the same integer, with no tie.  Near a half-integer (about 6e-5 of
-// inputs) the IEEE division decides.  Rounding t to an integer adds and
-// subtracts 1.5 * 2^23: for |t| < 2^22 the sum's last place is 1, so the
-// addition itself rounds t to nearest, ties to even.  `fast` is false for
-// rows whose scale is too small for a normal reciprocal; those always divide.
-// |x| <= absmax makes |q| <= 127 without a clamp.
-__device__ __forceinline__ float quant1_fast(float x, float s, float r, bool fast) {
-  if (fast) {
-    const float t = __fmul_rn(x, r);
-    const float n = __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f);
-    if (fabsf(__fsub_rn(t, n)) < 0.5f - 0x1p-15f) return n;
-  }
-  return float(quant1(x, s));
 }
 
 // integer-valued float in [-127, 127] -> its two's-complement low byte
@@ -79,39 +60,80 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   return r;
 }
 
+__device__ __forceinline__ uint64_t pack_f2(float lo, float hi) {
+  return (uint64_t(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float lo_f(uint64_t v) { return __uint_as_float(uint32_t(v)); }
+__device__ __forceinline__ float hi_f(uint64_t v) { return __uint_as_float(uint32_t(v >> 32)); }
+
+// The fast path of quant_store8 gives the same integer as quant1(x, s), as
+// an integer-valued float, cheaper.
+// With r = RN(1/s) (s normal) and t = RN(x * r): t = (x/s)(1 + e1)(1 + e2),
+// |e1|, |e2| <= 2^-24, and |x/s| <= 127 (1 + 2^-23), so |t - x/s| < 1.6e-5;
+// the FP32 quotient RN(x/s) is within 2^-18 of x/s.  Hence |t - RN(x/s)| <
+// 2^-15, and unless t lies within 2^-15 of a half-integer, RN(x/s) and t
+// round to the same integer, with no tie.  Near a half-integer (about 6e-5 of
+// inputs) the IEEE division decides.  Rounding t to an integer adds and
+// subtracts 1.5 * 2^23: for |t| < 2^22 the sum's last place is 1, so the
+// addition itself rounds t to nearest, ties to even.  `fast` is false for
+// rows whose scale is too small for a normal reciprocal; those always divide.
+// |x| <= absmax makes |q| <= 127 without a clamp.
+//
 // Quantises 8 values, stores them, and returns the sum of their squares
-// (exact: at most 8 * 127^2).
+// (exact: at most 8 * 127^2).  The work runs two values at a time on the
+// paired FP32 instructions (each half the same IEEE operation as the scalar
+// one), and the fallback is taken per vector: the fast results stand when
+// every one of the eight passes its test, else all eight take the IEEE
+// division, which gives the same integer wherever the test passes.  One
+// branch per vector instead of one per value: the quantiser is bound by
+// instruction issue otherwise.
 template <bool kQ8, bool kF16>
 __device__ __forceinline__ uint32_t quant_store8(uint4 v, float s, float r, bool fast,
                                                  int8_t* q8, uint16_t* qh, int64_t elem,
                                                  int64_t helem) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  float q[8];
+  const uint64_t r2 = pack_f2(r, r);
+  const uint64_t c2 = pack_f2(12582912.0f, 12582912.0f);
+  const float lim = 0.5f - 0x1p-15f;
+  uint64_t q2[4];
+  bool ok = fast;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    q[2 * j] = quant1_fast(__uint_as_float(w[j] << 16), s, r, fast);
-    q[2 * j + 1] = quant1_fast(__uint_as_float(w[j] & 0xFFFF0000u), s, r, fast);
+    // elements 2j (low half of w[j]) and 2j + 1 (high half), widened exactly
+    const uint64_t x2 = (uint64_t(w[j] & 0xFFFF0000u) << 32) | (w[j] << 16);
+    uint64_t t2, u2, d2;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(t2) : "l"(x2), "l"(r2));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(u2) : "l"(t2), "l"(c2));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(q2[j]) : "l"(u2), "l"(c2));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d2) : "l"(t2), "l"(q2[j]));
+    ok = ok && fabsf(lo_f(d2)) < lim && fabsf(hi_f(d2)) < lim;
+  }
+  if (!ok) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      q2[j] = pack_f2(float(quant1(__uint_as_float(w[j] << 16), s)),
+                      float(quant1(__uint_as_float(w[j] & 0xFFFF0000u), s)));
   }
   if constexpr (kQ8) {
     uint2 o;
-    o.x = f2s8_byte(q[0]) | (f2s8_byte(q[1]) << 8) | (f2s8_byte(q[2]) << 16) |
-          (f2s8_byte(q[3]) << 24);
-    o.y = f2s8_byte(q[4]) | (f2s8_byte(q[5]) << 8) | (f2s8_byte(q[6]) << 16) |
-          (f2s8_byte(q[7]) << 24);
+    o.x = f2s8_byte(lo_f(q2[0])) | (f2s8_byte(hi_f(q2[0])) << 8) |
+          (f2s8_byte(lo_f(q2[1])) << 16) | (f2s8_byte(hi_f(q2[1])) << 24);
+    o.y = f2s8_byte(lo_f(q2[2])) | (f2s8_byte(hi_f(q2[2])) << 8) |
+          (f2s8_byte(lo_f(q2[3])) << 16) | (f2s8_byte(hi_f(q2[3])) << 24);
     *reinterpret_cast<uint2*>(q8 + elem) = o;
   }
   if constexpr (kF16) {
     uint4 o;   // integers of magnitude <= 127 are exact in FP16
-    o.x = pack2_f16f(q[0], q[1]);
-    o.y = pack2_f16f(q[2], q[3]);
-    o.z = pack2_f16f(q[4], q[5]);
-    o.w = pack2_f16f(q[6], q[7]);
+    o.x = pack2_f16f(lo_f(q2[0]), hi_f(q2[0]));
+    o.y = pack2_f16f(lo_f(q2[1]), hi_f(q2[1]));
+    o.z = pack2_f16f(lo_f(q2[2]), hi_f(q2[2]));
+    o.w = pack2_f16f(lo_f(q2[3]), hi_f(q2[3]));
     *reinterpret_cast<uint4*>(qh + helem) = o;
   }
-  float ss = 0.f;
+  uint64_t ss2 = 0;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) ss = __fmaf_rn(q[j], q[j], ss);
-  return uint32_t(ss);
+  for (int j = 0; j < 4; ++j) asm("fma.rn.f32x2 %0, %1, %1, %2;" : "=l"(ss2) : "l"(q2[j]), "l"(ss2));
+  return uint32_t(lo_f(ss2)) + uint32_t(hi_f(ss2));
 }
 
 // A row's sums of q^2, one per norm segment.  Every sum is exact: it is at
@@ -241,8 +263,11 @@ quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int K, int8_t* __res
 // thread, so many rows are in flight per SM.
 constexpr int kRowThreads = 256;
 
+// Short rows: eight blocks resident per SM (32 registers a thread), so that
+// enough rows are in flight to keep HBM busy (measured at K = 5376: 32.8
+// against 37-39 us with the register count left free).
 template <int kVPT, bool kQ8, bool kF16>
-__global__ void __launch_bounds__(kRowThreads)
+__global__ void __launch_bounds__(kRowThreads, kVPT <= 3 ? 8 : 2)
 quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__ q8,
                      float* __restrict__ scale, uint16_t* __restrict__ qh, int ldh,
                      uint32_t* __restrict__ sq_max, uint32_t* __restrict__ seg_max,
@@ -296,6 +321,136 @@ quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__
       for (int w = 0; w < kRowThreads / 32; ++w) t.add(red_sq[w]);
       record_row_sq(sq_max, seg_max, row, t);
     }
+  }
+}
+
+// The same per-row work for long rows (K up to 24576), staged in shared
+// memory: a persistent
+// grid (two 256-thread blocks per SM), each block taking rows b, b + G,
+// b + 2G, ...  Thread 0 keeps `ring` rows in flight with untiled bulk copies
+// (one mbarrier per ring slot), so HBM latency is covered by the copies
+// rather than by the number of resident blocks, and a block passes one
+// barrier per row: the absmax partials of a row and the sum-of-squares
+// partials of the row before share it (double-buffered by row parity), and
+// a slot is refilled as soon as every thread has its vectors in registers.
+// Every wait is bounded; on a timeout the block records an error bit in
+// *err and stops.
+constexpr int kStagedThreads = 256;
+constexpr int kStagedSmem = 104 * 1024;   // row ring of a block: two blocks fit an SM
+constexpr uint32_t kErrQuantWait = 1u << 16;
+
+template <int kVPT, bool kQ8, bool kF16>
+__global__ void __launch_bounds__(kStagedThreads, 2)
+quant_act_staged_kernel(const uint16_t* __restrict__ x, int64_t M, int K, int ring, int slot_bytes,
+                        int8_t* __restrict__ q8, float* __restrict__ scale,
+                        uint16_t* __restrict__ qh, int ldh, uint32_t* __restrict__ sq_max,
+                        uint32_t* __restrict__ seg_max, int seg_len, uint32_t* __restrict__ err) {
+  namespace P = ptx;
+  extern __shared__ __align__(128) uint8_t rows_smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(rows_smem + size_t(ring) * slot_bytes);
+  __shared__ uint32_t red[2][kStagedThreads / 32];
+  __shared__ uint4 red_sq[2][kStagedThreads / 32];
+  __shared__ int give_up;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t G = gridDim.x;
+  const uint32_t row_bytes = uint32_t(K) * 2u;
+  const int nvec = K >> 3;
+  if (tid == 0) {
+    for (int i = 0; i < ring; ++i) P::mbar_init(&full[i], 1);
+    P::fence_mbar_init();
+    give_up = 0;
+    for (int i = 0; i < ring; ++i) {
+      const int64_t row = blockIdx.x + int64_t(i) * G;
+      if (row >= M) break;
+      P::mbar_arrive_expect_tx(&full[i], row_bytes);
+      P::bulk_load(P::smem_u32(rows_smem + size_t(i) * slot_bytes), x + row * int64_t(K),
+                   row_bytes, &full[i]);
+    }
+  }
+  __syncthreads();
+  int64_t it = 0;
+  for (;; ++it) {
+    const int64_t row = blockIdx.x + it * G;
+    if (row >= M) break;
+    const int slot = int(it % ring);
+    const int par = int(it & 1);
+    // this row's copy (bounded wait; a thread that gives up flags the block,
+    // which stops together after the barrier below)
+    const uint32_t bar = P::smem_u32(&full[slot]);
+    const uint32_t phase = uint32_t(it / ring) & 1u;
+    bool ok = P::mbar_test(bar, phase);
+    if (!ok) {
+      const uint64_t t0 = P::globaltimer();
+      while (!(ok = P::mbar_test(bar, phase))) {
+        if (P::globaltimer() - t0 > P::kWaitTimeoutNs) {
+          give_up = 1;
+          if (err) atomicOr(err, kErrQuantWait);
+          break;
+        }
+      }
+    }
+    const uint4* xr = reinterpret_cast<const uint4*>(rows_smem + size_t(slot) * slot_bytes);
+    uint4 v[kVPT];
+    uint32_t mbits = 0;
+#pragma unroll
+    for (int i = 0; i < kVPT; ++i) {
+      const int j = tid + kStagedThreads * i;
+      v[i] = (ok && j < nvec) ? xr[j] : make_uint4(0, 0, 0, 0);
+      mbits = max(mbits, vec_absmax_bits(v[i]));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mbits = max(mbits, __shfl_xor_sync(0xFFFFFFFFu, mbits, o));
+    if (lane == 0) red[par][warp] = mbits;
+    __syncthreads();
+    if (give_up) break;
+    if (tid == 0) {
+      // the slot's vectors are in registers: refill it
+      const int64_t nrow = row + int64_t(ring) * G;
+      if (nrow < M) {
+        P::mbar_arrive_expect_tx(&full[slot], row_bytes);
+        P::bulk_load(P::smem_u32(rows_smem + size_t(slot) * slot_bytes), x + nrow * int64_t(K),
+                     row_bytes, &full[slot]);
+      }
+      // the previous row's sums of squares
+      if (sq_max && it > 0) {
+        SegSq t;
+#pragma unroll
+        for (int w = 0; w < kStagedThreads / 32; ++w) t.add(red_sq[par ^ 1][w]);
+        record_row_sq(sq_max, seg_max, row - G, t);
+      }
+    }
+#pragma unroll
+    for (int w = 0; w < kStagedThreads / 32; ++w) mbits = max(mbits, red[par][w]);
+    const float s = row_scale(__uint_as_float(mbits << 16));
+    const float r = __frcp_rn(s);
+    const bool fast = s >= 0x1p-120f;
+    const int64_t base = row * int64_t(K), hbase = row * int64_t(ldh);
+    if constexpr (kF16) {   // zero the row's padding up to the coded row stride
+      for (int j = nvec + tid; j < (ldh >> 3); j += kStagedThreads)
+        *reinterpret_cast<uint4*>(qh + hbase + 8 * int64_t(j)) = make_uint4(0, 0, 0, 0);
+    }
+    SegSq sq;
+#pragma unroll
+    for (int i = 0; i < kVPT; ++i) {
+      const int j = tid + kStagedThreads * i;
+      if (j < nvec)
+        sq.add(8 * j, seg_len,
+               quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh, base + 8 * int64_t(j),
+                                       hbase + 8 * int64_t(j)));
+    }
+    if (tid == 0) scale[row] = s;
+    if (sq_max) {
+      sq.warp_sum();
+      if (lane == 0) sq.store(&red_sq[par][warp]);
+    }
+  }
+  // the last row's sums of squares
+  __syncthreads();
+  if (tid == 0 && sq_max && it > 0 && !give_up) {
+    SegSq t;
+#pragma unroll
+    for (int w = 0; w < kStagedThreads / 32; ++w) t.add(red_sq[(it - 1) & 1][w]);
+    record_row_sq(sq_max, seg_max, blockIdx.x + (it - 1) * G, t);
   }
 }
 
@@ -501,14 +656,50 @@ cudaError_t launch_rows(const uint16_t* x, int64_t M, int K, int8_t* q, float* s
   return cudaGetLastError();
 }
 
+template <int kVPT, bool kQ8, bool kF16>
+cudaError_t launch_staged_one(const uint16_t* x, int64_t M, int K, int8_t* q, float* s,
+                              uint16_t* qh, int ldh, uint32_t* sqm, uint32_t* err,
+                              cudaStream_t st) {
+  const int slot = (2 * K + 127) / 128 * 128;
+  const int ring = max(2, min(8, kStagedSmem / slot));
+  const size_t smem = size_t(ring) * slot + size_t(ring) * sizeof(uint64_t);
+  auto kern = quant_act_staged_kernel<kVPT, kQ8, kF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(smem));
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const int64_t blocks = M < 2 * int64_t(sms) ? M : 2 * int64_t(sms);
+  kern<<<unsigned(blocks), kStagedThreads, smem, st>>>(x, M, K, ring, slot, q, s, qh, ldh, sqm,
+                                                      seg_maxima(sqm, M), norm_segment_len(K),
+                                                      err);
+  return cudaGetLastError();
+}
+
+template <int kVPT>
+cudaError_t launch_staged(const uint16_t* x, int64_t M, int K, int8_t* q, float* s,
+                          uint16_t* qh, int ldh, uint32_t* sqm, uint32_t* err, cudaStream_t st) {
+  if (q && qh) return launch_staged_one<kVPT, true, true>(x, M, K, q, s, qh, ldh, sqm, err, st);
+  if (q) return launch_staged_one<kVPT, true, false>(x, M, K, q, s, qh, ldh, sqm, err, st);
+  return launch_staged_one<kVPT, false, true>(x, M, K, q, s, qh, ldh, sqm, err, st);
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t* q,
                                 float* scale, uint16_t* q_f16, int64_t ldh, uint32_t* sq_max,
-                                cudaStream_t s) {
+                                cudaStream_t s, uint32_t* err) {
   const int64_t nvec = K / 8;
+  // Short rows: one block per row, with enough blocks resident to keep HBM
+  // busy.  Longer rows (measured at K = 21504: 525 against 559 us), when the
+  // call has a status word for the bounded waits: rows staged in shared
+  // memory.
   if (nvec <= kRowThreads * 3)
     return launch_rows<3>(x, M, int(K), q, scale, q_f16, int(ldh), sq_max, s);
+  if (err && nvec <= kStagedThreads * 12)
+    return launch_staged<12>(x, M, int(K), q, scale, q_f16, int(ldh), sq_max, err, s);
   if (nvec <= kRowThreads * 12)
     return launch_rows<12>(x, M, int(K), q, scale, q_f16, int(ldh), sq_max, s);
   return launch_act<false>(x, M, int(K), q, scale, q_f16, int(ldh), sq_max, s);

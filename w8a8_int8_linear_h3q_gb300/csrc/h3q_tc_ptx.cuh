@@ -202,6 +202,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, uint6
       : "memory");
 }
 
+// Untiled bulk copy of `bytes` contiguous bytes from global memory into this
+// CTA's shared memory, completing that many transaction bytes on `bar`.  Both
+// addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Same, delivered to the same shared-memory offset (data and mbarrier) in
 // every CTA of the cluster named in `mask`.
 __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* map, uint64_t* bar,
