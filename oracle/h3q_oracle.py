@@ -41,6 +41,9 @@ taken where they are silent (each one also listed in the design notes):
   R6  masked tail chunks change nothing in the result: the quantiser is
       defined per row over exactly K elements.
 
+The group-wise affine scheme of [P2] and [P4] (weights only), a comparison
+point for the W8A8 path, has readings R10-R13 below, with its functions.
+
 Parity pins for every function here live in ``tests/test_oracle_pins.py``.
 """
 from __future__ import annotations
@@ -206,6 +209,124 @@ def snr_db(y, y_ref) -> float:
     if noise == 0.0:
         return float("inf")
     return 10.0 * np.log10(signal / noise)
+
+
+# --- the comparison scheme: group-wise affine weight-only quantisation ---------------
+# [P2] Operator tuning times Q8/g64 and Q4/g64 variants of the QKV, gate/up and
+# down GEMMs; [P4] adds affine INT8, INT6 and INT4 checkpoints.  That scheme is
+# weight-only: per output channel and group of 64 consecutive inputs a step and
+# an offset ("affine"), the weights dequantised for a BF16 GEMM with the BF16
+# activations unquantised.  The pages give no formula; the readings (also in
+# the design notes):
+#   R10  per group: lo = min, hi = max of its FP32 weights; alpha = RN((hi - lo)
+#       / (2^b - 1)), hi - lo rounded to FP32 first, one FP32 division;
+#       beta = lo; a group with hi == lo gets alpha = 1, and a positive range
+#       whose alpha underflows to 0 gets the smallest positive FP32;
+#   R11  q = clamp(rint(RN(RN(w - beta) / alpha)), 0, 2^b - 1): FP32 subtraction
+#       and division, ties to even;
+#   R12  the dequantised weight is w^ = BF16_RNE(RN_fp32(alpha q + beta)): one
+#       FP32 fused multiply-add, then BF16, the activations' type (a tensor-core
+#       MMA takes both operands in one type);
+#   R13 y = BF16_RNE(sum_k x_k w^_k + bias): the reference sum is evaluated in
+#       float64 (the products are exact), and a GPU result, whose FP32
+#       accumulation order is not fixed, is accepted within one BF16 ulp plus
+#       K 2^-23 sum_k |x_k w^_k|.
+
+AFFINE_GROUP = 64
+
+
+def quantize_affine(w: np.ndarray, bits: int = 8, group: int = AFFINE_GROUP):
+    """Group-wise affine quantisation of a weight [N, K] (FP32, or BF16 bits
+    widened exactly), K a multiple of ``group``; readings R10, R11.
+
+    Returns (q uint8 [N, K] in [0, 2^bits - 1], alpha float32 [N, K/group],
+    beta float32 [N, K/group]).
+    """
+    w = np.asarray(w)
+    if w.dtype == np.uint16:
+        w = widen_bf16(w)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n, k = w.shape
+    if k % group:
+        raise ValueError("K must be a multiple of the group size")
+    if not np.all(np.isfinite(w)):
+        raise ValueError("non-finite weight")
+    g = w.reshape(n, k // group, group)
+    lo = g.min(axis=2)
+    hi = g.max(axis=2)
+    levels = np.float32(2 ** bits - 1)
+    alpha = (hi - lo) / levels                                    # FP32 ops, RN
+    alpha = np.where(hi == lo, np.float32(1.0), alpha)
+    alpha = np.where((hi > lo) & (alpha == 0), _SMALLEST_F32, alpha).astype(np.float32)
+    beta = lo.astype(np.float32)
+    d = g - beta[:, :, None]                                      # FP32 subtraction
+    r = d / alpha[:, :, None]                                     # FP32 division
+    q = np.clip(np.rint(r), 0, levels).astype(np.uint8)
+    return q.reshape(n, k), alpha, beta
+
+
+def _exact_sum_or_none(a: np.ndarray, b: np.ndarray):
+    """a + b in float64 and a mask of the elements where that sum rounded
+    (Knuth's two-sum error term is non-zero)."""
+    s = a + b
+    bb = s - a
+    err = (a - (s - bb)) + (b - bb)
+    return s, err != 0
+
+
+def dequant_affine(q: np.ndarray, alpha: np.ndarray, beta: np.ndarray,
+                   group: int = AFFINE_GROUP) -> np.ndarray:
+    """R12: w^ = BF16_RNE(RN_fp32(alpha q + beta)) as BF16 bit patterns [N, K]."""
+    n, k = q.shape
+    qq = q.reshape(n, k // group, group).astype(np.float64)
+    a = alpha.astype(np.float64)[:, :, None]
+    b = beta.astype(np.float64)[:, :, None]
+    prod = qq * a                                   # exact: 24 + 8 significant bits
+    exact, rounded = _exact_sum_or_none(prod, np.broadcast_to(b, prod.shape))
+    if np.any(rounded):
+        # the float64 sum rounded (operands far apart in magnitude): redo those
+        # elements in exact rational arithmetic, then round to FP32 once
+        from fractions import Fraction
+        idx = np.argwhere(rounded)
+        for (i, j, t) in idx:
+            v = Fraction(float(qq[i, j, t])) * Fraction(float(a[i, j, 0])) + \
+                Fraction(float(b[i, j, 0]))
+            exact[i, j, t] = _fraction_to_f32(v)
+    f32 = exact.astype(np.float32)                  # RN to FP32 (exact cases: one rounding)
+    return round_to_bf16(f32.reshape(n, k))
+
+
+def _fraction_to_f32(v) -> float:
+    """Round an exact rational to the nearest FP32 (ties to even), as a float."""
+    import math
+    if v == 0:
+        return 0.0
+    sign = -1.0 if v < 0 else 1.0
+    v = abs(v)
+    e = math.floor(math.log2(v.numerator) - math.log2(v.denominator))
+    while 2 ** e > v:
+        e -= 1
+    while 2 ** (e + 1) <= v:
+        e += 1
+    q_exp = max(e, -126) - 23                      # FP32 spacing at this magnitude
+    from fractions import Fraction
+    scaled = v / Fraction(2) ** q_exp
+    n = scaled.numerator // scaled.denominator
+    rem = scaled - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return sign * float(Fraction(n) * Fraction(2) ** q_exp)
+
+
+def linear_affine(x_bits: np.ndarray, w_hat_bits: np.ndarray, bias_bits=None) -> dict:
+    """R13: the weight-only Linear on dequantised BF16 weights.  Returns the
+    float64 value v, sum_k |x_k w^_k| (for the tolerance) and y = BF16_RNE(v)."""
+    xf = widen_bf16(x_bits).astype(np.float64)
+    wf = widen_bf16(w_hat_bits).astype(np.float64)
+    v = xf @ wf.T
+    if bias_bits is not None:
+        v = v + widen_bf16(bias_bits).astype(np.float64)
+    return {"v": v, "absum": np.abs(xf) @ np.abs(wf).T, "y": round_to_bf16(v)}
 
 
 # --- the converter's scope rule (passthrough) -------------------------------------

@@ -358,3 +358,123 @@ def test_snr_closed_forms(oracle):
     noise = rng.standard_normal(1000) * 1e-3
     d = oracle.snr_db(ref + noise / 2, ref) - oracle.snr_db(ref + noise, ref)
     assert abs(d - 20 * np.log10(2)) < 1e-9
+
+
+# --- the group-wise affine comparison scheme (readings R10-R13) ------------------
+# "MLX implementation and experiment report", Operator tuning (Q8/g64, Q4/g64);
+# "[feat] Add MiniMax H3 MLX T2VA inference" (affine INT8/INT6/INT4 checkpoints).
+
+def _brute_affine_group(ws, bits):
+    ws = [Fraction(float(v)) for v in ws]
+    lo, hi = min(ws), max(ws)
+    levels = 2 ** bits - 1
+    if hi == lo:
+        alpha = Fraction(1)
+    else:
+        alpha = _fp32_rn(_fp32_rn(hi - lo) / levels)
+    q = [max(0, min(levels, _rne_int(_fp32_rn(_fp32_rn(v - lo) / alpha)))) for v in ws]
+    return q, alpha, lo
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_affine_brute_force_rationals(oracle, bits):
+    rng = np.random.default_rng(40 + bits)
+    w = (rng.standard_normal((3, 128)) * 0.05).astype(np.float32)
+    w[1, 64:] = np.float32(0.25)                       # a constant group
+    q, a, b = oracle.quantize_affine(w, bits=bits)
+    for n in range(3):
+        for g in range(2):
+            bq, ba, bb = _brute_affine_group(w[n, 64 * g:64 * g + 64], bits)
+            assert list(q[n, 64 * g:64 * g + 64]) == bq
+            assert Fraction(float(a[n, g])) == ba and Fraction(float(b[n, g])) == bb
+
+
+def test_affine_grid_reconstructs_exactly(oracle):
+    # values beta + j / 64 for j in 0..255 (both ends present): alpha comes out
+    # as exactly 1/64, q = j, and the dequantised weights are the inputs
+    rng = np.random.default_rng(44)
+    j = rng.integers(0, 256, (4, 256))
+    j[:, ::64] = 0
+    j[:, 1::64] = 255
+    w = (np.float32(-0.5) + j.astype(np.float32) / np.float32(64.0)).astype(np.float32)
+    q, a, b = oracle.quantize_affine(w, bits=8)
+    assert np.array_equal(q, j.astype(np.uint8))
+    assert np.all(a == np.float32(1 / 64)) and np.all(b == np.float32(-0.5))
+    wh = oracle.dequant_affine(q, a, b)
+    assert np.array_equal(oracle.widen_bf16(wh), w)       # every such value is a BF16 value
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_affine_extremes_and_error_bound(oracle, bits):
+    rng = np.random.default_rng(45 + bits)
+    w = (rng.standard_normal((16, 512)) * 0.02).astype(np.float32)
+    q, a, b = oracle.quantize_affine(w, bits=bits)
+    g = w.reshape(16, 8, 64)
+    qg = q.reshape(16, 8, 64)
+    # the group's minimum codes to 0 and its maximum to 2^bits - 1
+    assert np.all(np.take_along_axis(qg, g.argmin(2)[:, :, None], 2) == 0)
+    assert np.all(np.take_along_axis(qg, g.argmax(2)[:, :, None], 2) == 2 ** bits - 1)
+    # rint: |w - (alpha q + beta)| <= alpha / 2, up to the FP32 roundings
+    rec = qg.astype(np.float64) * a[:, :, None] + b[:, :, None]
+    assert np.all(np.abs(g - rec) <= a[:, :, None] * (0.5 + 2.0 ** -10))
+
+
+def test_affine_constant_group_and_rejects_non_finite(oracle):
+    w = np.full((2, 64), -0.375, np.float32)
+    q, a, b = oracle.quantize_affine(w)
+    assert np.all(q == 0) and np.all(a == 1.0) and np.all(b == np.float32(-0.375))
+    assert np.all(oracle.widen_bf16(oracle.dequant_affine(q, a, b)) == np.float32(-0.375))
+    w[1, 7] = np.nan
+    with pytest.raises(ValueError):
+        oracle.quantize_affine(w)
+
+
+def test_dequant_affine_one_fp32_rounding_then_bf16(oracle):
+    # brute force: RN_fp32(alpha q + beta) in rationals, then one BF16 rounding;
+    # the last group has beta far above alpha q, where the float64 sum itself
+    # rounds and the oracle takes its exact-rational path
+    rng = np.random.default_rng(47)
+    q = rng.integers(0, 256, (2, 128)).astype(np.uint8)
+    a = (rng.uniform(1e-4, 1e-2, (2, 2))).astype(np.float32)
+    b = (rng.uniform(-0.5, 0.5, (2, 2))).astype(np.float32)
+    a[1, 1] = np.float32(2.0 ** -40)
+    b[1, 1] = np.float32(2.0 ** 30 + 2.0 ** 7)
+    wh = oracle.dequant_affine(q, a, b)
+    for n in range(2):
+        for k in range(128):
+            g = k // 64
+            v = _fp32_rn(Fraction(int(q[n, k])) * Fraction(float(a[n, g])) +
+                         Fraction(float(b[n, g])))
+            want = oracle.round_to_bf16(np.array([float(v)], np.float64))[0]
+            assert wh[n, k] == want, (n, k)
+
+
+def test_linear_affine_brute_force(oracle):
+    rng = np.random.default_rng(48)
+    xb = oracle.round_to_bf16(rng.standard_normal((3, 128)))
+    wb = oracle.round_to_bf16(rng.standard_normal((5, 128)) * 0.1)
+    bias = oracle.round_to_bf16(rng.standard_normal(5))
+    out = oracle.linear_affine(xb, wb, bias)
+    xf, wf = oracle.widen_bf16(xb), oracle.widen_bf16(wb)
+    bf = oracle.widen_bf16(bias)
+    for m in range(3):
+        for n in range(5):
+            exact = sum(Fraction(float(xf[m, k])) * Fraction(float(wf[n, k])) for k in range(128))
+            exact += Fraction(float(bf[n]))
+            assert abs(Fraction(float(out["v"][m, n])) - exact) <= abs(exact) * Fraction(1, 2 ** 50)
+            assert out["absum"][m, n] == pytest.approx(
+                float(sum(abs(Fraction(float(xf[m, k])) * Fraction(float(wf[n, k])))
+                          for k in range(128))), rel=1e-12)
+
+
+def test_affine_q8_beats_q4(oracle):
+    # more levels, smaller steps: the 8-bit reconstruction error is below the
+    # 4-bit one by about the ratio of the steps (255 / 15 = 17)
+    rng = np.random.default_rng(49)
+    w = (rng.standard_normal((64, 1024)) * 0.02).astype(np.float32)
+    err = {}
+    for bits in (8, 4):
+        q, a, b = oracle.quantize_affine(w, bits=bits)
+        rec = (q.reshape(64, 16, 64).astype(np.float64) * a[:, :, None] + b[:, :, None])
+        err[bits] = float(np.sqrt(np.mean((rec.reshape(64, 1024) - w) ** 2)))
+    assert 12 < err[4] / err[8] < 22
