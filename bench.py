@@ -513,10 +513,11 @@ CONFIG_TABLE = ("tiny", "attn", "fc1", "fc2", "image_qkv", "image_gate_up", "ima
 
 def run_configs(args):
     """Per-workload table (not the contract line): for each seeded workload,
-    one Linear timed two ways with CUDA events, L2 flushed before each rep:
-    GEMM + epilogue on activations already coded in the workspace (reuse
-    mode), and the whole call from BF16 X (A2 + A3 + A4).  Prints one JSON
-    object per workload."""
+    one Linear timed with CUDA events, L2 flushed before each rep: GEMM +
+    epilogue on activations already coded in the workspace (reuse mode), the
+    whole call from BF16 X (A2 + A3 + A4), and the weight-only group-wise
+    affine comparison scheme's call on the same X.  Prints one JSON object
+    per workload."""
     import numpy as np
     import torch
     import w8a8_int8_linear_h3q_gb300 as h3q
@@ -530,7 +531,8 @@ def run_configs(args):
     for name in names:
         case = synth.WORKLOADS[name]()
         x = torch.from_numpy(case.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
-        wq, wsc = h3q.h3q_quantize_weights(torch.from_numpy(case.w[0]).to(dev))
+        w_dev = torch.from_numpy(case.w[0]).to(dev)
+        wq, wsc = h3q.h3q_quantize_weights(w_dev)
         bias = torch.from_numpy(case.bias_bits[0].view(np.int16)).view(torch.bfloat16).to(dev)
         del case
         Mc, Kc = x.shape
@@ -565,15 +567,33 @@ def run_configs(args):
         full()
         t_gemm = med_us(reuse, args.steps)
         chunked = h3q.h3q_linear_chunked_tiles(ws_buf, Mc, Kc)
+        ckpt = h3q.h3q_linear_checkpointed_tiles(ws_buf, Mc, Kc)
         ops = 2 * Mc * Nc * Kc
+        # the group-wise affine comparison scheme (weight-only Q8/g64) on the
+        # same Linear, from the same BF16 X
+        t_aff = None
+        if Kc % 64 == 0:
+            qa, ab = h3q.h3q_quantize_weights_affine(w_dev)
+            oa = h3q.h3q_linear_affine_w8(x, qa, ab, bias)
+
+            def affine():
+                h3q.h3q_linear_affine_w8(x, qa, ab, bias, y=oa["y"], status=oa["status"])
+
+            for _ in range(args.warmup):
+                affine()
+            t_aff = med_us(affine, args.steps)
+            del qa, ab, oa
         print(json.dumps({
             "workload": name, "M": Mc, "N": Nc, "K": Kc, "reps": args.steps,
             "gemm_us": t_gemm, "gemm_tops": ops / t_gemm / 1e6,
             "gemm_frac_of_bf16_peak": ops / t_gemm / 1e6 / peaks["bf16_tflops"],
             "call_us": t_full, "call_tops": ops / t_full / 1e6,
             "chunked_tiles": chunked, "tiles": -(-Mc // 128) * -(-Nc // 256),
+            "checkpointed_tiles": ckpt,
+            "affine_q8_call_us": t_aff,
+            "affine_q8_call_tops": ops / t_aff / 1e6 if t_aff else None,
             "peak": f"{peaks['bf16_tflops']} TFLOP/s bf16 burst ({peak_kind})"}), flush=True)
-        del x, wq, wsc, bias, xs, y, ws_buf
+        del x, w_dev, wq, wsc, bias, xs, y, ws_buf
         torch.cuda.empty_cache()
     return 0
 

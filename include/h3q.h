@@ -225,6 +225,46 @@ h3q_status h3q_linear_checkpointed_tiles(const void* workspace, int64_t M, int64
                                          int64_t* tiles, cudaStream_t stream);
 
 /*
+ * The group-wise affine comparison scheme (weight-only; "MLX implementation and
+ * experiment report", Operator tuning: Q8/g64 GEMMs; "[feat] Add MiniMax H3 MLX
+ * T2VA inference": affine INT8 checkpoints).  Not the W8A8 method: the
+ * activations stay BF16, and the weights carry a step and an offset per output
+ * channel and group of 64 inputs.  Offline quantisation:
+ *
+ *   w       [N, K] FP32 (w_dtype = H3Q_DTYPE_F32) or BF16 bits, K a multiple of 64
+ *   q_out   [N, K] unsigned 8-bit codes
+ *   ab_out  [N, K/64][2] FP32: per group the step a and the offset b, so that
+ *           the group's weights are represented by a q + b
+ *
+ * Per group: b = min, a = (max - min) / 255 (each an FP32 operation, rounded to
+ * nearest even; a = 1 for a constant group, the smallest positive FP32 when
+ * the quotient underflows), q = clamp(rint((w - b) / a), 0, 255).  Returns
+ * H3Q_ERR_NONFINITE if any weight is Inf or NaN, H3Q_ERR_UNSUPPORTED_SHAPE if
+ * K is not a multiple of 64.  SYNCHRONISES `stream` (offline call).
+ */
+h3q_status h3q_quantize_weights_affine(const void* w, int w_dtype, int64_t N, int64_t K,
+                                       uint8_t* q_out, float* ab_out, cudaStream_t stream);
+
+/*
+ * The weight-only Linear of the comparison scheme:
+ *   y[m, n] = BF16_RNE( sum_k x[m, k] w^[n, k] + bias[n] ),
+ *   w^[n, k] = BF16_RNE( RN_fp32( a q[n, k] + b ) )   (one FP32 FMA, then BF16)
+ * with the sum accumulated in FP32 on the tensor cores (order unspecified).
+ *
+ *   x       [M, K] BF16, K a multiple of 64        (read)
+ *   q, ab   as h3q_quantize_weights_affine wrote them (read)
+ *   bias    [N] BF16, or NULL                      (read)
+ *   y       [M, N] BF16                            (written)
+ *   status  one device uint32, zeroed by the call; nonzero after it if a
+ *           bounded device-side wait gave up (the outputs are then unspecified)
+ *
+ * Errors as h3q_linear_w8a8.  Enqueued on `stream`; does not synchronise.
+ */
+h3q_status h3q_linear_affine_w8(const uint16_t* x, const uint8_t* q, const float* ab,
+                                const uint16_t* bias, int64_t M, int64_t N, int64_t K,
+                                uint16_t* y, uint32_t* status, cudaStream_t stream);
+
+/*
  * A3 + A4 on the legacy warp-level INT8 tensor instruction (mma.sync
  * m16n8k32 s8 -> s32), exact by construction; the same arithmetic and output
  * as h3q_linear_w8a8 from pre-quantised activations.  Kept as the baseline

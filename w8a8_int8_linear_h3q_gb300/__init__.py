@@ -63,6 +63,10 @@ def _declare(lib):
     lib.h3q_linear_w8a8_mma_sync.restype = i32
     lib.h3q_linear_w8a8_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
     lib.h3q_linear_w8a8_noalloc.restype = i32
+    lib.h3q_quantize_weights_affine.argtypes = [vp, i32, i64, i64, vp, vp, vp]
+    lib.h3q_quantize_weights_affine.restype = i32
+    lib.h3q_linear_affine_w8.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
+    lib.h3q_linear_affine_w8.restype = i32
     return lib
 
 
@@ -141,6 +145,48 @@ def h3q_quantize_weights(w, q_out=None, scale_out=None, stream=None):
     _check(load().h3q_quantize_weights(_ptr(w), dt, N, K, _ptr(q_out), _ptr(scale_out),
                                        _stream(stream)), "h3q_quantize_weights")
     return q_out, scale_out
+
+
+def h3q_quantize_weights_affine(w, q_out=None, ab_out=None, stream=None):
+    """The group-wise affine comparison scheme, offline: FP32 or BF16 weight
+    [N, K] (K a multiple of 64) -> (uint8 codes [N, K], FP32 (step, offset)
+    pairs [N, K/64, 2]).  Synchronises."""
+    import torch
+    if w.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("weights must be float32 or bfloat16")
+    _need(w, w.dtype, None, "w")
+    N, K = w.shape
+    q_out = torch.empty((N, K), dtype=torch.uint8, device=w.device) if q_out is None else q_out
+    ab_out = (torch.empty((N, K // 64, 2), dtype=torch.float32, device=w.device)
+              if ab_out is None else ab_out)
+    _need(q_out, torch.uint8, (N, K), "q_out")
+    _need(ab_out, torch.float32, (N, K // 64, 2), "ab_out")
+    dt = H3Q_DTYPE_F32 if w.dtype == torch.float32 else H3Q_DTYPE_BF16
+    _check(load().h3q_quantize_weights_affine(_ptr(w), dt, N, K, _ptr(q_out), _ptr(ab_out),
+                                              _stream(stream)), "h3q_quantize_weights_affine")
+    return q_out, ab_out
+
+
+def h3q_linear_affine_w8(x, q, ab, bias=None, *, y=None, status=None, stream=None):
+    """The comparison scheme's weight-only Linear: BF16 x [M, K] against the
+    dequantised codes.  Returns {"y": BF16 [M, N], "status": int32 [1]} (the
+    status word is nonzero after the call if a device-side wait gave up)."""
+    import torch
+    _need(x, torch.bfloat16, None, "x")
+    _need(q, torch.uint8, None, "q")
+    M, K = x.shape
+    N = q.shape[0]
+    if q.shape[1] != K:
+        raise ValueError("x and q disagree on K")
+    _need(ab, torch.float32, (N, K // 64, 2), "ab")
+    if bias is not None:
+        _need(bias, torch.bfloat16, (N,), "bias")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if y is None else y
+    _need(y, torch.bfloat16, (M, N), "y")
+    status = torch.empty((4,), dtype=torch.int32, device=x.device) if status is None else status
+    _check(load().h3q_linear_affine_w8(_ptr(x), _ptr(q), _ptr(ab), _ptr(bias), M, N, K, _ptr(y),
+                                       _ptr(status), _stream(stream)), "h3q_linear_affine_w8")
+    return {"y": y, "status": status}
 
 
 def h3q_quantize_act(x, q_out=None, scale_out=None, stream=None):

@@ -245,6 +245,48 @@ h3q_status h3q_linear_checkpointed_tiles(const void* workspace, int64_t M, int64
   return read_status_word(workspace, M, K, 6, tiles, stream);
 }
 
+h3q_status h3q_quantize_weights_affine(const void* w, int w_dtype, int64_t N, int64_t K,
+                                       uint8_t* q_out, float* ab_out, cudaStream_t stream) {
+  if (!w || !q_out || !ab_out) return H3Q_ERR_INVALID_ARG;
+  if (w_dtype != H3Q_DTYPE_F32 && w_dtype != H3Q_DTYPE_BF16) return H3Q_ERR_INVALID_ARG;
+  if (h3q_status st = check_shape(1, N, K)) return st;
+  if (K % 64) return H3Q_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(w) || !aligned16(q_out) || !aligned16(ab_out)) return H3Q_ERR_MISALIGNED;
+  if (h3q_status st = check_device()) return st;
+  if (h3q_status st = from_cuda(h3q::launch_quantize_weights_affine(w, w_dtype, N, K, q_out,
+                                                                    ab_out, stream)))
+    return st;
+  // Offline call: read the steps back and reject any NaN-marked (non-finite) group.
+  std::vector<float> host(static_cast<size_t>(N) * size_t(K / 64) * 2);
+  if (cudaMemcpyAsync(host.data(), ab_out, host.size() * sizeof(float), cudaMemcpyDeviceToHost,
+                      stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return H3Q_ERR_CUDA;
+  for (size_t i = 0; i < host.size(); i += 2)
+    if (!(host[i] > 0.f && host[i] <= 3.4028234663852886e38f)) return H3Q_ERR_NONFINITE;
+  return H3Q_OK;
+}
+
+h3q_status h3q_linear_affine_w8(const uint16_t* x, const uint8_t* q, const float* ab,
+                                const uint16_t* bias, int64_t M, int64_t N, int64_t K,
+                                uint16_t* y, uint32_t* status, cudaStream_t stream) {
+  if (!x || !q || !ab || !y || !status) return H3Q_ERR_INVALID_ARG;
+  if (h3q_status st = check_shape(M, N, K)) return st;
+  if (K % 64) return H3Q_ERR_UNSUPPORTED_SHAPE;
+  const void* ptrs[] = {x, q, ab, bias, y, status};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return H3Q_ERR_MISALIGNED;
+  if (h3q_status st = check_device()) return st;
+  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), stream) != cudaSuccess) return H3Q_ERR_CUDA;
+  h3q::LinearGroup grp = {};
+  grp.G = 1;
+  grp.wq[0] = reinterpret_cast<const int8_t*>(q);
+  grp.bias[0] = bias;
+  grp.y[0] = y;
+  const float* abs_[1] = {ab};
+  return from_cuda(h3q::launch_gemm_affine(x, grp, abs_, M, N, K, status, stream));
+}
+
 h3q_status h3q_linear_w8a8_mma_sync(const int8_t* xq, const float* xs, const int8_t* wq,
                                     const float* ws, const uint16_t* bias, int64_t M, int64_t N,
                                     int64_t K, uint16_t* y, int32_t* acc_out,

@@ -118,6 +118,7 @@ static_assert(TM_A + A_SLOTS * SS * 32 <= TM_COLS, "TMEM columns");
 // activation ring, so the A ring may not be deeper than that ring
 static_assert(A_SLOTS <= B_SLOTS, "A ring deeper than the activation ring");
 constexpr uint32_t IDESC = P::idesc_f16_f32(2 * BM, BN);
+constexpr uint32_t IDESC_BF16 = P::idesc_bf16_f32(2 * BM, BN);
 constexpr uint64_t kExactBound = uint64_t(1) << 48;        // |a|^2 |w|^2 limit
 constexpr int NSEG = kNormSegs;
 static_assert(SS * BK == kSegQuantum, "norm segments are whole super-stages");
@@ -164,6 +165,7 @@ struct Outs {
   const uint16_t* bias[kMaxGroup];
   uint16_t* y[kMaxGroup];
   int32_t* acc[kMaxGroup];
+  const float2* ab[kMaxGroup];            // (affine mode) per channel and group: step, offset
 };
 
 struct Shape {
@@ -472,7 +474,37 @@ __device__ __forceinline__ uint32_t epilogue_checkpoints(Smem& sm, uint32_t ckpt
   return gt;
 }
 
+// Affine mode (the group-wise weight-only comparison scheme): A2 absent, B is
+// the BF16 activations themselves, the weights are 8-bit codes dequantised
+// by the converters (one group of 64 per k-block), the accumulation is the
+// plain FP32 one of a BF16 GEMM (no exactness test, every tile wide), and the
+// epilogue is y = BF16(acc + bias).  Only the A2-free path shares the
+// pipeline; what W8A8 computes is unchanged (the mode is a template
+// parameter, so its branches compile out).
+//
+// A4 for 32 consecutive tokens of this lane's channel row n in affine mode.
+__device__ __forceinline__ void emit_block_affine(const uint32_t (&d)[32], int mbase, float bn,
+                                                  int n, bool n_ok, const Shape& shp,
+                                                  uint16_t* __restrict__ Y) {
+  if (!n_ok) return;
+  uint16_t* yp = Y + int64_t(mbase) * shp.N + n;
+  const uint64_t b2 = (uint64_t(__float_as_uint(bn)) << 32) | __float_as_uint(bn);
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    const uint64_t t2 = (uint64_t(d[j + 1]) << 32) | d[j];
+    uint64_t v2;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(v2) : "l"(t2), "l"(b2));
+    uint32_t h2;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;"
+        : "=r"(h2)
+        : "f"(__uint_as_float(uint32_t(v2 >> 32))), "f"(__uint_as_float(uint32_t(v2))));
+    if (mbase + j < shp.M) yp[int64_t(j) * shp.N] = uint16_t(h2);
+    if (mbase + j + 1 < shp.M) yp[int64_t(j + 1) * shp.N] = uint16_t(h2 >> 16);
+  }
+}
+
 // 23 warps: at most 6 per SM sub-partition, so 80 registers a thread.
+template <bool kAffine>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constant__ WMaps wmaps,
                  const float* __restrict__ sa, const __grid_constant__ Outs outs, const Shape shp,
@@ -569,8 +601,10 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
       int g, mb, pair;
       tile_coords(shp, t, g, mb, pair);
       TilePlan plan;
-      const int path = tile_path(shp, amax, aseg, nwpart + g * shp.nt * kNormParts,
-                                 nwseg + g * shp.nt * kNormParts * NSEG, mb, pair, lane, plan);
+      const int path = kAffine ? TILE_WIDE
+                               : tile_path(shp, amax, aseg, nwpart + g * shp.nt * kNormParts,
+                                           nwseg + g * shp.nt * kNormParts * NSEG, mb, pair,
+                                           lane, plan);
       if (path == TILE_CHUNKED) {
         // the chunked kernel takes it (both CTAs reach the same verdict; the
         // even one lists it)
@@ -636,7 +670,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
 #pragma unroll
               for (int kk = 0; kk < BK / 16; ++kk)
                 P::mma_f16_ts_pair(tmem + TM_D, a_tmem + j * 32 + kk * 8,
-                                   bdesc + uint64_t(kk * 2), IDESC,
+                                   bdesc + uint64_t(kk * 2), kAffine ? IDESC_BF16 : IDESC,
                                    (ss > 0 || j > 0 || kk > 0) ? 1u : 0u);
             }
             P::mma_commit_pair_mc(&sm.empty_ss[slot], CLUSTER_MASK);
@@ -695,10 +729,25 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
     while (ok) {
       int t;
       if (!pop_tile_warp(sm, nq, abort_flag, err, ERR_CONVERT, t, lane) || t < 0) break;
+      // (affine mode) this lane's channel row and its groups' steps and offsets
+      const float2* ab_row = nullptr;
+      if constexpr (kAffine) {
+        int g, mb, pair;
+        tile_coords(shp, t, g, mb, pair);
+        const int n = (2 * pair + int(rank)) * BM + r;
+        ab_row = n < shp.N ? outs.ab[g] + int64_t(n) * shp.KB : nullptr;
+      }
       for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
         const uint32_t slot = gs % B_SLOTS, aslot = gs % A_SLOTS;
         const uint32_t wslot = gs % W_SLOTS;
         const int nkb = min(SS, shp.KB - ss * SS);
+        float2 abk[SS];
+        if constexpr (kAffine) {
+          // loaded before the wait below, which hides their latency
+#pragma unroll
+          for (int j = 0; j < SS; ++j)
+            abk[j] = (ab_row && j < nkb) ? __ldg(ab_row + ss * SS + j) : make_float2(0.f, 0.f);
+        }
         if (!P::mbar_wait_warp(&sm.full_w[wslot], (gs / W_SLOTS) & 1u, abort_flag, err,
                                ERR_CONVERT)) {
           ok = false;
@@ -713,12 +762,26 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
           for (int i = 0; i < 4; ++i)
             v[i] = *reinterpret_cast<const uint4*>(box + coff[4 * j + i]);
           uint32_t h[32];
+          if constexpr (kAffine) {
+            const uint64_t a2 = (uint64_t(__float_as_uint(abk[j].x)) << 32) |
+                                __float_as_uint(abk[j].x);
+            const uint64_t b2 = (uint64_t(__float_as_uint(abk[j].y)) << 32) |
+                                __float_as_uint(abk[j].y);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            P::s8x4_to_f16x4(v[i].x, h[8 * i + 0], h[8 * i + 1]);
-            P::s8x4_to_f16x4(v[i].y, h[8 * i + 2], h[8 * i + 3]);
-            P::s8x4_to_f16x4(v[i].z, h[8 * i + 4], h[8 * i + 5]);
-            P::s8x4_to_f16x4(v[i].w, h[8 * i + 6], h[8 * i + 7]);
+            for (int i = 0; i < 4; ++i) {
+              P::u8x4_affine_to_bf16x4(v[i].x, a2, b2, h[8 * i + 0], h[8 * i + 1]);
+              P::u8x4_affine_to_bf16x4(v[i].y, a2, b2, h[8 * i + 2], h[8 * i + 3]);
+              P::u8x4_affine_to_bf16x4(v[i].z, a2, b2, h[8 * i + 4], h[8 * i + 5]);
+              P::u8x4_affine_to_bf16x4(v[i].w, a2, b2, h[8 * i + 6], h[8 * i + 7]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              P::s8x4_to_f16x4(v[i].x, h[8 * i + 0], h[8 * i + 1]);
+              P::s8x4_to_f16x4(v[i].y, h[8 * i + 2], h[8 * i + 3]);
+              P::s8x4_to_f16x4(v[i].z, h[8 * i + 4], h[8 * i + 5]);
+              P::s8x4_to_f16x4(v[i].w, h[8 * i + 6], h[8 * i + 7]);
+            }
           }
           // the A slot is free once the pair MMAs of super-stage gs - A_SLOTS are done
           if (j == 0 && gs >= A_SLOTS) {
@@ -767,12 +830,13 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
       tile_coords(shp, t, g, mb, pair);
       const int n = (2 * pair + int(rank)) * BM + 32 * q + lane;
       const bool n_ok = n < shp.N;
-      const float swn = n_ok ? outs.sw[g][n] : 0.f;
+      // (affine mode: no scales)
+      const float swn = (!kAffine && n_ok) ? outs.sw[g][n] : 0.f;
       const uint16_t* bias = outs.bias[g];
       const float bn = (n_ok && bias) ? bf16_bits_to_float(bias[n]) : 0.f;
       const int m0 = mb * BN + 64 * cq;
-      const float sa0 = (m0 + lane < shp.M) ? sa[m0 + lane] : 0.f;
-      const float sa1 = (m0 + 32 + lane < shp.M) ? sa[m0 + 32 + lane] : 0.f;
+      const float sa0 = (!kAffine && m0 + lane < shp.M) ? sa[m0 + lane] : 0.f;
+      const float sa1 = (!kAffine && m0 + 32 + lane < shp.M) ? sa[m0 + 32 + lane] : 0.f;
       if (!P::mbar_wait_warp(&sm.dfull, gt & 1u, abort_flag, err, ERR_EPILOGUE)) break;
       P::tc_fence_after();
       uint32_t d0[32], d1[32];
@@ -782,8 +846,13 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
       P::tc_fence_before();
       P::mbar_arrive_cluster(dempty_pair);        // the MMAs of the next tile may start
       ++gt;
-      emit_block(d0, sa0, m0, swn, bn, n, n_ok, shp, outs.y[g], outs.acc[g], sa);
-      emit_block(d1, sa1, m0 + 32, swn, bn, n, n_ok, shp, outs.y[g], outs.acc[g], sa);
+      if constexpr (kAffine) {
+        emit_block_affine(d0, m0, bn, n, n_ok, shp, outs.y[g]);
+        emit_block_affine(d1, m0 + 32, bn, n, n_ok, shp, outs.y[g]);
+      } else {
+        emit_block(d0, sa0, m0, swn, bn, n, n_ok, shp, outs.y[g], outs.acc[g], sa);
+        emit_block(d1, sa1, m0 + 32, swn, bn, n, n_ok, shp, outs.y[g], outs.acc[g], sa);
+      }
     }
   }
 
@@ -802,25 +871,25 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-}  // namespace
-
-cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const LinearGroup& grp,
-                             int64_t M, int64_t N, int64_t K, const uint32_t* amax,
-                             const uint32_t* nwpart, uint32_t* status, uint2* list,
-                             cudaStream_t s) {
+// Both modes: act is [M, ld] 16-bit (ld a multiple of 64), viewed as
+// (64-element chunk, row, chunk index); one box is two k-blocks of 128 rows.
+// ab (affine mode only): per Linear the [N, K/64] (step, offset) pairs.
+template <bool kAffine>
+cudaError_t launch_wide(const uint16_t* act, int64_t ld, const float* sa, const LinearGroup& grp,
+                        const float* const* ab, int64_t M, int64_t N, int64_t K,
+                        const uint32_t* amax, const uint32_t* nwpart, uint32_t* status,
+                        uint2* list, cudaStream_t s) {
   EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
   if (!enc) return cudaErrorNotSupported;
-  // activations: a [M, ld] FP16 matrix viewed as (64-element chunk, row, chunk
-  // index); one box is two k-blocks of 128 rows
-  const int64_t ld = gemm_tc_coded_ld(K);
   CUtensorMap map;
   const cuuint64_t dims[3] = {cuuint64_t(BK), cuuint64_t(M), cuuint64_t(ld / BK)};
   const cuuint64_t strides[2] = {cuuint64_t(ld) * 2u, cuuint64_t(BK) * 2u};
   const cuuint32_t box[3] = {BK, BNH, SS};
   const cuuint32_t estr[3] = {1, 1, 1};
-  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t*>(act_f16), dims,
-          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  if (enc(&map, kAffine ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+          const_cast<uint16_t*>(act), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   // weights: [N, K] INT8 per Linear, boxes of 128 rows x 128 bytes (two k-blocks)
   WMaps wmaps;
@@ -837,6 +906,7 @@ cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const Lin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
     outs.sw[g] = grp.ws[src];
+    outs.ab[g] = ab ? reinterpret_cast<const float2*>(ab[src]) : nullptr;
     outs.bias[g] = grp.bias[src];
     outs.y[g] = grp.y[src];
     outs.acc[g] = grp.acc[src];
@@ -863,8 +933,8 @@ cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const Lin
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(gemm_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(kSmemBytes));
+  e = cudaFuncSetAttribute(gemm_wide_kernel<kAffine>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
   if (e != cudaSuccess) return e;
   const int clusters = shp.tiles < sms / CLUSTER ? shp.tiles : sms / CLUSTER;
   cudaLaunchConfig_t cfg = {};
@@ -882,8 +952,24 @@ cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const Lin
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemm_wide_kernel, map, wmaps, sa, outs, shp, amax, nwpart,
-                            status, list);
+  return cudaLaunchKernelEx(&cfg, gemm_wide_kernel<kAffine>, map, wmaps, sa, outs, shp, amax,
+                            nwpart, status, list);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const LinearGroup& grp,
+                             int64_t M, int64_t N, int64_t K, const uint32_t* amax,
+                             const uint32_t* nwpart, uint32_t* status, uint2* list,
+                             cudaStream_t s) {
+  return launch_wide<false>(act_f16, gemm_tc_coded_ld(K), sa, grp, nullptr, M, N, K, amax,
+                            nwpart, status, list, s);
+}
+
+cudaError_t launch_gemm_affine(const uint16_t* x, const LinearGroup& grp, const float* const* ab,
+                               int64_t M, int64_t N, int64_t K, uint32_t* status,
+                               cudaStream_t s) {
+  return launch_wide<true>(x, K, nullptr, grp, ab, M, N, K, nullptr, nullptr, status, nullptr, s);
 }
 
 }  // namespace h3q

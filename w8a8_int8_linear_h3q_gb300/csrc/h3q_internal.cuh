@@ -106,6 +106,20 @@ cudaError_t launch_gemm_wide(const uint16_t* act_f16, const float* sa, const Lin
                              const uint32_t* nwpart, uint32_t* status, uint2* list,
                              cudaStream_t s);
 
+// The group-wise affine comparison scheme (weight-only): y = BF16(x W^T + bias)
+// with W dequantised from 8-bit codes, per channel and group of 64 inputs
+// w = step q + offset (one FP32 FMA, then BF16).  x: BF16 [M, K], K a multiple
+// of 64; grp.wq: the codes [N, K] (unsigned); ab[g]: [N, K/64] (step, offset)
+// FP32 pairs; grp.ws and grp.acc unused.  status[0]: error bits.
+cudaError_t launch_gemm_affine(const uint16_t* x, const LinearGroup& grp, const float* const* ab,
+                               int64_t M, int64_t N, int64_t K, uint32_t* status, cudaStream_t s);
+
+// Offline group-wise affine quantisation of FP32 or BF16 weights [N, K] into
+// 8-bit codes and (step, offset) FP32 pairs [N, K/64]; a group holding Inf or
+// NaN gets a NaN step, which the caller turns into H3Q_ERR_NONFINITE.
+cudaError_t launch_quantize_weights_affine(const void* w, int w_dtype, int64_t N, int64_t K,
+                                           uint8_t* q, float* ab, cudaStream_t s);
+
 // A3 + A4 on the tcgen05 tensor cores (exact INT32 via FP16 MMA with chunked
 // FP32 accumulation).  act_f16: [M, gemm_tc_coded_ld(K)] FP16-coded INT8
 // activations, the padding beyond K zero.

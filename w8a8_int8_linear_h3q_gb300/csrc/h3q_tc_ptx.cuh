@@ -423,6 +423,42 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
 // INT8 x4 (one 32-bit word) -> two FP16x2 words holding the same integers,
 // exactly: bias each byte to b = q + 128 (XOR 0x80), splice it under the FP16
 // exponent of 1024 (0x64xx encodes 1024 + b), subtract 1152.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+  return (1u << 4)                                   // D format: F32
+         | (1u << 7) | (1u << 10)                    // A, B format: BF16
+         | (static_cast<uint32_t>(n >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(m >> 4) << 24);    // M / 16
+}
+
+// Four unsigned 8-bit codes -> four BF16 values a q + b (a and b the same in
+// both halves of a2 and b2): each byte, placed under the exponent of 2^23 by a
+// byte permute (selector nibbles 7, 6, 5 take the constant's upper bytes, the
+// last one the code's byte), becomes the FP32 2^23 + q (exact),
+// minus 2^23 (exact), one FMA (one rounding), then BF16 (round to nearest
+// even).  lo holds codes 0 and 1, hi codes 2 and 3, the first in the low half.
+__device__ __forceinline__ void u8x4_affine_to_bf16x4(uint32_t w, uint64_t a2, uint64_t b2,
+                                                      uint32_t& lo, uint32_t& hi) {
+  const uint32_t base = 0x4B000000u;                  // FP32 2^23
+  uint32_t f0, f1, f2, f3;
+  asm("prmt.b32 %0, %1, %2, 0x7650;" : "=r"(f0) : "r"(w), "r"(base));
+  asm("prmt.b32 %0, %1, %2, 0x7651;" : "=r"(f1) : "r"(w), "r"(base));
+  asm("prmt.b32 %0, %1, %2, 0x7652;" : "=r"(f2) : "r"(w), "r"(base));
+  asm("prmt.b32 %0, %1, %2, 0x7653;" : "=r"(f3) : "r"(w), "r"(base));
+  const uint64_t two23 = 0x4B0000004B000000ull;
+  const uint64_t p01 = (uint64_t(f1) << 32) | f0, p23 = (uint64_t(f3) << 32) | f2;
+  uint64_t q01, q23, r01, r23;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(q01) : "l"(p01), "l"(two23));
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(q23) : "l"(p23), "l"(two23));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r01) : "l"(q01), "l"(a2), "l"(b2));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r23) : "l"(q23), "l"(a2), "l"(b2));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;"
+      : "=r"(lo)
+      : "f"(__uint_as_float(uint32_t(r01 >> 32))), "f"(__uint_as_float(uint32_t(r01))));
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;"
+      : "=r"(hi)
+      : "f"(__uint_as_float(uint32_t(r23 >> 32))), "f"(__uint_as_float(uint32_t(r23))));
+}
+
 __device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t t = w ^ 0x80808080u;
   uint32_t a, b;
