@@ -260,9 +260,9 @@ def run_gpu(args):
 
     # A2, the weight-norm pre-pass (which returns at once when the activations
     # alone settle exactness), one single-accumulator GEMM launch for all four
-    # Linears and per Linear the chunked GEMM (which exits at once when no
-    # tile needs it), after a memset of the workspace's status words
-    launches_per_step = 3 + len(LINEARS)
+    # Linears and one chunked GEMM launch for all four (which exits at once
+    # when no tile needs it), after a memset of the workspace's status words
+    launches_per_step = 4
 
     for _ in range(args.warmup):
         flush.zero_()

@@ -102,18 +102,17 @@ h3q_status run_linear(const uint16_t* x, int8_t* xq, float* xs, const h3q::Linea
   if (h3q_status st =
           from_cuda(h3q::launch_weight_norms(grp, N, K, amax, M, nwpart, stream)))
     return st;
-  // A3 + A4: the tiles that are exact over the whole K, of every Linear in
-  // one launch; then, per Linear, the rest in K chunks (an empty launch when
-  // there are none).
+  // A3 + A4: the tiles kept on one accumulator (exact over the whole K, or
+  // through checked checkpoints), of every Linear in one launch; then the
+  // rest of every Linear in K chunks, in one more launch (which exits at
+  // once when there are none).
   if (h3q_status st = from_cuda(h3q::launch_gemm_wide(act, xs, grp, M, N, K, amax, nwpart,
                                                       status, list, stream)))
     return st;
   const size_t cap = h3q::fallback_list_capacity(M, N);
-  for (int g = 0; g < grp.G; ++g)
-    if (h3q_status st = from_cuda(h3q::launch_gemm_tc(act, xs, grp.wq[g], grp.ws[g], grp.bias[g],
-                                                      M, N, K, grp.y[g], grp.acc[g], status,
-                                                      list + g * cap, status + 2 + g, stream)))
-      return st;
+  if (h3q_status st = from_cuda(h3q::launch_gemm_tc(act, xs, grp, M, N, K, status, list,
+                                                    status + 2, cap, stream)))
+    return st;
   return H3Q_OK;
 }
 

@@ -117,6 +117,8 @@ struct __align__(1024) Smem {
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;   // + slack for 1024-byte alignment
 
 struct Shape {
+  int G;              // Linears of the call (they share the activations)
+  int list_cap;       // entries of one Linear's list
   int M, N, K;
   int KB;             // k-blocks
   int NSS;            // super-stages per tile
@@ -127,38 +129,65 @@ struct Shape {
   int tiles;          // cluster tiles: mt * ntc
 };
 
-// Cluster tile t -> token block mb and the channel block nb of CTA `rank`
-// (nb >= nt for the spare CTA of an odd channel-block count).  With a list,
-// entry t names the tile: {token block, channel-block pair}.
-__device__ __forceinline__ void tile_coords(const Shape& s, const uint2* list, int t,
-                                            uint32_t rank, int& mb, int& nb) {
+// The weight maps and per-Linear operands of a call's G Linears.
+struct Linears {
+  CUtensorMap w[kMaxGroup];
+  const float* sw[kMaxGroup];
+  const uint16_t* bias[kMaxGroup];
+  uint16_t* y[kMaxGroup];
+  int32_t* acc[kMaxGroup];
+};
+
+// Cluster tile t -> Linear g, token block mb and the channel block nb of CTA
+// `rank` (nb >= nt for the spare CTA of an odd channel-block count).  With
+// lists, the tiles run through Linear 0's list, then Linear 1's, ... (cnt:
+// the lists' lengths), and an entry names the tile: {token block,
+// channel-block pair}.
+__device__ __forceinline__ void tile_coords(const Shape& s, const uint2* list,
+                                            const uint32_t (&cnt)[kMaxGroup], int t,
+                                            uint32_t rank, int& g, int& mb, int& nb) {
   if (list) {
-    const uint2 e = list[t];
+    g = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxGroup - 1; ++i)
+      if (g == i && t >= int(cnt[i])) {
+        t -= int(cnt[i]);
+        g = i + 1;
+      }
+    const uint2 e = list[int64_t(g) * s.list_cap + t];
     mb = int(e.x);
     nb = int(e.y) * CLUSTER + int(rank);
     return;
   }
+  g = 0;
   const int per_group = GROUP_M * s.ntc;
-  const int g = t / per_group;
-  const int first_m = g * GROUP_M;
+  const int grp = t / per_group;                 // raster group of GROUP_M token blocks
+  const int first_m = grp * GROUP_M;
   const int gm = min(GROUP_M, s.mt - first_m);
-  const int r = t - g * per_group;
+  const int r = t - grp * per_group;
   mb = first_m + r % gm;
   nb = (r / gm) * CLUSTER + int(rank);
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
-               const __grid_constant__ CUtensorMap w_map, const float* __restrict__ sa,
-               const float* __restrict__ sw, const uint16_t* __restrict__ bias, const Shape shp,
-               uint16_t* __restrict__ Y, int32_t* __restrict__ ACC, uint32_t* __restrict__ err,
+gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constant__ Linears lin,
+               const float* __restrict__ sa, const Shape shp, uint32_t* __restrict__ err,
                const uint2* __restrict__ list, const uint32_t* __restrict__ list_len) {
-  // With a list this grid may be scheduled before the kernel that writes the
-  // list has finished (programmatic dependent launch): wait for it first.
-  // Every CTA then reads the same tile count, so all leave together (before
-  // any cluster barrier) when there is nothing to do.
+  // With lists this grid may be scheduled before the kernel that writes them
+  // has finished (programmatic dependent launch): wait for it first.  Every
+  // CTA then reads the same tile counts, so all leave together (before any
+  // cluster barrier) when there is nothing to do.
   if (list) ptx::grid_dependency_wait();
-  const int ntiles = list ? int(*list_len) : shp.tiles;
+  uint32_t cnt[kMaxGroup] = {};
+  int ntiles = shp.tiles;
+  if (list) {
+    ntiles = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxGroup; ++i) {
+      cnt[i] = i < shp.G ? list_len[i] : 0u;
+      ntiles += int(cnt[i]);
+    }
+  }
   if (ntiles == 0) return;
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -200,8 +229,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
       uint32_t gs = 0, gb = 0;             // super-stages seen, slots issued
       bool ok = true;
       for (int t = cid; ok && t < ntiles; t += ncl) {
-        int mb, nb;
-        tile_coords(shp, list, t, rank, mb, nb);
+        int g, mb, nb;
+        tile_coords(shp, list, cnt, t, rank, g, mb, nb);
         for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
           const uint32_t slot = gs % SLOTS;
           // the slot is free once both CTAs' MMAs finished its previous use
@@ -227,12 +256,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
   } else if (warp == WPROD_WARP) {
     // ---------------- TMA producer: INT8 weight tiles ----------------
     if (lane == 0) {
-      P::tma_prefetch_desc(&w_map);
+      for (int i = 0; i < shp.G; ++i) P::tma_prefetch_desc(&lin.w[i]);
       uint32_t gs = 0, gw = 0;
       bool ok = true;
       for (int t = cid; ok && t < ntiles; t += ncl) {
-        int mb, nb;
-        tile_coords(shp, list, t, rank, mb, nb);
+        int g, mb, nb;
+        tile_coords(shp, list, cnt, t, rank, g, mb, nb);
         const int wrow = min(nb, shp.nt - 1) * BM;
         for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
           const uint32_t slot = gs % W_SLOTS;
@@ -244,7 +273,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
           P::mbar_arrive_expect_tx(&sm.full_w[slot], (SS / 2) * W_BOX_BYTES);
 #pragma unroll
           for (int p = 0; p < SS / 2; ++p)
-            P::tma_load_2d(P::smem_u32(sm.w[slot][p]), &w_map, &sm.full_w[slot],
+            P::tma_load_2d(P::smem_u32(sm.w[slot][p]), &lin.w[g], &sm.full_w[slot],
                            (ss * SS + 2 * p) * BK, wrow);
           gw = gs + 1;
         }
@@ -360,8 +389,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
     uint32_t gc = 0;
     bool ok = true;
     for (int t = cid; ok && t < ntiles; t += ncl) {
-      int mb, nb;
-      tile_coords(shp, list, t, rank, mb, nb);
+      int g, mb, nb;
+      tile_coords(shp, list, cnt, t, rank, g, mb, nb);
       const int n = nb * BM + 32 * q + lane;
       const bool n_ok = n < shp.N;
       int rs[64];                                 // exact INT32 running sums
@@ -387,7 +416,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map,
       }
       if (!ok) break;
       // final: dequantise the exact INT32 sums of this tile
-      const float swn = n_ok ? sw[n] : 0.f;
+      const uint16_t* bias = lin.bias[g];
+      uint16_t* Y = lin.y[g];
+      int32_t* ACC = lin.acc[g];
+      const float swn = n_ok ? lin.sw[g][n] : 0.f;
       const float bn = (n_ok && bias) ? bf16_bits_to_float(bias[n]) : 0.f;
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
@@ -458,10 +490,9 @@ WorkspaceLayout workspace_layout(int64_t M, int64_t N, int64_t K, int G) {
   return l;
 }
 
-cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_t* qw,
-                           const float* sw, const uint16_t* bias, int64_t M, int64_t N,
-                           int64_t K, uint16_t* y, int32_t* acc, uint32_t* err,
-                           const uint2* list, const uint32_t* list_len, cudaStream_t s) {
+cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const LinearGroup& grp,
+                           int64_t M, int64_t N, int64_t K, uint32_t* err, const uint2* list,
+                           const uint32_t* list_len, size_t list_cap, cudaStream_t s) {
   EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder());
   if (!enc) return cudaErrorNotSupported;
   // activations: a [M, ld] FP16 matrix viewed as (64-element chunk, row, chunk index),
@@ -476,17 +507,27 @@ cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_
           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  // weights: [N, K] INT8, boxes of 128 rows x 128 bytes (two k-blocks)
-  CUtensorMap wmap;
+  // weights: [N, K] INT8 per Linear, boxes of 128 rows x 128 bytes (two k-blocks)
+  Linears lin = {};
   const cuuint64_t wdims[2] = {cuuint64_t(K), cuuint64_t(N)};
   const cuuint64_t wstrides[1] = {cuuint64_t(K)};
   const cuuint32_t wbox[2] = {2 * BK, BM};
-  if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(qw), wdims, wstrides,
-          wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+  for (int g = 0; g < kMaxGroup; ++g) {
+    // unused entries repeat the first Linear's (never read)
+    const int src = g < grp.G ? g : 0;
+    if (enc(&lin.w[g], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(grp.wq[src]), wdims,
+            wstrides, wbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    lin.sw[g] = grp.ws[src];
+    lin.bias[g] = grp.bias[src];
+    lin.y[g] = grp.y[src];
+    lin.acc[g] = grp.acc[src];
+  }
 
   Shape shp;
+  shp.G = list ? grp.G : 1;
+  shp.list_cap = int(list_cap);
   shp.M = int(M);
   shp.N = int(N);
   shp.K = int(K);
@@ -507,7 +548,9 @@ cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_
   e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(kSmemBytes));
   if (e != cudaSuccess) return e;
-  const int clusters = shp.tiles < sms / CLUSTER ? shp.tiles : sms / CLUSTER;
+  // with lists, as many clusters as the largest possible list total asks
+  const int64_t max_tiles = list ? int64_t(shp.G) * shp.tiles : shp.tiles;
+  const int clusters = max_tiles < sms / CLUSTER ? int(max_tiles) : sms / CLUSTER;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(clusters * CLUSTER));
   cfg.blockDim = dim3(THREADS);
@@ -522,8 +565,7 @@ cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = list ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, map, wmap, sa, sw, bias, shp, y, acc, err,
-                            list, list_len);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, map, lin, sa, shp, err, list, list_len);
 }
 
 }  // namespace h3q

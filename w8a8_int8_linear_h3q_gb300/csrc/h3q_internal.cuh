@@ -121,16 +121,15 @@ cudaError_t launch_quantize_weights_affine(const void* w, int w_dtype, int64_t N
                                            uint8_t* q, float* ab, cudaStream_t s);
 
 // A3 + A4 on the tcgen05 tensor cores (exact INT32 via FP16 MMA with chunked
-// FP32 accumulation).  act_f16: [M, gemm_tc_coded_ld(K)] FP16-coded INT8
-// activations, the padding beyond K zero.
+// FP32 accumulation) for the G Linears of grp.  act_f16: [M,
+// gemm_tc_coded_ld(K)] FP16-coded INT8 activations, the padding beyond K zero.
 // err: device status word (0 = ok; bits set when a bounded wait gave up).
-// list == NULL: every tile.  Otherwise only the *list_len tiles in `list`
-// (entries written by the wide kernel); the kernel exits at once when the
-// list is empty.
-cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const int8_t* qw,
-                           const float* sw, const uint16_t* bias, int64_t M, int64_t N,
-                           int64_t K, uint16_t* y, int32_t* acc, uint32_t* err,
-                           const uint2* list, const uint32_t* list_len, cudaStream_t s);
+// list == NULL: every tile of Linear 0.  Otherwise the tiles in the G lists
+// (Linear g's at list + g * list_cap, list_len[g] entries, written by the wide
+// kernel); the kernel exits at once when every list is empty.
+cudaError_t launch_gemm_tc(const uint16_t* act_f16, const float* sa, const LinearGroup& grp,
+                           int64_t M, int64_t N, int64_t K, uint32_t* err, const uint2* list,
+                           const uint32_t* list_len, size_t list_cap, cudaStream_t s);
 
 // cuTensorMapEncodeTiled, looked up through the runtime (no -lcuda); NULL if
 // the driver does not provide it.
