@@ -524,7 +524,64 @@ def legacy_tops(h3q, x, wq, wsc, bias, dev, reps=5):
     return 2 * M * N * K * reps / (a.elapsed_time(b) * 1e-3) / 1e12
 
 
-CONFIG_TABLE = ("tiny", "attn", "fc1", "fc2", "image_qkv", "image_gate_up", "image_down")
+CONFIG_TABLE = ("tiny", "attn", "fc1", "fc2", "image_qkv", "image_gate_up", "image_down",
+                "sweep_block")
+
+
+def run_sweep_block(h3q, synth, dev, flush, steps, warmup, peaks):
+    """One block of the 300-Linear sweep at M = 75647 tokens (device-generated
+    inputs, block 0): Q, K, V, O as one grouped call, then FC1 and FC2, each
+    from BF16 X.  The 50 blocks differ only in their weights, so the sweep's
+    time is 50 block times."""
+    import statistics
+    import torch
+    xs_bf = {K: synth.sweep_x(K, dev) for K in (synth.H3_WIDTH, synth.H3_MLP_WIDTH)}
+    lin = []
+    for j, (_, N, K) in enumerate(synth.SWEEP_LINEARS):
+        w, b = synth.sweep_weight(0, j, dev)
+        q, sc = h3q.h3q_quantize_weights(w)
+        del w
+        lin.append((q, sc, b, N, K))
+    M = synth.SWEEP_M
+    attn = lin[:4]
+    xs = torch.empty((M,), dtype=torch.float32, device=dev)
+    ya = [torch.empty((M, attn[0][3]), dtype=torch.bfloat16, device=dev) for _ in attn]
+    gws = torch.empty((h3q.h3q_linear_grouped_workspace_bytes(4, M, attn[0][3], attn[0][4]),),
+                      dtype=torch.uint8, device=dev)
+    mlp = []
+    for q, sc, b, N, K in lin[4:]:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty((h3q.h3q_linear_workspace_bytes(M, N, K),), dtype=torch.uint8,
+                         device=dev)
+        mlp.append((q, sc, b, N, K, y, ws))
+
+    def block():
+        h3q.h3q_linear_w8a8_grouped(xs_bf[synth.H3_WIDTH], [a[0] for a in attn],
+                                    [a[1] for a in attn], [a[2] for a in attn], xs=xs, ys=ya,
+                                    workspace=gws)
+        for q, sc, b, N, K, y, ws in mlp:
+            h3q.h3q_linear_w8a8(xs_bf[K], q, sc, b, xs=xs, y=y, workspace=ws)
+
+    for _ in range(warmup):
+        block()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        block()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)
+    t = statistics.median(ts)
+    ops = sum(2 * M * N * K for _, _, _, N, K in lin)
+    return {"workload": "sweep_block", "M": M, "linears": 6, "reps": steps,
+            "block_us": t, "block_tops": ops / t / 1e6,
+            "block_frac_of_bf16_peak": ops / t / 1e6 / peaks["bf16_tflops"],
+            "sweep_50_blocks_ms": 50 * t / 1e3,
+            "note": "Q,K,V,O grouped + FC1 + FC2, each from BF16 X (A2 included); "
+                    "50 blocks extrapolated from block 0"}
 
 
 def run_configs(args):
@@ -545,6 +602,11 @@ def run_configs(args):
     flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
     names = args.configs.split(",") if args.configs != "all" else CONFIG_TABLE
     for name in names:
+        if name == "sweep_block":
+            print(json.dumps(run_sweep_block(h3q, synth, dev, flush, min(args.steps, 10),
+                                             args.warmup, peaks)), flush=True)
+            torch.cuda.empty_cache()
+            continue
         case = synth.WORKLOADS[name]()
         x = torch.from_numpy(case.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
         w_dev = torch.from_numpy(case.w[0]).to(dev)
