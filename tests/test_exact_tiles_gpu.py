@@ -301,3 +301,35 @@ def test_norm_maxima_from_bf16_input(lib, oracle, dev, M, K):
         assert int(full[b]) == int(a2[rows].sum(1).max())
         for s in range(SEGS):
             assert int(seg[b, s]) == int(a2[rows, s * sl:(s + 1) * sl].sum(1).max())
+
+
+def test_tile_paths_and_outputs_are_deterministic(lib, oracle, dev):
+    # R9: every output is bitwise identical run to run, whichever way each tile
+    # went.  Here tiles take all three ways (one accumulator, checkpoints, the
+    # chunked kernel): ten calls must agree bit for bit, in their path counts
+    # too.
+    K, M, N = 4096, 900, 520
+    rng = np.random.default_rng(14)
+    xq = rng.integers(-127, 128, (M, K)).astype(np.int8)              # checkpoints hold
+    xq[:256] = np.round(rng.uniform(-1, 1, (256, K)) * 20).astype(np.int8)   # one accumulator
+    xq[512:768] = (np.where(rng.random(256) < 0.5, -127, 127)[:, None] *
+                   np.ones(K, np.int64)).astype(np.int8)              # chunked against wq[:256]
+    wq = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    wq[:256] = np.where(rng.random((256, K)) < 0.5, -127, 127)
+    xs = rng.uniform(2.0 ** -12, 2.0 ** -11, M).astype(np.float32)
+    ws = rng.uniform(2.0 ** -12, 2.0 ** -11, N).astype(np.float32)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    paths = tile_paths(xq, wq)
+    assert paths[0] > 0 and paths[1] > 0
+    first = None
+    for _ in range(10):
+        out = lib.h3q_linear_w8a8(None, t(wq), t(ws), None, xq=t(xq), xs=t(xs), want_acc=True)
+        got = (lib.h3q_linear_chunked_tiles(out["workspace"], M, K),
+               lib.h3q_linear_checkpointed_tiles(out["workspace"], M, K))
+        assert got == paths
+        y = out["y"].view(torch.int16).clone()
+        if first is None:
+            first = (y, out["acc"].clone())
+            check_exact(out["acc"].cpu().numpy(), oracle.gemm_int32(xq, wq), "acc")
+        else:
+            assert torch.equal(y, first[0]) and torch.equal(out["acc"], first[1])
