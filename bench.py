@@ -36,6 +36,10 @@ OPS_PER_STEP = 2 * M * N * K * len(LINEARS)
 WORKLOAD = ("attn projection: X BF16 [8192,5376] N(0,1)+0.5% x30 outliers; Q,K,V,O W [5376,5376] "
             "N(0,0.02)->per-channel INT8 + FP32 scales; BF16 bias N(0,0.1); seed 1")
 L2_FLUSH_BYTES = 512 << 20
+# The dense INT8 tensor rate of this part: sm_103a has no tcgen05 INT8 MMA, so
+# it is the legacy mma.sync m16n8k32 s8 instruction's, measured with
+# independent MMA chains on all 152 SMs (the design notes give the probe).
+INT8_DENSE_PEAK_TOPS = 150.0
 
 
 def _dist():
@@ -396,6 +400,12 @@ def run_gpu(args):
                        "chunked_tiles_per_linear": chunked,
                        "tiles_per_linear": -(-M // 128) * -(-N // 256)},
             "roofline": roofline,
+            "pct_of_dense_int8_peak": 100.0 * value / INT8_DENSE_PEAK_TOPS,
+            "dense_int8_peak": {"value": INT8_DENSE_PEAK_TOPS, "unit": "TOPS",
+                                "source": "measured: legacy mma.sync m16n8k32 s8, the only INT8 "
+                                          "tensor instruction of sm_103a; this path computes "
+                                          "the exact INT8 products on the FP16 tensor pipe "
+                                          "instead, see roofline"},
             "kernels": {"legacy_mma_sync_s8_tops": legacy_tops(h3q, x, wq[0], wsc[0], bias[0], dev),
                         "quantize_act_us": quant_avg_s * 1e6,
                         "quantize_act_gbs": quant_bytes / quant_avg_s / 1e9,
