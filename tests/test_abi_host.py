@@ -137,3 +137,32 @@ def test_grouped_linear_rejects_bad_args(cdll):
     assert f(A, NUL, A, 3, P3, P3, NUL, 4, 8, 60, P3, A, ws, NUL) == 2         # K % 16
     assert f(A, NUL, A, 3, P3, one_mis, NUL, 4, 8, 64, P3, A, ws, NUL) == 3    # misaligned scale
     assert f(A, NUL, A, 3, P3, P3, one_mis, 4, 8, 64, P3, A, ws, NUL) == 3     # misaligned bias
+
+
+def test_affine_entry_points_reject_bad_args(cdll):
+    q = cdll.h3q_quantize_weights_affine
+    # w, dtype, N, K, q_out, ab_out, stream
+    assert q(A, 2, 4, 64, A, A, NUL) == 1                # bad dtype
+    assert q(NUL, 0, 4, 64, A, A, NUL) == 1              # null weights
+    assert q(A, 0, 4, 64, A, NUL, NUL) == 1              # null (step, offset) output
+    assert q(A, 0, 4, 96, A, A, NUL) == 2                # K not a multiple of 64
+    assert q(A, 0, 0, 64, A, A, NUL) == 2                # N = 0
+    assert q(A, 0, 4, 64, MIS, A, NUL) == 3              # misaligned codes
+    f = cdll.h3q_linear_affine_w8
+    # x, q, ab, bias, M, N, K, y, status, stream
+    assert f(NUL, A, A, NUL, 4, 8, 64, A, A, NUL) == 1   # null x
+    assert f(A, A, A, NUL, 4, 8, 64, NUL, A, NUL) == 1   # null y
+    assert f(A, A, A, NUL, 4, 8, 64, A, NUL, NUL) == 1   # null status word
+    assert f(A, A, A, NUL, 4, 8, 80, A, A, NUL) == 2     # K % 64
+    assert f(A, A, A, NUL, 0, 8, 64, A, A, NUL) == 2     # M = 0
+    assert f(A, A, A, MIS, 4, 8, 64, A, A, NUL) == 3     # misaligned bias
+    assert f(A, A, MIS, NUL, 4, 8, 64, A, A, NUL) == 3   # misaligned steps
+
+
+def test_chunk_diagnostics_reject_bad_args(cdll):
+    n = ctypes.c_int64(0)
+    for fn in (cdll.h3q_linear_chunked_tiles, cdll.h3q_linear_checkpointed_tiles):
+        assert fn(NUL, 4, 64, ctypes.byref(n), NUL) == 1
+        assert fn(A, 4, 64, NUL, NUL) == 1
+        assert fn(A, 0, 64, ctypes.byref(n), NUL) == 2
+        assert fn(MIS, 4, 64, ctypes.byref(n), NUL) == 3
