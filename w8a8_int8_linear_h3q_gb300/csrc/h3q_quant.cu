@@ -577,10 +577,11 @@ int8_to_f16_kernel(const int8_t* __restrict__ q, int K, int ldh, uint16_t* __res
 // Weight-row norms for the GEMM's exactness test.  Every block first checks
 // whether any block of 256 tokens could fail the test against the largest
 // possible weight row (sum q^2 <= 128^2 K); if none can, the GEMM never reads
-// the norms and the block returns at once.  Otherwise block b (16 warps) sums
-// q^2 over weight rows 16b .. 16b+15 with DP4A on 16-byte loads, per norm
-// segment, and writes the largest whole-row sum to part[b] and the largest
-// sum of each segment s to part[nblocks + b * kNormSegs + s].  The sums are
+// the norms and the block returns at once.  Otherwise, for each group b of 16
+// weight rows (16b .. 16b+15; the blocks stride over the groups), the block's
+// 16 warps sum q^2 with DP4A on 16-byte loads, per norm segment, and write the
+// largest whole-row sum to part[b] and the largest sum of each segment s to
+// part[nblocks + b * kNormSegs + s].  The sums are
 // taken modulo 2^32, which is exact: K * 128^2 < 2^32 for every supported K.
 constexpr int kNormRows = 16;
 
@@ -589,7 +590,7 @@ struct WeightPtrs {
 };
 
 __global__ void __launch_bounds__(32 * kNormRows)
-weight_norm_kernel(const WeightPtrs wqs, int64_t N, int K, int blocks_per_linear,
+weight_norm_kernel(const WeightPtrs wqs, int64_t N, int K, int blocks_per_linear, int nblocks,
                    const uint32_t* __restrict__ amax, int mt2, uint32_t* __restrict__ part,
                    int seg_len) {
   // the quantiser that wrote amax may still be finishing (programmatic
@@ -606,52 +607,57 @@ weight_norm_kernel(const WeightPtrs wqs, int64_t N, int K, int blocks_per_linear
   __syncthreads();
   if (!needed) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // block b covers rows 16 (b mod blocks_per_linear) .. + 15 of Linear b / blocks_per_linear
-  const int g = int(blockIdx.x) / blocks_per_linear;
-  const int8_t* __restrict__ wq = wqs.w[g];
-  const int64_t n = int64_t(int(blockIdx.x) - g * blocks_per_linear) * kNormRows + warp;
-  SegSq sq;
-  if (n < N) {
-    // a 16-byte vector never straddles two segments (they are multiples of 128)
-    const uint4* row = reinterpret_cast<const uint4*>(wq + n * K);
-    const int nv = K >> 4;
-    int i = lane;
-    for (; i + 96 < nv; i += 128) {
-      uint4 v[4];
+  // grid-stride over the row groups: group b covers rows 16 (b mod
+  // blocks_per_linear) .. + 15 of Linear b / blocks_per_linear (a small grid,
+  // so that the early return above costs one wave of blocks)
+  for (int b = blockIdx.x; b < nblocks; b += gridDim.x) {
+    const int g = b / blocks_per_linear;
+    const int8_t* __restrict__ wq = wqs.w[g];
+    const int64_t n = int64_t(b - g * blocks_per_linear) * kNormRows + warp;
+    SegSq sq;
+    if (n < N) {
+      // a 16-byte vector never straddles two segments (they are multiples of 128)
+      const uint4* row = reinterpret_cast<const uint4*>(wq + n * K);
+      const int nv = K >> 4;
+      int i = lane;
+      for (; i + 96 < nv; i += 128) {
+        uint4 v[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = __ldg(row + i + 32 * u);
+        for (int u = 0; u < 4; ++u) v[u] = __ldg(row + i + 32 * u);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint32_t t = uint32_t(__dp4a(int(v[u].x), int(v[u].x), 0));
-        t = uint32_t(__dp4a(int(v[u].y), int(v[u].y), int(t)));
-        t = uint32_t(__dp4a(int(v[u].z), int(v[u].z), int(t)));
-        t = uint32_t(__dp4a(int(v[u].w), int(v[u].w), int(t)));
-        sq.add(16 * (i + 32 * u), seg_len, t);
+        for (int u = 0; u < 4; ++u) {
+          uint32_t t = uint32_t(__dp4a(int(v[u].x), int(v[u].x), 0));
+          t = uint32_t(__dp4a(int(v[u].y), int(v[u].y), int(t)));
+          t = uint32_t(__dp4a(int(v[u].z), int(v[u].z), int(t)));
+          t = uint32_t(__dp4a(int(v[u].w), int(v[u].w), int(t)));
+          sq.add(16 * (i + 32 * u), seg_len, t);
+        }
+      }
+      for (; i < nv; i += 32) {
+        const uint4 v = __ldg(row + i);
+        uint32_t t = uint32_t(__dp4a(int(v.x), int(v.x), 0));
+        t = uint32_t(__dp4a(int(v.y), int(v.y), int(t)));
+        t = uint32_t(__dp4a(int(v.z), int(v.z), int(t)));
+        t = uint32_t(__dp4a(int(v.w), int(v.w), int(t)));
+        sq.add(16 * i, seg_len, t);
       }
     }
-    for (; i < nv; i += 32) {
-      const uint4 v = __ldg(row + i);
-      uint32_t t = uint32_t(__dp4a(int(v.x), int(v.x), 0));
-      t = uint32_t(__dp4a(int(v.y), int(v.y), int(t)));
-      t = uint32_t(__dp4a(int(v.z), int(v.z), int(t)));
-      t = uint32_t(__dp4a(int(v.w), int(v.w), int(t)));
-      sq.add(16 * i, seg_len, t);
-    }
-  }
-  sq.warp_sum();
-  if (lane == 0) sq.store(&red[warp]);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t m = 0;
-    uint4 ms = make_uint4(0, 0, 0, 0);
+    sq.warp_sum();
+    if (lane == 0) sq.store(&red[warp]);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t m = 0;
+      uint4 ms = make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int w = 0; w < kNormRows; ++w) {
-      const uint4 r = red[w];
-      m = max(m, r.x + r.y + r.z + r.w);
-      ms = make_uint4(max(ms.x, r.x), max(ms.y, r.y), max(ms.z, r.z), max(ms.w, r.w));
+      for (int w = 0; w < kNormRows; ++w) {
+        const uint4 r = red[w];
+        m = max(m, r.x + r.y + r.z + r.w);
+        ms = make_uint4(max(ms.x, r.x), max(ms.y, r.y), max(ms.z, r.z), max(ms.w, r.w));
+      }
+      part[b] = m;
+      reinterpret_cast<uint4*>(part + nblocks)[b] = ms;
     }
-    part[blockIdx.x] = m;
-    reinterpret_cast<uint4*>(part + gridDim.x)[blockIdx.x] = ms;
+    __syncthreads();                              // red[] is rewritten next round
   }
 }
 
@@ -777,8 +783,15 @@ cudaError_t launch_weight_norms(const LinearGroup& grp, int64_t N, int64_t K,
   WeightPtrs wqs = {};
   for (int g = 0; g < grp.G; ++g) wqs.w[g] = grp.wq[g];
   const int per = static_cast<int>((N + 127) / 128 * kNormParts);
+  const int nblocks = per * grp.G;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(per) * static_cast<unsigned>(grp.G));
+  // one wave of resident blocks (four of 512 threads per SM)
+  cfg.gridDim = dim3(static_cast<unsigned>(nblocks < 4 * sms ? nblocks : 4 * sms));
   cfg.blockDim = dim3(32 * kNormRows);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -787,8 +800,8 @@ cudaError_t launch_weight_norms(const LinearGroup& grp, int64_t N, int64_t K,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const int mt2 = static_cast<int>((M + kNormTokens - 1) / kNormTokens);
-  return cudaLaunchKernelEx(&cfg, weight_norm_kernel, wqs, N, static_cast<int>(K), per, amax,
-                            mt2, nwpart, norm_segment_len(K));
+  return cudaLaunchKernelEx(&cfg, weight_norm_kernel, wqs, N, static_cast<int>(K), per, nblocks,
+                            amax, mt2, nwpart, norm_segment_len(K));
 }
 
 cudaError_t launch_int8_to_f16(const int8_t* q, int64_t M, int64_t K, int64_t ldh,
