@@ -265,6 +265,20 @@ h3q_status h3q_linear_affine_w8(const uint16_t* x, const uint8_t* q, const float
                                 uint16_t* y, uint32_t* status, cudaStream_t stream);
 
 /*
+ * Self-test of the device-side failure path (no counterpart on the pages).
+ * Every wait in the library's kernels is bounded: after the limit (2 s) the
+ * kernel sets a bit in the call's status word and returns, and the call then
+ * reports H3Q_ERR_TIMEOUT through h3q_workspace_status instead of hanging the
+ * GPU.  This entry point drives that path on purpose, without a fault: one
+ * thread waits with the same helper on an mbarrier that nothing arrives on.
+ *   status  one device uint32 (4-byte aligned), zeroed by the call
+ * Returns H3Q_ERR_TIMEOUT when the wait gave up and reported it (the expected
+ * result; the context stays usable), H3Q_OK if it did not.  SYNCHRONISES
+ * `stream`; takes about 2 s.
+ */
+h3q_status h3q_selftest_bounded_wait(uint32_t* status, cudaStream_t stream);
+
+/*
  * A3 + A4 on the legacy warp-level INT8 tensor instruction (mma.sync
  * m16n8k32 s8 -> s32), exact by construction; the same arithmetic and output
  * as h3q_linear_w8a8 from pre-quantised activations.  Kept as the baseline

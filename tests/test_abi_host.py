@@ -166,3 +166,8 @@ def test_chunk_diagnostics_reject_bad_args(cdll):
         assert fn(A, 4, 64, NUL, NUL) == 1
         assert fn(A, 0, 64, ctypes.byref(n), NUL) == 2
         assert fn(MIS, 4, 64, ctypes.byref(n), NUL) == 3
+
+
+def test_selftest_rejects_bad_args(cdll):
+    assert cdll.h3q_selftest_bounded_wait(NUL, NUL) == 1
+    assert cdll.h3q_selftest_bounded_wait(ctypes.c_void_p(0x10002), NUL) == 3

@@ -63,6 +63,8 @@ def _declare(lib):
     lib.h3q_linear_w8a8_mma_sync.restype = i32
     lib.h3q_linear_w8a8_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
     lib.h3q_linear_w8a8_noalloc.restype = i32
+    lib.h3q_selftest_bounded_wait.argtypes = [vp, vp]
+    lib.h3q_selftest_bounded_wait.restype = i32
     lib.h3q_quantize_weights_affine.argtypes = [vp, i32, i64, i64, vp, vp, vp]
     lib.h3q_quantize_weights_affine.restype = i32
     lib.h3q_linear_affine_w8.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
@@ -187,6 +189,15 @@ def h3q_linear_affine_w8(x, q, ab, bias=None, *, y=None, status=None, stream=Non
     _check(load().h3q_linear_affine_w8(_ptr(x), _ptr(q), _ptr(ab), _ptr(bias), M, N, K, _ptr(y),
                                        _ptr(status), _stream(stream)), "h3q_linear_affine_w8")
     return {"y": y, "status": status}
+
+
+def h3q_selftest_bounded_wait(status=None, stream=None) -> int:
+    """Drive a device-side bounded wait to its limit (about 2 s).  Returns the
+    status code: H3Q_ERR_TIMEOUT is the expected, healthy result."""
+    import torch
+    if status is None:
+        status = torch.empty((4,), dtype=torch.int32, device="cuda")
+    return int(load().h3q_selftest_bounded_wait(_ptr(status), _stream(stream)))
 
 
 def h3q_quantize_act(x, q_out=None, scale_out=None, stream=None):
