@@ -333,3 +333,20 @@ def test_tile_paths_and_outputs_are_deterministic(lib, oracle, dev):
             check_exact(out["acc"].cpu().numpy(), oracle.gemm_int32(xq, wq), "acc")
         else:
             assert torch.equal(y, first[0]) and torch.equal(out["acc"], first[1])
+
+
+@pytest.mark.parametrize("K", [1152, 1408])
+def test_checkpoints_with_uneven_segments(lib, oracle, dev, K):
+    # K = 1152: nine super-stages in segments of 3, 3, 3 and an empty fourth;
+    # K = 1408: eleven in 3, 3, 3, 2.  Random +-127 codes fail the whole-K test
+    # (|a|^2 |w|^2 up to 2 x 2^48) but hold with one checkpoint before the third
+    # segment; the planner must skip the empty segment and size the last run
+    # from the segments that exist
+    M, N = 300, 520
+    rng = np.random.default_rng(15 + K)
+    xq = np.where(rng.random((M, K)) < 0.5, -127, 127).astype(np.int8)
+    wq = np.where(rng.random((N, K)) < 0.5, -127, 127).astype(np.int8)
+    xs = np.full(M, 2.0 ** -9, np.float32)
+    ws = np.full(N, 2.0 ** -9, np.float32)
+    _, paths = _run(lib, oracle, dev, xq, wq, xs, ws, None)
+    assert paths == (0, math.ceil(M / 256) * math.ceil(N / 256))
