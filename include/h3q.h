@@ -16,8 +16,9 @@
  *        Linear adds the bias before the single rounding of the output).
  *
  * Conventions shared by every entry point
- *   - All tensor pointers are DEVICE pointers owned by the caller.  The
- *     library allocates no device memory and keeps no per-call state.
+ *   - All tensor pointers are DEVICE pointers owned by the caller, except the
+ *     host buffers of h3q_linear_w8a8_grouped_host.  The library allocates no
+ *     device memory and keeps no per-call state.
  *   - Layouts are dense and row-major with the last dimension contiguous:
  *     activations X [M, K] (tokens x in-features), weights W [N, K]
  *     (out-features x in-features, the nn.Linear layout), outputs [M, N].
@@ -198,6 +199,65 @@ h3q_status h3q_linear_w8a8_grouped(const uint16_t* x, int8_t* xq, float* xs, int
  */
 h3q_status h3q_workspace_status(const void* workspace, int64_t M, int64_t K,
                                 cudaStream_t stream);
+
+/*
+ * Bytes of device workspace for h3q_linear_w8a8_grouped_host: a grouped
+ * workspace for one chunk of min(chunk_rows, M) rows, then one status word
+ * per chunk.  0 if G is outside 1..4, a size is < 1, or chunk_rows is not a
+ * positive multiple of 16.
+ */
+size_t h3q_linear_w8a8_grouped_host_workspace_bytes(int G, int64_t M, int64_t N, int64_t K,
+                                                    int64_t chunk_rows);
+
+/*
+ * The grouped Linear (h3q_linear_w8a8_grouped, A2 + A3 + A4 with A2 once)
+ * from and to page-locked HOST memory: the one entry point that takes host
+ * pointers.  X is uploaded, and the G outputs downloaded, in row chunks that
+ * overlap both copy directions with the grouped calls.  The host link is the
+ * bound, and the outputs are G times the input, so the first chunks are small
+ * and the downloads start early: chunk sizes run first_rows, 2*first_rows, ...
+ * up to chunk_rows, then chunk_rows until M is covered.  Each output row is
+ * that of h3q_linear_w8a8_grouped on the same operands, bit for bit (the row
+ * chunks do not change any row's arithmetic: A2 is per token, and each output
+ * element depends on its own token row only).
+ *
+ *   x_host     [M, K] BF16, page-locked host memory (cudaHostAlloc or
+ *              cudaHostRegister); read.
+ *   G, wq, ws, bias
+ *              as in h3q_linear_w8a8_grouped (device pointers).
+ *   y_host     host array of G page-locked host pointers, [M, N] BF16 each;
+ *              written.
+ *   x_dev      [M, K] BF16 device staging for X; overwritten.
+ *   xs         [M] FP32 device; the activation scales are written.
+ *   y_dev      host array of G device pointers, [M, N] BF16 each; the
+ *              outputs are written there too.
+ *   chunk_rows steady chunk size, a positive multiple of 16.
+ *   first_rows first chunk size, a multiple of 16 in [16, chunk_rows];
+ *              0 picks chunk_rows / 4 rounded up to a multiple of 16.
+ *   workspace  >= h3q_linear_w8a8_grouped_host_workspace_bytes(G, M, N, K,
+ *              chunk_rows) bytes of device memory.
+ *   stream     the grouped calls run here; the copy streams start after the
+ *              work already queued on it.
+ *   h2d_stream, d2h_stream
+ *              the upload and download streams.  Overlap needs three distinct
+ *              streams that do not synchronise with one another (non-blocking
+ *              streams); equal streams still give the right result, serially.
+ *
+ * SYNCHRONISES: returns once y_host holds every output (or, after a failure,
+ * once nothing it enqueued is still running).  Returns H3Q_ERR_TIMEOUT if a
+ * bounded device-side wait of any chunk gave up; argument errors (including
+ * pageable host memory: H3Q_ERR_INVALID_ARG) come before anything is
+ * enqueued.  The library keeps a few CUDA events per device across calls
+ * (created on first use); calls from several host threads take turns.
+ */
+h3q_status h3q_linear_w8a8_grouped_host(const uint16_t* x_host, int G, const int8_t* const* wq,
+                                        const float* const* ws, const uint16_t* const* bias,
+                                        int64_t M, int64_t N, int64_t K,
+                                        uint16_t* const* y_host, uint16_t* x_dev, float* xs,
+                                        uint16_t* const* y_dev, int64_t chunk_rows,
+                                        int64_t first_rows, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream,
+                                        cudaStream_t h2d_stream, cudaStream_t d2h_stream);
 
 /*
  * Diagnostic: how many tiles of 128 tokens x 256 channels the last

@@ -171,3 +171,56 @@ def test_chunk_diagnostics_reject_bad_args(cdll):
 def test_selftest_rejects_bad_args(cdll):
     assert cdll.h3q_selftest_bounded_wait(NUL, NUL) == 1
     assert cdll.h3q_selftest_bounded_wait(ctypes.c_void_p(0x10002), NUL) == 3
+
+
+def test_host_pipeline_rejects_bad_args(cdll):
+    size = cdll.h3q_linear_w8a8_grouped_host_workspace_bytes
+    ws = size(2, 100, 8, 64, 32)
+    assert ws >= cdll.h3q_linear_grouped_workspace_bytes(2, 32, 8, 64)
+    assert size(2, 100, 8, 64, 24) == 0                  # chunk rows not a multiple of 16
+    assert size(2, 100, 8, 64, 0) == 0
+    assert size(0, 100, 8, 64, 32) == 0                  # G outside 1..4
+    assert size(5, 100, 8, 64, 32) == 0
+    assert size(2, 0, 8, 64, 32) == 0
+    # a chunk larger than M is sized for M rows
+    assert size(2, 20, 8, 64, 4096) < size(2, 4096, 8, 64, 4096)
+    f = cdll.h3q_linear_w8a8_grouped_host
+    arr = lambda *p: (ctypes.c_void_p * len(p))(*p)
+    P2 = arr(0x10000, 0x20000)
+    one_null = arr(0x10000, None)
+    one_mis = arr(0x10000, 0x10008)
+    # x_host, G, wq, ws, bias, M, N, K, y_host, x_dev, xs, y_dev, chunk, first,
+    # workspace, bytes, stream, h2d, d2h
+    def call(x_host=A, G=2, wq=P2, sc=P2, bias=NUL, M=100, N=8, K=64, y_host=P2, x_dev=A,
+             xs=A, y_dev=P2, chunk=32, first=0, work=A, nbytes=ws):
+        return f(x_host, G, wq, sc, bias, M, N, K, y_host, x_dev, xs, y_dev, chunk, first,
+                 work, nbytes, NUL, NUL, NUL)
+    assert call(G=0) == 1
+    assert call(G=5) == 1
+    assert call(x_host=NUL) == 1
+    assert call(y_host=NUL) == 1
+    assert call(y_host=one_null) == 1                    # a NULL host output
+    assert call(y_dev=one_null) == 1                     # a NULL device output
+    assert call(wq=one_null) == 1
+    assert call(xs=NUL) == 1
+    assert call(work=NUL) == 1
+    assert call(chunk=24) == 1                           # chunk rows not a multiple of 16
+    assert call(first=8) == 1                            # first chunk not a multiple of 16
+    assert call(first=48) == 1                           # first chunk above the steady size
+    assert call(nbytes=ws - 256) == 1                    # workspace too small
+    assert call(K=60) == 2                               # K % 16
+    assert call(M=0) == 2
+    assert call(x_host=MIS) == 3
+    assert call(y_dev=one_mis) == 3
+    assert call(y_host=one_mis) == 3
+    assert call(xs=MIS) == 3
+
+
+def test_host_pipeline_without_a_device_reports_no_device(cdll):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: this checks the no-device report only")
+    P2 = (ctypes.c_void_p * 2)(0x10000, 0x20000)
+    ws = cdll.h3q_linear_w8a8_grouped_host_workspace_bytes(2, 100, 8, 64, 32)
+    assert cdll.h3q_linear_w8a8_grouped_host(A, 2, P2, P2, NUL, 100, 8, 64, P2, A, A, P2, 32,
+                                             16, A, ws, NUL, NUL, NUL) == 7

@@ -55,6 +55,13 @@ def _declare(lib):
                                             ctypes.POINTER(vp), i64, i64, i64, ctypes.POINTER(vp),
                                             vp, sz, vp]
     lib.h3q_linear_w8a8_grouped.restype = i32
+    lib.h3q_linear_w8a8_grouped_host_workspace_bytes.argtypes = [i32, i64, i64, i64, i64]
+    lib.h3q_linear_w8a8_grouped_host_workspace_bytes.restype = sz
+    lib.h3q_linear_w8a8_grouped_host.argtypes = [vp, i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                                 ctypes.POINTER(vp), i64, i64, i64,
+                                                 ctypes.POINTER(vp), vp, vp, ctypes.POINTER(vp),
+                                                 i64, i64, vp, sz, vp, vp, vp]
+    lib.h3q_linear_w8a8_grouped_host.restype = i32
     lib.h3q_linear_chunked_tiles.argtypes = [vp, i64, i64, ctypes.POINTER(i64), vp]
     lib.h3q_linear_chunked_tiles.restype = i32
     lib.h3q_linear_checkpointed_tiles.argtypes = [vp, i64, i64, ctypes.POINTER(i64), vp]
@@ -105,6 +112,18 @@ def _need(t, dtype, shape, name):
     import torch
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _need_pinned(t, dtype, shape, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_pinned():
+        raise TypeError(f"{name} must be a page-locked (pinned) CPU tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -338,6 +357,71 @@ def h3q_linear_w8a8_grouped(x, wqs, wss, biases=None, *, xq=None, xs=None, ys=No
         None if biases is None else arr(biases), M, N, K, arr(ys), _ptr(workspace), wbytes,
         _stream(stream)), "h3q_linear_w8a8_grouped")
     return {"ys": ys, "xs": xs, "workspace": workspace}
+
+
+def h3q_linear_w8a8_grouped_host_workspace_bytes(G: int, M: int, N: int, K: int,
+                                                 chunk_rows: int) -> int:
+    return int(load().h3q_linear_w8a8_grouped_host_workspace_bytes(G, M, N, K, chunk_rows))
+
+
+def h3q_linear_w8a8_grouped_host(x_host, wqs, wss, biases=None, *, ys_host=None, x_dev=None,
+                                 xs=None, ys_dev=None, chunk_rows=2048, first_rows=0,
+                                 workspace=None, stream=None, h2d_stream=None, d2h_stream=None):
+    """The grouped Linear from and to page-locked host memory: ``x_host`` is a
+    pinned CPU BF16 tensor [M, K]; the outputs ``ys`` are pinned CPU BF16
+    tensors [M, N].  X goes up and the outputs come down in row chunks that
+    overlap the copies with the grouped calls (on ``stream``; the copies on
+    ``h2d_stream`` and ``d2h_stream``).  Device staging (``x_dev``, ``xs``,
+    ``ys_dev``), the workspace, the host outputs and the copy streams are
+    allocated here when not given.  Synchronises.  Returns a dict with ``ys``
+    (host), ``ys_dev``, ``x_dev``, ``xs`` and the ``workspace``."""
+    import torch
+    G = len(wqs)
+    if not 1 <= G <= 4 or len(wss) != G or (biases is not None and len(biases) != G):
+        raise ValueError("1..4 Linears, with one scale vector (and bias) each")
+    for w in wqs:
+        _need(w, torch.int8, tuple(wqs[0].shape), "wq")
+    N, K = wqs[0].shape
+    dev = wqs[0].device
+    _need_pinned(x_host, torch.bfloat16, None, "x_host")
+    M = x_host.shape[0]
+    if x_host.shape[1] != K:
+        raise ValueError("x_host and wq disagree on K")
+    for sc in wss:
+        _need(sc, torch.float32, (N,), "ws")
+    if biases is not None:
+        for b in biases:
+            if b is not None:
+                _need(b, torch.bfloat16, (N,), "bias")
+    if ys_host is None:
+        ys_host = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(G)]
+    for y in ys_host:
+        _need_pinned(y, torch.bfloat16, (M, N), "y_host")
+    if x_dev is None:
+        x_dev = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    if xs is None:
+        xs = torch.empty((M,), dtype=torch.float32, device=dev)
+    if ys_dev is None:
+        ys_dev = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(G)]
+    _need(x_dev, torch.bfloat16, (M, K), "x_dev")
+    _need(xs, torch.float32, (M,), "xs")
+    for y in ys_dev:
+        _need(y, torch.bfloat16, (M, N), "y_dev")
+    need = h3q_linear_w8a8_grouped_host_workspace_bytes(G, M, N, K, chunk_rows)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
+    wbytes = workspace.numel() * workspace.element_size()
+    if h2d_stream is None:
+        h2d_stream = torch.cuda.Stream(dev)
+    if d2h_stream is None:
+        d2h_stream = torch.cuda.Stream(dev)
+    arr = lambda ts: (ctypes.c_void_p * G)(*[None if t is None else t.data_ptr() for t in ts])
+    _check(load().h3q_linear_w8a8_grouped_host(
+        _ptr(x_host), G, arr(wqs), arr(wss), None if biases is None else arr(biases), M, N, K,
+        arr(ys_host), _ptr(x_dev), _ptr(xs), arr(ys_dev), chunk_rows, first_rows,
+        _ptr(workspace), wbytes, _stream(stream), _stream(h2d_stream), _stream(d2h_stream)),
+        "h3q_linear_w8a8_grouped_host")
+    return {"ys": ys_host, "ys_dev": ys_dev, "x_dev": x_dev, "xs": xs, "workspace": workspace}
 
 
 def h3q_linear_chunked_tiles(workspace, M: int, K: int, stream=None) -> int:

@@ -5,13 +5,16 @@
 #include <cstdlib>
 #include <vector>
 
+#include "h3q_abi_checks.cuh"
 #include "h3q_internal.cuh"
 
-namespace {
+namespace h3q {
 
+namespace {
 constexpr int64_t kMaxK = 133143;            // K * 127^2 < 2^31
 constexpr int64_t kMaxRows = (int64_t(1) << 31) - 65536;
 constexpr int64_t kMaxN = int64_t(65535) * 128;
+}  // namespace
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -44,8 +47,15 @@ h3q_status from_cuda(cudaError_t e) {
   return H3Q_ERR_CUDA;
 }
 
-// The launch sequence of a (grouped) Linear call; the per-Linear pointers are
-// already checked.
+}  // namespace h3q
+
+namespace {
+
+using h3q::aligned16;
+using h3q::check_device;
+using h3q::check_shape;
+using h3q::from_cuda;
+
 // Word `index` of the status block of a workspace last used with (M, K).
 h3q_status read_status_word(const void* workspace, int64_t M, int64_t K, int index,
                             int64_t* value, cudaStream_t stream) {
@@ -63,6 +73,8 @@ h3q_status read_status_word(const void* workspace, int64_t M, int64_t K, int ind
   return H3Q_OK;
 }
 
+// The launch sequence of a (grouped) Linear call; the per-Linear pointers are
+// already checked.
 h3q_status run_linear(const uint16_t* x, int8_t* xq, float* xs, const h3q::LinearGroup& grp,
                       int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream) {
