@@ -286,24 +286,28 @@ h3q_status h3q_linear_checkpointed_tiles(const void* workspace, int64_t M, int64
 
 /*
  * The group-wise affine comparison scheme (weight-only; "MLX implementation and
- * experiment report", Operator tuning: Q8/g64 GEMMs; "[feat] Add MiniMax H3 MLX
- * T2VA inference": affine INT8 checkpoints).  Not the W8A8 method: the
- * activations stay BF16, and the weights carry a step and an offset per output
- * channel and group of 64 inputs.  Offline quantisation:
+ * experiment report", Operator tuning: Q8/g64 and Q4/g64 GEMMs; "[feat] Add
+ * MiniMax H3 MLX T2VA inference": affine INT8/INT6/INT4 checkpoints).  Not the
+ * W8A8 method: the activations stay BF16, and the weights carry a step and an
+ * offset per output channel and group of 64 inputs.  Offline quantisation:
  *
  *   w       [N, K] FP32 (w_dtype = H3Q_DTYPE_F32) or BF16 bits, K a multiple of 64
- *   q_out   [N, K] unsigned 8-bit codes
+ *   bits    8 (Q8/g64) or 4 (Q4/g64)
+ *   q_out   [N, K] unsigned codes in [0, 2^bits - 1], one per byte (4-bit codes
+ *           are not packed: the GEMM reads both widths alike)
  *   ab_out  [N, K/64][2] FP32: per group the step a and the offset b, so that
  *           the group's weights are represented by a q + b
  *
- * Per group: b = min, a = (max - min) / 255 (each an FP32 operation, rounded to
- * nearest even; a = 1 for a constant group, the smallest positive FP32 when
- * the quotient underflows), q = clamp(rint((w - b) / a), 0, 255).  Returns
+ * Per group, with L = 2^bits - 1: b = min, a = (max - min) / L (each an FP32
+ * operation, rounded to nearest even; a = 1 for a constant group, the
+ * smallest positive FP32 when the quotient underflows), q = clamp(rint((w -
+ * b) / a), 0, L).  Returns H3Q_ERR_INVALID_ARG for another bits,
  * H3Q_ERR_NONFINITE if any weight is Inf or NaN, H3Q_ERR_UNSUPPORTED_SHAPE if
  * K is not a multiple of 64.  SYNCHRONISES `stream` (offline call).
  */
-h3q_status h3q_quantize_weights_affine(const void* w, int w_dtype, int64_t N, int64_t K,
-                                       uint8_t* q_out, float* ab_out, cudaStream_t stream);
+h3q_status h3q_quantize_weights_affine(const void* w, int w_dtype, int bits, int64_t N,
+                                       int64_t K, uint8_t* q_out, float* ab_out,
+                                       cudaStream_t stream);
 
 /*
  * The weight-only Linear of the comparison scheme:

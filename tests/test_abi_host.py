@@ -141,13 +141,15 @@ def test_grouped_linear_rejects_bad_args(cdll):
 
 def test_affine_entry_points_reject_bad_args(cdll):
     q = cdll.h3q_quantize_weights_affine
-    # w, dtype, N, K, q_out, ab_out, stream
-    assert q(A, 2, 4, 64, A, A, NUL) == 1                # bad dtype
-    assert q(NUL, 0, 4, 64, A, A, NUL) == 1              # null weights
-    assert q(A, 0, 4, 64, A, NUL, NUL) == 1              # null (step, offset) output
-    assert q(A, 0, 4, 96, A, A, NUL) == 2                # K not a multiple of 64
-    assert q(A, 0, 0, 64, A, A, NUL) == 2                # N = 0
-    assert q(A, 0, 4, 64, MIS, A, NUL) == 3              # misaligned codes
+    # w, dtype, bits, N, K, q_out, ab_out, stream
+    assert q(A, 2, 8, 4, 64, A, A, NUL) == 1             # bad dtype
+    assert q(NUL, 0, 8, 4, 64, A, A, NUL) == 1           # null weights
+    assert q(A, 0, 8, 4, 64, A, NUL, NUL) == 1           # null (step, offset) output
+    for bits in (0, 2, 6, 16):
+        assert q(A, 0, bits, 4, 64, A, A, NUL) == 1      # only 8 and 4 bits
+    assert q(A, 0, 4, 4, 96, A, A, NUL) == 2             # K not a multiple of 64
+    assert q(A, 0, 8, 0, 64, A, A, NUL) == 2             # N = 0
+    assert q(A, 0, 8, 4, 64, MIS, A, NUL) == 3           # misaligned codes
     f = cdll.h3q_linear_affine_w8
     # x, q, ab, bias, M, N, K, y, status, stream
     assert f(NUL, A, A, NUL, 4, 8, 64, A, A, NUL) == 1   # null x

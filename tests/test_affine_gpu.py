@@ -1,5 +1,5 @@
 """GPU parity of the group-wise affine comparison scheme (weight-only; "MLX
-implementation and experiment report", Operator tuning: Q8/g64).
+implementation and experiment report", Operator tuning: Q8/g64 and Q4/g64).
 
 Bar: codes, steps and offsets bit-exact against the oracle; the Linear's BF16
 outputs within one BF16 ulp plus the FP32 accumulation bound K 2^-23
@@ -46,16 +46,18 @@ def _check_affine_y(oracle, y_bits, ref, K):
     return float(np.max(err / tol))
 
 
+@pytest.mark.parametrize("bits", [8, 4])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_quantize_weights_affine_matches_oracle(lib, oracle, dev, dtype):
+def test_quantize_weights_affine_matches_oracle(lib, oracle, dev, dtype, bits):
     rng = np.random.default_rng(80)
     w = (rng.standard_normal((300, 1024)) * 0.02).astype(np.float32)
     w[3, 64:128] = np.float32(0.125)                        # a constant group
     w[7, :64] *= np.float32(1e-36)                          # a tiny-range group
     wt = torch.from_numpy(w).to(dev).to(dtype)
-    q, ab = lib.h3q_quantize_weights_affine(wt)
+    q, ab = lib.h3q_quantize_weights_affine(wt, bits=bits)
     w_in = wt.float().cpu().numpy()                          # the values the kernel saw
-    oq, oa, ob = oracle.quantize_affine(w_in)
+    oq, oa, ob = oracle.quantize_affine(w_in, bits=bits)
+    assert int(q.max()) == 2 ** bits - 1 and int(q.min()) == 0
     assert np.array_equal(q.cpu().numpy(), oq)
     got = ab.cpu().numpy()
     assert np.array_equal(got[:, :, 0].view(np.uint32), oa.view(np.uint32))
@@ -71,18 +73,20 @@ def test_quantize_weights_affine_rejects_non_finite(lib, dev, bad):
     assert e.value.status == lib.H3Q_ERR_NONFINITE
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 1, 64), (7, 3, 128), (129, 264, 192), (300, 100, 5376),
-                                   (33, 520, 14336), (517, 300, 1024)])
-def test_linear_affine_parity_ragged(lib, oracle, dev, M, N, K):
+@pytest.mark.parametrize("M,N,K,bits", [(1, 1, 64, 8), (7, 3, 128, 8), (129, 264, 192, 8),
+                                        (300, 100, 5376, 8), (33, 520, 14336, 8),
+                                        (517, 300, 1024, 8), (7, 3, 128, 4), (300, 100, 5376, 4),
+                                        (517, 300, 1024, 4)])
+def test_linear_affine_parity_ragged(lib, oracle, dev, M, N, K, bits):
     rng = np.random.default_rng(M * 7 + N + K)
     xb = oracle.round_to_bf16(rng.standard_normal((M, K)))
     w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
     bias = oracle.round_to_bf16(rng.standard_normal(N) * 0.1)
-    q, ab = lib.h3q_quantize_weights_affine(torch.from_numpy(w).to(dev))
+    q, ab = lib.h3q_quantize_weights_affine(torch.from_numpy(w).to(dev), bits=bits)
     out = lib.h3q_linear_affine_w8(_bf16_dev(xb, dev), q, ab, _bf16_dev(bias, dev))
     torch.cuda.synchronize()
     assert int(out["status"][0]) == 0
-    oq, oa, ob = oracle.quantize_affine(w)
+    oq, oa, ob = oracle.quantize_affine(w, bits=bits)
     ref = oracle.linear_affine(xb, oracle.dequant_affine(oq, oa, ob), bias)
     _check_affine_y(oracle, _bits(out["y"]), ref, K)
 

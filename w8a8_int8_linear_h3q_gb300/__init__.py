@@ -72,7 +72,7 @@ def _declare(lib):
     lib.h3q_linear_w8a8_noalloc.restype = i32
     lib.h3q_selftest_bounded_wait.argtypes = [vp, vp]
     lib.h3q_selftest_bounded_wait.restype = i32
-    lib.h3q_quantize_weights_affine.argtypes = [vp, i32, i64, i64, vp, vp, vp]
+    lib.h3q_quantize_weights_affine.argtypes = [vp, i32, i32, i64, i64, vp, vp, vp]
     lib.h3q_quantize_weights_affine.restype = i32
     lib.h3q_linear_affine_w8.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
     lib.h3q_linear_affine_w8.restype = i32
@@ -168,10 +168,11 @@ def h3q_quantize_weights(w, q_out=None, scale_out=None, stream=None):
     return q_out, scale_out
 
 
-def h3q_quantize_weights_affine(w, q_out=None, ab_out=None, stream=None):
+def h3q_quantize_weights_affine(w, q_out=None, ab_out=None, stream=None, bits=8):
     """The group-wise affine comparison scheme, offline: FP32 or BF16 weight
-    [N, K] (K a multiple of 64) -> (uint8 codes [N, K], FP32 (step, offset)
-    pairs [N, K/64, 2]).  Synchronises."""
+    [N, K] (K a multiple of 64) -> (uint8 codes [N, K] in [0, 2^bits - 1], FP32
+    (step, offset) pairs [N, K/64, 2]); bits 8 (Q8/g64) or 4 (Q4/g64, one code
+    per byte).  Synchronises."""
     import torch
     if w.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("weights must be float32 or bfloat16")
@@ -183,8 +184,9 @@ def h3q_quantize_weights_affine(w, q_out=None, ab_out=None, stream=None):
     _need(q_out, torch.uint8, (N, K), "q_out")
     _need(ab_out, torch.float32, (N, K // 64, 2), "ab_out")
     dt = H3Q_DTYPE_F32 if w.dtype == torch.float32 else H3Q_DTYPE_BF16
-    _check(load().h3q_quantize_weights_affine(_ptr(w), dt, N, K, _ptr(q_out), _ptr(ab_out),
-                                              _stream(stream)), "h3q_quantize_weights_affine")
+    _check(load().h3q_quantize_weights_affine(_ptr(w), dt, bits, N, K, _ptr(q_out),
+                                              _ptr(ab_out), _stream(stream)),
+           "h3q_quantize_weights_affine")
     return q_out, ab_out
 
 

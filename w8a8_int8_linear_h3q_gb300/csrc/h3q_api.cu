@@ -256,16 +256,18 @@ h3q_status h3q_linear_checkpointed_tiles(const void* workspace, int64_t M, int64
   return read_status_word(workspace, M, K, 6, tiles, stream);
 }
 
-h3q_status h3q_quantize_weights_affine(const void* w, int w_dtype, int64_t N, int64_t K,
-                                       uint8_t* q_out, float* ab_out, cudaStream_t stream) {
+h3q_status h3q_quantize_weights_affine(const void* w, int w_dtype, int bits, int64_t N,
+                                       int64_t K, uint8_t* q_out, float* ab_out,
+                                       cudaStream_t stream) {
   if (!w || !q_out || !ab_out) return H3Q_ERR_INVALID_ARG;
   if (w_dtype != H3Q_DTYPE_F32 && w_dtype != H3Q_DTYPE_BF16) return H3Q_ERR_INVALID_ARG;
+  if (bits != 8 && bits != 4) return H3Q_ERR_INVALID_ARG;
   if (h3q_status st = check_shape(1, N, K)) return st;
   if (K % 64) return H3Q_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(w) || !aligned16(q_out) || !aligned16(ab_out)) return H3Q_ERR_MISALIGNED;
   if (h3q_status st = check_device()) return st;
-  if (h3q_status st = from_cuda(h3q::launch_quantize_weights_affine(w, w_dtype, N, K, q_out,
-                                                                    ab_out, stream)))
+  if (h3q_status st = from_cuda(h3q::launch_quantize_weights_affine(w, w_dtype, bits, N, K,
+                                                                    q_out, ab_out, stream)))
     return st;
   // Offline call: read the steps back and reject any NaN-marked (non-finite) group.
   std::vector<float> host(static_cast<size_t>(N) * size_t(K / 64) * 2);

@@ -115,10 +115,11 @@ cudaError_t launch_gemm_affine(const uint16_t* x, const LinearGroup& grp, const 
                                int64_t M, int64_t N, int64_t K, uint32_t* status, cudaStream_t s);
 
 // Offline group-wise affine quantisation of FP32 or BF16 weights [N, K] into
-// 8-bit codes and (step, offset) FP32 pairs [N, K/64]; a group holding Inf or
-// NaN gets a NaN step, which the caller turns into H3Q_ERR_NONFINITE.
-cudaError_t launch_quantize_weights_affine(const void* w, int w_dtype, int64_t N, int64_t K,
-                                           uint8_t* q, float* ab, cudaStream_t s);
+// `bits`-bit codes (8 or 4; one code per byte) and (step, offset) FP32 pairs
+// [N, K/64]; a group holding Inf or NaN gets a NaN step, which the caller
+// turns into H3Q_ERR_NONFINITE.
+cudaError_t launch_quantize_weights_affine(const void* w, int w_dtype, int bits, int64_t N,
+                                           int64_t K, uint8_t* q, float* ab, cudaStream_t s);
 
 // A3 + A4 on the tcgen05 tensor cores (exact INT32 via FP16 MMA with chunked
 // FP32 accumulation) for the G Linears of grp.  act_f16: [M,

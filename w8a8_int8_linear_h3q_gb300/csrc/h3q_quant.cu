@@ -491,14 +491,15 @@ quant_weight_kernel(const T* __restrict__ w, int64_t N, int K, int8_t* __restric
 
 // Group-wise affine quantisation of weight rows (the comparison scheme;
 // offline, plain): one warp per row, one group of 64 at a time, two values
-// per lane.  Per group: lo, hi = min, max; step = RN(RN(hi - lo) / 255)
-// (1 for a constant group, the smallest positive FP32 if it underflows);
-// offset = lo; q = clamp(rint(RN(RN(w - lo) / step)), 0, 255).  A group with
-// Inf or NaN gets a NaN step and zero codes.
+// per lane.  With L = 2^bits - 1 levels (255 or 15), per group: lo, hi = min,
+// max; step = RN(RN(hi - lo) / L) (1 for a constant group, the smallest
+// positive FP32 if it underflows); offset = lo; q = clamp(rint(RN(RN(w - lo) /
+// step)), 0, L), one code per byte.  A group with Inf or NaN gets a NaN step
+// and zero codes.
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
-quant_weight_affine_kernel(const T* __restrict__ w, int64_t N, int K, uint8_t* __restrict__ q,
-                           float2* __restrict__ ab) {
+quant_weight_affine_kernel(const T* __restrict__ w, int64_t N, int K, int levels,
+                           uint8_t* __restrict__ q, float2* __restrict__ ab) {
   const int lane = threadIdx.x & 31;
   const int64_t row = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   if (row >= N) return;
@@ -515,12 +516,12 @@ quant_weight_affine_kernel(const T* __restrict__ w, int64_t N, int K, uint8_t* _
       lo = fminf(lo, __shfl_xor_sync(0xFFFFFFFFu, lo, o));
       hi = fmaxf(hi, __shfl_xor_sync(0xFFFFFFFFu, hi, o));
     }
-    float step = __fdiv_rn(__fsub_rn(hi, lo), 255.f);
+    float step = __fdiv_rn(__fsub_rn(hi, lo), float(levels));
     if (hi == lo) step = 1.f;
     else if (step == 0.f) step = __int_as_float(1);
     const auto code = [&](float v) {
       const int c = __float2int_rn(__fdiv_rn(__fsub_rn(v, lo), step));
-      return uint8_t(bad ? 0 : max(0, min(255, c)));
+      return uint8_t(bad ? 0 : max(0, min(levels, c)));
     };
     q[row * int64_t(K) + k0] = code(v0);
     q[row * int64_t(K) + k1] = code(v1);
@@ -763,16 +764,17 @@ cudaError_t launch_quantize_weights(const void* w, int w_dtype, int64_t N, int64
   return cudaGetLastError();
 }
 
-cudaError_t launch_quantize_weights_affine(const void* w, int w_dtype, int64_t N, int64_t K,
-                                           uint8_t* q, float* ab, cudaStream_t s) {
+cudaError_t launch_quantize_weights_affine(const void* w, int w_dtype, int bits, int64_t N,
+                                           int64_t K, uint8_t* q, float* ab, cudaStream_t s) {
   const dim3 grid(unsigned((N + kWarps - 1) / kWarps)), block(kWarps * 32);
   float2* ab2 = reinterpret_cast<float2*>(ab);
+  const int levels = (1 << bits) - 1;
   if (w_dtype == H3Q_DTYPE_F32)
     quant_weight_affine_kernel<float><<<grid, block, 0, s>>>(static_cast<const float*>(w), N,
-                                                             int(K), q, ab2);
+                                                             int(K), levels, q, ab2);
   else
     quant_weight_affine_kernel<uint16_t><<<grid, block, 0, s>>>(
-        static_cast<const uint16_t*>(w), N, int(K), q, ab2);
+        static_cast<const uint16_t*>(w), N, int(K), levels, q, ab2);
   return cudaGetLastError();
 }
 
