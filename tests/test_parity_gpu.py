@@ -341,3 +341,27 @@ def test_workspace_status_after_a_normal_call(lib, dev):
     qw, sw = lib.h3q_quantize_weights(torch.from_numpy(c.w[0]).to(dev))
     o = lib.h3q_linear_w8a8(_bf16_dev(c.x_bits, dev), qw, sw, None)
     assert lib.h3q_workspace_status(o["workspace"], 300, 2048) == lib.H3Q_OK
+
+
+def test_output_bits_depend_on_the_operands_only(lib, dev):
+    # A4 forms y from (acc, s_a, s_w, bias) by the same FP32 operations on
+    # every path, so the bits cannot depend on how a row was computed: with or
+    # without the raw accumulators, in one call or in row chunks that end
+    # inside a 32-token block, on the hot kernel or the legacy mma.sync one.
+    # Half a million outputs make near-ties of the BF16 rounding certain, where
+    # two different FP32 evaluations would disagree.
+    M, N, K = 1000, 520, 5376
+    c = synth.make_linear(M, N, K, seed=91, outlier_p=0.005, outlier_mul=30)
+    x = _bf16_dev(c.x_bits, dev)
+    qw, sw = lib.h3q_quantize_weights(torch.from_numpy(c.w[0]).to(dev))
+    b = _bf16_dev(c.bias_bits[0], dev)
+    full = lib.h3q_linear_w8a8(x, qw, sw, b, want_xq=True)
+    with_acc = lib.h3q_linear_w8a8(x, qw, sw, b, want_acc=True)
+    parts = [lib.h3q_linear_w8a8(x[r0:r1].contiguous(), qw, sw, b)["y"]
+             for r0, r1 in ((0, 100), (100, 333), (333, 1000))]
+    legacy = lib.h3q_linear_w8a8_mma_sync(full["xq"], full["xs"], qw, sw, b)
+    torch.cuda.synchronize()
+    ref = full["y"].view(torch.int16)
+    assert torch.equal(with_acc["y"].view(torch.int16), ref)
+    assert torch.equal(torch.cat(parts).view(torch.int16), ref)
+    assert torch.equal(legacy["y"].view(torch.int16), ref)

@@ -49,21 +49,33 @@ static __device__ __noinline__ float epilogue_value_careful(int acc, float sa, f
   return __fadd_rn(s, __fadd_rn(err, t_lo));
 }
 
-// Cheap path first.  P = RN(RN(float(acc) * sa) * sw) carries a relative
-// error below 3 * 2^-24 (three roundings, with the intermediate and P both
-// finite and far above the subnormal range), and v = RN(P + bias) adds at most
-// 2^-24 |v|.  When |v| >= 2^-10 |P| the total is below 2^-12 |v|, far under
-// half a BF16 ulp (>= 2^-9 |v|), so one BF16 rounding of v lands within one
-// ulp of the exact value.  Cancellation (|v| < 2^-10 |P|), a non-finite or
-// tiny P, or a tiny v take the exact path.
+// The scales of the cheap path: s_a zero or in [2^-60, 2^45], s_w in
+// [2^-40, 2^45].  Then c = RN(s_a * s_w) is zero or in [2^-100, 2^90], and for
+// 1 <= |acc| <= 2^31, P = RN(float(acc) * c) is zero or in [2^-100, 2^121]:
+// finite and normal.
+__device__ __forceinline__ bool epilogue_scales_in_range(float sa, float sw) {
+  return (sa == 0.f || (sa >= 0x1p-60f && sa <= 0x1p45f)) && (sw >= 0x1p-40f && sw <= 0x1p45f);
+}
+
+// Cheap path first: c = RN(s_a * s_w), P = RN(float(acc) * c + 0), v = RN(P +
+// bias).  The +0 addend (one fused operation, no extra rounding) makes every
+// zero product +0, whatever the signs of its factors, so a zero accumulator
+// held as -0 in FP32 gives the same bits as the integer 0.
+// float(acc) is exact up to |acc| = 2^24 and within 2^-24 relative above, so P
+// carries a relative error below 3 * 2^-24, and v adds at most 2^-24 |v|.  When
+// |v| >= 2^-10 |P| the total is below 2^-12 |v|, far under half a BF16 ulp
+// (>= 2^-9 |v|), so one BF16 rounding of v lands within one ulp of the exact
+// value.  Cancellation (|v| < 2^-10 |P|) or scales outside the range above
+// take the exact path.  Every kernel forms y by these same operations (the
+// hot kernel's paired FP32 instructions perform them two tokens at a time),
+// so y depends on (acc, s_a, s_w, bias) alone: not on the kernel, the tile or
+// the call that produced the accumulator.
 __device__ __forceinline__ float epilogue_value(int acc, float sa, float sw, float bias) {
-  const float t = __fmul_rn(__int2float_rn(acc), sa);
-  const float p = __fmul_rn(t, sw);
-  const float v = __fadd_rn(p, bias);
-  const float at = fabsf(t), ap = fabsf(p), av = fabsf(v);
-  if (at <= 3.0e38f && at >= 0x1p-100f && ap <= 3.0e38f && ap >= 0x1p-100f &&
-      av >= 0x1p-110f && av >= ap * 0x1p-10f)
-    return v;
+  if (epilogue_scales_in_range(sa, sw)) {
+    const float p = __fmaf_rn(__int2float_rn(acc), __fmul_rn(sa, sw), 0.f);
+    const float v = __fadd_rn(p, bias);
+    if (fabsf(v) >= fabsf(p) * 0x1p-10f) return v;
+  }
   if (acc == 0) return bias;
   return epilogue_value_careful(acc, sa, sw, bias);
 }

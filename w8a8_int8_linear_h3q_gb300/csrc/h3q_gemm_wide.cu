@@ -352,8 +352,9 @@ __device__ __forceinline__ void emit_block(const uint32_t (&d)[32], float sa_l, 
                                            float swn, float bn, int n, bool n_ok,
                                            const Shape& shp, uint16_t* __restrict__ Y,
                                            int32_t* __restrict__ ACC, const float* __restrict__ sa_all) {
-  const bool s_in = (sa_l == 0.f || (sa_l >= 0x1p-60f && sa_l <= 0x1p45f)) &&
-                    (swn >= 0x1p-40f && swn <= 0x1p45f);
+  // every token's scales in the cheap path's range: the paired form of
+  // epilogue_value, bit for bit
+  const bool s_in = epilogue_scales_in_range(sa_l, swn);
   if (__all_sync(0xFFFFFFFFu, s_in) && !ACC && Y && mbase + 32 <= shp.M) {
     uint16_t* yp = Y + int64_t(mbase) * shp.N + n;
     const float* sa_ptr = sa_all + mbase;
@@ -370,7 +371,7 @@ __device__ __forceinline__ void emit_block(const uint32_t (&d)[32], float sa_l, 
       const uint64_t t2 = (uint64_t(d[j + 1]) << 32) | d[j];
       uint64_t c2, p2, v2;
       asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(c2) : "l"(sa2), "l"(sw2));
-      asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p2) : "l"(t2), "l"(c2));
+      asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(p2) : "l"(t2), "l"(c2), "l"(uint64_t(0)));
       asm("add.rn.f32x2 %0, %1, %2;" : "=l"(v2) : "l"(p2), "l"(b2));
       const float pa = __uint_as_float(uint32_t(p2)), pb = __uint_as_float(uint32_t(p2 >> 32));
       float va = __uint_as_float(uint32_t(v2)), vb = __uint_as_float(uint32_t(v2 >> 32));
