@@ -210,6 +210,16 @@ size_t h3q_linear_w8a8_grouped_host_workspace_bytes(int G, int64_t M, int64_t N,
                                                     int64_t chunk_rows);
 
 /*
+ * The row chunks h3q_linear_w8a8_grouped_host makes of M rows with these
+ * chunk_rows and first_rows (0 = the default first chunk): returns how many
+ * there are, and writes the first min(count, capacity) chunk sizes to
+ * rows_out (which may be NULL).  Returns -1 for arguments the pipeline
+ * rejects.  Host-only: touches no device.
+ */
+int64_t h3q_linear_w8a8_grouped_host_chunks(int64_t M, int64_t chunk_rows, int64_t first_rows,
+                                            int64_t* rows_out, int64_t capacity);
+
+/*
  * The grouped Linear (h3q_linear_w8a8_grouped, A2 + A3 + A4 with A2 once)
  * from and to page-locked HOST memory: the one entry point that takes host
  * pointers.  X is uploaded, and the G outputs downloaded, in row chunks that

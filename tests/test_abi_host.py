@@ -226,3 +226,38 @@ def test_host_pipeline_without_a_device_reports_no_device(cdll):
     ws = cdll.h3q_linear_w8a8_grouped_host_workspace_bytes(2, 100, 8, 64, 32)
     assert cdll.h3q_linear_w8a8_grouped_host(A, 2, P2, P2, NUL, 100, 8, 64, P2, A, A, P2, 32,
                                              16, A, ws, NUL, NUL, NUL) == 7
+
+
+@pytest.mark.parametrize("M,chunk,first", [(8192, 2048, 0), (8192, 1024, 256), (77, 16, 16),
+                                           (1000, 256, 64), (5, 2048, 0), (2048, 2048, 2048),
+                                           (75647, 4096, 16), (1, 16, 0)])
+def test_host_pipeline_chunk_plan(cdll, M, chunk, first):
+    # the plan the pinned-host pipeline follows: it covers M exactly; chunks
+    # ramp from the first size by doubling up to the steady size; every chunk
+    # but the last is a multiple of 16 rows (so each chunk's row blocks stay
+    # 16-byte aligned); and the count fits the workspace's status slots
+    import w8a8_int8_linear_h3q_gb300 as h3q
+    rows = h3q.h3q_linear_w8a8_grouped_host_chunks(M, chunk, first)
+    assert sum(rows) == M and all(r >= 1 for r in rows)
+    f = first or max(16, -(-(chunk // 4) // 16) * 16)
+    want, r = [], f
+    while sum(want) < M:
+        want.append(min(r, M - sum(want)))
+        r = min(2 * r, chunk)
+    assert rows == want
+    assert all(r % 16 == 0 for r in rows[:-1])
+    slots = len(rows) * 4
+    call = cdll.h3q_linear_grouped_workspace_bytes(2, min(chunk, M), 8, 64)
+    assert cdll.h3q_linear_w8a8_grouped_host_workspace_bytes(2, M, 8, 64, chunk) >= call + slots
+
+
+def test_host_pipeline_chunk_plan_rejects_bad_args(cdll):
+    import w8a8_int8_linear_h3q_gb300 as h3q
+    f = cdll.h3q_linear_w8a8_grouped_host_chunks
+    assert f(0, 32, 0, None, 0) == -1                    # M = 0
+    assert f(100, 24, 0, None, 0) == -1                  # chunk not a multiple of 16
+    assert f(100, 32, 8, None, 0) == -1                  # first not a multiple of 16
+    assert f(100, 32, 48, None, 0) == -1                 # first above the steady size
+    assert f(100, 32, 0, None, 0) == 4                   # count only: 16, 32, 32, 20
+    with pytest.raises(ValueError):
+        h3q.h3q_linear_w8a8_grouped_host_chunks(100, 24)

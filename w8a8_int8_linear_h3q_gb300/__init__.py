@@ -57,6 +57,8 @@ def _declare(lib):
     lib.h3q_linear_w8a8_grouped.restype = i32
     lib.h3q_linear_w8a8_grouped_host_workspace_bytes.argtypes = [i32, i64, i64, i64, i64]
     lib.h3q_linear_w8a8_grouped_host_workspace_bytes.restype = sz
+    lib.h3q_linear_w8a8_grouped_host_chunks.argtypes = [i64, i64, i64, ctypes.POINTER(i64), i64]
+    lib.h3q_linear_w8a8_grouped_host_chunks.restype = i64
     lib.h3q_linear_w8a8_grouped_host.argtypes = [vp, i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
                                                  ctypes.POINTER(vp), i64, i64, i64,
                                                  ctypes.POINTER(vp), vp, vp, ctypes.POINTER(vp),
@@ -364,6 +366,18 @@ def h3q_linear_w8a8_grouped(x, wqs, wss, biases=None, *, xq=None, xs=None, ys=No
 def h3q_linear_w8a8_grouped_host_workspace_bytes(G: int, M: int, N: int, K: int,
                                                  chunk_rows: int) -> int:
     return int(load().h3q_linear_w8a8_grouped_host_workspace_bytes(G, M, N, K, chunk_rows))
+
+
+def h3q_linear_w8a8_grouped_host_chunks(M: int, chunk_rows: int = 2048, first_rows: int = 0) -> list:
+    """Sizes of the row chunks h3q_linear_w8a8_grouped_host makes of M rows."""
+    lib = load()
+    n = int(lib.h3q_linear_w8a8_grouped_host_chunks(M, chunk_rows, first_rows, None, 0))
+    if n < 0:
+        raise ValueError("chunk_rows must be a positive multiple of 16 and first_rows 0 or a "
+                         "multiple of 16 in [16, chunk_rows]; M >= 1")
+    out = (ctypes.c_int64 * n)()
+    lib.h3q_linear_w8a8_grouped_host_chunks(M, chunk_rows, first_rows, out, n)
+    return list(out)
 
 
 def h3q_linear_w8a8_grouped_host(x_host, wqs, wss, biases=None, *, ys_host=None, x_dev=None,

@@ -90,6 +90,17 @@ size_t h3q_linear_w8a8_grouped_host_workspace_bytes(int G, int64_t M, int64_t N,
          round256(size_t(max_chunks(M, chunk_rows)) * sizeof(uint32_t));
 }
 
+int64_t h3q_linear_w8a8_grouped_host_chunks(int64_t M, int64_t chunk_rows, int64_t first_rows,
+                                            int64_t* rows_out, int64_t capacity) {
+  if (M < 1 || chunk_rows < kRowQuantum || chunk_rows % kRowQuantum) return -1;
+  if (first_rows == 0) first_rows = default_first_rows(chunk_rows);
+  if (first_rows < kRowQuantum || first_rows % kRowQuantum || first_rows > chunk_rows) return -1;
+  const std::vector<std::pair<int64_t, int64_t>> plan = chunk_plan(M, chunk_rows, first_rows);
+  for (size_t c = 0; rows_out && c < plan.size() && int64_t(c) < capacity; ++c)
+    rows_out[c] = plan[c].second - plan[c].first;
+  return int64_t(plan.size());
+}
+
 h3q_status h3q_linear_w8a8_grouped_host(const uint16_t* x_host, int G, const int8_t* const* wq,
                                         const float* const* ws, const uint16_t* const* bias,
                                         int64_t M, int64_t N, int64_t K,
