@@ -350,3 +350,41 @@ def test_checkpoints_with_uneven_segments(lib, oracle, dev, K):
     ws = np.full(N, 2.0 ** -9, np.float32)
     _, paths = _run(lib, oracle, dev, xq, wq, xs, ws, None)
     assert paths == (0, math.ceil(M / 256) * math.ceil(N / 256))
+
+
+def test_mixed_paths_match_the_legacy_exact_path(lib, oracle, dev):
+    # 9 token blocks x 9 channel-block pairs = 81 cluster tiles on every path
+    # at once.  Token block 8's activations are all +-127.  Against them,
+    # channel pair 4's +-127 weights fail even the per-segment test (the
+    # chunked kernel takes the tile), pair 5's single-outlier rows pass the
+    # whole-K test (one accumulator), and the Gaussian rows of pairs 6-8 pass
+    # only per segment (checkpoints); the other token blocks mix the first two.
+    # Every output and accumulator must equal the legacy mma.sync path's,
+    # which is exact INT32 by construction, bit for bit.
+    M, N, K = 2304, 2176, 8192
+    rng = np.random.default_rng(95)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x[2048:] = np.where(rng.random((M - 2048, K)) < 0.5, -1.0, 1.0)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    w[1024:1280] = np.where(rng.random((256, K)) < 0.5, -0.02, 0.02)
+    w[1280:1536] = rng.standard_normal((256, K)).astype(np.float32) * 1e-4
+    w[1280:1536, 7] = 0.5
+    xb = oracle.round_to_bf16(x)
+    b = oracle.round_to_bf16(rng.standard_normal(N) * 0.1)
+    qw, sw = lib.h3q_quantize_weights(torch.from_numpy(w).to(dev))
+    xt, bt = _bf16_dev(xb, dev), _bf16_dev(b, dev)
+    out = lib.h3q_linear_w8a8(xt, qw, sw, bt, want_acc=True, want_xq=True)
+    chunked = lib.h3q_linear_chunked_tiles(out["workspace"], M, K)
+    ckpt = lib.h3q_linear_checkpointed_tiles(out["workspace"], M, K)
+    legacy = lib.h3q_linear_w8a8_mma_sync(out["xq"], out["xs"], qw, sw, bt, want_acc=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out["acc"], legacy["acc"])
+    assert torch.equal(out["y"].view(torch.int16), legacy["y"].view(torch.int16))
+    assert chunked >= 2, chunked                    # pair 4 of block 8: two 128-token tiles
+    assert ckpt >= 3, ckpt                          # pairs 6-8 of block 8, at least
+    rows = np.unique(np.concatenate([np.arange(2040, 2056), np.arange(M - 8, M),
+                                     rng.integers(0, M, 16)]))
+    ref = oracle.linear(xb[rows], *oracle.quantize_weights(w), b)
+    rt = torch.from_numpy(rows).to(dev)
+    check_exact(out["acc"][rt].cpu().numpy(), ref["acc"], "acc")
+    check_y(_bits(out["y"][rt]), ref["v"])
