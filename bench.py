@@ -229,7 +229,8 @@ def run_gpu(args):
         wsc.append(s)
         bias.append(torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(dev))
     xs = torch.empty((M,), dtype=torch.float32, device=dev)
-    ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in LINEARS]
+    ys_all = torch.empty((len(LINEARS), M, N), dtype=torch.bfloat16, device=dev)
+    ys = [ys_all[i] for i in range(len(LINEARS))]
     workspace = torch.empty((h3q.h3q_linear_workspace_bytes(M, N, K),), dtype=torch.uint8,
                             device=dev)
     flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
@@ -317,7 +318,10 @@ def run_gpu(args):
     # outputs are four times the input): the library pipelines row chunks on
     # three streams, the first chunks small so that the downloads start early.
     x_pin = x_host.pin_memory()
-    y_pin = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in LINEARS]
+    # the four outputs as one [4, M, N] buffer on each side: a chunk's
+    # downloads are then one copy
+    y_pin_all = torch.empty((len(LINEARS), M, N), dtype=torch.bfloat16).pin_memory()
+    y_pin = [y_pin_all[i] for i in range(len(LINEARS))]
     e2e_steps = 0 if args.no_e2e else max(2, min(args.steps, 5))
     E2E_CHUNK = 2048
     h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)

@@ -240,7 +240,10 @@ int64_t h3q_linear_w8a8_grouped_host_chunks(int64_t M, int64_t chunk_rows, int64
  *   x_dev      [M, K] BF16 device staging for X; overwritten.
  *   xs         [M] FP32 device; the activation scales are written.
  *   y_dev      host array of G device pointers, [M, N] BF16 each; the
- *              outputs are written there too.
+ *              outputs are written there too.  When the G outputs are the
+ *              consecutive [M, N] blocks of one [G, M, N] buffer on each side,
+ *              a chunk's downloads are one 2D copy, which the link carries
+ *              faster (if the runtime refuses that copy, they go one by one).
  *   chunk_rows steady chunk size, a positive multiple of 16.
  *   first_rows first chunk size, a multiple of 16 in [16, chunk_rows];
  *              0 picks chunk_rows / 4 rounded up to a multiple of 16.

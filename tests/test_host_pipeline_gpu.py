@@ -129,3 +129,26 @@ def test_host_pipeline_attn_workload(lib, oracle, dev):
     for g in range(G):
         want = oracle.linear(c.x_bits[rows], *oracle.quantize_weights(c.w[g]), c.bias_bits[g])
         check_y(_bits(out["ys"][g][torch.from_numpy(rows)]), want["v"])
+
+
+def test_host_pipeline_equally_spaced_outputs(lib, oracle, dev):
+    # the G outputs as one [G, M, N] buffer on each side: a chunk's downloads
+    # go as one 2D copy; the results are those of the grouped device call
+    M, N, K, G = 700, 264, 1040, 3
+    c = synth.make_linear(M, N, K, seed=97, n_linears=G, outlier_p=0.005, outlier_mul=30)
+    wq, ws, b = _operands(lib, c, dev, G, drop_bias=True)
+    x_host = _bf16(c.x_bits).pin_memory()
+    yh = torch.zeros((G, M, N), dtype=torch.bfloat16).pin_memory()
+    yd = torch.empty((G, M, N), dtype=torch.bfloat16, device=dev)
+    out = lib.h3q_linear_w8a8_grouped_host(x_host, wq, ws, b, ys_host=[yh[g] for g in range(G)],
+                                           ys_dev=[yd[g] for g in range(G)], chunk_rows=256,
+                                           first_rows=48)
+    ref = lib.h3q_linear_w8a8_grouped(x_host.to(dev), wq, ws, b)
+    torch.cuda.synchronize()
+    for g in range(G):
+        assert _same(yh[g], ref["ys"][g]), f"Linear {g}: host output differs"
+        assert _same(yd[g], ref["ys"][g])
+        want = oracle.linear(c.x_bits, *oracle.quantize_weights(c.w[g]),
+                             None if b[g] is None else c.bias_bits[g])
+        check_y(_bits(yh[g]), want["v"])
+    assert out["ys"][0].data_ptr() == yh[0].data_ptr()

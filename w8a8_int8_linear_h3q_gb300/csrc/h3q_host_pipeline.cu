@@ -161,6 +161,14 @@ h3q_status h3q_linear_w8a8_grouped_host(const uint16_t* x_host, int G, const int
       cudaStreamWaitEvent(d2h_stream, ev_fork, 0) != cudaSuccess)
     return H3Q_ERR_CUDA;
 
+  // The G outputs as one [G, M, N] buffer on each side: a chunk's G
+  // downloads are one 2D copy (fewer, larger copies run faster).  Outputs
+  // that only happen to lie back to back in separate allocations may be
+  // refused as one copy; then the copies go one by one.
+  bool even = G > 1;
+  for (int g = 1; even && g < G; ++g)
+    even = y_host[g] - y_host[g - 1] == M * N && y_dev[g] - y_dev[g - 1] == M * N;
+
   size_t done = 0;  // chunks fully enqueued
   for (size_t c = 0; c < nchunks && st == H3Q_OK; ++c) {
     const int64_t r0 = plan[c].first, rows = plan[c].second - plan[c].first;
@@ -185,10 +193,22 @@ h3q_status h3q_linear_w8a8_grouped_host(const uint16_t* x_host, int G, const int
       st = H3Q_ERR_CUDA;
       break;
     }
-    for (int g = 0; g < G && st == H3Q_OK; ++g)
-      if (cudaMemcpyAsync(y_host[g] + r0 * N, y_dev[g] + r0 * N, size_t(rows * N) * 2u,
-                          cudaMemcpyDeviceToHost, d2h_stream) != cudaSuccess)
-        st = H3Q_ERR_CUDA;
+    if (even) {
+      // the chunk's rows of all G outputs in one copy
+      const size_t pitch = size_t(M * N) * 2u;
+      if (cudaMemcpy2DAsync(y_host[0] + r0 * N, pitch, y_dev[0] + r0 * N, pitch,
+                            size_t(rows * N) * 2u, size_t(G), cudaMemcpyDeviceToHost,
+                            d2h_stream) != cudaSuccess) {
+        cudaGetLastError();   // refused at the call, nothing enqueued
+        even = false;
+      }
+    }
+    if (!even) {
+      for (int g = 0; g < G && st == H3Q_OK; ++g)
+        if (cudaMemcpyAsync(y_host[g] + r0 * N, y_dev[g] + r0 * N, size_t(rows * N) * 2u,
+                            cudaMemcpyDeviceToHost, d2h_stream) != cudaSuccess)
+          st = H3Q_ERR_CUDA;
+    }
     if (st == H3Q_OK) ++done;
   }
   // Join both copy streams into `stream` and wait for everything enqueued,
