@@ -409,8 +409,9 @@ def h3q_linear_w8a8_grouped_host(x_host, wqs, wss, biases=None, *, ys_host=None,
         for b in biases:
             if b is not None:
                 _need(b, torch.bfloat16, (N,), "bias")
-    if ys_host is None:
-        ys_host = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(G)]
+    if ys_host is None:   # one [G, M, N] buffer: a chunk's downloads are then one copy
+        yh = torch.empty((G, M, N), dtype=torch.bfloat16).pin_memory()
+        ys_host = [yh[g] for g in range(G)]
     for y in ys_host:
         _need_pinned(y, torch.bfloat16, (M, N), "y_host")
     if x_dev is None:
@@ -418,7 +419,8 @@ def h3q_linear_w8a8_grouped_host(x_host, wqs, wss, biases=None, *, ys_host=None,
     if xs is None:
         xs = torch.empty((M,), dtype=torch.float32, device=dev)
     if ys_dev is None:
-        ys_dev = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(G)]
+        yd = torch.empty((G, M, N), dtype=torch.bfloat16, device=dev)
+        ys_dev = [yd[g] for g in range(G)]
     _need(x_dev, torch.bfloat16, (M, K), "x_dev")
     _need(xs, torch.float32, (M,), "xs")
     for y in ys_dev:
