@@ -70,14 +70,18 @@ def test_host_pipeline_matches_grouped_call_and_oracle(lib, oracle, dev, M, N, K
 
 
 def test_host_pipeline_on_one_stream(lib, dev):
-    # uploads, calls and downloads all on the current stream: serial, same result
+    # uploads, calls and downloads all on the current stream, into separately
+    # allocated outputs (one download per output and chunk): serial, and the
+    # same result as three streams with one [G, M, N] buffer (2D downloads)
     M, N, K, G = 500, 200, 1040, 2
     c = synth.make_linear(M, N, K, seed=71, n_linears=G)
     wq, ws, b = _operands(lib, c, dev, G, drop_bias=False)
     x_host = _bf16(c.x_bits).pin_memory()
     s = torch.cuda.current_stream(dev)
-    one = lib.h3q_linear_w8a8_grouped_host(x_host, wq, ws, b, chunk_rows=128, h2d_stream=s,
-                                           d2h_stream=s)
+    sep_host = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(G)]
+    sep_dev = [torch.empty((M + 1, N), dtype=torch.bfloat16, device=dev)[:M] for _ in range(G)]
+    one = lib.h3q_linear_w8a8_grouped_host(x_host, wq, ws, b, ys_host=sep_host, ys_dev=sep_dev,
+                                           chunk_rows=128, h2d_stream=s, d2h_stream=s)
     three = lib.h3q_linear_w8a8_grouped_host(x_host, wq, ws, b, chunk_rows=128)
     for g in range(G):
         assert _same(one["ys"][g], three["ys"][g])
