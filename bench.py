@@ -24,6 +24,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -67,7 +68,8 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        # the raw samples (the JSON line carries their summary)
+        self.path = os.path.join(tempfile.gettempdir(), f"h3q_clocks_rank{index}_{os.getpid()}.csv")
 
     def start(self):
         try:
