@@ -404,6 +404,21 @@ def test_affine_grid_reconstructs_exactly(oracle):
     assert np.array_equal(oracle.widen_bf16(wh), w)       # every such value is a BF16 value
 
 
+def test_affine_4bit_grid_reconstructs_exactly(oracle):
+    # the 4-bit case of the grid above: beta + j / 16 for j in 0..15 (both
+    # ends present) gives alpha = (15/16) / 15 = 1/16 exactly, q = j, and
+    # dequantised weights equal to the inputs
+    rng = np.random.default_rng(46)
+    j = rng.integers(0, 16, (4, 128))
+    j[:, ::64] = 0
+    j[:, 1::64] = 15
+    w = (np.float32(0.25) + j.astype(np.float32) / np.float32(16.0)).astype(np.float32)
+    q, a, b = oracle.quantize_affine(w, bits=4)
+    assert np.array_equal(q, j.astype(np.uint8))
+    assert np.all(a == np.float32(1 / 16)) and np.all(b == np.float32(0.25))
+    assert np.array_equal(oracle.widen_bf16(oracle.dequant_affine(q, a, b)), w)
+
+
 @pytest.mark.parametrize("bits", [8, 4])
 def test_affine_extremes_and_error_bound(oracle, bits):
     rng = np.random.default_rng(45 + bits)
