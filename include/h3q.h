@@ -35,6 +35,8 @@
  *     anything is enqueued.  A launch failure returns H3Q_ERR_CUDA; faults of
  *     already-enqueued work surface at the caller's next synchronisation.
  *   - Results are bitwise deterministic run to run.
+ *   - An entry point that does not synchronise puts all its work on `stream`,
+ *     so it can be captured in a CUDA graph and replayed.
  */
 #ifndef H3Q_H
 #define H3Q_H

@@ -108,3 +108,35 @@ def test_grouped_attn_workload_matches_separate_calls(lib, dev):
     for g in range(4):
         one = lib.h3q_linear_w8a8(x, q[g][0], q[g][1], b[g])
         assert _same(grp["ys"][g], one["y"])
+
+
+def test_grouped_call_replays_from_a_cuda_graph(lib, dev):
+    # a call that does not synchronise enqueues everything on the caller's
+    # stream (the memset and the programmatic-dependent launches), so it can be
+    # captured in a CUDA graph; replays give the eager call's bits
+    M, N, K, G = 300, 264, 5376, 3
+    c = synth.make_linear(M, N, K, seed=93, n_linears=G, outlier_p=0.005, outlier_mul=30)
+    x = _bf16_dev(c.x_bits, dev)
+    q = [lib.h3q_quantize_weights(torch.from_numpy(w).to(dev)) for w in c.w]
+    wq, ws = [w for w, _ in q], [s for _, s in q]
+    b = [_bf16_dev(bb, dev) for bb in c.bias_bits]
+    ref = lib.h3q_linear_w8a8_grouped(x, wq, ws, b)
+    ys = [torch.empty_like(y) for y in ref["ys"]]
+    xs = torch.empty_like(ref["xs"])
+    work = torch.empty_like(ref["workspace"])
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        lib.h3q_linear_w8a8_grouped(x, wq, ws, b, xs=xs, ys=ys, workspace=work, stream=side)
+        side.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            lib.h3q_linear_w8a8_grouped(x, wq, ws, b, xs=xs, ys=ys, workspace=work, stream=side)
+    for rep in range(2):
+        for y in ys:
+            y.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for g in range(G):
+            assert _same(ys[g], ref["ys"][g]), (rep, g)
+        assert lib.h3q_workspace_status(work, M, K) == lib.H3Q_OK
