@@ -252,10 +252,40 @@ def test_image_operator_shapes_sampled(lib, oracle, dev, name):
                   rows=_sample_rows(c.M, 105 + len(name)))
 
 
+@pytest.fixture(scope="module")
+def fc2_case():
+    return synth.fc2()
+
+
 @pytest.mark.slow
-def test_fc2_workload_sampled(lib, oracle, dev):
-    c = synth.fc2()
+def test_fc2_workload_sampled(lib, oracle, dev, fc2_case):
+    c = fc2_case
     _linear_check(lib, oracle, dev, c.x_bits, c.w[0], c.bias_bits[0], rows=_sample_rows(c.M, 103))
+
+
+@pytest.mark.slow
+def test_fc2_every_row_against_the_legacy_exact_kernel(lib, dev, fc2_case):
+    """All 32768 x 5376 outputs of fc2 against the legacy mma.sync INT8 kernel
+    on the same INT8 operands.  That kernel is exact by construction (INT32
+    accumulation in the instruction) and is itself checked against the oracle
+    (test_legacy_mma_sync_entry_point), so every 256-token tile's path --
+    single accumulator, checkpoints, or the chunked kernel -- is checked here,
+    not only the sampled rows.  y must match bit for bit as well: the output
+    depends on (acc, s_a, s_w, bias) alone."""
+    c = fc2_case
+    x = _bf16_dev(c.x_bits, dev)
+    qw, sw = lib.h3q_quantize_weights(torch.from_numpy(c.w[0]).to(dev))
+    b = _bf16_dev(c.bias_bits[0], dev)
+    out = lib.h3q_linear_w8a8(x, qw, sw, b, want_acc=True, want_xq=True)
+    del x
+    ckpt = lib.h3q_linear_checkpointed_tiles(out["workspace"], c.M, c.K)
+    leg = lib.h3q_linear_w8a8_mma_sync(out["xq"], out["xs"], qw, sw, b, want_acc=True)
+    torch.cuda.synchronize()
+    bad = int((out["acc"] != leg["acc"]).sum())
+    assert bad == 0, f"{bad} INT32 accumulators differ from the legacy exact kernel"
+    assert torch.equal(out["y"].view(torch.int16), leg["y"].view(torch.int16))
+    # the workload does exercise the checkpointed path (about half its tiles)
+    assert ckpt > 0
 
 
 def test_epilogue_deep_cancellation(lib, oracle, dev):

@@ -58,3 +58,26 @@ def test_sweep_block_sampled(lib, oracle, dev, sweep_inputs, block):
         assert lib.h3q_workspace_status(out["workspace"], M, K) == lib.H3Q_OK
         del out
         torch.cuda.empty_cache()
+
+
+def test_sweep_block0_fc2_every_row_against_the_legacy_exact_kernel(lib, dev, sweep_inputs):
+    """Block 0's FC2 (75647 x 5376 x 21504): every output against the legacy
+    mma.sync INT8 kernel on the same INT8 operands (exact by construction and
+    oracle-checked on its own), so every tile's accumulation path is checked."""
+    j = 5
+    name, N, K = synth.SWEEP_LINEARS[j]
+    M = synth.SWEEP_M
+    w, b = synth.sweep_weight(0, j, dev)
+    qw, sw = lib.h3q_quantize_weights(w)
+    del w
+    out = lib.h3q_linear_w8a8(sweep_inputs[K], qw, sw, b, want_acc=True, want_xq=True)
+    ws = out.pop("workspace")
+    ckpt = lib.h3q_linear_checkpointed_tiles(ws, M, K)
+    del ws
+    torch.cuda.empty_cache()
+    leg = lib.h3q_linear_w8a8_mma_sync(out["xq"], out["xs"], qw, sw, b, want_acc=True)
+    torch.cuda.synchronize()
+    bad = int((out["acc"] != leg["acc"]).sum())
+    assert bad == 0, f"{name}: {bad} INT32 accumulators differ from the legacy exact kernel"
+    assert torch.equal(out["y"].view(torch.int16), leg["y"].view(torch.int16))
+    assert ckpt >= 0

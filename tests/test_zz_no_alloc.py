@@ -4,10 +4,12 @@ It serves callers that may not allocate device memory at call time (for
 example an engine plugin handed only its input and output buffers); its
 scratch is a fixed 16 MiB array inside the library.  Through the C-ABI, two
 calls in a row must give the same results as h3q_linear_w8a8 with a
-caller-provided workspace: INT32 accumulators and INT8 activations bit for
-bit, BF16 outputs within one BF16 ulp of each other (here they are computed by
-the same kernels, so they are in fact identical).  This file is collected last
-on purpose.
+caller-provided workspace.  Both run the same kernels on the same operands, and
+the library's outputs depend on the operands alone, so everything is compared
+bit for bit: INT32 accumulators, activation scales and BF16 outputs (a shared-
+scratch fault could otherwise hide inside a one-ulp tolerance).  After each
+call the scratch's status word, read with h3q_linear_w8a8_noalloc_status, must
+be clear.  This file is collected last on purpose.
 """
 import numpy as np
 import pytest
@@ -20,15 +22,6 @@ pytestmark = pytest.mark.gpu
 
 def _bf16(bits, dev):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
-
-
-def _ulp_distance(a, b):
-    """Distance in BF16 ulps between two BF16 tensors (same sign assumed)."""
-    ia = a.view(torch.int16).to(torch.int32)
-    ib = b.view(torch.int16).to(torch.int32)
-    ka = torch.where(ia < 0, -(ia & 0x7FFF), ia)
-    kb = torch.where(ib < 0, -(ib & 0x7FFF), ib)
-    return (ka - kb).abs()
 
 
 def test_noalloc_matches_workspace_entry_point_twice():
@@ -45,12 +38,16 @@ def test_noalloc_matches_workspace_entry_point_twice():
         torch.cuda.synchronize()
         assert torch.equal(got["acc"], ref["acc"]), f"call {call}: INT32 accumulators differ"
         assert torch.equal(got["xs"].view(torch.int32), ref["xs"].view(torch.int32))
-        assert int(_ulp_distance(got["y"], ref["y"]).max()) <= 1, f"call {call}: BF16 outputs"
-        # pre-quantised activations as well
+        assert torch.equal(got["y"].view(torch.int16), ref["y"].view(torch.int16)), \
+            f"call {call}: BF16 outputs differ"
+        assert h3q.h3q_linear_w8a8_noalloc_status(M, K) == h3q.H3Q_OK
+        # pre-quantised activations as well (the INT8 -> FP16 coding path)
         got2 = h3q.h3q_linear_w8a8_noalloc(None, qw, sw, b, xq=ref["xq"], xs=ref["xs"],
                                            want_acc=True)
         torch.cuda.synchronize()
         assert torch.equal(got2["acc"], ref["acc"])
+        assert torch.equal(got2["y"].view(torch.int16), ref["y"].view(torch.int16))
+        assert h3q.h3q_linear_w8a8_noalloc_status(M, K) == h3q.H3Q_OK
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():

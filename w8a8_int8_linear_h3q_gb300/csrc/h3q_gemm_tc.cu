@@ -43,10 +43,10 @@
 //
 // Tile: 128 output channels (MMA M, TMEM lanes) x 128 tokens (MMA N).
 // CTAs run in clusters of two that take adjacent channel blocks of the same
-// token block: each loads two of a super-stage's four activation tiles and
-// multicasts them to both, which halves the activation bytes fetched from L2,
-// and a slot is refilled only after both CTAs' MMAs have finished with it
-// (their completions are multicast to both producers).  Persistent
+// token block (the fallback list names such channel-block pairs); each CTA
+// loads all four activation tiles of a super-stage into its own shared
+// memory, so the two CTAs share those tiles through L2 only, and a slot is
+// refilled once this CTA's own MMAs have finished with it.  Persistent
 // clusters walk the cluster tiles in groups of 16 token blocks so that the
 // concurrently running tiles share weight and activation tiles in L2.
 //
@@ -81,8 +81,7 @@ constexpr int MAX_SS_PER_CHUNK = 4;     // 16 k-blocks = 1024 K: exact FP32 chun
 constexpr int SLOTS = 2;                // super-stage slots: activations (SMEM), FP16 weights (TMEM)
 constexpr int W_SLOTS = 3;              // super-stage slots: INT8 weights (SMEM)
 constexpr int GROUP_M = 16;             // token blocks per raster group
-constexpr int CLUSTER = 2;              // CTAs sharing one activation tile (multicast)
-constexpr uint16_t CLUSTER_MASK = (1u << CLUSTER) - 1;
+constexpr int CLUSTER = 2;              // CTAs on adjacent channel blocks of one token block
 constexpr int NUM_CONV_WARPS = 4;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int WPROD_WARP = 2;
@@ -107,7 +106,7 @@ struct __align__(1024) Smem {
   uint64_t full_w[W_SLOTS];             // a slot's INT8 weights have landed
   uint64_t empty_w[W_SLOTS];            // the converters have read them
   uint64_t full_a[SLOTS];               // A converted and B landed for a super-stage
-  uint64_t empty_s[SLOTS];              // both CTAs' MMAs are done with a slot
+  uint64_t empty_s[SLOTS];              // this CTA's MMAs are done with a slot
   uint64_t dfull[2];
   uint64_t dempty[2];
   uint64_t mma_done;
@@ -203,7 +202,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constan
     for (int i = 0; i < SLOTS; ++i) {
       P::mbar_init(&sm.full_b[i], 1);
       P::mbar_init(&sm.full_a[i], NUM_CONV_WARPS * 32);
-      P::mbar_init(&sm.empty_s[i], CLUSTER);      // one multicast commit per CTA
+      P::mbar_init(&sm.empty_s[i], 1);            // this CTA's commit
     }
     for (int i = 0; i < 2; ++i) {
       P::mbar_init(&sm.dfull[i], 1);
@@ -216,7 +215,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constan
   if (warp == 1) P::tmem_alloc(&sm.tmem_base, TM_COLS);
   P::tc_fence_before();
   __syncthreads();
-  P::cluster_sync();                              // peers' barriers exist before multicasts
+  P::cluster_sync();                              // both CTAs of the cluster have started
   P::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   const uint32_t rank = P::cluster_rank();
@@ -233,16 +232,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constan
         tile_coords(shp, list, cnt, t, rank, g, mb, nb);
         for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
           const uint32_t slot = gs % SLOTS;
-          // the slot is free once both CTAs' MMAs finished its previous use
+          // the slot is free once this CTA's MMAs finished its previous use
           if (!P::mbar_wait(&sm.empty_s[slot], ((gs / SLOTS) & 1u) ^ 1u, abort_flag, err,
                             ERR_PRODUCER)) {
             ok = false;
             break;
           }
-          // all four activation tiles land here: this CTA's two and the peer's two
+          // the super-stage's four activation tiles, two per copy (each box is
+          // two whole k-block tiles); boxes past the last k-block arrive as zeros
           P::mbar_arrive_expect_tx(&sm.full_b[slot], SS * B_STAGE_BYTES);
-          P::tma_load_3d_mc(P::smem_u32(sm.b[slot][2 * rank]), &act_map, &sm.full_b[slot], 0,
-                            mb * BN, ss * SS + 2 * int(rank), CLUSTER_MASK);
+#pragma unroll
+          for (int h = 0; h < SS / 2; ++h)
+            P::tma_load_3d(P::smem_u32(sm.b[slot][2 * h]), &act_map, &sm.full_b[slot], 0,
+                           mb * BN, ss * SS + 2 * h);
           gb = gs + 1;
         }
       }
@@ -314,7 +316,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constan
                 P::mma_f16_ts(d_tmem, a_tmem + j * 32 + kk * 8, bdesc + uint64_t(kk * 2), IDESC,
                               (ss > ss0 || j > 0 || kk > 0) ? 1u : 0u);
             }
-            P::mma_commit_mc(&sm.empty_s[slot], CLUSTER_MASK);
+            P::mma_commit(&sm.empty_s[slot]);
           }
           if (!ok) break;
           P::mma_commit(&sm.dfull[buf]);
@@ -445,7 +447,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constan
     P::tc_fence_after();
     P::tmem_dealloc(tmem, TM_COLS);
   }
-  P::cluster_sync();                              // no peer still signals or writes here
+  P::cluster_sync();                              // both CTAs leave together
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,

@@ -214,17 +214,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-// Same, delivered to the same shared-memory offset (data and mbarrier) in
-// every CTA of the cluster named in `mask`.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* map, uint64_t* bar,
-                                               int x, int y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
-
 // 3-D tiled load into this CTA's shared memory.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint64_t* bar, int x,
                                             int y, int z) {
@@ -232,16 +221,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint6
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-
-// 3-D tiled load, multicast like tma_load_2d_mc.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void* map, uint64_t* bar,
-                                               int x, int y, int z, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "h"(mask)
       : "memory");
 }
 
@@ -306,15 +285,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-
-// As mma_commit, arriving on the mbarrier at the same offset in every CTA of `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
       : "memory");
 }
 
