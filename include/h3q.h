@@ -358,6 +358,19 @@ h3q_status h3q_linear_affine_w8(const uint16_t* x, const uint8_t* q, const float
 h3q_status h3q_selftest_bounded_wait(uint32_t* status, cudaStream_t stream);
 
 /*
+ * Throughput probe of the one INT8 tensor instruction of sm_103 (no
+ * counterpart on the pages; it supplies the denominator of "% of dense INT8
+ * peak").  sm_103a has no INT8 tcgen05 MMA, so the part's INT8 tensor rate is
+ * that of the warp-level mma.sync m16n8k32 s8 x s8 -> s32.  Every warp of a
+ * full grid (4 blocks of 8 warps per SM) runs 8 independent accumulator
+ * chains of it for about 40 ms; the launch is timed with CUDA events on
+ * `stream`, and 8192 operations per instruction (2 * 16 * 8 * 32) over that
+ * time are written to *tops (TOPS, 1e12 operations per second).  Allocates no
+ * device memory; SYNCHRONISES `stream`.
+ */
+h3q_status h3q_probe_mma_s8_tops(double* tops, cudaStream_t stream);
+
+/*
  * A3 + A4 on the legacy warp-level INT8 tensor instruction (mma.sync
  * m16n8k32 s8 -> s32), exact by construction; the same arithmetic and output
  * as h3q_linear_w8a8 from pre-quantised activations.  Kept as the baseline
@@ -388,17 +401,32 @@ h3q_status h3q_linear_w8a8_mma_sync(const int8_t* xq, const float* xs, const int
  * 16 MiB (16777216 bytes) are rejected with H3Q_ERR_UNSUPPORTED_SHAPE; at
  * N = K = 5376 that allows M up to 1559 tokens.
  *
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  All calls share the one array and each rewrites what it needs of
- * it, so calls whose work overlaps on the GPU (different streams, or
- * concurrent host threads) race and must be serialised by the caller.
- * Enqueued on `stream`; does not synchronise.
+ * The first call in a CUDA context looks up the array's device address (with
+ * the device current) and keeps it for that context; make that first call
+ * before any stream capture.  After cudaDeviceReset the device has a new
+ * context, and the next call looks the address up again.  All calls share the
+ * one array and each rewrites what it needs of it, so calls whose work
+ * overlaps on the GPU (different streams, or concurrent host threads) race
+ * and must be serialised by the caller.  Enqueued on `stream`; does not
+ * synchronise.  A bounded device-side wait that gives up (it cannot on a
+ * healthy GPU) leaves the outputs unspecified and sets the status word in the
+ * built-in scratch: read it with h3q_linear_w8a8_noalloc_status.
  */
 h3q_status h3q_linear_w8a8_noalloc(const uint16_t* x, int8_t* xq, float* xs,
                                    const int8_t* wq, const float* ws, const uint16_t* bias,
                                    int64_t M, int64_t N, int64_t K,
                                    uint16_t* y, int32_t* acc_out, cudaStream_t stream);
+
+/*
+ * Status of the last h3q_linear_w8a8_noalloc on the current device (called
+ * with the same M and K, and no other no-alloc call since): H3Q_OK, or
+ * H3Q_ERR_TIMEOUT if one of its bounded device-side waits gave up -- what
+ * h3q_workspace_status reports for a caller-provided workspace (the pages
+ * have no counterpart).  Shapes that h3q_linear_w8a8_noalloc rejects give
+ * H3Q_ERR_UNSUPPORTED_SHAPE.  SYNCHRONISES `stream` to read the status word;
+ * allocates nothing.
+ */
+h3q_status h3q_linear_w8a8_noalloc_status(int64_t M, int64_t K, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

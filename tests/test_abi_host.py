@@ -108,11 +108,32 @@ def test_status_and_legacy_entry_points_reject_bad_args(cdll):
     assert g(A, A, A, A, NUL, 4, 8, 64, MIS, NUL, NUL) == 3
 
 
+def test_noalloc_scratch_bound_and_status_args(cdll):
+    # the built-in scratch is 16 MiB: at N = K = 5376 it holds M = 1559 rows, not 1560
+    assert cdll.h3q_linear_workspace_bytes(1559, 5376, 5376) <= 16 << 20
+    assert cdll.h3q_linear_workspace_bytes(1560, 5376, 5376) > 16 << 20
+    st = cdll.h3q_linear_w8a8_noalloc_status
+    assert st(0, 5376, NUL) == 2                          # M < 1
+    assert st(4, 8, NUL) == 2                             # K < 16
+    assert st(4096, 5376, NUL) == 2                       # beyond the scratch
+    f = cdll.h3q_linear_w8a8_noalloc
+    # x, xq, xs, wq, ws, bias, M, N, K, y, acc, stream
+    assert f(NUL, NUL, A, A, A, NUL, 4, 8, 64, A, NUL, NUL) == 1     # no x and no xq
+    assert f(A, NUL, A, A, A, NUL, 4, 8, 64, NUL, NUL, NUL) == 1     # no output
+    assert f(A, NUL, A, A, A, NUL, 4096, 128, 5376, A, NUL, NUL) == 2  # beyond the scratch
+
+
 def test_valid_args_without_a_device_report_no_device(cdll):
     import torch
     if torch.cuda.is_available():
         pytest.skip("a GPU is present: this checks the no-device report only")
     assert cdll.h3q_quantize_act(A, 4, 64, A, A, NUL) == 7
+    # the no-alloc entry points check the device before looking up their scratch
+    assert cdll.h3q_linear_w8a8_noalloc(A, NUL, A, A, A, NUL, 4, 8, 64, A, NUL, NUL) == 7
+    assert cdll.h3q_linear_w8a8_noalloc_status(4, 64, NUL) == 7
+    t = ctypes.c_double(-1.0)
+    assert cdll.h3q_probe_mma_s8_tops(ctypes.byref(t), NUL) == 7
+    assert t.value == 0.0
 
 
 def test_grouped_linear_rejects_bad_args(cdll):
@@ -168,6 +189,10 @@ def test_chunk_diagnostics_reject_bad_args(cdll):
         assert fn(A, 4, 64, NUL, NUL) == 1
         assert fn(A, 0, 64, ctypes.byref(n), NUL) == 2
         assert fn(MIS, 4, 64, ctypes.byref(n), NUL) == 3
+
+
+def test_probe_rejects_bad_args(cdll):
+    assert cdll.h3q_probe_mma_s8_tops(NUL, NUL) == 1
 
 
 def test_selftest_rejects_bad_args(cdll):

@@ -72,6 +72,10 @@ def _declare(lib):
     lib.h3q_linear_w8a8_mma_sync.restype = i32
     lib.h3q_linear_w8a8_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
     lib.h3q_linear_w8a8_noalloc.restype = i32
+    lib.h3q_probe_mma_s8_tops.argtypes = [ctypes.POINTER(ctypes.c_double), vp]
+    lib.h3q_probe_mma_s8_tops.restype = i32
+    lib.h3q_linear_w8a8_noalloc_status.argtypes = [i64, i64, vp]
+    lib.h3q_linear_w8a8_noalloc_status.restype = i32
     lib.h3q_selftest_bounded_wait.argtypes = [vp, vp]
     lib.h3q_selftest_bounded_wait.restype = i32
     lib.h3q_quantize_weights_affine.argtypes = [vp, i32, i32, i64, i64, vp, vp, vp]
@@ -221,6 +225,15 @@ def h3q_selftest_bounded_wait(status=None, stream=None) -> int:
     if status is None:
         status = torch.empty((4,), dtype=torch.int32, device="cuda")
     return int(load().h3q_selftest_bounded_wait(_ptr(status), _stream(stream)))
+
+
+def h3q_probe_mma_s8_tops(stream=None) -> float:
+    """Measured rate (TOPS) of the legacy mma.sync m16n8k32 s8 instruction,
+    the one INT8 tensor instruction of sm_103.  Synchronises; about 40 ms."""
+    t = ctypes.c_double(0.0)
+    _check(load().h3q_probe_mma_s8_tops(ctypes.byref(t), _stream(stream)),
+           "h3q_probe_mma_s8_tops")
+    return float(t.value)
 
 
 def h3q_quantize_act(x, q_out=None, scale_out=None, stream=None):
@@ -529,3 +542,10 @@ def h3q_linear_w8a8_noalloc(x, wq, ws, bias=None, *, xq=None, xs=None, y=None, a
     if acc_out is not None:
         out["acc"] = acc_out
     return out
+
+
+def h3q_linear_w8a8_noalloc_status(M: int, K: int, stream=None) -> int:
+    """Status word of the last h3q_linear_w8a8_noalloc (same M and K) on the
+    current device: 0 = ok, H3Q_ERR_TIMEOUT if a bounded device-side wait gave
+    up.  Synchronises."""
+    return int(load().h3q_linear_w8a8_noalloc_status(M, K, _stream(stream)))
