@@ -37,10 +37,17 @@ OPS_PER_STEP = 2 * M * N * K * len(LINEARS)
 WORKLOAD = ("attn projection: X BF16 [8192,5376] N(0,1)+0.5% x30 outliers; Q,K,V,O W [5376,5376] "
             "N(0,0.02)->per-channel INT8 + FP32 scales; BF16 bias N(0,0.1); seed 1")
 L2_FLUSH_BYTES = 512 << 20
-# The dense INT8 tensor rate of this part: sm_103a has no tcgen05 INT8 MMA, so
-# it is the legacy mma.sync m16n8k32 s8 instruction's, measured with
-# independent MMA chains on all 152 SMs (the design notes give the probe).
-INT8_DENSE_PEAK_TOPS = 150.0
+# The GB300 datasheet INT8 figure: NVIDIA's GB300 NVL72 specification table
+# gives "INT8 Tensor Core" as 23 POPS for the 72-GPU rack, under the table's
+# sparsity footnote; per GPU that is about 319 TOPS with 2:4 sparsity and 160
+# TOPS dense.  (From the public product page; there is no network here to
+# re-check it, so the line also carries the rate measured on the part itself:
+# sm_103a has no INT8 tcgen05 MMA, and h3q_probe_mma_s8_tops times its one
+# INT8 tensor instruction, mma.sync m16n8k32 s8.)
+DATASHEET_INT8 = {"rack_pops": 23.0, "gpus": 72, "sparse_tops_per_gpu": 23e3 / 72,
+                  "dense_tops_per_gpu": 23e3 / 72 / 2,
+                  "source": "NVIDIA GB300 NVL72 specifications table (public product page): "
+                            "INT8 Tensor Core 23 POPS per 72 GPUs, with sparsity; dense = half"}
 
 
 def _dist():
@@ -154,6 +161,26 @@ def cpu_oracle_sample(case, qws, target_s: float = 12.0):
     return ops / t_total / 1e12, rows_done, t_total, _cpu_threads()
 
 
+def _cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def _cpu_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -198,6 +225,7 @@ def run_reference(args):
             "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "linears": 4,
                        "step_rows": chunk},
             "cpu_baseline": {"value": tops, "unit": "TOPS", "cores": _cpu_threads(),
+                             "nproc": os.cpu_count(), "cpu_model": _cpu_model(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": tops, "unit": "TOPS", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -363,6 +391,7 @@ def run_gpu(args):
         chunked.append(h3q.h3q_linear_chunked_tiles(workspace, M, K, stream=stream))
 
     peaks, peak_kind = _peaks()
+    int8_probe = h3q.h3q_probe_mma_s8_tops()
     gemm_avg_s = statistics.mean(gemm_ms) * 1e-3
     gemm_tflops = 2 * M * N * K / gemm_avg_s / 1e12
     quant_avg_s = time_quantize_act(h3q, x, flush)
@@ -373,7 +402,11 @@ def run_gpu(args):
     roofline = {"bound": "tensor", "achieved": gemm_tflops, "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": gemm_tflops / peaks["bf16_tflops"],
                 "traffic": traffic, "traffic_source": traffic_note,
-                "algorithmic_bytes_per_launch": 2 * M * K + N * K + 2 * M * N + 4 * M + 6 * N,
+                # INT8 activations and weights, BF16 output, FP32 scales, BF16 bias
+                "algorithmic_bytes_per_launch": M * K + N * K + 2 * M * N + 4 * M + 6 * N,
+                # what this design must move at least: the tensor cores read the
+                # activations FP16-coded (2 bytes each), as A2 wrote them
+                "traffic_design": 2 * M * K + N * K + 2 * M * N + 4 * M + 6 * N,
                 "kernel": gemm_kernel_name(h3q),
                 "timed_as": "whole reuse-mode Linear call: status memset + weight-norm "
                             "pre-pass + gemm_wide_kernel + the chunked kernel's launch",
@@ -391,12 +424,17 @@ def run_gpu(args):
                        "chunked_tiles_per_linear": chunked,
                        "tiles_per_linear": -(-M // 128) * -(-N // 256)},
             "roofline": roofline,
-            "pct_of_dense_int8_peak": 100.0 * value / INT8_DENSE_PEAK_TOPS,
-            "dense_int8_peak": {"value": INT8_DENSE_PEAK_TOPS, "unit": "TOPS",
-                                "source": "measured: legacy mma.sync m16n8k32 s8, the only INT8 "
-                                          "tensor instruction of sm_103a; this path computes "
-                                          "the exact INT8 products on the FP16 tensor pipe "
-                                          "instead, see roofline"},
+            "pct_of_dense_int8_peak": 100.0 * value / int8_probe,
+            "pct_of_datasheet_dense_int8": 100.0 * value / DATASHEET_INT8["dense_tops_per_gpu"],
+            "dense_int8_peak": {"measured": int8_probe, "unit": "TOPS",
+                                "measured_by": "h3q_probe_mma_s8_tops: mma.sync m16n8k32 s8, "
+                                               "the one INT8 tensor instruction of sm_103a, 8 "
+                                               "independent chains per warp, 32 warps per SM, "
+                                               "CUDA events",
+                                "datasheet": DATASHEET_INT8,
+                                "note": "this path computes the exact INT8 products on the "
+                                        "FP16 tensor pipe instead (no INT8 tcgen05 MMA on "
+                                        "sm_103a); its roofline is the measured BF16 peak"},
             "kernels": {"legacy_mma_sync_s8_tops": legacy_tops(h3q, x, wq[0], wsc[0], bias[0], dev),
                         "quantize_act_us": quant_avg_s * 1e6,
                         "quantize_act_gbs": quant_bytes / quant_avg_s / 1e9,
@@ -420,16 +458,148 @@ def run_gpu(args):
                     "d2h_bytes_per_step": 2 * M * N * len(LINEARS)},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks}
+    if not args.no_large:
+        del gws, workspace
+        torch.cuda.empty_cache()
+        for name in ("fc1", "fc2"):
+            for k, v in time_large_linear(h3q, synth, name, dev, flush, peaks).items():
+                line["kernels"][f"{name}_{k}"] = v
+            torch.cuda.empty_cache()
+        line["kernels"].update(time_sweep(h3q, synth, dev, local, peaks))
+        torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         qws = [(q.cpu().numpy(), s.cpu().numpy()) for q, s in zip(wq, wsc)]
         tops, rows, secs, thr = cpu_oracle_sample(case, qws)
-        line["cpu_baseline"] = {"value": tops, "unit": "TOPS", "cores": thr, "kind": "oracle",
+        line["cpu_baseline"] = {"value": tops, "unit": "TOPS", "cores": thr,
+                                "nproc": os.cpu_count(), "cpu_model": _cpu_model(),
+                                "kind": "oracle",
                                 "sample": f"{rows} token rows x 4 Linears (A2+A3+A4), {secs:.1f} s"}
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def time_large_linear(h3q, synth, name, dev, flush, peaks, reps=5):
+    """One fc1 or fc2 Linear at full size (device-drawn inputs of the
+    workload's distributions): median of `reps` CUDA-event timings, L2
+    flushed before each, of the whole call from BF16 X (A2 + A3 + A4) and of
+    a reuse-mode call (the GEMM with its epilogue, on the coded activations
+    the previous call left in the workspace)."""
+    import torch
+    x, w, b = synth.device_case(name, dev)
+    qw, sw = h3q.h3q_quantize_weights(w)          # offline A1 (untimed)
+    del w
+    Mc, Kc = x.shape
+    Nc = qw.shape[0]
+    xs = torch.empty((Mc,), dtype=torch.float32, device=dev)
+    y = torch.empty((Mc, Nc), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty((h3q.h3q_linear_workspace_bytes(Mc, Nc, Kc),), dtype=torch.uint8,
+                     device=dev)
+
+    def call(src):
+        h3q.h3q_linear_w8a8(src, qw, sw, b, xs=xs, y=y, workspace=ws)
+
+    def med_us(src):
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            call(src)
+            e.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(e) * 1e3)
+        return statistics.median(ts)
+
+    for _ in range(2):
+        call(x)
+    torch.cuda.synchronize()
+    t_call = med_us(x)
+    call(x)
+    t_gemm = med_us(None)
+    ops = 2 * Mc * Nc * Kc
+    out = {"shape": [Mc, Nc, Kc], "gemm_us": t_gemm, "gemm_tops": ops / t_gemm / 1e6,
+           "gemm_frac": ops / t_gemm / 1e6 / peaks["bf16_tflops"],
+           "call_us": t_call, "call_tops": ops / t_call / 1e6,
+           "call_frac": ops / t_call / 1e6 / peaks["bf16_tflops"],
+           "checkpointed_tiles": h3q.h3q_linear_checkpointed_tiles(ws, Mc, Kc),
+           "chunked_tiles": h3q.h3q_linear_chunked_tiles(ws, Mc, Kc)}
+    del x, qw, sw, b, xs, y, ws
+    return out
+
+
+def time_sweep(h3q, synth, dev, local, peaks, passes=2):
+    """The full 300-Linear sweep: 50 blocks, each with its own seeded weights
+    (17.3 GB of INT8 weights resident), M = 75647 tokens.  A block is Q, K, V,
+    O as one grouped call on X5 [M, 5376], FC1 on X5 and FC2 on X21
+    [M, 21504], each call quantising its BF16 input (A2 included); the blocks
+    are not chained.  One untimed pass, then `passes` passes, each timed whole
+    with CUDA events, clocks sampled meanwhile.  The inputs are far larger than
+    L2, so no flush is needed between passes."""
+    import torch
+    M = synth.SWEEP_M
+    W5, W21 = synth.H3_WIDTH, synth.H3_MLP_WIDTH
+    xs_bf = {K: synth.sweep_x(K, dev) for K in (W5, W21)}
+    t0 = time.perf_counter()
+    blocks = []
+    for blk in range(synth.H3_BLOCKS):
+        lin = []
+        for j in range(len(synth.SWEEP_LINEARS)):
+            w, bias = synth.sweep_weight(blk, j, dev)
+            q, sc = h3q.h3q_quantize_weights(w)     # offline A1 (untimed)
+            del w
+            lin.append((q, sc, bias))
+        blocks.append(lin)
+    setup_s = time.perf_counter() - t0
+    weight_bytes = sum(q.numel() for lin in blocks for q, _, _ in lin)
+    xs = torch.empty((M,), dtype=torch.float32, device=dev)
+    ya = [torch.empty((M, W5), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    y1 = torch.empty((M, W21), dtype=torch.bfloat16, device=dev)
+    y2 = torch.empty((M, W5), dtype=torch.bfloat16, device=dev)
+    wsa = torch.empty((h3q.h3q_linear_grouped_workspace_bytes(4, M, W5, W5),), dtype=torch.uint8,
+                      device=dev)
+    ws1 = torch.empty((h3q.h3q_linear_workspace_bytes(M, W21, W5),), dtype=torch.uint8,
+                      device=dev)
+    ws2 = torch.empty((h3q.h3q_linear_workspace_bytes(M, W5, W21),), dtype=torch.uint8,
+                      device=dev)
+
+    def sweep_pass():
+        for lin in blocks:
+            att = lin[:4]
+            h3q.h3q_linear_w8a8_grouped(xs_bf[W5], [a[0] for a in att], [a[1] for a in att],
+                                        [a[2] for a in att], xs=xs, ys=ya, workspace=wsa)
+            q, sc, bias = lin[4]
+            h3q.h3q_linear_w8a8(xs_bf[W5], q, sc, bias, xs=xs, y=y1, workspace=ws1)
+            q, sc, bias = lin[5]
+            h3q.h3q_linear_w8a8(xs_bf[W21], q, sc, bias, xs=xs, y=y2, workspace=ws2)
+
+    sweep_pass()
+    torch.cuda.synchronize()
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    ms = []
+    for _ in range(passes):
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        sweep_pass()
+        e.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(e))
+    clocks = clk.stop()
+    ops = synth.H3_BLOCKS * sum(2 * M * n * k for _, n, k in synth.SWEEP_LINEARS)
+    t = statistics.median(ms)
+    del blocks, xs_bf, ya, y1, y2, wsa, ws1, ws2
+    return {"sweep_total_ms": t, "sweep_passes_ms": ms, "sweep_tops": ops / t / 1e9,
+            "sweep_frac": ops / t / 1e9 / peaks["bf16_tflops"],
+            "sweep_linears": synth.H3_BLOCKS * len(synth.SWEEP_LINEARS),
+            "sweep_weight_bytes": weight_bytes, "sweep_setup_s": setup_s,
+            "sweep_clocks": clocks,
+            "sweep_note": "50 blocks x (Q,K,V,O grouped + FC1 + FC2), distinct weights per "
+                          "block, M=75647, every call from BF16 X (A2 included); timed whole, "
+                          "not extrapolated"}
 
 
 def copy_bandwidth(x, x_pin, y, y_pin, stream, reps=5):
@@ -453,15 +623,20 @@ def gemm_kernel_name(h3q) -> str:
     return "gemm_wide_kernel"
 
 
-# The dominant kernel's DRAM traffic comes from an ncu capture summarised in
-# profiles/; it is reported only while the kernel's sources are the ones that
-# were captured (their SHA-256 is recorded beside the figure): the files that
-# compile into the kernel (the C-ABI header declares nothing it uses).
+# The dominant kernel's DRAM traffic per launch (dram__bytes_read.sum +
+# dram__bytes_write.sum) on the attn Linear, from one ncu capture (its summary
+# is committed under profiles/, named for the kernel and workload), with the
+# SHA-256 of the kernel's sources when it was taken.  It is reported only while
+# those sources are unchanged: the files that compile into the kernel (the
+# C-ABI header declares nothing it uses).
 WIDE_SOURCES = ["w8a8_int8_linear_h3q_gb300/csrc/h3q_gemm_wide.cu",
                 "w8a8_int8_linear_h3q_gb300/csrc/h3q_tc_ptx.cuh",
                 "w8a8_int8_linear_h3q_gb300/csrc/h3q_epilogue.cuh",
                 "w8a8_int8_linear_h3q_gb300/csrc/h3q_internal.cuh"]
-WIDE_PROFILE = "profiles/gemm_wide_attn_8192x5376x5376.md"
+WIDE_TRAFFIC = {"bytes_per_launch": 281974016,
+                "source_sha256": "1a1496c3c8a70810596d489f2cb2eba5e1f4180539f6b089262017c236f4da11",
+                "capture": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one "
+                           "reuse-mode gemm_wide_kernel launch, attn Linear 8192x5376x5376"}
 
 
 def wide_sources_sha256() -> str:
@@ -474,23 +649,10 @@ def wide_sources_sha256() -> str:
 
 
 def profiled_traffic():
-    """(bytes per launch, note) from the committed ncu summary, or (None, why)."""
-    try:
-        text = open(os.path.join(ROOT, WIDE_PROFILE)).read()
-    except OSError:
-        return None, "no ncu summary"
-    fields = {}
-    for line in text.splitlines():
-        line = line.strip().lstrip("-* ").strip("`")
-        for key in ("traffic_bytes_per_launch:", "source_sha256:"):
-            if line.startswith(key):
-                fields[key[:-1]] = line[len(key):].strip()
-    if fields.get("source_sha256") != wide_sources_sha256():
+    """(bytes per launch, note) of the last ncu capture, or (None, why)."""
+    if WIDE_TRAFFIC["source_sha256"] != wide_sources_sha256():
         return None, "kernel changed since the ncu capture"
-    try:
-        return int(fields["traffic_bytes_per_launch"]), f"ncu capture, {WIDE_PROFILE}"
-    except (KeyError, ValueError):
-        return None, "no traffic figure in the ncu summary"
+    return WIDE_TRAFFIC["bytes_per_launch"], WIDE_TRAFFIC["capture"]
 
 
 def time_quantize_act(h3q, x, flush, reps=10):
@@ -687,6 +849,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-large", action="store_true",
+                    help="skip the fc1 / fc2 Linears and the full 300-Linear sweep")
     ap.add_argument("--configs", default=None,
                     help="instead of the contract line, print a per-workload table: 'all' or "
                          "a comma list of " + ",".join(CONFIG_TABLE))

@@ -210,5 +210,40 @@ def sweep_weight(block: int, j: int, device):
     return w, b
 
 
+# --- fc1 / fc2 drawn on the device (bench timing only) ----------------------------
+
+def device_case(name: str, device):
+    """The fc1 or fc2 workload with the same shapes and distributions as
+    ``fc1()`` / ``fc2()``, drawn on ``device`` by torch's counter-based CUDA
+    generator (seeded by SeedSequence([seed, 1]), seed 2 or 3) instead of
+    numpy on the host, where a 32768 x 21504 draw takes tens of seconds.  Used
+    where only the distribution matters (timing: the exactness checks of the
+    GEMM depend on the norms of the coded rows, which these draws share with
+    the host recipe); parity tests use the host recipe's bytes.  Returns
+    (X BF16 [M, K], W FP32 [N, K], bias BF16 [N]) on ``device``."""
+    import torch
+    if name == "fc1":
+        M, N, K, seed, std = 32767, H3_MLP_WIDTH, H3_WIDTH, 2, 0.015
+    elif name == "fc2":
+        M, N, K, seed, std = 32768, H3_WIDTH, H3_MLP_WIDTH, 3, 0.01
+    else:
+        raise ValueError(f"device_case: fc1 or fc2, not {name!r}")
+    g = torch.Generator(device=device)
+    g.manual_seed(_sweep_seed_of(seed, 1))
+    z = torch.randn((M, K), generator=g, device=device, dtype=torch.float32)
+    if name == "fc2":
+        z = z * torch.sigmoid(z)            # SiLU of the normal draw (input preparation)
+    x = z.to(torch.bfloat16)
+    del z
+    w = torch.randn((N, K), generator=g, device=device, dtype=torch.float32) * std
+    b = (torch.randn((N,), generator=g, device=device, dtype=torch.float32) * 0.1).to(torch.bfloat16)
+    return x, w, b
+
+
+def _sweep_seed_of(*path: int) -> int:
+    ss = np.random.SeedSequence(list(path))
+    return int(ss.generate_state(1, dtype=np.uint64)[0] & ((1 << 63) - 1))
+
+
 WORKLOADS = {"tiny": tiny, "attn": attn, "fc1": fc1, "fc2": fc2, "image_qkv": image_qkv,
              "image_gate_up": image_gate_up, "image_down": image_down}

@@ -30,11 +30,6 @@ __device__ __forceinline__ int quant1(float x, float s) {
   return max(-kQMax, min(kQMax, q));
 }
 
-// integer-valued float in [-127, 127] -> its two's-complement low byte
-__device__ __forceinline__ uint32_t f2s8_byte(float n) {
-  return uint32_t(__float_as_int(__fadd_rn(n, 12582912.0f)) - 0x4B400000) & 0xFFu;
-}
-
 __device__ __forceinline__ uint32_t pack2_f16(int a, int b) {
   return uint32_t(__half_as_ushort(__int2half_rn(a))) |
          (uint32_t(__half_as_ushort(__int2half_rn(b))) << 16);
@@ -79,6 +74,11 @@ __device__ __forceinline__ float hi_f(uint64_t v) { return __uint_as_float(uint3
 // rows whose scale is too small for a normal reciprocal; those always divide.
 // |x| <= absmax makes |q| <= 127 without a clamp.
 //
+// The rounding sum u = RN(t + 1.5 * 2^23) of an integer n in [-127, 127] is
+// the FP32 pattern 0x4B400000 + n (its last place is 1), so u's low byte is
+// n's two's-complement byte: the INT8 output is packed from those bytes with
+// byte permutes, with no further conversion.
+//
 // Quantises 8 values, stores them, and returns the sum of their squares
 // (exact: at most 8 * 127^2).  The work runs two values at a time on the
 // paired FP32 instructions (each half the same IEEE operation as the scalar
@@ -95,7 +95,14 @@ __device__ __forceinline__ uint32_t quant_store8(uint4 v, float s, float r, bool
   const uint64_t r2 = pack_f2(r, r);
   const uint64_t c2 = pack_f2(12582912.0f, 12582912.0f);
   const float lim = 0.5f - 0x1p-15f;
+  // the low bytes of a pair's rounding sums: the pair's two INT8 codes
+  const auto bytes2 = [](uint64_t u2) {
+    uint32_t b;
+    asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(b) : "r"(uint32_t(u2)), "r"(uint32_t(u2 >> 32)));
+    return b;
+  };
   uint64_t q2[4];
+  uint32_t p[4];
   bool ok = fast;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -107,19 +114,25 @@ __device__ __forceinline__ uint32_t quant_store8(uint4 v, float s, float r, bool
     asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(q2[j]) : "l"(u2), "l"(c2));
     asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d2) : "l"(t2), "l"(q2[j]));
     ok = ok && fabsf(lo_f(d2)) < lim && fabsf(hi_f(d2)) < lim;
+    if constexpr (kQ8) p[j] = bytes2(u2);
   }
   if (!ok) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < 4; ++j) {
       q2[j] = pack_f2(float(quant1(__uint_as_float(w[j] << 16), s)),
                       float(quant1(__uint_as_float(w[j] & 0xFFFF0000u), s)));
+      if constexpr (kQ8) {
+        uint64_t u2;
+        asm("add.rn.f32x2 %0, %1, %2;" : "=l"(u2) : "l"(q2[j]), "l"(c2));   // exact
+        p[j] = bytes2(u2);
+      }
+    }
   }
   if constexpr (kQ8) {
+    // elements 0..7 in order
     uint2 o;
-    o.x = f2s8_byte(lo_f(q2[0])) | (f2s8_byte(hi_f(q2[0])) << 8) |
-          (f2s8_byte(lo_f(q2[1])) << 16) | (f2s8_byte(hi_f(q2[1])) << 24);
-    o.y = f2s8_byte(lo_f(q2[2])) | (f2s8_byte(hi_f(q2[2])) << 8) |
-          (f2s8_byte(lo_f(q2[3])) << 16) | (f2s8_byte(hi_f(q2[3])) << 24);
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(o.x) : "r"(p[0]), "r"(p[1]));
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(o.y) : "r"(p[2]), "r"(p[3]));
     *reinterpret_cast<uint2*>(q8 + elem) = o;
   }
   if constexpr (kF16) {
@@ -263,18 +276,40 @@ quant_act_kernel(const uint16_t* __restrict__ x, int64_t M, int K, int8_t* __res
 // thread, so many rows are in flight per SM.
 constexpr int kRowThreads = 256;
 
+// Running maximum of |x| over the BF16 pairs of w: max.xorsign.abs keeps
+// max(|a|, |b|) per half (with the XOR of the signs, dropped at the end).
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t m, uint32_t w) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(w));
+  return r;
+}
+
+// The row kernel keeps its per-element work short, since a row's work is
+// spread over 256 threads and any per-row step is repeated by all 8 warps:
+//   - the absmax takes one paired BF16 instruction per 32-bit word;
+//   - one warp turns the block's maximum into the scale s and its reciprocal
+//     and publishes them through shared memory (the IEEE division and
+//     reciprocal run once per row, not once per warp);
+//   - with norm maxima requested (kSq), each thread stores the sum of q^2 of
+//     each of its vectors in shared memory, and four warps then add up one
+//     norm segment each while a fifth adds up the whole row.
 // Short rows: eight blocks resident per SM (32 registers a thread), so that
-// enough rows are in flight to keep HBM busy (measured at K = 5376: 32.8
-// against 37-39 us with the register count left free).
-template <int kVPT, bool kQ8, bool kF16>
-__global__ void __launch_bounds__(kRowThreads, kVPT <= 3 ? 8 : 2)
+// enough rows are in flight to keep HBM busy; six (40 registers) when INT8
+// codes are written, whose byte packing needs a few more registers (at 32
+// they spill).
+template <int kVPT, bool kQ8, bool kF16, bool kSq>
+__global__ void __launch_bounds__(kRowThreads, kVPT <= 3 ? (kQ8 ? 6 : 8) : 2)
 quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__ q8,
                      float* __restrict__ scale, uint16_t* __restrict__ qh, int ldh,
                      uint32_t* __restrict__ sq_max, uint32_t* __restrict__ seg_max,
                      int seg_len) {
-  __shared__ uint32_t red[kRowThreads / 32];
-  __shared__ uint4 red_sq[kRowThreads / 32];
+  constexpr int kWarpsPerRow = kRowThreads / 32;
+  static_assert(kWarpsPerRow > kNormSegs, "a warp per norm segment and one for the row");
+  __shared__ uint32_t red[kWarpsPerRow];
+  __shared__ float2 sr;
+  __shared__ uint32_t vsq[kSq ? kRowThreads * kVPT : 1];   // per-vector sums of q^2
   const int64_t row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvec = K >> 3;
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * int64_t(K));
   const int64_t base = row * int64_t(K), hbase = row * int64_t(ldh);
@@ -283,43 +318,61 @@ quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__
       *reinterpret_cast<uint4*>(qh + hbase + 8 * int64_t(j)) = make_uint4(0, 0, 0, 0);
   }
   uint4 v[kVPT];
-  uint32_t mbits = 0;
+  uint32_t m2 = 0;
 #pragma unroll
   for (int i = 0; i < kVPT; ++i) {
     const int j = threadIdx.x + kRowThreads * i;
     if (j < nvec) {
       v[i] = ld_stream(xr + j);
-      mbits = max(mbits, vec_absmax_bits(v[i]));
+      m2 = bf16x2_absmax(bf16x2_absmax(m2, v[i].x), v[i].y);
+      m2 = bf16x2_absmax(bf16x2_absmax(m2, v[i].z), v[i].w);
     }
   }
+  uint32_t mbits = max(m2 & 0x7FFFu, (m2 >> 16) & 0x7FFFu);
 #pragma unroll
   for (int o = 16; o; o >>= 1) mbits = max(mbits, __shfl_xor_sync(0xFFFFFFFFu, mbits, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mbits;
+  if (lane == 0) red[warp] = mbits;
   __syncthreads();
+  if (warp == 0) {
+    uint32_t m = lane < kWarpsPerRow ? red[lane] : 0u;
 #pragma unroll
-  for (int w = 0; w < kRowThreads / 32; ++w) mbits = max(mbits, red[w]);
-  const float s = row_scale(__uint_as_float(mbits << 16));
-  const float r = __frcp_rn(s);
+    for (int o = kWarpsPerRow / 2; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) {
+      const float sc = row_scale(__uint_as_float(m << 16));
+      sr = make_float2(sc, __frcp_rn(sc));
+      scale[row] = sc;
+    }
+  }
+  __syncthreads();
+  const float s = sr.x, r = sr.y;
   const bool fast = s >= 0x1p-120f;
-  SegSq sq;
 #pragma unroll
   for (int i = 0; i < kVPT; ++i) {
     const int j = threadIdx.x + kRowThreads * i;
-    if (j < nvec)
-      sq.add(8 * j, seg_len,
-             quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh, base + 8 * int64_t(j),
-                                     hbase + 8 * int64_t(j)));
+    if (j < nvec) {
+      const uint32_t sq = quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh,
+                                                  base + 8 * int64_t(j), hbase + 8 * int64_t(j));
+      if constexpr (kSq) vsq[j] = sq;
+    }
   }
-  if (threadIdx.x == 0) scale[row] = s;
-  if (sq_max) {
-    sq.warp_sum();
-    if ((threadIdx.x & 31) == 0) sq.store(&red_sq[threadIdx.x >> 5]);
+  if constexpr (kSq) {
     __syncthreads();
-    if (threadIdx.x == 0) {
-      SegSq t;
+    // every sum below is exact: a row's sum of q^2 is at most 127^2 K < 2^32
+    if (warp <= kNormSegs) {
+      const int segv = seg_len >> 3;                  // vectors per norm segment
+      const int j0 = warp < kNormSegs ? warp * segv : 0;
+      const int j1 = warp < kNormSegs ? min(nvec, j0 + segv) : nvec;
+      uint32_t t = 0;
+      for (int j = j0 + lane; j < j1; j += 32) t += vsq[j];
 #pragma unroll
-      for (int w = 0; w < kRowThreads / 32; ++w) t.add(red_sq[w]);
-      record_row_sq(sq_max, seg_max, row, t);
+      for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+      if (lane == 0) {
+        const int64_t b = row >> 8;
+        if (warp == kNormSegs)
+          atomicMax(sq_max + b, t);
+        else if (t)
+          atomicMax(seg_max + b * kNormSegs + warp, t);
+      }
     }
   }
 }
@@ -685,21 +738,29 @@ cudaError_t launch_act(const uint16_t* x, int64_t M, int K, int8_t* q, float* s,
   return cudaGetLastError();
 }
 
+template <int kVPT, bool kQ8, bool kF16>
+void launch_rows_sq(dim3 grid, cudaStream_t st, const uint16_t* x, int K, int8_t* q, float* s,
+                    uint16_t* qh, int ldh, uint32_t* sqm, uint32_t* sgm, int sl) {
+  if (sqm)
+    quant_act_row_kernel<kVPT, kQ8, kF16, true><<<grid, kRowThreads, 0, st>>>(x, K, q, s, qh,
+                                                                             ldh, sqm, sgm, sl);
+  else
+    quant_act_row_kernel<kVPT, kQ8, kF16, false><<<grid, kRowThreads, 0, st>>>(x, K, q, s, qh,
+                                                                              ldh, sqm, sgm, sl);
+}
+
 template <int kVPT>
 cudaError_t launch_rows(const uint16_t* x, int64_t M, int K, int8_t* q, float* s, uint16_t* qh,
                         int ldh, uint32_t* sqm, cudaStream_t st) {
-  const dim3 grid(static_cast<unsigned>(M)), block(kRowThreads);
+  const dim3 grid(static_cast<unsigned>(M));
   uint32_t* sgm = seg_maxima(sqm, M);
   const int sl = norm_segment_len(K);
   if (q && qh)
-    quant_act_row_kernel<kVPT, true, true><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh, sqm,
-                                                                   sgm, sl);
+    launch_rows_sq<kVPT, true, true>(grid, st, x, K, q, s, qh, ldh, sqm, sgm, sl);
   else if (q)
-    quant_act_row_kernel<kVPT, true, false><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh, sqm,
-                                                                    sgm, sl);
+    launch_rows_sq<kVPT, true, false>(grid, st, x, K, q, s, qh, ldh, sqm, sgm, sl);
   else
-    quant_act_row_kernel<kVPT, false, true><<<grid, block, 0, st>>>(x, K, q, s, qh, ldh, sqm,
-                                                                    sgm, sl);
+    launch_rows_sq<kVPT, false, true>(grid, st, x, K, q, s, qh, ldh, sqm, sgm, sl);
   return cudaGetLastError();
 }
 
