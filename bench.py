@@ -396,6 +396,7 @@ def run_gpu(args):
     gemm_tflops = 2 * M * N * K / gemm_avg_s / 1e12
     quant_avg_s = time_quantize_act(h3q, x, flush)
     quant_bytes = 2 * M * K + M * K + 4 * M       # BF16 in, INT8 out, FP32 scales
+    copy_s = time_same_size_copy(quant_bytes, dev)
     a2_call_s = (statistics.median(q_call_ms) - statistics.median(gemm_ms)) * 1e-3
     a2_call_bytes = 2 * M * K + 2 * M * K + 4 * M  # BF16 in, FP16-coded out, FP32 scales
     traffic, traffic_note = profiled_traffic()
@@ -439,6 +440,11 @@ def run_gpu(args):
                         "quantize_act_us": quant_avg_s * 1e6,
                         "quantize_act_gbs": quant_bytes / quant_avg_s / 1e9,
                         "quantize_act_hbm_frac": quant_bytes / quant_avg_s / 1e9 / peaks["hbm_gbs"],
+                        "quantize_act_timing": "steady state: back-to-back launches over "
+                                               "rotating copies of X and outputs (> 4x L2)",
+                        "same_size_copy_us": copy_s * 1e6,
+                        "same_size_copy_hbm_frac": quant_bytes / copy_s / 1e9 / peaks["hbm_gbs"],
+                        "quantize_act_frac_of_same_size_copy": copy_s / quant_avg_s,
                         "quantize_act_in_call_us": a2_call_s * 1e6,
                         "quantize_act_in_call_hbm_frac":
                             a2_call_bytes / a2_call_s / 1e9 / peaks["hbm_gbs"] if a2_call_s > 0
@@ -655,22 +661,53 @@ def profiled_traffic():
     return WIDE_TRAFFIC["bytes_per_launch"], WIDE_TRAFFIC["capture"]
 
 
-def time_quantize_act(h3q, x, flush, reps=10):
-    """Average device time of A2 alone (BF16 -> INT8 + scales), L2 flushed."""
+def time_quantize_act(h3q, x, flush, launches=36):
+    """Average device time of A2 alone (BF16 -> INT8 + scales) in steady
+    state: back-to-back launches between two CUDA events, rotating over copies
+    of X (and of the outputs) that together exceed L2 by far, so every launch
+    reads its X from DRAM and finds the previous launch's outputs dirty in L2,
+    as in a stream of layers.  (A write flush before a single launch would
+    instead leave L2 full of the flush buffer's dirty lines, whose write-back
+    the short kernel would pay for; timing single launches from the host would
+    add the launch latency.)"""
     import torch
-    xq = torch.empty((M, K), dtype=torch.int8, device=x.device)
-    xs = torch.empty((M,), dtype=torch.float32, device=x.device)
-    h3q.h3q_quantize_act(x, xq, xs)
-    tot = 0.0
-    for _ in range(reps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        h3q.h3q_quantize_act(x, xq, xs)
-        b.record()
-        torch.cuda.synchronize()
-        tot += a.elapsed_time(b)
-    return tot / reps * 1e-3
+    copies = max(2, -(-L2_FLUSH_BYTES // (3 * x.numel())))   # inputs + outputs: 4x L2 or more
+    xs_in = [x.clone() for _ in range(copies)]
+    outs = [(torch.empty((M, K), dtype=torch.int8, device=x.device),
+             torch.empty((M,), dtype=torch.float32, device=x.device)) for _ in range(copies)]
+    for i in range(copies):
+        h3q.h3q_quantize_act(xs_in[i], *outs[i])
+    flush.zero_()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(launches):
+        h3q.h3q_quantize_act(xs_in[i % copies], *outs[i % copies])
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / launches * 1e-3
+
+
+def time_same_size_copy(nbytes, dev, launches=36):
+    """Steady-state time of a plain device copy moving `nbytes` (half read,
+    half written), rotating over buffers that together exceed L2 by far, as
+    time_quantize_act does: the rate a kernel of that size can reach, against
+    which the whole-GPU copy peak (measured on gigabytes) overstates it."""
+    import torch
+    half = nbytes // 2
+    copies = max(2, -(-L2_FLUSH_BYTES // nbytes))
+    src = [torch.ones((half,), dtype=torch.uint8, device=dev) for _ in range(copies)]
+    dst = [torch.empty((half,), dtype=torch.uint8, device=dev) for _ in range(copies)]
+    for i in range(copies):
+        dst[i].copy_(src[i])
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(launches):
+        dst[i % copies].copy_(src[(i + 1) % copies])
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / launches * 1e-3
 
 
 def legacy_tops(h3q, x, wq, wsc, bias, dev, reps=5):
@@ -747,6 +784,79 @@ def run_sweep_block(h3q, synth, dev, flush, steps, warmup, peaks):
             "sweep_50_blocks_ms": 50 * t / 1e3,
             "note": "Q,K,V,O grouped + FC1 + FC2, each from BF16 X (A2 included); "
                     "50 blocks extrapolated from block 0"}
+
+
+KERNEL_CASES = ("attn", "attn_grouped", "fc1", "fc2", "quantize_act")
+
+
+def run_kernel_case(args):
+    """One kernel's workload run on its own, for profiling (ncu) and quick
+    timing: `--warmup` untimed calls, then `--steps` calls, each timed with
+    CUDA events after an L2 flush, and one line of medians.  attn: a
+    reuse-mode attention Linear (8192 x 5376 x 5376); attn_grouped: the
+    grouped Q, K, V, O call from BF16 X; fc1 / fc2: reuse-mode calls on
+    device-drawn inputs of those workloads; quantize_act: A2 alone on the
+    attention X (INT8 out)."""
+    import numpy as np
+    import torch
+    import w8a8_int8_linear_h3q_gb300 as h3q
+    import synth
+    h3q.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+    name = args.kernel_case
+    if name in ("fc1", "fc2"):
+        x, w, b = synth.device_case(name, dev)
+        lin = [(*h3q.h3q_quantize_weights(w), b)]
+        del w
+    else:
+        case = synth.attn()
+        x = torch.from_numpy(case.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        n_lin = 4 if name == "attn_grouped" else 1
+        lin = []
+        for w, bb in list(zip(case.w, case.bias_bits))[:n_lin]:
+            q, sc = h3q.h3q_quantize_weights(torch.from_numpy(w).to(dev))
+            lin.append((q, sc, torch.from_numpy(bb.view(np.int16)).view(torch.bfloat16).to(dev)))
+        del case
+    Mc, Kc = x.shape
+    Nc = lin[0][0].shape[0]
+    xs = torch.empty((Mc,), dtype=torch.float32, device=dev)
+    if name == "quantize_act":
+        xq = torch.empty((Mc, Kc), dtype=torch.int8, device=dev)
+        fn = lambda: h3q.h3q_quantize_act(x, xq, xs)
+        ops = None
+    elif name == "attn_grouped":
+        ys = [torch.empty((Mc, Nc), dtype=torch.bfloat16, device=dev) for _ in lin]
+        ws = torch.empty((h3q.h3q_linear_grouped_workspace_bytes(len(lin), Mc, Nc, Kc),),
+                         dtype=torch.uint8, device=dev)
+        fn = lambda: h3q.h3q_linear_w8a8_grouped(x, [a[0] for a in lin], [a[1] for a in lin],
+                                                 [a[2] for a in lin], xs=xs, ys=ys, workspace=ws)
+        ops = 2 * Mc * Nc * Kc * len(lin)
+    else:
+        q, sc, b = lin[0]
+        y = torch.empty((Mc, Nc), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty((h3q.h3q_linear_workspace_bytes(Mc, Nc, Kc),), dtype=torch.uint8,
+                         device=dev)
+        h3q.h3q_linear_w8a8(x, q, sc, b, xs=xs, y=y, workspace=ws)       # codes the activations
+        fn = lambda: h3q.h3q_linear_w8a8(None, q, sc, b, xs=xs, y=y, workspace=ws)
+        ops = 2 * Mc * Nc * Kc
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        e.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(e) * 1e3)
+    t = statistics.median(ts)
+    print(json.dumps({"kernel_case": name, "M": Mc, "N": Nc, "K": Kc, "median_us": t,
+                      "tops": ops / t / 1e6 if ops else None, "calls": args.steps}), flush=True)
+    return 0
 
 
 def run_configs(args):
@@ -854,11 +964,16 @@ def main():
     ap.add_argument("--configs", default=None,
                     help="instead of the contract line, print a per-workload table: 'all' or "
                          "a comma list of " + ",".join(CONFIG_TABLE))
+    ap.add_argument("--kernel-case", default=None, choices=KERNEL_CASES,
+                    help="instead of the contract line, run one kernel's workload on its own "
+                         "(for profiling): " + ",".join(KERNEL_CASES))
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.kernel_case:
+        return run_kernel_case(args)
     if args.configs:
         return run_configs(args)
     return run_gpu(args)

@@ -57,24 +57,24 @@ __device__ __forceinline__ bool epilogue_scales_in_range(float sa, float sw) {
   return (sa == 0.f || (sa >= 0x1p-60f && sa <= 0x1p45f)) && (sw >= 0x1p-40f && sw <= 0x1p45f);
 }
 
-// Cheap path first: c = RN(s_a * s_w), P = RN(float(acc) * c + 0), v = RN(P +
-// bias).  The +0 addend (one fused operation, no extra rounding) makes every
-// zero product +0, whatever the signs of its factors, so a zero accumulator
-// held as -0 in FP32 gives the same bits as the integer 0.
-// float(acc) is exact up to |acc| = 2^24 and within 2^-24 relative above, so P
-// carries a relative error below 3 * 2^-24, and v adds at most 2^-24 |v|.  When
-// |v| >= 2^-10 |P| the total is below 2^-12 |v|, far under half a BF16 ulp
-// (>= 2^-9 |v|), so one BF16 rounding of v lands within one ulp of the exact
-// value.  Cancellation (|v| < 2^-10 |P|) or scales outside the range above
-// take the exact path.  Every kernel forms y by these same operations (the
-// hot kernel's paired FP32 instructions perform them two tokens at a time),
-// so y depends on (acc, s_a, s_w, bias) alone: not on the kernel, the tile or
-// the call that produced the accumulator.
+// Cheap path first: c = RN(s_a * s_w), then v = RN(float(acc) * c + bias), one
+// fused multiply-add.  float(acc) is exact up to |acc| = 2^24 and within 2^-24
+// relative above, and c is within 2^-24 relative, so the FMA's exact argument
+// differs from the exact value by at most 2^-23 |acc c|, and its rounding adds
+// at most 2^-24 |v|.  When |v| >= 2^-10 |bias|, |acc c| = |v - bias| <= 1025 |v|
+// (up to those rounding terms), so the total is below 2^-12 |v|, far under
+// half a BF16 ulp (>= 2^-9 |v|), and one BF16 rounding of v lands within one
+// ulp of the exact value.  A zero accumulator gives v = bias exactly.
+// Cancellation (|v| < 2^-10 |bias|) or scales outside the range above take
+// the exact path; with acc != 0 the check also keeps v a normal FP32 number
+// (|acc c| >= 2^-100 when the scales are in range).  Every kernel forms y by
+// these same operations (the hot kernel's paired FP32 instructions perform
+// them two tokens at a time), so y depends on (acc, s_a, s_w, bias) alone: not
+// on the kernel, the tile or the call that produced the accumulator.
 __device__ __forceinline__ float epilogue_value(int acc, float sa, float sw, float bias) {
   if (epilogue_scales_in_range(sa, sw)) {
-    const float p = __fmaf_rn(__int2float_rn(acc), __fmul_rn(sa, sw), 0.f);
-    const float v = __fadd_rn(p, bias);
-    if (fabsf(v) >= fabsf(p) * 0x1p-10f) return v;
+    const float v = __fmaf_rn(__int2float_rn(acc), __fmul_rn(sa, sw), bias);
+    if (fabsf(v) >= fabsf(bias) * 0x1p-10f) return v;
   }
   if (acc == 0) return bias;
   return epilogue_value_careful(acc, sa, sw, bias);
@@ -82,6 +82,14 @@ __device__ __forceinline__ float epilogue_value(int acc, float sa, float sw, flo
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(uint32_t(b) << 16);
+}
+
+// A bias element as the epilogue uses it: its FP32 value, with -0 taken as +0
+// (adding +0 leaves every other value unchanged).  A zero accumulator then
+// gives v = +0 + bias with the same bits whether the accumulator is held as
+// the integer 0 or as an FP32 sum that came out -0.
+__device__ __forceinline__ float bias_value(uint16_t b) {
+  return __fadd_rn(bf16_bits_to_float(b), 0.f);
 }
 
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float v) {

@@ -137,8 +137,8 @@ gemm_mma_s8_kernel(const int8_t* __restrict__ A, const float* __restrict__ sa,
     if (n >= N) continue;
     const bool two = n + 1 < N;
     const float sw0 = sw[n], sw1 = two ? sw[n + 1] : 0.f;
-    const float b0 = bias ? __uint_as_float(uint32_t(bias[n]) << 16) : 0.f;
-    const float b1 = (bias && two) ? __uint_as_float(uint32_t(bias[n + 1]) << 16) : 0.f;
+    const float b0 = bias ? bias_value(bias[n]) : 0.f;
+    const float b1 = (bias && two) ? bias_value(bias[n + 1]) : 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
 #pragma unroll

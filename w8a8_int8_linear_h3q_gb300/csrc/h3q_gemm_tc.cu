@@ -422,7 +422,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constan
       uint16_t* Y = lin.y[g];
       int32_t* ACC = lin.acc[g];
       const float swn = n_ok ? lin.sw[g][n] : 0.f;
-      const float bn = (n_ok && bias) ? bf16_bits_to_float(bias[n]) : 0.f;
+      const float bn = (n_ok && bias) ? bias_value(bias[n]) : 0.f;
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
         const int m0 = mb * BN + 64 * half + 32 * blk;

@@ -95,7 +95,6 @@ constexpr int B_SLOTS = 4;              // super-stage slots: activation halves 
 constexpr int A_SLOTS = 2;              // super-stage slots: FP16 weights (TMEM)
 constexpr int W_SLOTS = 4;              // super-stage slots: INT8 weights (SMEM)
 constexpr int SQ = 4;                   // tile-queue entries
-constexpr int GROUP_M = 8;              // token blocks per raster group
 constexpr int CLUSTER = 2;
 constexpr uint16_t CLUSTER_MASK = (1u << CLUSTER) - 1;
 constexpr int MMA_WARP = 1;
@@ -180,6 +179,8 @@ struct Shape {
   int list_cap;       // entries of one Linear's fallback list
   int seg_ss;         // super-stages per norm segment
   uint64_t wmax2;     // 128^2 K: no weight row's sum of squares exceeds it
+  int panel;          // raster panel: token blocks (wpanel 0) or channel-block pairs (1)
+  int wpanel;
 };
 
 // A TILE_CKPT tile's plan: where the accumulator is checked, and the largest
@@ -192,17 +193,26 @@ struct TilePlan {
 
 // Cluster tile t -> Linear g, token block mb (256 tokens) and channel-block
 // pair.  The Linears alternate fastest, so concurrent tiles of different
-// Linears read the same activation tiles.
+// Linears read the same activation tiles.  The tiles are walked in panels:
+// either `panel` token blocks at a time, with every channel-block pair of
+// them before the next panel (the panel's activations stay in L2 while the
+// weights stream past), or `panel` channel-block pairs at a time, with every
+// token block of them (the panel's weights stay, the activations stream).
+// Within a panel its own index runs fastest, so the concurrent tiles of a
+// round share the streamed operand's tiles too.
 __device__ __forceinline__ void tile_coords(const Shape& s, int t, int& g, int& mb, int& pair) {
   g = t % s.G;
   t /= s.G;
-  const int per_group = GROUP_M * s.ntc;
-  const int grp = t / per_group;               // raster group of GROUP_M token blocks
-  const int first_m = grp * GROUP_M;
-  const int gm = min(GROUP_M, s.mt - first_m);
+  const int span = s.wpanel ? s.ntc : s.mt;    // the panel's dimension
+  const int across = s.wpanel ? s.mt : s.ntc;  // walked once per panel
+  const int per_group = s.panel * across;
+  const int grp = t / per_group;
+  const int first = grp * s.panel;
+  const int gp = min(s.panel, span - first);
   const int r = t - grp * per_group;
-  mb = first_m + r % gm;
-  pair = r / gm;
+  const int a = first + r % gp, b = r / gp;
+  mb = s.wpanel ? b : a;
+  pair = s.wpanel ? a : b;
 }
 
 // Warp-collective: tile_path past its first test.  Lanes 0-15 read the pair's 16
@@ -338,16 +348,14 @@ __device__ __forceinline__ void list_for_chunked(const Shape& shp, uint32_t* sta
 // The epilogue's instructions compete for issue slots with the converter
 // warps, which are on the critical path right after a tile's accumulator is
 // released, so the common case is kept short (and runs two tokens per
-// instruction where it can).  Per element: c = RN(s_a s_w),
-// P = RN(t c) (relative error below 2^-23) and v = RN(P + bias) (at most
-// 2^-24 |v| more).  Whenever |v| >= 2^-10 |P| the total is below 2^-12 |v|,
-// under half a BF16 ulp, so one BF16 rounding of v is within one ulp of the
-// exact value.  Scales in the checked ranges keep c in [2^-100, 2^90], so for
-// t != 0 P is a finite normal number and the check also keeps v far above
-// the subnormal range; t = 0 gives v = bias exactly.  An element that fails
-// the check (deep cancellation with the bias) takes the error-free path.
-// Blocks with scales outside those ranges, ragged token tails and the raw
-// INT32 output take the general per-element path.
+// instruction where it can).  Per element: c = RN(s_a s_w) and
+// v = RN(t c + bias), one FMA; the error argument is epilogue_value's
+// (h3q_epilogue.cuh): whenever |v| >= 2^-10 |bias| (a threshold formed once
+// per channel), one BF16 rounding of v is within one ulp of the exact value,
+// and t = 0 gives v = bias exactly.  An element that fails the check (deep
+// cancellation with the bias) takes the error-free path.  Blocks with scales
+// outside the checked ranges, ragged token tails and the raw INT32 output
+// take the general per-element path.
 __device__ __forceinline__ void emit_block(const uint32_t (&d)[32], float sa_l, int mbase,
                                            float swn, float bn, int n, bool n_ok,
                                            const Shape& shp, uint16_t* __restrict__ Y,
@@ -362,6 +370,7 @@ __device__ __forceinline__ void emit_block(const uint32_t (&d)[32], float sa_l, 
     // operations as the scalar ones, half the instructions)
     const uint64_t sw2 = (uint64_t(__float_as_uint(swn)) << 32) | __float_as_uint(swn);
     const uint64_t b2 = (uint64_t(__float_as_uint(bn)) << 32) | __float_as_uint(bn);
+    const float bthr = fabsf(bn) * 0x1p-10f;
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
       // both tokens' scales in one broadcast load (every lane reads the same 8 bytes)
@@ -369,15 +378,13 @@ __device__ __forceinline__ void emit_block(const uint32_t (&d)[32], float sa_l, 
       const float sa_a = sab.x, sa_b = sab.y;
       const uint64_t sa2 = (uint64_t(__float_as_uint(sa_b)) << 32) | __float_as_uint(sa_a);
       const uint64_t t2 = (uint64_t(d[j + 1]) << 32) | d[j];
-      uint64_t c2, p2, v2;
+      uint64_t c2, v2;
       asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(c2) : "l"(sa2), "l"(sw2));
-      asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(p2) : "l"(t2), "l"(c2), "l"(uint64_t(0)));
-      asm("add.rn.f32x2 %0, %1, %2;" : "=l"(v2) : "l"(p2), "l"(b2));
-      const float pa = __uint_as_float(uint32_t(p2)), pb = __uint_as_float(uint32_t(p2 >> 32));
+      asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(v2) : "l"(t2), "l"(c2), "l"(b2));
       float va = __uint_as_float(uint32_t(v2)), vb = __uint_as_float(uint32_t(v2 >> 32));
-      if (!(fabsf(va) >= fabsf(pa) * 0x1p-10f))
+      if (!(fabsf(va) >= bthr))
         va = epilogue_value_careful(__float2int_rn(__uint_as_float(d[j])), sa_a, swn, bn);
-      if (!(fabsf(vb) >= fabsf(pb) * 0x1p-10f))
+      if (!(fabsf(vb) >= bthr))
         vb = epilogue_value_careful(__float2int_rn(__uint_as_float(d[j + 1])), sa_b, swn, bn);
       uint32_t h2;
       asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h2) : "f"(vb), "f"(va));
@@ -834,7 +841,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
       // (affine mode: no scales)
       const float swn = (!kAffine && n_ok) ? outs.sw[g][n] : 0.f;
       const uint16_t* bias = outs.bias[g];
-      const float bn = (n_ok && bias) ? bf16_bits_to_float(bias[n]) : 0.f;
+      const float bn = (n_ok && bias) ? bias_value(bias[n]) : 0.f;
       const int m0 = mb * BN + 64 * cq;
       const float sa0 = (!kAffine && m0 + lane < shp.M) ? sa[m0 + lane] : 0.f;
       const float sa1 = (!kAffine && m0 + 32 + lane < shp.M) ? sa[m0 + 32 + lane] : 0.f;
@@ -871,6 +878,24 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The raster's panel.  By default, panels of 8 token blocks with every
+// channel-block pair of them (measured best for the grouped attention call,
+// fc1 and fc2: larger token panels, channel-pair panels and evict-first L2
+// hints on the streamed operand all read more from DRAM, because the
+// persistent clusters drift apart in time and a shared tile leaves L2 before
+// its last reader comes).  When the weights of all G Linears (one byte per
+// element in both modes) fit in kAllWeightsBytes, one panel holds every
+// channel-block pair: the weights stay in L2 and each token block is read
+// once (a single attention Linear: 212 -> 139 MB read per launch).
+constexpr int kTokenPanel = 8;
+constexpr double kAllWeightsBytes = 48.0 * (1 << 20);
+
+void choose_raster(Shape& s) {
+  const double weights = double(s.G) * double(s.N) * double(s.K);
+  s.wpanel = weights <= kAllWeightsBytes ? 1 : 0;
+  s.panel = s.wpanel ? s.ntc : kTokenPanel;
+}
 
 // Both modes: act is [M, ld] 16-bit (ld a multiple of 64), viewed as
 // (64-element chunk, row, chunk index); one box is two k-blocks of 128 rows.
@@ -928,6 +953,7 @@ cudaError_t launch_wide(const uint16_t* act, int64_t ld, const float* sa, const 
   shp.list_cap = int(fallback_list_capacity(M, N));
   shp.seg_ss = norm_segment_len(K) / kSegQuantum;
   shp.wmax2 = uint64_t(128 * 128) * uint64_t(K);
+  choose_raster(shp);
 
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);

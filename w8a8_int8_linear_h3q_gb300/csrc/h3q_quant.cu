@@ -284,7 +284,7 @@ __device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t m, uint32_t w) {
   return r;
 }
 
-// The row kernel keeps its per-element work short, since a row's work is
+// The row kernels keep their per-element work short, since a row's work is
 // spread over 256 threads and any per-row step is repeated by all 8 warps:
 //   - the absmax takes one paired BF16 instruction per 32-bit word;
 //   - one warp turns the block's maximum into the scale s and its reciprocal
@@ -293,37 +293,46 @@ __device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t m, uint32_t w) {
 //   - with norm maxima requested (kSq), each thread stores the sum of q^2 of
 //     each of its vectors in shared memory, and four warps then add up one
 //     norm segment each while a fifth adds up the whole row.
-// Short rows: eight blocks resident per SM (32 registers a thread), so that
-// enough rows are in flight to keep HBM busy; six (40 registers) when INT8
-// codes are written, whose byte packing needs a few more registers (at 32
-// they spill).
+template <int kVPT, bool kSq>
+struct RowSmem {
+  uint32_t red[kRowThreads / 32];
+  float2 sr;
+  uint32_t vsq[kSq ? kRowThreads * kVPT : 1];   // per-vector sums of q^2
+};
+
+// This thread's vectors of row `row` (j = threadIdx.x + 256 i), streamed past L1.
+template <int kVPT>
+__device__ __forceinline__ void load_row(const uint16_t* __restrict__ x, int64_t row, int K,
+                                         int nvec, uint4 (&v)[kVPT]) {
+  const uint4* xr = reinterpret_cast<const uint4*>(x + row * int64_t(K));
+#pragma unroll
+  for (int i = 0; i < kVPT; ++i) {
+    const int j = int(threadIdx.x) + kRowThreads * i;
+    if (j < nvec) v[i] = ld_stream(xr + j);
+  }
+}
+
+// Block-collective: quantise one row held in registers (v, as load_row left
+// it).  Three block barriers (two without kSq).
 template <int kVPT, bool kQ8, bool kF16, bool kSq>
-__global__ void __launch_bounds__(kRowThreads, kVPT <= 3 ? (kQ8 ? 6 : 8) : 2)
-quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__ q8,
-                     float* __restrict__ scale, uint16_t* __restrict__ qh, int ldh,
-                     uint32_t* __restrict__ sq_max, uint32_t* __restrict__ seg_max,
-                     int seg_len) {
+__device__ __forceinline__ void quant_row(RowSmem<kVPT, kSq>& sm, const uint4 (&v)[kVPT],
+                                          int64_t row, int K, int nvec,
+                                          int8_t* __restrict__ q8, float* __restrict__ scale,
+                                          uint16_t* __restrict__ qh, int ldh,
+                                          uint32_t* __restrict__ sq_max,
+                                          uint32_t* __restrict__ seg_max, int seg_len) {
   constexpr int kWarpsPerRow = kRowThreads / 32;
   static_assert(kWarpsPerRow > kNormSegs, "a warp per norm segment and one for the row");
-  __shared__ uint32_t red[kWarpsPerRow];
-  __shared__ float2 sr;
-  __shared__ uint32_t vsq[kSq ? kRowThreads * kVPT : 1];   // per-vector sums of q^2
-  const int64_t row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nvec = K >> 3;
-  const uint4* xr = reinterpret_cast<const uint4*>(x + row * int64_t(K));
   const int64_t base = row * int64_t(K), hbase = row * int64_t(ldh);
   if constexpr (kF16) {   // zero the row's padding up to the coded row stride
     for (int j = nvec + int(threadIdx.x); j < (ldh >> 3); j += kRowThreads)
       *reinterpret_cast<uint4*>(qh + hbase + 8 * int64_t(j)) = make_uint4(0, 0, 0, 0);
   }
-  uint4 v[kVPT];
   uint32_t m2 = 0;
 #pragma unroll
   for (int i = 0; i < kVPT; ++i) {
-    const int j = threadIdx.x + kRowThreads * i;
-    if (j < nvec) {
-      v[i] = ld_stream(xr + j);
+    if (int(threadIdx.x) + kRowThreads * i < nvec) {
       m2 = bf16x2_absmax(bf16x2_absmax(m2, v[i].x), v[i].y);
       m2 = bf16x2_absmax(bf16x2_absmax(m2, v[i].z), v[i].w);
     }
@@ -331,28 +340,28 @@ quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__
   uint32_t mbits = max(m2 & 0x7FFFu, (m2 >> 16) & 0x7FFFu);
 #pragma unroll
   for (int o = 16; o; o >>= 1) mbits = max(mbits, __shfl_xor_sync(0xFFFFFFFFu, mbits, o));
-  if (lane == 0) red[warp] = mbits;
+  if (lane == 0) sm.red[warp] = mbits;
   __syncthreads();
   if (warp == 0) {
-    uint32_t m = lane < kWarpsPerRow ? red[lane] : 0u;
+    uint32_t m = lane < kWarpsPerRow ? sm.red[lane] : 0u;
 #pragma unroll
     for (int o = kWarpsPerRow / 2; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     if (lane == 0) {
       const float sc = row_scale(__uint_as_float(m << 16));
-      sr = make_float2(sc, __frcp_rn(sc));
+      sm.sr = make_float2(sc, __frcp_rn(sc));
       scale[row] = sc;
     }
   }
   __syncthreads();
-  const float s = sr.x, r = sr.y;
+  const float s = sm.sr.x, r = sm.sr.y;
   const bool fast = s >= 0x1p-120f;
 #pragma unroll
   for (int i = 0; i < kVPT; ++i) {
-    const int j = threadIdx.x + kRowThreads * i;
+    const int j = int(threadIdx.x) + kRowThreads * i;
     if (j < nvec) {
       const uint32_t sq = quant_store8<kQ8, kF16>(v[i], s, r, fast, q8, qh,
                                                   base + 8 * int64_t(j), hbase + 8 * int64_t(j));
-      if constexpr (kSq) vsq[j] = sq;
+      if constexpr (kSq) sm.vsq[j] = sq;
     }
   }
   if constexpr (kSq) {
@@ -363,7 +372,7 @@ quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__
       const int j0 = warp < kNormSegs ? warp * segv : 0;
       const int j1 = warp < kNormSegs ? min(nvec, j0 + segv) : nvec;
       uint32_t t = 0;
-      for (int j = j0 + lane; j < j1; j += 32) t += vsq[j];
+      for (int j = j0 + lane; j < j1; j += 32) t += sm.vsq[j];
 #pragma unroll
       for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
       if (lane == 0) {
@@ -375,6 +384,24 @@ quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__
       }
     }
   }
+}
+
+// One block per row: eight resident per SM for short rows (32 registers a
+// thread), two for rows of up to 12 * 256 vectors.  (With INT8 codes out the
+// short-row kernel spills 24 bytes at 32 registers; measured, eight blocks
+// with the spill beat six without it: 24.9 against 25.8 us at 8192 x 5376.)
+template <int kVPT, bool kQ8, bool kF16, bool kSq>
+__global__ void __launch_bounds__(kRowThreads, kVPT <= 3 ? 8 : 2)
+quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__ q8,
+                     float* __restrict__ scale, uint16_t* __restrict__ qh, int ldh,
+                     uint32_t* __restrict__ sq_max, uint32_t* __restrict__ seg_max,
+                     int seg_len) {
+  __shared__ RowSmem<kVPT, kSq> sm;
+  const int nvec = K >> 3;
+  uint4 v[kVPT];
+  load_row<kVPT>(x, blockIdx.x, K, nvec, v);
+  quant_row<kVPT, kQ8, kF16, kSq>(sm, v, blockIdx.x, K, nvec, q8, scale, qh, ldh, sq_max,
+                                  seg_max, seg_len);
 }
 
 // The same per-row work for long rows (K up to 24576), staged in shared
@@ -801,9 +828,11 @@ cudaError_t launch_quantize_act(const uint16_t* x, int64_t M, int64_t K, int8_t*
                                 cudaStream_t s, uint32_t* err) {
   const int64_t nvec = K / 8;
   // Short rows: one block per row, with enough blocks resident to keep HBM
-  // busy.  Longer rows (measured at K = 21504: 525 against 559 us), when the
-  // call has a status word for the bounded waits: rows staged in shared
-  // memory.
+  // busy (a persistent grid that loads the next row while it quantises the
+  // current one measured slower: 26.6 against 25.9 us alone, 33.5 against
+  // 30.3 us in a call).  Longer rows (measured at K = 21504: 525 against 559
+  // us), when the call has a status word for the bounded waits: rows staged
+  // in shared memory.
   if (nvec <= kRowThreads * 3)
     return launch_rows<3>(x, M, int(K), q, scale, q_f16, int(ldh), sq_max, s);
   if (err && nvec <= kStagedThreads * 12)
