@@ -639,10 +639,11 @@ WIDE_SOURCES = ["w8a8_int8_linear_h3q_gb300/csrc/h3q_gemm_wide.cu",
                 "w8a8_int8_linear_h3q_gb300/csrc/h3q_tc_ptx.cuh",
                 "w8a8_int8_linear_h3q_gb300/csrc/h3q_epilogue.cuh",
                 "w8a8_int8_linear_h3q_gb300/csrc/h3q_internal.cuh"]
-WIDE_TRAFFIC = {"bytes_per_launch": 281974016,
-                "source_sha256": "1a1496c3c8a70810596d489f2cb2eba5e1f4180539f6b089262017c236f4da11",
-                "capture": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one "
-                           "reuse-mode gemm_wide_kernel launch, attn Linear 8192x5376x5376"}
+WIDE_TRAFFIC = {"bytes_per_launch": 128295168 + 74402560,
+                "source_sha256": "abd010ee8e5a1581a4d2ee9962a77998955cbbf652d4656c961b0b1225c204d2",
+                "capture": "ncu --set full, one reuse-mode gemm_wide_kernel launch, attn Linear "
+                           "8192x5376x5376 (python bench.py --kernel-case attn --steps 3 "
+                           "--warmup 3; profiles/gemm_wide_attn_8192x5376x5376.md)"}
 
 
 def wide_sources_sha256() -> str:
@@ -786,7 +787,8 @@ def run_sweep_block(h3q, synth, dev, flush, steps, warmup, peaks):
                     "50 blocks extrapolated from block 0"}
 
 
-KERNEL_CASES = ("attn", "attn_grouped", "fc1", "fc2", "quantize_act")
+KERNEL_CASES = ("attn", "attn_grouped", "fc1", "fc2", "quantize_act", "image_down",
+                "image_qkv_affine")
 
 
 def run_kernel_case(args):
@@ -796,7 +798,10 @@ def run_kernel_case(args):
     reuse-mode attention Linear (8192 x 5376 x 5376); attn_grouped: the
     grouped Q, K, V, O call from BF16 X; fc1 / fc2: reuse-mode calls on
     device-drawn inputs of those workloads; quantize_act: A2 alone on the
-    attention X (INT8 out)."""
+    attention X (INT8 out); image_down: a reuse-mode call on the H3-Image down
+    projection (4096 x 5376 x 14336, checkpointed tiles); image_qkv_affine: the
+    group-wise affine comparison scheme's Linear on the H3-Image fused QKV
+    shape (4096 x 21504 x 5376, Q8/g64)."""
     import numpy as np
     import torch
     import w8a8_int8_linear_h3q_gb300 as h3q
@@ -810,6 +815,14 @@ def run_kernel_case(args):
         x, w, b = synth.device_case(name, dev)
         lin = [(*h3q.h3q_quantize_weights(w), b)]
         del w
+    elif name in ("image_down", "image_qkv_affine"):
+        case = synth.WORKLOADS["image_down" if name == "image_down" else "image_qkv"]()
+        x = torch.from_numpy(case.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+        w = torch.from_numpy(case.w[0]).to(dev)
+        b = torch.from_numpy(case.bias_bits[0].view(np.int16)).view(torch.bfloat16).to(dev)
+        lin = [((*h3q.h3q_quantize_weights_affine(w),) if name == "image_qkv_affine"
+                else (*h3q.h3q_quantize_weights(w),)) + (b,)]
+        del w, case
     else:
         case = synth.attn()
         x = torch.from_numpy(case.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -826,6 +839,11 @@ def run_kernel_case(args):
         xq = torch.empty((Mc, Kc), dtype=torch.int8, device=dev)
         fn = lambda: h3q.h3q_quantize_act(x, xq, xs)
         ops = None
+    elif name == "image_qkv_affine":
+        qa, ab, b = lin[0]
+        oa = h3q.h3q_linear_affine_w8(x, qa, ab, b)
+        fn = lambda: h3q.h3q_linear_affine_w8(x, qa, ab, b, y=oa["y"], status=oa["status"])
+        ops = 2 * Mc * Nc * Kc
     elif name == "attn_grouped":
         ys = [torch.empty((Mc, Nc), dtype=torch.bfloat16, device=dev) for _ in lin]
         ws = torch.empty((h3q.h3q_linear_grouped_workspace_bytes(len(lin), Mc, Nc, Kc),),

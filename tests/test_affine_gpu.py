@@ -125,3 +125,39 @@ def test_linear_affine_image_workloads_sampled(lib, oracle, dev, name):
                                c.bias_bits[0][cols])
     y = out["y"][torch.from_numpy(rows).to(dev)][:, torch.from_numpy(cols).to(dev)]
     _check_affine_y(oracle, _bits(y.contiguous()), ref, K)
+
+
+@pytest.mark.parametrize("bits,K,jmax", [(8, 1024, 8), (4, 1024, 8), (8, 5376, 4), (4, 5376, 4)])
+def test_linear_affine_exact_where_fp32_sums_are_exact(lib, oracle, dev, bits, K, jmax):
+    """A tight pin for the comparison scheme's Linear.  The general bound above
+    must allow the worst FP32 summation error, since the tensor cores' order is
+    not fixed; here the inputs sit on coarse grids that make every product and
+    every partial sum exact in FP32, in any order: activations j 2^-3 (|j| <=
+    jmax), weights k 2^-6 with every group holding the grid's two ends (so the
+    step is exactly 2^-6 and the dequantised weights are the k 2^-6
+    themselves), biases on 2^-9.  Then the sums are multiples of 2^-9 below
+    2^22 of those units, the bias adds exactly, and each output must be the
+    exact value rounded once to BF16, bit for bit."""
+    M, N = 300, 264
+    rng = np.random.default_rng(90 + bits + K)
+    L = 2 ** bits - 1
+    kmin, kmax = -(L + 1) // 2, L // 2                      # Q8: -128..127, Q4: -8..7
+    kk = rng.integers(kmin, kmax + 1, size=(N, K))
+    kk[:, 0::64], kk[:, 1::64] = kmin, kmax
+    w = (kk * 2.0 ** -6).astype(np.float32)
+    xb = oracle.round_to_bf16(rng.integers(-jmax, jmax + 1, size=(M, K)) * 2.0 ** -3)
+    bias = oracle.round_to_bf16(rng.integers(-64, 65, size=N) * 2.0 ** -9)
+    q, ab = lib.h3q_quantize_weights_affine(torch.from_numpy(w).to(dev), bits=bits)
+    assert bool((ab[:, :, 0] == 2.0 ** -6).all())
+    out = lib.h3q_linear_affine_w8(_bf16_dev(xb, dev), q, ab, _bf16_dev(bias, dev))
+    torch.cuda.synchronize()
+    assert int(out["status"][0]) == 0
+    oq, oa, ob = oracle.quantize_affine(w, bits=bits)
+    what = oracle.dequant_affine(oq, oa, ob)
+    assert np.array_equal(oracle.widen_bf16(what).astype(np.float64), kk * 2.0 ** -6)
+    ref = oracle.linear_affine(xb, what, bias)
+    assert np.all(ref["absum"] * 2 ** 9 < 2 ** 22)
+    got = _bits(out["y"])
+    bad = got != ref["y"]
+    assert not np.any(bad), (f"{int(bad.sum())} outputs differ from the once-rounded exact "
+                             f"value; first at {tuple(np.argwhere(bad)[0])}")
