@@ -441,7 +441,11 @@ def run_gpu(args):
                         "quantize_act_gbs": quant_bytes / quant_avg_s / 1e9,
                         "quantize_act_hbm_frac": quant_bytes / quant_avg_s / 1e9 / peaks["hbm_gbs"],
                         "quantize_act_timing": "steady state: back-to-back launches over "
-                                               "rotating copies of X and outputs (> 4x L2)",
+                                               "rotating copies of X and outputs (> 4x L2); "
+                                               "h3q_quantize_act launches with programmatic "
+                                               "dependent launch, so each launch's ramp "
+                                               "overlaps the previous one's tail (the "
+                                               "same-size torch copy does not)",
                         "same_size_copy_us": copy_s * 1e6,
                         "same_size_copy_hbm_frac": quant_bytes / copy_s / 1e9 / peaks["hbm_gbs"],
                         "quantize_act_frac_of_same_size_copy": copy_s / quant_avg_s,

@@ -100,7 +100,10 @@ h3q_status h3q_quantize_weights(const void* w, int w_dtype, int64_t N, int64_t K
  *   scale_out [M] FP32, written
  *
  * Non-finite activations are outside the contract: no check is made and the
- * affected rows' results are unspecified (no fault).
+ * affected rows' results are unspecified (no fault).  The kernel is launched
+ * with programmatic dependent launch: its blocks may be scheduled while the
+ * previous kernel on `stream` finishes, and wait for that kernel's results
+ * before they read x, so stream order is kept.
  */
 h3q_status h3q_quantize_act(const uint16_t* x, int64_t M, int64_t K,
                             int8_t* q_out, float* scale_out, cudaStream_t stream);

@@ -397,6 +397,11 @@ quant_act_row_kernel(const uint16_t* __restrict__ x, int K, int8_t* __restrict__
                      uint32_t* __restrict__ sq_max, uint32_t* __restrict__ seg_max,
                      int seg_len) {
   __shared__ RowSmem<kVPT, kSq> sm;
+  // with programmatic dependent launch: let the next grid be scheduled once
+  // every block has started, and wait for the previous grid's writes before
+  // reading X (both return at once without the launch attribute)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int nvec = K >> 3;
   uint4 v[kVPT];
   load_row<kVPT>(x, blockIdx.x, K, nvec, v);
@@ -766,14 +771,33 @@ cudaError_t launch_act(const uint16_t* x, int64_t M, int K, int8_t* q, float* s,
 }
 
 template <int kVPT, bool kQ8, bool kF16>
-void launch_rows_sq(dim3 grid, cudaStream_t st, const uint16_t* x, int K, int8_t* q, float* s,
-                    uint16_t* qh, int ldh, uint32_t* sqm, uint32_t* sgm, int sl) {
-  if (sqm)
+cudaError_t launch_rows_sq(dim3 grid, cudaStream_t st, const uint16_t* x, int K, int8_t* q,
+                           float* s, uint16_t* qh, int ldh, uint32_t* sqm, uint32_t* sgm,
+                           int sl) {
+  if (sqm) {
     quant_act_row_kernel<kVPT, kQ8, kF16, true><<<grid, kRowThreads, 0, st>>>(x, K, q, s, qh,
                                                                              ldh, sqm, sgm, sl);
-  else
-    quant_act_row_kernel<kVPT, kQ8, kF16, false><<<grid, kRowThreads, 0, st>>>(x, K, q, s, qh,
-                                                                              ldh, sqm, sgm, sl);
+    return cudaGetLastError();
+  }
+  // Where the quantiser runs on its own (h3q_quantize_act), it is launched
+  // with programmatic dependent launch: its blocks may be scheduled while the
+  // previous kernel on the stream finishes, and they wait for that kernel's
+  // writes (griddepcontrol.wait) before they read X.  Back to back, that
+  // overlaps each launch's ramp with the previous launch's tail: 24.95 ->
+  // 22.7 us at 8192 x 5376 in steady state.  (Inside a Linear call the
+  // quantiser follows the memset of the workspace's status block, which this
+  // attribute does not overlap.)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kRowThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, quant_act_row_kernel<kVPT, kQ8, kF16, false>, x, K, q, s, qh,
+                            ldh, sqm, sgm, sl);
 }
 
 template <int kVPT>
@@ -782,13 +806,9 @@ cudaError_t launch_rows(const uint16_t* x, int64_t M, int K, int8_t* q, float* s
   const dim3 grid(static_cast<unsigned>(M));
   uint32_t* sgm = seg_maxima(sqm, M);
   const int sl = norm_segment_len(K);
-  if (q && qh)
-    launch_rows_sq<kVPT, true, true>(grid, st, x, K, q, s, qh, ldh, sqm, sgm, sl);
-  else if (q)
-    launch_rows_sq<kVPT, true, false>(grid, st, x, K, q, s, qh, ldh, sqm, sgm, sl);
-  else
-    launch_rows_sq<kVPT, false, true>(grid, st, x, K, q, s, qh, ldh, sqm, sgm, sl);
-  return cudaGetLastError();
+  if (q && qh) return launch_rows_sq<kVPT, true, true>(grid, st, x, K, q, s, qh, ldh, sqm, sgm, sl);
+  if (q) return launch_rows_sq<kVPT, true, false>(grid, st, x, K, q, s, qh, ldh, sqm, sgm, sl);
+  return launch_rows_sq<kVPT, false, true>(grid, st, x, K, q, s, qh, ldh, sqm, sgm, sl);
 }
 
 template <int kVPT, bool kQ8, bool kF16>
