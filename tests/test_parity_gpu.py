@@ -395,3 +395,29 @@ def test_output_bits_depend_on_the_operands_only(lib, dev):
     assert torch.equal(with_acc["y"].view(torch.int16), ref)
     assert torch.equal(torch.cat(parts).view(torch.int16), ref)
     assert torch.equal(legacy["y"].view(torch.int16), ref)
+
+
+def test_quantize_act_waits_for_the_kernel_that_writes_x(lib, oracle, dev):
+    """h3q_quantize_act is launched with programmatic dependent launch: its
+    blocks may start while the previous kernel on the stream is finishing, and
+    must wait for it before reading X.  Here a kernel rewrites X right before
+    each call (alternating between two inputs; both are enqueued behind a
+    GPU-side sleep, so the quantiser's launch is processed while the copy runs);
+    every call's codes and scales must be those of the X just written."""
+    M, K = 8192, 5376
+    srcs = [_act(M, K, seed=s, special=False) for s in (11, 12)]
+    refs = [oracle.quantize_act(b) for b in srcs]
+    src_dev = [_bf16_dev(b, dev) for b in srcs]
+    x = torch.empty_like(src_dev[0])
+    q = torch.empty((M, K), dtype=torch.int8, device=dev)
+    s = torch.empty((M,), dtype=torch.float32, device=dev)
+    rows = torch.arange(0, M, 97, device=dev)
+    for i in range(6):
+        torch.cuda._sleep(1_000_000)             # keep the GPU busy while both are enqueued
+        x.copy_(src_dev[i % 2])                  # the producer kernel
+        lib.h3q_quantize_act(x, q, s)
+        got_q = q[rows].cpu().numpy()
+        got_s = s.cpu().numpy()
+        rq, rs = refs[i % 2]
+        check_exact(got_q, rq[rows.cpu().numpy()], f"q_a after write {i}")
+        check_exact(got_s, rs, f"s_a after write {i}")
