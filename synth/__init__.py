@@ -179,9 +179,14 @@ SWEEP_LINEARS = (("q", H3_WIDTH, H3_WIDTH), ("k", H3_WIDTH, H3_WIDTH),
                  ("fc1", H3_MLP_WIDTH, H3_WIDTH), ("fc2", H3_WIDTH, H3_MLP_WIDTH))
 
 
-def _sweep_seed(*path: int) -> int:
-    ss = np.random.SeedSequence([4, *path])
+def _seed_of(*path: int) -> int:
+    """A 63-bit torch generator seed from numpy's SeedSequence(path)."""
+    ss = np.random.SeedSequence(list(path))
     return int(ss.generate_state(1, dtype=np.uint64)[0] & ((1 << 63) - 1))
+
+
+def _sweep_seed(*path: int) -> int:
+    return _seed_of(4, *path)
 
 
 def sweep_x(K: int, device, M: int = SWEEP_M):
@@ -229,7 +234,7 @@ def device_case(name: str, device):
     else:
         raise ValueError(f"device_case: fc1 or fc2, not {name!r}")
     g = torch.Generator(device=device)
-    g.manual_seed(_sweep_seed_of(seed, 1))
+    g.manual_seed(_seed_of(seed, 1))
     z = torch.randn((M, K), generator=g, device=device, dtype=torch.float32)
     if name == "fc2":
         z = z * torch.sigmoid(z)            # SiLU of the normal draw (input preparation)
@@ -238,11 +243,6 @@ def device_case(name: str, device):
     w = torch.randn((N, K), generator=g, device=device, dtype=torch.float32) * std
     b = (torch.randn((N,), generator=g, device=device, dtype=torch.float32) * 0.1).to(torch.bfloat16)
     return x, w, b
-
-
-def _sweep_seed_of(*path: int) -> int:
-    ss = np.random.SeedSequence(list(path))
-    return int(ss.generate_state(1, dtype=np.uint64)[0] & ((1 << 63) - 1))
 
 
 WORKLOADS = {"tiny": tiny, "attn": attn, "fc1": fc1, "fc2": fc2, "image_qkv": image_qkv,
