@@ -341,6 +341,35 @@ def run_gpu(args):
     # A2 inside the call: the Q call (A2 + GEMM) less a reuse-mode call (GEMM)
     q_call_ms = [e[0].elapsed_time(e[1]) for e in pl_events]
 
+    # the same grouped step captured once in a CUDA graph and replayed (a
+    # secondary figure; the headline times the eager call)
+    graph_ms = None
+    try:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            h3q.h3q_linear_w8a8_grouped(x, wq, wsc, bias, xs=xs, ys=ys, workspace=gws,
+                                        stream=side)
+            side.synchronize()
+            with torch.cuda.graph(graph, stream=side):
+                h3q.h3q_linear_w8a8_grouped(x, wq, wsc, bias, xs=xs, ys=ys, workspace=gws,
+                                            stream=side)
+        torch.cuda.synchronize()
+        g_ms = []
+        for _ in range(min(args.steps, 20)):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            g_ms.append(a.elapsed_time(b))
+        graph_ms = max_over_ranks(statistics.median(g_ms), world, dev)
+        del graph
+    except RuntimeError as e:                      # reported, not fatal
+        graph_ms = f"capture failed: {e}"
+
     # end to end through the public API with host buffers: one call of
     # h3q_linear_w8a8_grouped_host per step uploads X from pinned host memory,
     # runs the grouped hot path and downloads the four outputs into pinned host
@@ -455,6 +484,9 @@ def run_gpu(args):
                             else None,
                         "gemm_us_per_linear": gemm_avg_s * 1e6,
                         "per_linear_step_tops": per_linear_tops,
+                        "step_graph_replay_ms": graph_ms,
+                        "step_graph_replay_tops": OPS_PER_STEP / (graph_ms * 1e-3) / 1e12
+                        if isinstance(graph_ms, float) else None,
                         "per_linear_step_ms": pl_ms / pl_steps,
                         "gemm_tops": gemm_tflops},
             "e2e": {"value": e2e_value, "unit": "TOPS", "ms_per_step":
