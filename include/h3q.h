@@ -425,9 +425,9 @@ h3q_status h3q_linear_w8a8_noalloc(const uint16_t* x, int8_t* xq, float* xs,
  * with the same M and K, and no other no-alloc call since): H3Q_OK, or
  * H3Q_ERR_TIMEOUT if one of its bounded device-side waits gave up -- what
  * h3q_workspace_status reports for a caller-provided workspace (the pages
- * have no counterpart).  Shapes that h3q_linear_w8a8_noalloc rejects give
- * H3Q_ERR_UNSUPPORTED_SHAPE.  SYNCHRONISES `stream` to read the status word;
- * allocates nothing.
+ * have no counterpart).  An M and K whose workspace would not fit the built-in
+ * scratch even at N = 1 give H3Q_ERR_UNSUPPORTED_SHAPE.  SYNCHRONISES `stream`
+ * to read the status word; allocates nothing.
  */
 h3q_status h3q_linear_w8a8_noalloc_status(int64_t M, int64_t K, cudaStream_t stream);
 
