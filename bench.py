@@ -343,7 +343,7 @@ def run_gpu(args):
 
     # the same grouped step captured once in a CUDA graph and replayed (a
     # secondary figure; the headline times the eager call)
-    graph_ms = None
+    graph_ms, graph_note = float("inf"), None
     try:
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
@@ -365,10 +365,15 @@ def run_gpu(args):
             b.record(stream)
             torch.cuda.synchronize()
             g_ms.append(a.elapsed_time(b))
-        graph_ms = max_over_ranks(statistics.median(g_ms), world, dev)
+        graph_ms = statistics.median(g_ms)
         del graph
     except RuntimeError as e:                      # reported, not fatal
-        graph_ms = f"capture failed: {e}"
+        graph_note = f"capture failed: {e}"
+    # every rank takes part in the reduction, whether or not its capture worked
+    # (a failed rank sends infinity, so the slowest-rank figure reports it)
+    graph_ms = max_over_ranks(graph_ms if graph_note is None else float("inf"), world, dev)
+    if graph_ms == float("inf"):
+        graph_ms = graph_note or "capture failed on another rank"
 
     # end to end through the public API with host buffers: one call of
     # h3q_linear_w8a8_grouped_host per step uploads X from pinned host memory,
