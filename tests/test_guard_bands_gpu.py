@@ -141,3 +141,23 @@ def test_host_pipeline_staging_stays_inside_its_buffers(lib, dev):
     for i, g in enumerate(ys_dev):
         assert g.intact(), f"device output {i}: a guard byte changed"
         assert torch.equal(out["ys"][i].view(torch.int16), g.t.cpu().view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K", [(129, 131, 1040), (1559, 5376, 5376), (7, 1, 16)])
+def test_noalloc_writes_stay_inside_their_buffers(lib, dev, M, N, K):
+    """The allocation-free entry point writes only its outputs (its scratch is
+    internal): guard bands around y, the raw accumulators and the activation
+    scales, on ragged shapes up to the built-in scratch's edge (M = 1559 at
+    N = K = 5376)."""
+    x, w, b = _operands(M, N, K, seed=M + N + K + 5, dev=dev)
+    qw, sw = lib.h3q_quantize_weights(w)
+    y = Guarded((M, N), torch.bfloat16, dev)
+    acc = Guarded((M, N), torch.int32, dev)
+    xs = Guarded((M,), torch.float32, dev)
+    lib.h3q_linear_w8a8_noalloc(x, qw, sw, b, xs=xs.t, y=y.t, acc_out=acc.t)
+    torch.cuda.synchronize()
+    assert y.intact() and acc.intact() and xs.intact()
+    assert lib.h3q_linear_w8a8_noalloc_status(M, K) == lib.H3Q_OK
+    ref = lib.h3q_linear_w8a8(x, qw, sw, b, want_acc=True)
+    assert torch.equal(acc.t, ref["acc"])
+    assert torch.equal(y.t.view(torch.int16), ref["y"].view(torch.int16))
