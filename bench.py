@@ -14,8 +14,8 @@ Linear (multiply and add counted separately), whole-job over all ranks.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
 Under torchrun every rank runs an independent replica (the projection shards
-by token rows with no exchange; see the design notes), and rank 0 prints one
-JSON line.
+by token rows with no exchange, so no collective touches the data path), and
+rank 0 prints one JSON line.
 """
 from __future__ import annotations
 

@@ -25,7 +25,7 @@ and a biased BF16 Linear whose bias is added before the one rounding of the
 output ([P2] What the default preserves, the "addmm epilogue" bullet).
 
 The pages print no formula for the quantiser or the epilogue.  The readings
-taken where they are silent (each one also listed in the design notes):
+taken where they are silent:
   R1  scale = absmax / 127 as one IEEE FP32 division, round to nearest even;
   R2  q = clamp(rint(x / scale), -127, 127): FP32 division by the scale (not a
       multiply by 127/absmax), ties to even, -128 never produced;
@@ -216,8 +216,7 @@ def snr_db(y, y_ref) -> float:
 # down GEMMs; [P4] adds affine INT8, INT6 and INT4 checkpoints.  That scheme is
 # weight-only: per output channel and group of 64 consecutive inputs a step and
 # an offset ("affine"), the weights dequantised for a BF16 GEMM with the BF16
-# activations unquantised.  The pages give no formula; the readings (also in
-# the design notes):
+# activations unquantised.  The pages give no formula; the readings:
 #   R10  per group: lo = min, hi = max of its FP32 weights; alpha = RN((hi - lo)
 #       / (2^b - 1)), hi - lo rounded to FP32 first, one FP32 division;
 #       beta = lo; a group with hi == lo gets alpha = 1, and a positive range
