@@ -426,6 +426,8 @@ def run_gpu(args):
 
     peaks, peak_kind = _peaks()
     int8_probe = h3q.h3q_probe_mma_s8_tops()
+    f16_pair_probe = h3q.h3q_probe_mma_f16_pair_tflops(False)
+    f16_pair_probe_ss = h3q.h3q_probe_mma_f16_pair_tflops(True)
     gemm_avg_s = statistics.mean(gemm_ms) * 1e-3
     gemm_tflops = 2 * M * N * K / gemm_avg_s / 1e12
     quant_avg_s = time_quantize_act(h3q, x, flush)
@@ -470,6 +472,18 @@ def run_gpu(args):
                                 "note": "this path computes the exact INT8 products on the "
                                         "FP16 tensor pipe instead (no INT8 tcgen05 MMA on "
                                         "sm_103a); its roofline is the measured BF16 peak"},
+            # the ceiling of the instruction the GEMM issues, measured alone: the
+            # tensor-pipe share of the GEMM and of the step read against it
+            "instruction_peak": {"instruction": "tcgen05.mma.cta_group::2.kind::f16, "
+                                                "M = N = 256, K = 16, A in TMEM, B in shared "
+                                                "memory (the hot GEMM's form)",
+                                 "measured_tflops": f16_pair_probe,
+                                 "a_in_smem_tflops": f16_pair_probe_ss,
+                                 "measured_by": "h3q_probe_mma_f16_pair_tflops: one CTA pair "
+                                                "per two SMs issuing MMAs back to back over "
+                                                "resident operands, CUDA events",
+                                 "gemm_frac": gemm_tflops / f16_pair_probe,
+                                 "step_frac": value / f16_pair_probe},
             "kernels": {"legacy_mma_sync_s8_tops": legacy_tops(h3q, x, wq[0], wsc[0], bias[0], dev),
                         "quantize_act_us": quant_avg_s * 1e6,
                         "quantize_act_gbs": quant_bytes / quant_avg_s / 1e9,

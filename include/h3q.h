@@ -374,6 +374,25 @@ h3q_status h3q_selftest_bounded_wait(uint32_t* status, cudaStream_t stream);
 h3q_status h3q_probe_mma_s8_tops(double* tops, cudaStream_t stream);
 
 /*
+ * Throughput probe of the FP16 tensor instruction the hot GEMM issues (no
+ * counterpart on the pages; it supplies the ceiling that the GEMM's
+ * tensor-pipe share is read against): tcgen05.mma.cta_group::2.kind::f16,
+ * M = N = 256, K = 16, FP32 accumulator in TMEM, B K-major in shared memory
+ * with the 128-byte swizzle, and A in TMEM (a_in_smem = 0, the hot kernel's
+ * form) or in shared memory (a_in_smem = 1).  One CTA pair per two SMs, as
+ * many as can be resident at once, each issuing 65536 MMAs back to back over
+ * one resident k-block of small-integer operands (about 4 ms); the launch is
+ * timed with CUDA events on `stream`, and 2 * 256 * 256 * 16 operations per
+ * MMA over that time are written to *tflops (1e12 per second).
+ *
+ *   H3Q_ERR_INVALID_ARG  tflops NULL, or a_in_smem not 0 or 1
+ *   H3Q_ERR_TIMEOUT      the bounded wait for the MMAs gave up (2 s)
+ *
+ * Allocates no device memory; SYNCHRONISES `stream`.
+ */
+h3q_status h3q_probe_mma_f16_pair_tflops(double* tflops, int a_in_smem, cudaStream_t stream);
+
+/*
  * A3 + A4 on the legacy warp-level INT8 tensor instruction (mma.sync
  * m16n8k32 s8 -> s32), exact by construction; the same arithmetic and output
  * as h3q_linear_w8a8 from pre-quantised activations.  Kept as the baseline

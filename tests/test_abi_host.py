@@ -134,6 +134,9 @@ def test_valid_args_without_a_device_report_no_device(cdll):
     t = ctypes.c_double(-1.0)
     assert cdll.h3q_probe_mma_s8_tops(ctypes.byref(t), NUL) == 7
     assert t.value == 0.0
+    t = ctypes.c_double(-1.0)
+    assert cdll.h3q_probe_mma_f16_pair_tflops(ctypes.byref(t), 0, NUL) == 7
+    assert t.value == 0.0
 
 
 def test_grouped_linear_rejects_bad_args(cdll):
@@ -193,6 +196,10 @@ def test_chunk_diagnostics_reject_bad_args(cdll):
 
 def test_probe_rejects_bad_args(cdll):
     assert cdll.h3q_probe_mma_s8_tops(NUL, NUL) == 1
+    t = ctypes.c_double(0.0)
+    assert cdll.h3q_probe_mma_f16_pair_tflops(NUL, 0, NUL) == 1
+    assert cdll.h3q_probe_mma_f16_pair_tflops(ctypes.byref(t), 2, NUL) == 1
+    assert cdll.h3q_probe_mma_f16_pair_tflops(ctypes.byref(t), -1, NUL) == 1
 
 
 def test_selftest_rejects_bad_args(cdll):

@@ -74,6 +74,8 @@ def _declare(lib):
     lib.h3q_linear_w8a8_noalloc.restype = i32
     lib.h3q_probe_mma_s8_tops.argtypes = [ctypes.POINTER(ctypes.c_double), vp]
     lib.h3q_probe_mma_s8_tops.restype = i32
+    lib.h3q_probe_mma_f16_pair_tflops.argtypes = [ctypes.POINTER(ctypes.c_double), i32, vp]
+    lib.h3q_probe_mma_f16_pair_tflops.restype = i32
     lib.h3q_linear_w8a8_noalloc_status.argtypes = [i64, i64, vp]
     lib.h3q_linear_w8a8_noalloc_status.restype = i32
     lib.h3q_selftest_bounded_wait.argtypes = [vp, vp]
@@ -233,6 +235,18 @@ def h3q_probe_mma_s8_tops(stream=None) -> float:
     t = ctypes.c_double(0.0)
     _check(load().h3q_probe_mma_s8_tops(ctypes.byref(t), _stream(stream)),
            "h3q_probe_mma_s8_tops")
+    return float(t.value)
+
+
+def h3q_probe_mma_f16_pair_tflops(a_in_smem: bool = False, stream=None) -> float:
+    """Measured rate (TFLOP/s) of tcgen05.mma.cta_group::2.kind::f16 at
+    M = N = 256, K = 16, the instruction of the hot GEMM: A in TMEM (the
+    kernel's form) or, with a_in_smem, in shared memory.  Synchronises;
+    about 4 ms."""
+    t = ctypes.c_double(0.0)
+    _check(load().h3q_probe_mma_f16_pair_tflops(ctypes.byref(t), 1 if a_in_smem else 0,
+                                                _stream(stream)),
+           "h3q_probe_mma_f16_pair_tflops")
     return float(t.value)
 
 
