@@ -223,32 +223,37 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constan
 
   if (warp == 0) {
     // ---------------- TMA producer: activation tiles ----------------
-    if (lane == 0) {
-      P::tma_prefetch_desc(&act_map);
-      uint32_t gs = 0, gb = 0;             // super-stages seen, slots issued
-      bool ok = true;
-      for (int t = cid; ok && t < ntiles; t += ncl) {
-        int g, mb, nb;
-        tile_coords(shp, list, cnt, t, rank, g, mb, nb);
-        for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
-          const uint32_t slot = gs % SLOTS;
-          // the slot is free once this CTA's MMAs finished its previous use
-          if (!P::mbar_wait(&sm.empty_s[slot], ((gs / SLOTS) & 1u) ^ 1u, abort_flag, err,
-                            ERR_PRODUCER)) {
-            ok = false;
-            break;
-          }
-          // the super-stage's four activation tiles, two per copy (each box is
-          // two whole k-block tiles); boxes past the last k-block arrive as zeros
+    // warp-uniform: the waits by the whole warp, the copies by one elected lane
+    const uint32_t leader = P::elect_one();
+    if (leader) P::tma_prefetch_desc(&act_map);
+    uint32_t gs = 0, gb = 0;             // super-stages seen, slots issued
+    bool ok = true;
+    for (int t = cid; ok && t < ntiles; t += ncl) {
+      int g, mb, nb;
+      tile_coords(shp, list, cnt, t, rank, g, mb, nb);
+      for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
+        const uint32_t slot = gs % SLOTS;
+        // the slot is free once this CTA's MMAs finished its previous use
+        if (!P::mbar_wait_warp(&sm.empty_s[slot], ((gs / SLOTS) & 1u) ^ 1u, abort_flag, err,
+                               ERR_PRODUCER)) {
+          ok = false;
+          break;
+        }
+        // the super-stage's four activation tiles, two per copy (each box is
+        // two whole k-block tiles); boxes past the last k-block arrive as zeros
+        if (leader) {
           P::mbar_arrive_expect_tx(&sm.full_b[slot], SS * B_STAGE_BYTES);
 #pragma unroll
           for (int h = 0; h < SS / 2; ++h)
             P::tma_load_3d(P::smem_u32(sm.b[slot][2 * h]), &act_map, &sm.full_b[slot], 0,
                            mb * BN, ss * SS + 2 * h);
-          gb = gs + 1;
         }
+        __syncwarp();
+        gb = gs + 1;
       }
-      // no copy may still be landing in shared memory when the CTA exits
+    }
+    // no copy may still be landing in shared memory when the CTA exits
+    if (leader) {
       int no_abort = 0;
       volatile int* never = &no_abort;   // this drain does not follow the abort flag
       for (uint32_t i = gb > SLOTS ? gb - SLOTS : 0; i < gb; ++i)
@@ -257,29 +262,34 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constan
     __syncwarp();
   } else if (warp == WPROD_WARP) {
     // ---------------- TMA producer: INT8 weight tiles ----------------
-    if (lane == 0) {
+    const uint32_t leader = P::elect_one();
+    if (leader)
       for (int i = 0; i < shp.G; ++i) P::tma_prefetch_desc(&lin.w[i]);
-      uint32_t gs = 0, gw = 0;
-      bool ok = true;
-      for (int t = cid; ok && t < ntiles; t += ncl) {
-        int g, mb, nb;
-        tile_coords(shp, list, cnt, t, rank, g, mb, nb);
-        const int wrow = min(nb, shp.nt - 1) * BM;
-        for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
-          const uint32_t slot = gs % W_SLOTS;
-          if (!P::mbar_wait(&sm.empty_w[slot], ((gs / W_SLOTS) & 1u) ^ 1u, abort_flag, err,
-                            ERR_PRODUCER)) {
-            ok = false;
-            break;
-          }
+    uint32_t gs = 0, gw = 0;
+    bool ok = true;
+    for (int t = cid; ok && t < ntiles; t += ncl) {
+      int g, mb, nb;
+      tile_coords(shp, list, cnt, t, rank, g, mb, nb);
+      const int wrow = min(nb, shp.nt - 1) * BM;
+      for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
+        const uint32_t slot = gs % W_SLOTS;
+        if (!P::mbar_wait_warp(&sm.empty_w[slot], ((gs / W_SLOTS) & 1u) ^ 1u, abort_flag, err,
+                               ERR_PRODUCER)) {
+          ok = false;
+          break;
+        }
+        if (leader) {
           P::mbar_arrive_expect_tx(&sm.full_w[slot], (SS / 2) * W_BOX_BYTES);
 #pragma unroll
           for (int p = 0; p < SS / 2; ++p)
             P::tma_load_2d(P::smem_u32(sm.w[slot][p]), &lin.w[g], &sm.full_w[slot],
                            (ss * SS + 2 * p) * BK, wrow);
-          gw = gs + 1;
         }
+        __syncwarp();
+        gw = gs + 1;
       }
+    }
+    if (leader) {
       int no_abort = 0;
       volatile int* never = &no_abort;
       for (uint32_t i = gw > W_SLOTS ? gw - W_SLOTS : 0; i < gw; ++i)
@@ -288,41 +298,55 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_constan
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer: one wait and one commit per 16 MMAs ----------------
-    if (lane == 0) {
-      uint32_t gs = 0, gc = 0;            // super-stage and chunk counters
-      bool ok = true;
-      for (int t = cid; ok && t < ntiles; t += ncl) {
-        for (int c = 0; ok && c < shp.nchunks; ++c, ++gc) {
-          const int ss0 = c * shp.sspc, ss1 = min(shp.NSS, ss0 + shp.sspc);
-          const uint32_t buf = gc & 1u;
-          if (!P::mbar_wait(&sm.dempty[buf], ((gc >> 1) & 1u) ^ 1u, abort_flag, err, ERR_MMA)) {
+    // The whole warp runs the loop (warp-uniform waits, addresses and
+    // descriptors) and one elected lane issues every MMA and commit: a loop run
+    // by one lane alone loses issue slots to the busy warps of its SM
+    // sub-partition, and the tensor pipe then waits for its MMAs.
+    const uint32_t leader = P::elect_one();
+    uint32_t gs = 0, gc = 0;            // super-stage and chunk counters
+    bool ok = true;
+    for (int t = cid; ok && t < ntiles; t += ncl) {
+      for (int c = 0; ok && c < shp.nchunks; ++c, ++gc) {
+        const int ss0 = c * shp.sspc, ss1 = min(shp.NSS, ss0 + shp.sspc);
+        const uint32_t buf = gc & 1u;
+        if (!P::mbar_wait_warp(&sm.dempty[buf], ((gc >> 1) & 1u) ^ 1u, abort_flag, err,
+                               ERR_MMA)) {
+          ok = false;
+          break;
+        }
+        const uint32_t d_tmem = tmem + TM_D + buf * BN;
+        for (int ss = ss0; ss < ss1; ++ss, ++gs) {
+          const uint32_t slot = gs % SLOTS;
+          if (!P::mbar_wait_warp(&sm.full_a[slot], (gs / SLOTS) & 1u, abort_flag, err, ERR_MMA)) {
             ok = false;
             break;
           }
-          const uint32_t d_tmem = tmem + TM_D + buf * BN;
-          for (int ss = ss0; ss < ss1; ++ss, ++gs) {
-            const uint32_t slot = gs % SLOTS;
-            if (!P::mbar_wait(&sm.full_a[slot], (gs / SLOTS) & 1u, abort_flag, err, ERR_MMA)) {
-              ok = false;
-              break;
-            }
-            P::tc_fence_after();
-            const uint32_t a_tmem = tmem + TM_A + slot * (SS * 32);
-            const int nkb = min(SS, shp.KB - ss * SS);
-            for (int j = 0; j < nkb; ++j) {
-              const uint64_t bdesc = P::smem_desc_sw128(P::smem_u32(sm.b[slot][j]));
+          P::tc_fence_after();
+          const uint32_t a_tmem = tmem + TM_A + slot * (SS * 32);
+          const int nkb = min(SS, shp.KB - ss * SS);
+          uint64_t bdesc[SS];
+#pragma unroll
+          for (int j = 0; j < SS; ++j) bdesc[j] = P::smem_desc_sw128(P::smem_u32(sm.b[slot][j]));
+          if (leader) {
+#pragma unroll
+            for (int j = 0; j < SS; ++j) {
+              if (j >= nkb) break;
 #pragma unroll
               for (int kk = 0; kk < BK / 16; ++kk)
-                P::mma_f16_ts(d_tmem, a_tmem + j * 32 + kk * 8, bdesc + uint64_t(kk * 2), IDESC,
-                              (ss > ss0 || j > 0 || kk > 0) ? 1u : 0u);
+                P::mma_f16_ts(d_tmem, a_tmem + j * 32 + kk * 8, bdesc[j] + uint64_t(kk * 2),
+                              IDESC, (ss > ss0 || j > 0 || kk > 0) ? 1u : 0u);
             }
             P::mma_commit(&sm.empty_s[slot]);
           }
-          if (!ok) break;
-          P::mma_commit(&sm.dfull[buf]);
+          __syncwarp();
         }
+        if (!ok) break;
+        if (leader) P::mma_commit(&sm.dfull[buf]);
+        __syncwarp();
       }
-      // every MMA this thread issued has finished before TMEM is freed
+    }
+    // every MMA the leader issued has finished before TMEM is freed
+    if (leader) {
       P::mma_commit(&sm.mma_done);
       int no_abort = 0;
       volatile int* never = &no_abort;

@@ -298,15 +298,20 @@ __device__ __forceinline__ bool pop_tile(Smem& sm, uint32_t& nq, volatile int* a
   return true;
 }
 
-// Warp-collective take (with the entry's checkpoint bits); one arrival for
-// the warp.
+// Warp-collective take (with the entry's checkpoint bits, or its whole
+// checkpoint plan); one arrival for the warp.
 __device__ __forceinline__ bool pop_tile_warp(Smem& sm, uint32_t& nq, volatile int* abort_flag,
                                               uint32_t* err, uint32_t code, int& t, int lane,
-                                              uint32_t* ckpt = nullptr) {
+                                              uint32_t* ckpt = nullptr, TilePlan* plan = nullptr) {
   const uint32_t q = nq % SQ;
   if (!P::mbar_wait_warp(&sm.q_full[q], (nq / SQ) & 1u, abort_flag, err, code)) return false;
   t = sm.q_tile[q];
   if (ckpt) *ckpt = sm.q_ckpt[q];
+  if (plan) {
+    plan->ckpt = sm.q_ckpt[q];
+    if (plan->ckpt)
+      for (int i = 0; i < 2 * NSEG; ++i) plan->aw[i] = sm.q_aw[q][i];
+  }
   __syncwarp();
   if (lane == 0) P::mbar_arrive(&sm.q_empty[q]);
   ++nq;
@@ -568,32 +573,38 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
 
   if (warp == 0) {
     // ---------------- TMA producer: activation tiles ----------------
-    if (lane == 0) {
-      P::tma_prefetch_desc(&act_map);
-      uint32_t gs = 0, gb = 0, nq = 0;
-      bool ok = true;
-      for (;;) {
-        int t;
-        if (!pop_tile(sm, nq, abort_flag, err, ERR_PRODUCER, t) || t < 0) break;
-        int g, mb, pair;
-        tile_coords(shp, t, g, mb, pair);
-        const int row0 = mb * BN + int(rank) * BNH;
-        for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
-          const uint32_t slot = gs % B_SLOTS;
-          // the slot is free once the pair MMAs of its previous super-stage are done
-          if (!P::mbar_wait(&sm.empty_ss[slot], ((gs / B_SLOTS) & 1u) ^ 1u, abort_flag, err,
-                            ERR_PRODUCER)) {
-            ok = false;
-            break;
-          }
-          // this CTA's 128 tokens of the super-stage's two k-blocks
-          P::mbar_arrive_expect_tx(&sm.full_b[slot], SS * B_KBLOCK_BYTES);
-          P::tma_load_3d(P::smem_u32(sm.b[slot][0]), &act_map, &sm.full_b[slot], 0, row0, ss * SS);
-          gb = gs + 1;
+    // warp-uniform, like the MMA issuer: one elected lane issues the copies
+    const uint32_t leader = P::elect_one();
+    if (leader) P::tma_prefetch_desc(&act_map);
+    uint32_t gs = 0, gb = 0, nq = 0;
+    bool ok = true;
+    for (;;) {
+      int t;
+      if (!pop_tile_warp(sm, nq, abort_flag, err, ERR_PRODUCER, t, lane) || t < 0) break;
+      int g, mb, pair;
+      tile_coords(shp, t, g, mb, pair);
+      const int row0 = mb * BN + int(rank) * BNH;
+      for (int ss = 0; ss < shp.NSS; ++ss, ++gs) {
+        const uint32_t slot = gs % B_SLOTS;
+        // the slot is free once the pair MMAs of its previous super-stage are done
+        if (!P::mbar_wait_warp(&sm.empty_ss[slot], ((gs / B_SLOTS) & 1u) ^ 1u, abort_flag, err,
+                               ERR_PRODUCER)) {
+          ok = false;
+          break;
         }
-        if (!ok) break;
+        // this CTA's 128 tokens of the super-stage's two k-blocks
+        if (leader) {
+          P::mbar_arrive_expect_tx(&sm.full_b[slot], SS * B_KBLOCK_BYTES);
+          P::tma_load_3d(P::smem_u32(sm.b[slot][0]), &act_map, &sm.full_b[slot], 0, row0,
+                         ss * SS);
+        }
+        __syncwarp();
+        gb = gs + 1;
       }
-      // no copy may still be landing in shared memory when the CTA exits
+      if (!ok) break;
+    }
+    // no copy may still be landing in shared memory when the CTA exits
+    if (leader) {
       int no_abort = 0;
       volatile int* never = &no_abort;   // this drain does not follow the abort flag
       for (uint32_t i = gb > B_SLOTS ? gb - B_SLOTS : 0; i < gb; ++i)
@@ -603,6 +614,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
   } else if (warp == SCHED_WARP) {
     // ---------------- scheduler + TMA producer: INT8 weight tiles ----------------
     if (lane < shp.G) P::tma_prefetch_desc(&wmaps.m[lane]);
+    const uint32_t wleader = P::elect_one();
     uint32_t gs = 0, gw = 0, nq = 0;
     bool ok = true;
     for (int t = cid; t < shp.tiles; t += ncl) {
@@ -622,21 +634,26 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
       if (lane == 0) {
         ok = push_tile(sm, nq, t, path == TILE_CKPT ? &plan : nullptr, abort_flag, err);
         if (ok && path == TILE_CKPT && rank == 0) atomicAdd(status + 6, 1u);
-        const int wrow = min(2 * pair + int(rank), shp.nt - 1) * BM;
-        for (int ss = 0; ok && ss < shp.NSS; ++ss, ++gs) {
-          const uint32_t slot = gs % W_SLOTS;
-          if (!P::mbar_wait(&sm.empty_w[slot], ((gs / W_SLOTS) & 1u) ^ 1u, abort_flag, err,
-                            ERR_SCHED)) {
-            ok = false;
-            break;
-          }
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, int(ok), 0) != 0;
+      // the weight copies: warp-uniform waits, one elected lane issues
+      const int wrow = min(2 * pair + int(rank), shp.nt - 1) * BM;
+      for (int ss = 0; ok && ss < shp.NSS; ++ss, ++gs) {
+        const uint32_t slot = gs % W_SLOTS;
+        if (!P::mbar_wait_warp(&sm.empty_w[slot], ((gs / W_SLOTS) & 1u) ^ 1u, abort_flag, err,
+                               ERR_SCHED)) {
+          ok = false;
+          break;
+        }
+        if (wleader) {
           P::mbar_arrive_expect_tx(&sm.full_w[slot], W_BOX_BYTES);
           P::tma_load_2d(P::smem_u32(sm.w[slot]), &wmaps.m[g], &sm.full_w[slot], ss * SS * BK,
                          wrow);
-          gw = gs + 1;
         }
+        __syncwarp();
+        gw = gs + 1;
       }
-      if (!__shfl_sync(0xFFFFFFFFu, int(ok), 0)) break;
+      if (!ok) break;
     }
     if (lane == 0) {
       if (ok) push_tile(sm, nq, -1, nullptr, abort_flag, err);
@@ -648,15 +665,23 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
     __syncwarp();
   } else if (warp == MMA_WARP) {
     // ---------------- MMA issuer (even CTA): one wait and one commit per 8 MMAs ----------------
-    if (lane == 0 && rank == 0) {
+    // The whole warp runs the loop, so that its waits, addresses and
+    // descriptors are warp-uniform, and one elected lane issues every MMA and
+    // commit.  (A loop run by one lane alone loses issue slots to the other
+    // warps of its SM sub-partition -- here a converter and four epilogue
+    // warps -- and the tensor pipe then waits for its MMAs.)
+    if (rank == 0) {
+      uint32_t leader_lane;
+      const uint32_t leader = P::elect_one(&leader_lane);
       uint32_t gs = 0, gt = 0, nq = 0;
       bool ok = true;
       for (;;) {
         int t;
         TilePlan pl;
-        if (!pop_tile(sm, nq, abort_flag, err, ERR_MMA, t, &pl) || t < 0) break;
+        if (!pop_tile_warp(sm, nq, abort_flag, err, ERR_MMA, t, lane, nullptr, &pl) || t < 0)
+          break;
         // both epilogues have copied out the previous tile's accumulator
-        if (!P::mbar_wait(&sm.dempty, (gt & 1u) ^ 1u, abort_flag, err, ERR_MMA)) break;
+        if (!P::mbar_wait_warp(&sm.dempty, (gt & 1u) ^ 1u, abort_flag, err, ERR_MMA)) break;
         bool check_failed = false;
         uint32_t pending = pl.ckpt;                 // checkpoints still ahead
         // the super-stages run by run, a checkpoint between runs (the inner
@@ -665,28 +690,37 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
           const int ss_end = pending ? (__ffs(pending) - 1) * shp.seg_ss : shp.NSS;
           for (; ss < ss_end; ++ss, ++gs) {
             const uint32_t slot = gs % B_SLOTS, aslot = gs % A_SLOTS;
-            if (!P::mbar_wait(&sm.full_a[aslot], (gs / A_SLOTS) & 1u, abort_flag, err,
-                              ERR_MMA)) {
+            if (!P::mbar_wait_warp(&sm.full_a[aslot], (gs / A_SLOTS) & 1u, abort_flag, err,
+                                   ERR_MMA)) {
               ok = false;
               break;
             }
             P::tc_fence_after();
             const uint32_t a_tmem = tmem + TM_A + aslot * (SS * 32);
             const int nkb = min(SS, shp.KB - ss * SS);
-            for (int j = 0; j < nkb; ++j) {
-              const uint64_t bdesc = P::smem_desc_sw128(P::smem_u32(sm.b[slot][j]));
+            const uint64_t bdesc0 = P::smem_desc_sw128(P::smem_u32(sm.b[slot][0]));
+            const uint64_t bdesc1 = P::smem_desc_sw128(P::smem_u32(sm.b[slot][1]));
+            if (leader) {
 #pragma unroll
-              for (int kk = 0; kk < BK / 16; ++kk)
-                P::mma_f16_ts_pair(tmem + TM_D, a_tmem + j * 32 + kk * 8,
-                                   bdesc + uint64_t(kk * 2), kAffine ? IDESC_BF16 : IDESC,
-                                   (ss > 0 || j > 0 || kk > 0) ? 1u : 0u);
+              for (int j = 0; j < SS; ++j) {
+                if (j >= nkb) break;
+                const uint64_t bdesc = j ? bdesc1 : bdesc0;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                  P::mma_f16_ts_pair(tmem + TM_D, a_tmem + j * 32 + kk * 8,
+                                     bdesc + uint64_t(kk * 2), kAffine ? IDESC_BF16 : IDESC,
+                                     (ss > 0 || j > 0 || kk > 0) ? 1u : 0u);
+              }
+              P::mma_commit_pair_mc(&sm.empty_ss[slot], CLUSTER_MASK);
             }
-            P::mma_commit_pair_mc(&sm.empty_ss[slot], CLUSTER_MASK);
+            __syncwarp();
           }
           if (!ok || !pending) break;
           const int seg = __ffs(pending) - 1;
           pending &= pending - 1u;
-          const int r = mma_checkpoint(sm, pl, seg, gt, abort_flag, err);
+          int r = 0;
+          if (leader) r = mma_checkpoint(sm, pl, seg, gt, abort_flag, err);
+          r = __shfl_sync(0xFFFFFFFFu, r, int(leader_lane));
           ++gt;
           if (r < 0) {
             ok = false;
@@ -695,9 +729,9 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
           check_failed = check_failed || r > 0;
         }
         if (!ok) break;
-        P::mma_commit_pair_mc(&sm.dfull, CLUSTER_MASK);
+        if (leader) P::mma_commit_pair_mc(&sm.dfull, CLUSTER_MASK);
         ++gt;
-        if (check_failed) {
+        if (check_failed && leader) {
           // its outputs are rewritten by the chunked kernel, which runs after
           // this grid has completed
           int g, mb, pair;
@@ -705,12 +739,15 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
           list_for_chunked(shp, status, list, g, mb, pair);
           atomicAdd(status + 7, 1u);
         }
+        __syncwarp();
       }
-      // every MMA this thread issued has finished before TMEM is freed
-      P::mma_commit_pair_mc(&sm.mma_done, 1);
-      int no_abort = 0;
-      volatile int* never = &no_abort;
-      P::mbar_wait(&sm.mma_done, 0, never, err, ERR_TEARDOWN);
+      // every MMA the leader issued has finished before TMEM is freed
+      if (leader) {
+        P::mma_commit_pair_mc(&sm.mma_done, 1);
+        int no_abort = 0;
+        volatile int* never = &no_abort;
+        P::mbar_wait(&sm.mma_done, 0, never, err, ERR_TEARDOWN);
+      }
     } else if (lane == 0) {
       // the odd CTA issues nothing; it takes the tiles from the queue like
       // every other role so that the queue slots are released

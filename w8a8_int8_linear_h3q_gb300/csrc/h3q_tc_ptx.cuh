@@ -224,6 +224,20 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint6
       : "memory");
 }
 
+// Elects one lane of the (converged) calling warp: 1 on that lane, 0 on the
+// others; its lane id goes to *leader_lane if given.  A loop that the whole
+// warp runs, with one elected lane issuing the asynchronous copies or MMAs,
+// keeps its waits, addresses and descriptors warp-uniform; the same loop run
+// by one lane alone was measured to lose most of its issue rate to busy warps
+// on its SM sub-partition.
+__device__ __forceinline__ uint32_t elect_one(uint32_t* leader_lane = nullptr) {
+  uint32_t l, is;
+  asm volatile("{\n.reg .pred p;\nelect.sync %0|p, 0xffffffff;\nselp.u32 %1, 1, 0, p;\n}"
+               : "=r"(l), "=r"(is));
+  if (leader_lane) *leader_lane = l;
+  return is;
+}
+
 // --- clusters -------------------------------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_rank() {
