@@ -694,8 +694,8 @@ WIDE_SOURCES = ["w8a8_int8_linear_h3q_gb300/csrc/h3q_gemm_wide.cu",
                 "w8a8_int8_linear_h3q_gb300/csrc/h3q_tc_ptx.cuh",
                 "w8a8_int8_linear_h3q_gb300/csrc/h3q_epilogue.cuh",
                 "w8a8_int8_linear_h3q_gb300/csrc/h3q_internal.cuh"]
-WIDE_TRAFFIC = {"bytes_per_launch": 128295168 + 74402560,
-                "source_sha256": "abd010ee8e5a1581a4d2ee9962a77998955cbbf652d4656c961b0b1225c204d2",
+WIDE_TRAFFIC = {"bytes_per_launch": 128396544 + 74504448,
+                "source_sha256": "61eb5a9659d2cf43746171a3a5c5335429cfb1844c0d1d5f7f0c7bed978ec4f8",
                 "capture": "ncu --set full, one reuse-mode gemm_wide_kernel launch, attn Linear "
                            "8192x5376x5376 (python bench.py --kernel-case attn --steps 3 "
                            "--warmup 3; profiles/gemm_wide_attn_8192x5376x5376.md)"}
