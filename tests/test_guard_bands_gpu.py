@@ -52,9 +52,11 @@ def _operands(M, N, K, seed, dev):
     return x, w, b
 
 
+# odd N keeps 2-byte output stores; even N takes the paired 4-byte stores, whose last pair
+# ends exactly at the row's end (256 x 130, 1024 x 5382)
 SHAPES = [(1, 1, 16), (127, 131, 16), (129, 257, 1040), (255, 1, 1040), (257, 131, 5376),
           (1, 5383, 5376), (129, 5383, 1040), (257, 257, 5376), (32767, 131, 1040),
-          (32767, 5383, 5376)]
+          (32767, 5383, 5376), (256, 130, 1040), (1024, 5382, 5376)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)

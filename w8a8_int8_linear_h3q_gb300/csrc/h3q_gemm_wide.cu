@@ -361,6 +361,8 @@ __device__ __forceinline__ void list_for_chunked(const Shape& shp, uint32_t* sta
 // cancellation with the bias) takes the error-free path.  Blocks with scales
 // outside the checked ranges, ragged token tails and the raw INT32 output
 // take the general per-element path.
+__device__ __forceinline__ int lane_id() { return int(threadIdx.x & 31u); }
+
 __device__ __forceinline__ void emit_block(const uint32_t (&d)[32], float sa_l, int mbase,
                                            float swn, float bn, int n, bool n_ok,
                                            const Shape& shp, uint16_t* __restrict__ Y,
@@ -369,7 +371,15 @@ __device__ __forceinline__ void emit_block(const uint32_t (&d)[32], float sa_l, 
   // epilogue_value, bit for bit
   const bool s_in = epilogue_scales_in_range(sa_l, swn);
   if (__all_sync(0xFFFFFFFFu, s_in) && !ACC && Y && mbase + 32 <= shp.M) {
-    uint16_t* yp = Y + int64_t(mbase) * shp.N + n;
+    // adjacent lanes pair up: after one exchange, the even lane stores channels n, n + 1 of
+    // token j and the odd lane those of token j + 1, as one 4-byte store each (even N only,
+    // which keeps every pair 4-byte aligned)
+    const bool pairs = (shp.N & 1) == 0;
+    const int odd = lane_id() & 1;
+    const uint32_t sel = odd ? 0x3276u : 0x5410u;
+    uint16_t* yp = pairs ? Y + int64_t(mbase + odd) * shp.N + (n - odd)
+                         : Y + int64_t(mbase) * shp.N + n;
+    const bool pair_ok = (n - odd) < shp.N;
     const float* sa_ptr = sa_all + mbase;
     // two tokens at a time with the paired FP32 instructions (the same IEEE
     // operations as the scalar ones, half the instructions)
@@ -393,7 +403,12 @@ __device__ __forceinline__ void emit_block(const uint32_t (&d)[32], float sa_l, 
         vb = epilogue_value_careful(__float2int_rn(__uint_as_float(d[j + 1])), sa_b, swn, bn);
       uint32_t h2;
       asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(h2) : "f"(vb), "f"(va));
-      if (n_ok) {
+      if (pairs) {
+        const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, h2, 1);
+        uint32_t out;
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(out) : "r"(h2), "r"(other), "r"(sel));
+        if (pair_ok) *reinterpret_cast<uint32_t*>(yp + int64_t(j) * shp.N) = out;
+      } else if (n_ok) {
         yp[int64_t(j) * shp.N] = uint16_t(h2);
         yp[int64_t(j + 1) * shp.N] = uint16_t(h2 >> 16);
       }
