@@ -694,8 +694,8 @@ WIDE_SOURCES = ["w8a8_int8_linear_h3q_gb300/csrc/h3q_gemm_wide.cu",
                 "w8a8_int8_linear_h3q_gb300/csrc/h3q_tc_ptx.cuh",
                 "w8a8_int8_linear_h3q_gb300/csrc/h3q_epilogue.cuh",
                 "w8a8_int8_linear_h3q_gb300/csrc/h3q_internal.cuh"]
-WIDE_TRAFFIC = {"bytes_per_launch": 128396544 + 74504448,
-                "source_sha256": "61eb5a9659d2cf43746171a3a5c5335429cfb1844c0d1d5f7f0c7bed978ec4f8",
+WIDE_TRAFFIC = {"bytes_per_launch": 128430336 + 74942464,
+                "source_sha256": "58bc7c2bb59557812850b6fdb3610694d1b1543233c9b1d47701178e1e365ab1",
                 "capture": "ncu --set full, one reuse-mode gemm_wide_kernel launch, attn Linear "
                            "8192x5376x5376 (python bench.py --kernel-case attn --steps 3 "
                            "--warmup 3; profiles/gemm_wide_attn_8192x5376x5376.md)"}
