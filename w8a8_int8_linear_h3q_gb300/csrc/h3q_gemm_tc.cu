@@ -52,7 +52,8 @@
 //
 // Warp roles (480 threads):
 //   warp 0      TMA producer of the activation tiles (2 super-stage slots)
-//   warp 1      TMEM allocator and MMA issuer (one thread)
+//   warp 1      TMEM allocator and MMA issuer (the whole warp runs the loop,
+//               one elected lane issues)
 //   warp 2      TMA producer of the INT8 weight tiles (3 super-stage slots)
 //   warps 3-6   converters: INT8 weights -> FP16 -> TMEM (2 super-stages)
 //   warps 7-14  epilogue: chunk drains into INT32 running sums, then

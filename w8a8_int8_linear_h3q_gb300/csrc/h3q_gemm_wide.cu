@@ -55,14 +55,15 @@
 // accumulator for them, and each CTA's shared memory holds only its half of
 // the tile's tokens (128), which the pair MMA reads from both.  Half-size
 // activation stages let the activation ring be four super-stages deep, and
-// each CTA refills its own stages with no wait on the other.  One thread of
-// the even CTA issues every MMA; it waits on barriers that both CTAs'
-// converter and epilogue threads arrive on, and its commits arrive in both
-// CTAs.
+// each CTA refills its own stages with no wait on the other.  One elected
+// lane of the even CTA's MMA warp issues every MMA, while the whole warp runs
+// the loop and waits on barriers that both CTAs' converter and epilogue
+// threads arrive on; its commits arrive in both CTAs.
 //
 // Warp roles (736 threads per CTA):
 //   warp 0      TMA producer of this CTA's activation half (4 super-stages)
-//   warp 1      TMEM allocator; MMA issuer (one thread, even CTA only)
+//   warp 1      TMEM allocator; MMA issuer (the whole warp runs the loop,
+//               one elected lane issues; even CTA only)
 //   warp 2      tile scheduler (exactness test, fallback list) and TMA
 //               producer of this CTA's INT8 weight tiles (4 super-stages)
 //   warps 3-6   converters: INT8 weights -> FP16 -> TMEM (2 super-stages)
@@ -281,7 +282,8 @@ __device__ __forceinline__ int tile_path(const Shape& s, const uint32_t* amax,
 }
 
 // Single-thread take of the next queue entry (and, if `plan` is given, its
-// checkpoint plan).  False on a timeout or abort.
+// checkpoint plan).  False on a timeout or abort.  (The odd CTA's MMA warp
+// uses it; every loop on the hot path uses the warp-collective form below.)
 __device__ __forceinline__ bool pop_tile(Smem& sm, uint32_t& nq, volatile int* abort_flag,
                                          uint32_t* err, uint32_t code, int& t,
                                          TilePlan* plan = nullptr) {
@@ -429,7 +431,8 @@ __device__ __forceinline__ void emit_block(const uint32_t (&d)[32], float sa_l, 
 }
 
 // The MMA issuer's checkpoint before norm segment `seg` (out of line and
-// outside the issue loop, whose speed it would otherwise cost).  The MMAs
+// outside the issue loop, whose speed it would otherwise cost; called by the
+// elected lane that issued the MMAs, since its commit must follow them).  The MMAs
 // issued so far complete into the accumulator, the
 // epilogues read it (exact so far) and each reports the largest magnitude of
 // its block, tagged with this event's number (gt + 1); then the run that
