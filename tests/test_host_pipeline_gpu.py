@@ -156,3 +156,34 @@ def test_host_pipeline_equally_spaced_outputs(lib, oracle, dev):
                              None if b[g] is None else c.bias_bits[g])
         check_y(_bits(yh[g]), want["v"])
     assert out["ys"][0].data_ptr() == yh[0].data_ptr()
+
+
+def test_prepared_host_call_repeats_on_new_inputs(lib, oracle, dev):
+    """GroupedHostCall checks and marshals once; each call reads the current
+    contents of x_host and gives what the one-shot function gives on it."""
+    M, N, K, G = 700, 264, 1040, 3
+    c1 = synth.make_linear(M, N, K, seed=91, n_linears=G, outlier_p=0.005, outlier_mul=30)
+    c2 = synth.make_linear(M, N, K, seed=92, n_linears=G, outlier_p=0.005, outlier_mul=30)
+    wq, ws, b = _operands(lib, c1, dev, G, drop_bias=True)
+    x_host = _bf16(c1.x_bits).pin_memory()
+    call = lib.GroupedHostCall(x_host, wq, ws, b, chunk_rows=256, first_rows=64)
+    for c in (c1, c2, c1):
+        x_host.copy_(_bf16(c.x_bits))
+        ys = [y.clone() for y in call()]
+        ref = lib.h3q_linear_w8a8_grouped_host(x_host, wq, ws, b, chunk_rows=256, first_rows=64)
+        for g in range(G):
+            assert _same(ys[g], ref["ys"][g]), f"Linear {g}: prepared call differs"
+    want = oracle.linear(c1.x_bits, *oracle.quantize_weights(c1.w[0]), c1.bias_bits[0])
+    check_y(_bits(ys[0]), want["v"])
+
+
+def test_prepared_host_call_checks_its_arguments(lib, dev):
+    M, N, K = 64, 64, 64
+    wq = [torch.zeros((N, K), dtype=torch.int8, device=dev)]
+    ws = [torch.ones((N,), dtype=torch.float32, device=dev)]
+    with pytest.raises(TypeError):
+        lib.GroupedHostCall(torch.zeros((M, K), dtype=torch.bfloat16), wq, ws)   # not pinned
+    with pytest.raises(TypeError):
+        lib.GroupedHostCall(torch.zeros((M, K), dtype=torch.float32).pin_memory(), wq, ws)
+    with pytest.raises(ValueError):
+        lib.GroupedHostCall(torch.zeros((M, K + 16), dtype=torch.bfloat16).pin_memory(), wq, ws)

@@ -110,34 +110,51 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+_torch = None
+
+
+def _tm():
+    """torch, imported on first use (the checks below run on every call, so
+    they keep their per-tensor cost to one combined test)."""
+    global _torch
+    if _torch is None:
+        import torch
+        _torch = torch
+    return _torch
+
+
 def _stream(stream):
-    import torch
-    s = torch.cuda.current_stream() if stream is None else stream
+    s = _tm().cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
 
 
 def _need(t, dtype, shape, name):
-    import torch
+    torch = _tm()
+    if (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype is dtype and t.is_contiguous()
+            and (shape is None or t.shape == tuple(shape))):
+        return
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    if shape is not None and tuple(t.shape) != tuple(shape):
-        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
 def _need_pinned(t, dtype, shape, name):
-    import torch
+    torch = _tm()
+    if (isinstance(t, torch.Tensor) and not t.is_cuda and t.dtype is dtype
+            and t.is_contiguous() and (shape is None or t.shape == tuple(shape))
+            and t.is_pinned()):
+        return
     if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_pinned():
         raise TypeError(f"{name} must be a page-locked (pinned) CPU tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    if shape is not None and tuple(t.shape) != tuple(shape):
-        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
 def _check(status, where):
@@ -407,6 +424,77 @@ def h3q_linear_w8a8_grouped_host_chunks(M: int, chunk_rows: int = 2048, first_ro
     return list(out)
 
 
+class GroupedHostCall:
+    """h3q_linear_w8a8_grouped_host with its arguments checked, its buffers
+    allocated and its C arguments marshalled once; calling the object runs
+    the call again on the same tensors.  For repeated steps: write the next
+    step's X into ``x_host`` (it is read at each call) and call.  Every call
+    still uploads X, runs the grouped Linear and downloads the outputs, and
+    synchronises.  The object keeps its tensors alive."""
+
+    def __init__(self, x_host, wqs, wss, biases=None, *, ys_host=None, x_dev=None, xs=None,
+                 ys_dev=None, chunk_rows=2048, first_rows=0, workspace=None, stream=None,
+                 h2d_stream=None, d2h_stream=None):
+        torch = _tm()
+        G = len(wqs)
+        if not 1 <= G <= 4 or len(wss) != G or (biases is not None and len(biases) != G):
+            raise ValueError("1..4 Linears, with one scale vector (and bias) each")
+        for w in wqs:
+            _need(w, torch.int8, tuple(wqs[0].shape), "wq")
+        N, K = wqs[0].shape
+        dev = wqs[0].device
+        _need_pinned(x_host, torch.bfloat16, None, "x_host")
+        M = x_host.shape[0]
+        if x_host.shape[1] != K:
+            raise ValueError("x_host and wq disagree on K")
+        for sc in wss:
+            _need(sc, torch.float32, (N,), "ws")
+        if biases is not None:
+            for b in biases:
+                if b is not None:
+                    _need(b, torch.bfloat16, (N,), "bias")
+        if ys_host is None:   # one [G, M, N] buffer: a chunk's downloads are then one copy
+            yh = torch.empty((G, M, N), dtype=torch.bfloat16).pin_memory()
+            ys_host = [yh[g] for g in range(G)]
+        for y in ys_host:
+            _need_pinned(y, torch.bfloat16, (M, N), "y_host")
+        if x_dev is None:
+            x_dev = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+        if xs is None:
+            xs = torch.empty((M,), dtype=torch.float32, device=dev)
+        if ys_dev is None:
+            yd = torch.empty((G, M, N), dtype=torch.bfloat16, device=dev)
+            ys_dev = [yd[g] for g in range(G)]
+        _need(x_dev, torch.bfloat16, (M, K), "x_dev")
+        _need(xs, torch.float32, (M,), "xs")
+        for y in ys_dev:
+            _need(y, torch.bfloat16, (M, N), "y_dev")
+        need = h3q_linear_w8a8_grouped_host_workspace_bytes(G, M, N, K, chunk_rows)
+        if workspace is None:
+            workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
+        wbytes = workspace.numel() * workspace.element_size()
+        if stream is None:
+            stream = torch.cuda.current_stream(dev)
+        if h2d_stream is None:
+            h2d_stream = torch.cuda.Stream(dev)
+        if d2h_stream is None:
+            d2h_stream = torch.cuda.Stream(dev)
+        arr = lambda ts: (ctypes.c_void_p * G)(*[None if t is None else t.data_ptr() for t in ts])
+        self._keep = (x_host, list(wqs), list(wss), biases, ys_host, x_dev, xs, ys_dev, workspace,
+                      stream, h2d_stream, d2h_stream)
+        self._args = (_ptr(x_host), G, arr(wqs), arr(wss), None if biases is None else arr(biases),
+                      M, N, K, arr(ys_host), _ptr(x_dev), _ptr(xs), arr(ys_dev), chunk_rows,
+                      first_rows, _ptr(workspace), wbytes, _stream(stream), _stream(h2d_stream),
+                      _stream(d2h_stream))
+        self._fn = load().h3q_linear_w8a8_grouped_host
+        self.ys = ys_host
+        self.ys_dev, self.x_dev, self.xs, self.workspace = ys_dev, x_dev, xs, workspace
+
+    def __call__(self):
+        _check(self._fn(*self._args), "h3q_linear_w8a8_grouped_host")
+        return self.ys
+
+
 def h3q_linear_w8a8_grouped_host(x_host, wqs, wss, biases=None, *, ys_host=None, x_dev=None,
                                  xs=None, ys_dev=None, chunk_rows=2048, first_rows=0,
                                  workspace=None, stream=None, h2d_stream=None, d2h_stream=None):
@@ -417,56 +505,15 @@ def h3q_linear_w8a8_grouped_host(x_host, wqs, wss, biases=None, *, ys_host=None,
     ``h2d_stream`` and ``d2h_stream``).  Device staging (``x_dev``, ``xs``,
     ``ys_dev``), the workspace, the host outputs and the copy streams are
     allocated here when not given.  Synchronises.  Returns a dict with ``ys``
-    (host), ``ys_dev``, ``x_dev``, ``xs`` and the ``workspace``."""
-    import torch
-    G = len(wqs)
-    if not 1 <= G <= 4 or len(wss) != G or (biases is not None and len(biases) != G):
-        raise ValueError("1..4 Linears, with one scale vector (and bias) each")
-    for w in wqs:
-        _need(w, torch.int8, tuple(wqs[0].shape), "wq")
-    N, K = wqs[0].shape
-    dev = wqs[0].device
-    _need_pinned(x_host, torch.bfloat16, None, "x_host")
-    M = x_host.shape[0]
-    if x_host.shape[1] != K:
-        raise ValueError("x_host and wq disagree on K")
-    for sc in wss:
-        _need(sc, torch.float32, (N,), "ws")
-    if biases is not None:
-        for b in biases:
-            if b is not None:
-                _need(b, torch.bfloat16, (N,), "bias")
-    if ys_host is None:   # one [G, M, N] buffer: a chunk's downloads are then one copy
-        yh = torch.empty((G, M, N), dtype=torch.bfloat16).pin_memory()
-        ys_host = [yh[g] for g in range(G)]
-    for y in ys_host:
-        _need_pinned(y, torch.bfloat16, (M, N), "y_host")
-    if x_dev is None:
-        x_dev = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
-    if xs is None:
-        xs = torch.empty((M,), dtype=torch.float32, device=dev)
-    if ys_dev is None:
-        yd = torch.empty((G, M, N), dtype=torch.bfloat16, device=dev)
-        ys_dev = [yd[g] for g in range(G)]
-    _need(x_dev, torch.bfloat16, (M, K), "x_dev")
-    _need(xs, torch.float32, (M,), "xs")
-    for y in ys_dev:
-        _need(y, torch.bfloat16, (M, N), "y_dev")
-    need = h3q_linear_w8a8_grouped_host_workspace_bytes(G, M, N, K, chunk_rows)
-    if workspace is None:
-        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
-    wbytes = workspace.numel() * workspace.element_size()
-    if h2d_stream is None:
-        h2d_stream = torch.cuda.Stream(dev)
-    if d2h_stream is None:
-        d2h_stream = torch.cuda.Stream(dev)
-    arr = lambda ts: (ctypes.c_void_p * G)(*[None if t is None else t.data_ptr() for t in ts])
-    _check(load().h3q_linear_w8a8_grouped_host(
-        _ptr(x_host), G, arr(wqs), arr(wss), None if biases is None else arr(biases), M, N, K,
-        arr(ys_host), _ptr(x_dev), _ptr(xs), arr(ys_dev), chunk_rows, first_rows,
-        _ptr(workspace), wbytes, _stream(stream), _stream(h2d_stream), _stream(d2h_stream)),
-        "h3q_linear_w8a8_grouped_host")
-    return {"ys": ys_host, "ys_dev": ys_dev, "x_dev": x_dev, "xs": xs, "workspace": workspace}
+    (host), ``ys_dev``, ``x_dev``, ``xs`` and the ``workspace``.  (For repeated
+    calls on the same tensors, GroupedHostCall checks and marshals once.)"""
+    c = GroupedHostCall(x_host, wqs, wss, biases, ys_host=ys_host, x_dev=x_dev, xs=xs,
+                        ys_dev=ys_dev, chunk_rows=chunk_rows, first_rows=first_rows,
+                        workspace=workspace, stream=stream, h2d_stream=h2d_stream,
+                        d2h_stream=d2h_stream)
+    c()
+    return {"ys": c.ys, "ys_dev": c.ys_dev, "x_dev": c.x_dev, "xs": c.xs,
+            "workspace": c.workspace}
 
 
 def h3q_linear_chunked_tiles(workspace, M: int, K: int, stream=None) -> int:
