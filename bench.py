@@ -695,8 +695,8 @@ WIDE_SOURCES = ["w8a8_int8_linear_h3q_gb300/csrc/h3q_gemm_wide.cu",
                 "w8a8_int8_linear_h3q_gb300/csrc/h3q_tc_ptx.cuh",
                 "w8a8_int8_linear_h3q_gb300/csrc/h3q_epilogue.cuh",
                 "w8a8_int8_linear_h3q_gb300/csrc/h3q_internal.cuh"]
-WIDE_TRAFFIC = {"bytes_per_launch": 128430336 + 74942464,
-                "source_sha256": "539b7d20043ab3bdea8f62bd0adc77ae14a5a56dad8ed9b3525e6d938cc7e66f",
+WIDE_TRAFFIC = {"bytes_per_launch": 128485888 + 74615552,
+                "source_sha256": "62e908619aed333261a4a233907ea825ceb8eb70a576b00d5e32bab187b1e980",
                 "capture": "ncu --set full, one reuse-mode gemm_wide_kernel launch, attn Linear "
                            "8192x5376x5376 (python bench.py --kernel-case attn --steps 3 "
                            "--warmup 3; profiles/gemm_wide_attn_8192x5376x5376.md)"}

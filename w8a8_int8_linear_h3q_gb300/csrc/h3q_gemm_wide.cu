@@ -105,8 +105,9 @@ constexpr int NUM_CONV_WARPS = 4;
 constexpr int EPI_WARP0 = CONV_WARP0 + NUM_CONV_WARPS;
 constexpr int NUM_EPI_WARPS = 16;
 constexpr int THREADS = 32 * (EPI_WARP0 + NUM_EPI_WARPS);
-// every role but the scheduler takes each tile from the queue: one arrival
-// per producer or MMA thread, one per converter or epilogue warp
+// every warp but the scheduler takes each tile from the queue, with one
+// arrival per warp: the activation producer, the MMA warp, the converters
+// and the epilogue
 constexpr int QUEUE_READERS = 2 + NUM_CONV_WARPS + NUM_EPI_WARPS;
 constexpr int B_KBLOCK_BYTES = BNH * BK * 2;               // 16 KB
 constexpr int W_BOX_BYTES = BM * SS * BK;                  // 16 KB: 128 rows x 2 k-blocks
@@ -279,25 +280,6 @@ __device__ __forceinline__ int tile_path(const Shape& s, const uint32_t* amax,
   const uint64_t a = amax[mb];
   if (a * s.wmax2 <= kExactBound) return TILE_WIDE;
   return tile_path_norms(s, a, aseg, nwpart, nwseg, mb, pair, lane, plan);
-}
-
-// Single-thread take of the next queue entry (and, if `plan` is given, its
-// checkpoint plan).  False on a timeout or abort.  (The odd CTA's MMA warp
-// uses it; every loop on the hot path uses the warp-collective form below.)
-__device__ __forceinline__ bool pop_tile(Smem& sm, uint32_t& nq, volatile int* abort_flag,
-                                         uint32_t* err, uint32_t code, int& t,
-                                         TilePlan* plan = nullptr) {
-  const uint32_t q = nq % SQ;
-  if (!P::mbar_wait(&sm.q_full[q], (nq / SQ) & 1u, abort_flag, err, code)) return false;
-  t = sm.q_tile[q];
-  if (plan) {
-    plan->ckpt = sm.q_ckpt[q];
-    if (plan->ckpt)
-      for (int i = 0; i < 2 * NSEG; ++i) plan->aw[i] = sm.q_aw[q][i];
-  }
-  P::mbar_arrive(&sm.q_empty[q]);
-  ++nq;
-  return true;
 }
 
 // Warp-collective take (with the entry's checkpoint bits, or its whole
@@ -766,13 +748,13 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap act_map, const __grid_const
         volatile int* never = &no_abort;
         P::mbar_wait(&sm.mma_done, 0, never, err, ERR_TEARDOWN);
       }
-    } else if (lane == 0) {
-      // the odd CTA issues nothing; it takes the tiles from the queue like
-      // every other role so that the queue slots are released
+    } else {
+      // the odd CTA issues nothing; its MMA warp takes the tiles from the
+      // queue like every other role so that the queue slots are released
       uint32_t nq = 0;
       for (;;) {
         int t;
-        if (!pop_tile(sm, nq, abort_flag, err, ERR_MMA, t) || t < 0) break;
+        if (!pop_tile_warp(sm, nq, abort_flag, err, ERR_MMA, t, lane) || t < 0) break;
       }
     }
     __syncwarp();
