@@ -293,3 +293,19 @@ def test_host_pipeline_chunk_plan_rejects_bad_args(cdll):
     assert f(100, 32, 0, None, 0) == 4                   # count only: 16, 32, 32, 20
     with pytest.raises(ValueError):
         h3q.h3q_linear_w8a8_grouped_host_chunks(100, 24)
+
+
+def test_binding_checks_tensors_before_any_device_work():
+    """The Python binding's argument checks (one combined test per tensor)
+    reject host tensors where device tensors are required, with the error
+    naming the argument, before the library is asked to do anything."""
+    torch = pytest.importorskip("torch")
+    import w8a8_int8_linear_h3q_gb300 as h3q
+    wq = [torch.zeros((64, 64), dtype=torch.int8)]
+    ws = [torch.ones((64,), dtype=torch.float32)]
+    with pytest.raises(TypeError, match="wq must be a CUDA tensor"):
+        h3q.GroupedHostCall(torch.zeros((64, 64), dtype=torch.bfloat16), wq, ws)
+    with pytest.raises(TypeError, match="must be a CUDA tensor"):
+        h3q._need(torch.zeros((4,), dtype=torch.float32), torch.float32, (4,), "xs")
+    with pytest.raises(TypeError, match="page-locked"):
+        h3q._need_pinned(torch.zeros((4,), dtype=torch.float32), torch.float32, (4,), "x_host")
