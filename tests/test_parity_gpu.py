@@ -288,6 +288,35 @@ def test_fc2_every_row_against_the_legacy_exact_kernel(lib, dev, fc2_case):
     assert ckpt > 0
 
 
+@pytest.mark.slow
+def test_attn_grouped_step_every_row_against_the_legacy_exact_kernel(lib, dev):
+    """The headline step itself: one grouped call over Q, K, V and O of the
+    attention workload (8192 x 5376 x 5376 each).  Every output of the four
+    Linears must equal, bit for bit, the legacy mma.sync INT8 kernel's on the
+    same INT8 operands (that kernel is exact by construction and checked
+    against the oracle, and y depends on (acc, s_a, s_w, bias) alone).  The
+    activation codes come from h3q_quantize_act, whose scales must equal the
+    grouped call's."""
+    c = synth.attn()
+    x = _bf16_dev(c.x_bits, dev)
+    qws, sws, bs = [], [], []
+    for w, bb in zip(c.w, c.bias_bits):
+        q, s = lib.h3q_quantize_weights(torch.from_numpy(w).to(dev))
+        qws.append(q)
+        sws.append(s)
+        bs.append(_bf16_dev(bb, dev))
+    out = lib.h3q_linear_w8a8_grouped(x, qws, sws, bs)
+    xq, xs = lib.h3q_quantize_act(x)
+    del x
+    torch.cuda.synchronize()
+    assert torch.equal(out["xs"], xs), "the grouped call's activation scales differ from A2's"
+    for g in range(4):
+        leg = lib.h3q_linear_w8a8_mma_sync(xq, xs, qws[g], sws[g], bs[g])
+        torch.cuda.synchronize()
+        bad = int((out["ys"][g].view(torch.int16) != leg["y"].view(torch.int16)).sum())
+        assert bad == 0, f"Linear {'QKVO'[g]}: {bad} outputs differ from the legacy exact kernel"
+
+
 def test_epilogue_deep_cancellation(lib, oracle, dev):
     # Row 0's bias is -BF16(acc * s_a * s_w), so v there is the small residual
     # left after cancellation; an FP32 evaluation that rounds the product first
