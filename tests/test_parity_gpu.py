@@ -289,6 +289,30 @@ def test_fc2_every_row_against_the_legacy_exact_kernel(lib, dev, fc2_case):
 
 
 @pytest.mark.slow
+@pytest.mark.parametrize("name", ["fc1", "image_qkv", "image_down"])
+def test_workload_every_row_against_the_legacy_exact_kernel(lib, dev, name):
+    """The same every-row check as fc2's on three more full-size workloads:
+    fc1 (ragged M = 32767, 21504 channels), the H3-Image fused QKV and
+    image_down, where every tile keeps one accumulator only by way of a
+    checkpoint.  INT32 accumulators and BF16 outputs must equal the legacy
+    exact kernel's bit for bit."""
+    c = synth.WORKLOADS[name]()
+    x = _bf16_dev(c.x_bits, dev)
+    qw, sw = lib.h3q_quantize_weights(torch.from_numpy(c.w[0]).to(dev))
+    b = _bf16_dev(c.bias_bits[0], dev)
+    out = lib.h3q_linear_w8a8(x, qw, sw, b, want_acc=True, want_xq=True)
+    del x
+    ckpt = lib.h3q_linear_checkpointed_tiles(out["workspace"], c.M, c.K)
+    leg = lib.h3q_linear_w8a8_mma_sync(out["xq"], out["xs"], qw, sw, b, want_acc=True)
+    torch.cuda.synchronize()
+    bad = int((out["acc"] != leg["acc"]).sum())
+    assert bad == 0, f"{name}: {bad} INT32 accumulators differ from the legacy exact kernel"
+    assert torch.equal(out["y"].view(torch.int16), leg["y"].view(torch.int16))
+    if name == "image_down":
+        assert ckpt > 0           # the checkpointed path is the one under test here
+
+
+@pytest.mark.slow
 def test_attn_grouped_step_every_row_against_the_legacy_exact_kernel(lib, dev):
     """The headline step itself: one grouped call over Q, K, V and O of the
     attention workload (8192 x 5376 x 5376 each).  Every output of the four
