@@ -66,3 +66,41 @@ def test_random_shapes_match_the_legacy_exact_kernel(lib):
         calls += 1
     # the budget covers many calls, and both the checkpointed and the chunked path
     assert calls > 100 and ckpt > 0 and chunked > 0, (calls, ckpt, chunked)
+
+
+def test_random_grouped_calls_match_separate_calls(lib):
+    """The grouped launch on random shapes: G = 1..4 Linears sharing X (their
+    tiles interleaved in one launch, with per-Linear fallback lists), each
+    output equal bit for bit to that Linear's own single call, and the
+    activation scales equal too.  Seeded; a fixed time budget."""
+    dev = torch.device("cuda:0")
+    rng = np.random.default_rng(20261204)
+    t0 = time.time()
+    calls = 0
+    while time.time() - t0 < BUDGET_S:
+        G = int(rng.integers(1, 5))
+        M = int(rng.choice([1, 33, 256, 257, 700, 2049]))
+        N = int(rng.choice([8, 130, 257, 512, 1000]))
+        K = int(16 * rng.integers(1, 1400))
+        kind = int(rng.integers(0, 4))
+        g = torch.Generator(device=dev)
+        g.manual_seed(int(rng.integers(1 << 31)))
+        x, _ = _inputs(kind, M, 1, K, g, dev)
+        qws, sws, bs = [], [], []
+        for i in range(G):
+            _, w = _inputs(kind, 1, N, K, g, dev)
+            q, s = lib.h3q_quantize_weights(w)
+            qws.append(q)
+            sws.append(s)
+            bs.append((torch.randn((N,), generator=g, device=dev) * 0.1).to(torch.bfloat16)
+                      if rng.integers(0, 2) else None)
+        out = lib.h3q_linear_w8a8_grouped(x, qws, sws, bs)
+        for i in range(G):
+            one = lib.h3q_linear_w8a8(x, qws[i], sws[i], bs[i])
+            torch.cuda.synchronize()
+            what = f"G={G} Linear {i} M={M} N={N} K={K} inputs={kind}"
+            assert torch.equal(one["xs"], out["xs"]), f"{what}: activation scales differ"
+            assert torch.equal(one["y"].view(torch.int16), out["ys"][i].view(torch.int16)), \
+                f"{what}: outputs differ from the single call"
+        calls += 1
+    assert calls > 30, calls
