@@ -29,6 +29,7 @@ int main(void) {
   /* argument errors come back before any device work */
   printf("%d\n", (int)h3q_quantize_act(NULL, 4, 64, NULL, NULL, NULL));
   printf("%d\n", (int)h3q_probe_mma_s8_tops(NULL, NULL));
+  printf("%d\n", (int)h3q_probe_mma_f16_pair_tflops(NULL, 0, NULL));
   return 0;
 }
 """
@@ -67,3 +68,4 @@ def test_header_compiles_as_c99_and_links(tmp_path):
     assert lines[3] == "6: 64 128 256 256 256 40"
     assert int(lines[4]) == 1                    # H3Q_ERR_INVALID_ARG
     assert int(lines[5]) == 1
+    assert int(lines[6]) == 1                    # the FP16 probe: no output pointer
